@@ -1,0 +1,255 @@
+"""Oracle for the ZeRO stage-1/2/3 sharded mixed-precision step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (the ``zero_sharded_mixed_gb300`` package and its CUDA library)
+never imports, links or calls anything here, and nothing here imports the
+product package.
+
+Two parts:
+
+* ``zero_oracle.c`` -- plain scalar C (built with ``-O2 -ffp-contract=off``):
+  layout, reduce-scatter as a mean, fp32 AdamW with bias correction and
+  decoupled weight decay, round-to-nearest-even bf16 cast, all-gather, the
+  ZeRO-1/2 step over simulated ranks, the plain data-parallel step, and the
+  two gradient-accumulation orders.  The numpy wrappers below only marshal
+  arrays into it.
+* ``formulas.py`` -- the per-GPU model-state bytes and the per-GPU
+  communication bytes of each stage ("ZeRO and FSDP", sections "Memory per
+  GPU" and "Communication volume").
+
+Every function's pins (what fixes it other than itself) live in
+``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from .formulas import zero_comm_bytes, zero_memory  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "zero_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -ffp-contract=off: every fp32 multiply and add is rounded on its own, as the
+# C source is written; gcc would otherwise fuse them on aarch64.
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc), if stale."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        p = ctypes.c_void_p
+        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f32.restype = f32
+        lib.oracle_f32_to_bf16.argtypes = [f32]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_cast_bf16.argtypes = [p, p, i64]
+        lib.oracle_cast_bf16.restype = None
+        lib.oracle_layout.argtypes = [p, i32, i32, i64, i64, p, p]
+        lib.oracle_layout.restype = ctypes.c_int
+        lib.oracle_reduce_mean_bf16.argtypes = [p, i32, i64, i64, f32, p]
+        lib.oracle_reduce_mean_bf16.restype = None
+        lib.oracle_reduce_mean_f32.argtypes = [p, i32, i64, i64, f32, p]
+        lib.oracle_reduce_mean_f32.restype = None
+        lib.oracle_bias_corrections.argtypes = [f32, f32, i64, p, p]
+        lib.oracle_bias_corrections.restype = None
+        lib.oracle_adamw.argtypes = [p, p, p, p, i64, f32, f32, f32, f32, f32, i64]
+        lib.oracle_adamw.restype = None
+        lib.oracle_zero_step.argtypes = [p, i32, i64, p, p, p, p, i32,
+                                         f32, f32, f32, f32, f32, i64]
+        lib.oracle_zero_step.restype = ctypes.c_int
+        lib.oracle_dp_step.argtypes = [p, i32, i64, p, p, p, p,
+                                       f32, f32, f32, f32, f32, i64]
+        lib.oracle_dp_step.restype = ctypes.c_int
+        lib.oracle_accumulate_local.argtypes = [p, p, i64, i32]
+        lib.oracle_accumulate_local.restype = None
+        lib.oracle_accumulate_reduce.argtypes = [p, p, i32, i64, i64, i32]
+        lib.oracle_accumulate_reduce.restype = None
+        lib.oracle_all_gather_bf16.argtypes = [p, i32, i64, p]
+        lib.oracle_all_gather_bf16.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, f"expected bf16 bit patterns as uint16, got {a.dtype}"
+    return a
+
+
+def _f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.float32, f"expected float32, got {a.dtype}"
+    return a
+
+
+class AdamW:
+    """AdamW hyper-parameters; every one of them an fp32 value."""
+
+    def __init__(self, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1):
+        self.lr = float(np.float32(lr))
+        self.beta1 = float(np.float32(beta1))
+        self.beta2 = float(np.float32(beta2))
+        self.eps = float(np.float32(eps))
+        self.weight_decay = float(np.float32(weight_decay))
+
+    def args(self):
+        return (self.lr, self.beta1, self.beta2, self.eps, self.weight_decay)
+
+
+# --------------------------------------------------------------------------
+# wrappers
+# --------------------------------------------------------------------------
+
+def bf16_to_f32(h) -> np.ndarray:
+    """Widen bf16 bit patterns to fp32 (exact)."""
+    h = np.asarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def cast_bf16(x) -> np.ndarray:
+    """Round fp32 to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    x = _f32(x)
+    y = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_cast_bf16(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def layout(numels, n_dp: int, align: int = 8, bucket: int = 500_000_000):
+    """Returns dict(n, shard, padded, bucket, n_buckets, offsets) or raises ValueError."""
+    numel = np.ascontiguousarray(np.asarray(numels, dtype=np.int64).reshape(-1))
+    offsets = np.zeros(max(numel.size, 1), dtype=np.int64)
+    out = np.zeros(5, dtype=np.int64)
+    rc = _load().oracle_layout(_ptr(numel) if numel.size else None, numel.size, n_dp, align,
+                               bucket, _ptr(offsets), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"no layout for n_dp={n_dp} align={align} bucket={bucket} (rc={rc})")
+    n, s, p, bq, nb = (int(x) for x in out)
+    return dict(n=n, shard=s, padded=p, bucket=bq, n_buckets=nb,
+                offsets=offsets[: numel.size].copy())
+
+
+def reduce_mean(src, divisor: float) -> np.ndarray:
+    """Mean over rows (ranks) of a 2-D array: bf16 (uint16) or fp32 rows."""
+    src = np.ascontiguousarray(src)
+    assert src.ndim == 2
+    n_src, n = src.shape
+    g = np.empty(n, dtype=np.float32)
+    if src.dtype == np.uint16:
+        _load().oracle_reduce_mean_bf16(_ptr(src), n_src, n, n, float(np.float32(divisor)), _ptr(g))
+    else:
+        src = _f32(src)
+        _load().oracle_reduce_mean_f32(_ptr(src), n_src, n, n, float(np.float32(divisor)), _ptr(g))
+    return g
+
+
+def bias_corrections(hp: AdamW, t: int):
+    b1 = ctypes.c_float()
+    b2 = ctypes.c_float()
+    _load().oracle_bias_corrections(hp.beta1, hp.beta2, t, ctypes.byref(b1), ctypes.byref(b2))
+    return np.float32(b1.value), np.float32(b2.value)
+
+
+def adamw(w, m, v, g, hp: AdamW, t: int):
+    """Returns new (w, m, v); the inputs are not modified."""
+    w = _f32(w).copy()
+    m = _f32(m).copy()
+    v = _f32(v).copy()
+    g = _f32(g)
+    assert w.shape == m.shape == v.shape == g.shape
+    _load().oracle_adamw(_ptr(w), _ptr(m), _ptr(v), _ptr(g), w.size, *hp.args(), t)
+    return w, m, v
+
+
+def zero_step(grads, w_shards, m_shards, v_shards, hp: AdamW, t: int, n_copies: int = 1):
+    """ZeRO-1/2 step over n_dp simulated ranks.
+
+    grads: (n_dp, P) uint16 bf16; w/m/v_shards: (n_dp, S) fp32.
+    Returns (full_w (n_copies, P) uint16, w, m, v) -- new arrays, inputs untouched.
+    """
+    grads = _u16(grads)
+    n_dp, p = grads.shape
+    w = _f32(w_shards).copy()
+    m = _f32(m_shards).copy()
+    v = _f32(v_shards).copy()
+    assert w.shape == (n_dp, p // n_dp) and p % n_dp == 0
+    s = p // n_dp
+    full = np.empty((n_copies, p), dtype=np.uint16)
+    rc = _load().oracle_zero_step(_ptr(grads), n_dp, s, _ptr(w), _ptr(m), _ptr(v), _ptr(full),
+                                  n_copies, *hp.args(), t)
+    assert rc == 0, rc
+    return full, w, m, v
+
+
+def dp_step(grads, w_full, m_full, v_full, hp: AdamW, t: int):
+    """Plain data parallelism: every rank holds (n_dp, P) full copies."""
+    grads = _u16(grads)
+    n_dp, p = grads.shape
+    w = _f32(w_full).copy()
+    m = _f32(m_full).copy()
+    v = _f32(v_full).copy()
+    assert w.shape == (n_dp, p)
+    full = np.empty((n_dp, p), dtype=np.uint16)
+    rc = _load().oracle_dp_step(_ptr(grads), n_dp, p, _ptr(w), _ptr(m), _ptr(v), _ptr(full),
+                                *hp.args(), t)
+    assert rc == 0, rc
+    return full, w, m, v
+
+
+def accumulate_local(acc, g, first: bool) -> np.ndarray:
+    g = _u16(g)
+    acc = np.zeros(g.shape, np.float32) if acc is None else _f32(acc).copy()
+    _load().oracle_accumulate_local(_ptr(acc), _ptr(g), g.size, int(bool(first)))
+    return acc
+
+
+def accumulate_reduce(acc, src, first: bool) -> np.ndarray:
+    src = _u16(src)
+    n_src, n = src.shape
+    acc = np.zeros(n, np.float32) if acc is None else _f32(acc).copy()
+    _load().oracle_accumulate_reduce(_ptr(acc), _ptr(src), n_src, n, n, int(bool(first)))
+    return acc
+
+
+def all_gather(shards) -> np.ndarray:
+    shards = _u16(shards)
+    n_dp, s = shards.shape
+    full = np.empty(n_dp * s, dtype=np.uint16)
+    _load().oracle_all_gather_bf16(_ptr(shards), n_dp, s, _ptr(full))
+    return full
+
+
+def rs_adamw_reference(src, divisor, w, m, v, hp: AdamW, t: int):
+    """Mean of source rows, then AdamW, then cast: the per-element definition of
+    one fused update call.  Returns (out_bf16, w, m, v)."""
+    g = reduce_mean(src, divisor)
+    w2, m2, v2 = adamw(w, m, v, g, hp, t)
+    return cast_bf16(w2), w2, m2, v2

@@ -1,0 +1,26 @@
+"""ZeRO stage-1/2/3 sharded mixed-precision step for GB300 (sm_103a).
+
+The compute lives in ``libzero_gb300.so`` (hand-written CUDA kernels behind a
+C ABI, declared in ``include/zero_gb300.h``); ``binding`` is a thin ctypes layer
+with the same names.  The library is loaded on first use of a binding name, so
+importing ``zero_sharded_mixed_gb300.inputs`` alone does not need a GPU or a
+built library.  There is no CPU fallback: if the library is missing, every
+binding call raises.
+"""
+from __future__ import annotations
+
+_BINDING_NAMES = {
+    "ZeroError", "ZeroLayout", "ZeroAdamW", "lib_path", "load",
+    "zero_layout", "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate",
+    "zero_status_check", "zero_strerror", "zero_memory_bytes", "zero_comm_bytes",
+    "zero_bucket_range", "zero_shard_range",
+    "ZERO_BF16", "ZERO_F32", "ZERO_OUT_FULL", "ZERO_OUT_SHARD",
+    "ZERO_ACC_LOCAL", "ZERO_ACC_REDUCE", "ZERO_MAX_SRC",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)
