@@ -1,0 +1,207 @@
+/*
+ * zero_gb300.h -- C ABI of libzero_gb300.so: the ZeRO stage-1/2/3 sharded
+ * mixed-precision optimizer step on one GB300 (sm_103a).
+ *
+ * The n_dp data-parallel ranks are simulated as separate buffers in the one
+ * GPU's memory: rank r's full local gradient is its own buffer, rank o's shard
+ * of the fp32 master weights and Adam moments is its own range, and a
+ * "collective" is a kernel reading and writing those buffers.
+ *
+ * Conventions for every call:
+ *  - Return value: 0 (ZERO_OK) or a negative ZERO_E* code; zero_strerror()
+ *    names it.  A call that returns an error has enqueued nothing.
+ *  - Memory: the caller owns every buffer.  The library never allocates or
+ *    frees device memory and never synchronizes, except zero_status_check().
+ *    Every buffer argument must be device memory of the current device
+ *    (checked: host or other-device pointers give ZERO_EINVAL) and at least
+ *    element-aligned (2 bytes for bf16, 4 for fp32; else ZERO_EALIGN).  When all
+ *    the pointers of a call, after offsetting to the start of the range, are
+ *    16-byte aligned the kernels move 128-bit vectors; otherwise the same
+ *    kernels run element by element (still on the GPU).  The library cannot see
+ *    buffer lengths: extents stated below are the caller's responsibility (the
+ *    Python binding checks them against the tensors it is given).
+ *  - bf16 values are passed as uint16_t bit patterns.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Work is enqueued on it asynchronously.
+ *  - Pointer arrays (`src`, `shards`) are HOST arrays of device pointers.
+ *
+ * Notation ("ZeRO and FSDP", section "The idea, one stage at a time"): all
+ * parameters are flattened into one vector of N elements and cut into n_dp
+ * equal contiguous shards; rank r owns shard r.  Here the shard length is
+ * S = round_up(ceil(N / n_dp), align), the padded length P = n_dp * S, and the
+ * padding tail [N, P) holds zeros in every buffer.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = -1,   /* an argument is out of its domain (null, range, mode, pointer kind) */
+    ZERO_EALIGN = -2,   /* a pointer is not aligned to its element size */
+    ZERO_ERANGE = -3,   /* a size does not fit (int64 overflow, too many sources) */
+    ZERO_ECUDA = -4,    /* the CUDA runtime reported an error (launch or earlier async fault) */
+    ZERO_ETIMEOUT = -5  /* reserved: a bounded device-side wait gave up */
+};
+
+/* ---- enums -------------------------------------------------------------- */
+enum { ZERO_BF16 = 0, ZERO_F32 = 1 };                 /* source element type */
+enum { ZERO_OUT_FULL = 0, ZERO_OUT_SHARD = 1 };       /* where the bf16 result goes */
+enum { ZERO_ACC_LOCAL = 0, ZERO_ACC_REDUCE = 1 };     /* accumulation mode */
+
+#define ZERO_MAX_SRC 64   /* most source buffers one call reads */
+
+/* ---- structures --------------------------------------------------------- */
+
+/* A flat layout (one model under ZeRO-1/2, or one unit under ZeRO-3). */
+typedef struct {
+    int64_t n;          /* N: real elements */
+    int64_t padded_n;   /* P = n_dp * shard */
+    int64_t shard;      /* S: elements per rank, a multiple of align */
+    int64_t align;      /* a: shard alignment in elements */
+    int64_t bucket;     /* bucket length in elements, a multiple of align */
+    int64_t n_buckets;  /* ceil(P / bucket); 0 when P == 0 */
+    int32_t n_dp;       /* number of (simulated) data-parallel ranks */
+    int32_t reserved;   /* zero */
+} zero_layout_t;
+
+/* AdamW hyper-parameters for one step. */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    int32_t reserved;   /* zero */
+    int64_t step;       /* t, starting at 1 */
+} zero_adamw_t;
+
+/* ---- layout --------------------------------------------------------------
+ * "ZeRO and FSDP", "The idea, one stage at a time" (flatten into one vector,
+ * n_dp equal contiguous shards, rank r owns shard r); "ZeRO Optimizer, in
+ * depth", "Worked example" (reduce buckets of 5e8 elements by default).
+ *
+ * numel[n_tensors]: element counts in flattening order (tensors are laid end
+ *   to end, no gaps).  align >= 1; bucket_elems >= 1 (rounded up to a multiple
+ *   of align).  offsets_out (host, n_tensors entries, may be NULL) receives each
+ *   tensor's flat offset.  out (host) receives the layout.
+ * Errors: ZERO_EINVAL (n_dp < 1, align < 1, bucket_elems < 1, negative numel,
+ *   null out / numel), ZERO_ERANGE (sizes overflow).  Host-only; no CUDA call. */
+int zero_layout(const int64_t* numel, int32_t n_tensors, int32_t n_dp, int64_t align,
+                int64_t bucket_elems, int64_t* offsets_out, zero_layout_t* out);
+
+/* Bucket b covers the flat range [*begin, *end) = [b*bucket, min((b+1)*bucket, P)).
+ * ZERO_EINVAL unless 0 <= b < n_buckets.  Host-only. */
+int zero_bucket_range(const zero_layout_t* L, int64_t b, int64_t* begin, int64_t* end);
+
+/* Rank r owns [*begin, *end) = [r*S, (r+1)*S); *valid_end = min(max(N, begin), end)
+ * is where its real elements stop.  ZERO_EINVAL unless 0 <= r < n_dp.  Host-only. */
+int zero_shard_range(const zero_layout_t* L, int32_t rank, int64_t* begin, int64_t* end,
+                     int64_t* valid_end);
+
+/* ---- the fused step ------------------------------------------------------
+ * "ZeRO and FSDP", "The idea, one stage at a time" (stage 1: reduce-scatter so
+ * rank r receives the averaged gradient of shard r, update the fp32 master
+ * shard, cast to bf16, all-gather; stage 2: the same per gradient bucket as
+ * it becomes ready) and exercise "A sharded Adam step" (Adam with bias
+ * correction at step t); AdamW's decoupled weight decay per the optimizer
+ * blocks of "DeepSpeed ZeRO", "The configuration file".
+ *
+ * For every flat index i in [begin, end):
+ *   g      = (sum over r = 0..n_src-1 of src[r][i - src_base]) / divisor
+ *            (fp32, ranks in ascending order from +0.0f, one IEEE division)
+ *   m      = b1*m + (1-b1)*g;   v = b2*v + (1-b2)*g*g
+ *   w      = w - (lr*wd)*w;     w = w - lr*((m/bc1) / (sqrt(v/bc2) + eps))
+ *   out    = bf16 round-to-nearest-even of w
+ * with bc1 = 1 - b1^t, bc2 = 1 - b2^t evaluated in fp64 on the host and
+ * rounded to fp32, every other operation one IEEE fp32 rounding (no FMA).
+ *
+ * Indexing: rank_begin..rank_end-1 are the owners whose shards this call
+ *   updates; [begin, end) must lie inside [rank_begin*S, rank_end*S).
+ *   master/m/v point at rank_begin's shard; the state of flat index i is at
+ *   [i - rank_begin*S] (the owned shards of consecutive ranks are contiguous).
+ *   out_mode ZERO_OUT_FULL: out_bf16 is the full flat bf16 weight buffer of P
+ *   elements and receives [i] -- the all-gather of stages 1 and 2.
+ *   out_mode ZERO_OUT_SHARD: out_bf16 is laid out like master and receives
+ *   [i - rank_begin*S] -- the stage-3 owner updating its own bf16 shard.
+ *   src[r] (n_src of them, 1 <= n_src <= ZERO_MAX_SRC) is read at [i - src_base];
+ *   src_dtype ZERO_BF16 (per-rank bf16 gradients) or ZERO_F32 (accumulated
+ *   fp32 gradients).  src_base <= begin.  divisor > 0 and finite (n_dp for a
+ *   mean over ranks, n_dp*K after K accumulated micro-batches).
+ * Sources are read only; master, m, v and out are updated in place.
+ * Errors: ZERO_EINVAL (null, range outside the owned shards, bad mode/dtype,
+ *   hp->step < 1, non-finite hyper-parameter, divisor <= 0, pointer not device
+ *   memory), ZERO_ERANGE (n_src > ZERO_MAX_SRC), ZERO_EALIGN, ZERO_ECUDA. */
+int zero_reduce_scatter_adamw(const zero_layout_t* L,
+                              const void* const* src, int32_t n_src, int32_t src_dtype,
+                              int64_t src_base, float divisor,
+                              int32_t rank_begin, int32_t rank_end,
+                              int64_t begin, int64_t end,
+                              float* master, float* m, float* v,
+                              uint16_t* out_bf16, int32_t out_mode,
+                              const zero_adamw_t* hp, void* stream);
+
+/* ---- stage-3 gather ------------------------------------------------------
+ * "DeepSpeed ZeRO", "Stage 3 step by step" and "ZeRO and FSDP", "FSDP, ZeRO-3
+ * inside PyTorch": before a unit (layer) runs, its weights are all-gathered
+ * from the n_dp shards into one full buffer, used, then released.
+ *
+ * full_out[o*S + k] = shards[o][k] for o < unit->n_dp, k < unit->shard; full_out
+ * holds unit->padded_n bf16 elements.  shards is a host array of unit->n_dp
+ * device pointers, each to unit->shard bf16 elements.  Releasing the gathered
+ * buffer is the caller's: it simply reuses the buffer for another unit.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_gather_layer(const zero_layout_t* unit, const uint16_t* const* shards,
+                      uint16_t* full_out, void* stream);
+
+/* ---- gradient accumulation / stage-3 layer reduce-scatter ----------------
+ * "ZeRO and FSDP", "The idea, one stage at a time", paragraph on gradient
+ * accumulation: stage 1 adds each micro-batch's full local gradient into a full
+ * buffer and communicates once per step; stage 2 (and stage 3) must
+ * reduce-scatter after every micro-batch.  Also the stage-3 per-layer gradient
+ * reduce-scatter ("Stage 3 step by step", step 4).
+ *
+ * For every flat index i in [begin, end):
+ *   ZERO_ACC_LOCAL  (n_src == 1): x = src[0][i - src_base]
+ *   ZERO_ACC_REDUCE (n_src >= 1): x = sum over r of src[r][i - src_base]
+ *                                  (fp32, ascending r, from +0.0f)
+ *   dst[i - dst_base] = first ? x : dst[i - dst_base] + x
+ * The result is a sum; the mean's division happens in
+ * zero_reduce_scatter_adamw (divisor n_dp*K).  [begin, end) inside [0, P);
+ * src_base <= begin; dst_base <= begin.
+ * Errors: ZERO_EINVAL, ZERO_ERANGE, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_accumulate(const zero_layout_t* L, int32_t mode,
+                    const void* const* src, int32_t n_src, int32_t src_dtype, int64_t src_base,
+                    float* dst, int64_t dst_base, int64_t begin, int64_t end,
+                    int32_t first, void* stream);
+
+/* ---- status ---------------------------------------------------------------
+ * Synchronizes `stream` and returns ZERO_ECUDA if it (or an earlier launch on
+ * this thread) failed, else ZERO_OK.  The only call that blocks. */
+int zero_status_check(void* stream);
+
+/* Static string for a status code (never NULL). */
+const char* zero_strerror(int code);
+
+/* ---- accounting helpers (host-only) ---------------------------------------
+ * "ZeRO and FSDP", "Memory per GPU": model-state bytes per GPU with 2-byte
+ * weights and gradients and k_bytes of optimizer state per parameter:
+ * stage 0: 16N, 1: 4N + 12N/n_dp, 2: 2N + 14N/n_dp, 3: 16N/n_dp (for k = 12).
+ * "ZeRO and FSDP", "Communication volume": bytes each GPU sends per step under
+ * ring collectives with the exact (n_dp-1)/n_dp factor.
+ * ZERO_EINVAL for a stage outside 0..3, n_dp < 1, n < 0 or null out. */
+int zero_memory_bytes(double n, int32_t n_dp, int32_t stage, double k_bytes, double* out);
+int zero_comm_bytes(double n, int32_t n_dp, int32_t stage, double param_bytes,
+                    double grad_bytes, double* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_GB300_H */

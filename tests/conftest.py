@@ -26,3 +26,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def zlib():
+    """The built C-ABI library (compiled in-tree for sm_103a if stale)."""
+    from zero_sharded_mixed_gb300 import binding, build
+    build.build()
+    binding.load()
+    return binding
+
+
+@pytest.fixture(scope="session")
+def cuda_device():
+    import torch
+    torch.cuda.init()
+    return torch.device("cuda", 0)

@@ -1,0 +1,194 @@
+"""CPU tests of the C ABI: the library builds and loads, exports every function
+the header declares, its host-only calls agree with the oracle, and argument
+checks reject bad calls before any CUDA call is made (no kernel runs here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import formulas
+from zero_sharded_mixed_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zero_gb300.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(zero_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(zlib):
+    names = _declared()
+    assert {"zero_layout", "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate",
+            "zero_status_check", "zero_strerror"} <= set(names)
+    lib = ctypes.CDLL(zlib.lib_path)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_layout_matches_oracle(zlib):
+    rng = np.random.default_rng(0)
+    for _ in range(3000):
+        numels = rng.integers(0, 300, size=rng.integers(0, 5)).tolist()
+        n_dp = int(rng.integers(1, 17))
+        a = int(rng.choice([1, 2, 8, 64]))
+        B = int(rng.integers(1, 2000))
+        L, offs = zlib.zero_layout(numels, n_dp, align=a, bucket_elems=B, with_offsets=True)
+        ref = oracle.layout(numels, n_dp, align=a, bucket=B)
+        got = (L.n, L.shard, L.padded_n, L.bucket, L.n_buckets, L.n_dp, L.align)
+        assert got == (ref["n"], ref["shard"], ref["padded"], ref["bucket"], ref["n_buckets"], n_dp, a)
+        assert offs == ref["offsets"].tolist()
+
+
+def test_workload_layouts_match_oracle(zlib):
+    for numels, n_dp in [(inputs.gpt2xl_numels(), 8), (inputs.gpt2xl_numels(), 4),
+                         (inputs.llama7b_numels(), 8), ([1 << 20], 4)]:
+        L, offs = zlib.zero_layout(numels, n_dp, with_offsets=True)
+        ref = oracle.layout(numels, n_dp)
+        assert (L.n, L.shard, L.padded_n, L.n_buckets) == (ref["n"], ref["shard"], ref["padded"],
+                                                          ref["n_buckets"])
+        assert offs == ref["offsets"].tolist()
+    for unit in inputs.llama7b_units():
+        L = zlib.zero_layout(unit, 8)
+        ref = oracle.layout(unit, 8)
+        assert (L.shard, L.padded_n) == (ref["shard"], ref["padded"])
+
+
+@pytest.mark.parametrize("args", [
+    dict(n_dp=0), dict(align=0), dict(bucket_elems=0), dict(numels=[3, -1]),
+])
+def test_layout_errors(zlib, args):
+    kw = dict(numels=[10], n_dp=2, align=8, bucket_elems=8)
+    kw.update(args)
+    with pytest.raises(zlib.ZeroError) as e:
+        zlib.zero_layout(kw.pop("numels"), **kw)
+    assert e.value.code == zlib.ZERO_EINVAL
+    with pytest.raises(zlib.ZeroError) as e:
+        zlib.zero_layout([2 ** 61, 2 ** 61], 2)
+    assert e.value.code == zlib.ZERO_ERANGE
+
+
+def test_bucket_and_shard_ranges(zlib):
+    L = zlib.zero_layout([1000], 3, align=8, bucket_elems=100)
+    assert (L.shard, L.padded_n, L.bucket, L.n_buckets) == (336, 1008, 104, 10)
+    spans = [zlib.zero_bucket_range(L, b) for b in range(L.n_buckets)]
+    assert spans[0] == (0, 104) and spans[-1] == (936, 1008)
+    assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+    assert [zlib.zero_shard_range(L, r) for r in range(3)] == [(0, 336, 336), (336, 672, 672),
+                                                                (672, 1008, 1000)]
+    for bad in (-1, L.n_buckets):
+        with pytest.raises(zlib.ZeroError):
+            zlib.zero_bucket_range(L, bad)
+    with pytest.raises(zlib.ZeroError):
+        zlib.zero_shard_range(L, 3)
+    # a rank whose shard is all padding
+    L = zlib.zero_layout([9], 4, align=8)
+    assert zlib.zero_shard_range(L, 3) == (24, 32, 24)
+
+
+def test_memory_and_comm_helpers_match_oracle(zlib):
+    for N in (0, 1, 1000, 7e9, 7.5e9):
+        for n in (1, 2, 8, 64):
+            for s in range(4):
+                assert zlib.zero_memory_bytes(N, n, s) == pytest.approx(formulas.zero_memory(N, n, s),
+                                                                        rel=1e-12, abs=1e-9)
+                assert zlib.zero_comm_bytes(N, n, s, 2, 4) == pytest.approx(
+                    formulas.zero_comm_bytes(N, n, s, 2, 4), rel=1e-12, abs=1e-9)
+    for bad in (-1, 4):
+        with pytest.raises(zlib.ZeroError):
+            zlib.zero_memory_bytes(10, 2, bad)
+        with pytest.raises(zlib.ZeroError):
+            zlib.zero_comm_bytes(10, 2, bad)
+
+
+def test_strerror(zlib):
+    assert zlib.zero_strerror(0) == "ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert zlib.zero_strerror(code) and zlib.zero_strerror(code) != "unknown status code"
+    assert zlib.zero_strerror(42) == "unknown status code"
+
+
+# --------------------------------------------------------------------------
+# argument checks that return before any CUDA call (fake, aligned pointers)
+# --------------------------------------------------------------------------
+
+FAKE = 0x10000   # never dereferenced: every case below fails a pure argument check
+
+
+def _rs_call(zlib, **over):
+    L = zlib.zero_layout([4096], 4)
+    hp = zlib.ZeroAdamW.make(step=1)
+    a = dict(L=ctypes.byref(L), src=None, n_src=4, dtype=zlib.ZERO_BF16, src_base=0, divisor=4.0,
+             rb=0, re=4, begin=0, end=4096, w=FAKE, m=FAKE, v=FAKE, out=FAKE,
+             mode=zlib.ZERO_OUT_FULL, hp=ctypes.byref(hp), stream=None)
+    n_ptr = over.pop("n_ptrs", 4)
+    ptrs = over.pop("ptrs", [FAKE] * n_ptr)
+    a["src"] = (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+    if "hp_fields" in over:
+        for k, val in over.pop("hp_fields").items():
+            setattr(hp, k, val)
+    if "L_fields" in over:
+        for k, val in over.pop("L_fields").items():
+            setattr(L, k, val)
+    a.update(over)
+    return zlib.load().zero_reduce_scatter_adamw(
+        a["L"], a["src"], a["n_src"], a["dtype"], a["src_base"], a["divisor"], a["rb"], a["re"],
+        a["begin"], a["end"], a["w"], a["m"], a["v"], a["out"], a["mode"], a["hp"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(L=None), -1), (dict(hp=None), -1), (dict(w=None), -1), (dict(out=None), -1),
+    (dict(n_src=0), -1), (dict(n_src=65, n_ptrs=65), -3), (dict(dtype=7), -1), (dict(mode=2), -1),
+    (dict(rb=-1), -1), (dict(re=5), -1), (dict(rb=2, re=2), -1),
+    (dict(rb=1, re=2, begin=0, end=1024), -1),        # range outside the owned shards
+    (dict(begin=10, end=5), -1), (dict(end=4097), -1), (dict(src_base=8), -1),
+    (dict(divisor=0.0), -1), (dict(divisor=float("inf")), -1), (dict(divisor=-1.0), -1),
+    (dict(hp_fields=dict(step=0)), -1), (dict(hp_fields=dict(beta1=1.0)), -1),
+    (dict(hp_fields=dict(lr=float("nan"))), -1),
+    (dict(L_fields=dict(padded_n=4095)), -1),
+    (dict(ptrs=[FAKE, FAKE, 0, FAKE]), -1),
+    (dict(ptrs=[FAKE, FAKE + 1, FAKE, FAKE]), -2), (dict(w=FAKE + 2), -2), (dict(out=FAKE + 1), -2),
+    (dict(begin=100, end=100), 0),                    # empty range: nothing to do
+])
+def test_rs_adamw_argument_checks(zlib, over, code):
+    assert _rs_call(zlib, **over) == code
+
+
+def test_accumulate_and_gather_argument_checks(zlib):
+    lib = zlib.load()
+    L = zlib.zero_layout([4096], 4)
+    src = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    acc = lib.zero_accumulate
+    Lp = ctypes.byref(L)
+    assert acc(Lp, 9, src, 4, 0, 0, FAKE, 0, 0, 4096, 1, None) == -1        # mode
+    assert acc(Lp, 0, src, 2, 0, 0, FAKE, 0, 0, 4096, 1, None) == -1        # LOCAL takes 1 source
+    assert acc(Lp, 1, src, 0, 0, 0, FAKE, 0, 0, 4096, 1, None) == -1
+    assert acc(Lp, 1, src, 65, 0, 0, FAKE, 0, 0, 4096, 1, None) == -3
+    assert acc(Lp, 1, src, 4, 3, 0, FAKE, 0, 0, 4096, 1, None) == -1        # dtype
+    assert acc(Lp, 1, src, 4, 0, 0, FAKE, 0, 0, 4097, 1, None) == -1        # past P
+    assert acc(Lp, 1, src, 4, 0, 0, FAKE, 8, 0, 4096, 1, None) == -1        # dst_base > begin
+    assert acc(Lp, 1, src, 4, 0, 0, FAKE + 2, 0, 0, 4096, 1, None) == -2    # dst alignment
+    assert acc(Lp, 1, src, 4, 0, 0, None, 0, 0, 4096, 1, None) == -1
+    assert acc(Lp, 1, src, 4, 0, 0, FAKE, 0, 64, 64, 1, None) == 0          # empty
+    g = lib.zero_gather_layer
+    assert g(None, src, FAKE, None) == -1
+    assert g(Lp, src, None, None) == -1
+    bad = (ctypes.c_void_p * 4)(FAKE, 0, FAKE, FAKE)
+    assert g(Lp, bad, FAKE, None) == -1
+    odd = (ctypes.c_void_p * 4)(FAKE, FAKE + 1, FAKE, FAKE)
+    assert g(Lp, odd, FAKE, None) == -2
+    empty = zlib.zero_layout([0], 4)
+    assert g(ctypes.byref(empty), src, FAKE, None) == 0
+
+
+def test_missing_library_fails_loudly(zlib, monkeypatch, tmp_path):
+    from zero_sharded_mixed_gb300 import binding
+    monkeypatch.setattr(binding, "lib_path", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(ImportError):
+        binding.load()

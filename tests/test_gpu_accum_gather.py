@@ -1,0 +1,180 @@
+"""Parity of the accumulation kernels, the stage-3 gather and the ZeRO-3 per-unit
+sequence against the oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from zero_sharded_mixed_gb300 import inputs
+from zero_sharded_mixed_gb300 import step as zstep
+
+pytestmark = pytest.mark.gpu
+
+HP = oracle.AdamW()
+
+
+def _hp(zb, t):
+    return zb.ZeroAdamW.make(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay, t)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("start", [0, 3])
+def test_accumulate_local(zlib, cuda_device, dtype, start):
+    zb = zlib
+    N = 20_011
+    L = zb.zero_layout([N], 1, align=1)
+    rng = np.random.default_rng(11)
+    acc = torch.zeros(N, device="cuda")
+    ref = np.zeros(N, np.float32)
+    for k in range(3):
+        x = (rng.standard_normal(N) * 1e-3).astype(np.float32)
+        if dtype == "bf16":
+            xb = oracle.cast_bf16(x)
+            src, code = inputs.from_bf16_bits(xb, "cuda"), zb.ZERO_BF16
+            xr = oracle.bf16_to_f32(xb)
+        else:
+            src, code, xr = torch.from_numpy(x).cuda(), zb.ZERO_F32, x
+        zb.zero_accumulate(L, zb.ZERO_ACC_LOCAL, [src], code, 0, acc, 0, start, N, k == 0)
+        ref[start:] = xr[start:] if k == 0 else ref[start:] + xr[start:]
+    torch.cuda.synchronize()
+    parity.assert_bit_exact_f32(acc[start:], ref[start:])
+    assert not parity.f32(acc)[:start].any()
+
+
+@pytest.mark.parametrize("n_src", [1, 2, 3, 4, 8, 16, 64])
+def test_accumulate_reduce(zlib, cuda_device, n_src):
+    zb = zlib
+    N = 8 * 2500 + 5
+    L = zb.zero_layout([N], 1)
+    g = inputs.grads_bf16(n_src, N, L.padded_n, seed=n_src, step=0)
+    srcs = [g[r].cuda() for r in range(n_src)]
+    A = torch.zeros(L.padded_n, device="cuda")
+    ref = None
+    for k in range(2):
+        zb.zero_accumulate(L, zb.ZERO_ACC_REDUCE, srcs, zb.ZERO_BF16, 0, A, 0, 0, L.padded_n, k == 0)
+        ref = oracle.accumulate_reduce(ref, parity.bits(g), first=(k == 0))
+    torch.cuda.synchronize()
+    parity.assert_bit_exact_f32(A, ref)
+
+
+def test_accumulation_paths_small(zlib, cuda_device):
+    """Gradient accumulation in small: n_dp = 4, K = 4 micro-batches; ZeRO-1
+    (local fp32 accumulation, one reduce-scatter) and ZeRO-2 (reduce-scatter per
+    micro-batch), each against its own oracle order, then against each other."""
+    zb = zlib
+    N, n_dp, K = 30_011, 4, 4
+    L = zb.zero_layout([N], n_dp, bucket_elems=4096)
+    P = L.padded_n
+    w0 = inputs.master_weights(N, P, seed=4)
+    s1 = [w0.cuda(), torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")]
+    s2 = [w0.cuda(), torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")]
+    o1 = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    o2 = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    acc = [torch.empty(P, device="cuda") for _ in range(n_dp)]
+    A = torch.empty(P, device="cuda")
+    micro = [inputs.grads_bf16(n_dp, N, P, seed=4, step=1, micro=k) for k in range(K)]
+    for k, g in enumerate(micro):
+        gd = [g[r].cuda() for r in range(n_dp)]
+        zstep.zero1_accumulate_micro(L, gd, acc, first=(k == 0))
+        zstep.zero2_accumulate_micro(L, gd, A, first=(k == 0))
+    zstep.zero1_finish(L, acc, K, *s1, o1, _hp(zb, 1))
+    zstep.zero2_finish(L, A, K, *s2, o2, _hp(zb, 1))
+    torch.cuda.synchronize()
+    # oracle, ZeRO-1 order
+    acc_ref = [None] * n_dp
+    for k, g in enumerate(micro):
+        gb = parity.bits(g)
+        for r in range(n_dp):
+            acc_ref[r] = oracle.accumulate_local(acc_ref[r], gb[r], first=(k == 0))
+    for r in range(n_dp):
+        parity.assert_bit_exact_f32(acc[r], acc_ref[r])
+    zero = np.zeros(P, np.float32)
+    out1, *st1 = oracle.rs_adamw_reference(np.stack(acc_ref), n_dp * K, parity.f32(w0), zero, zero, HP, 1)
+    parity.assert_state(s1, st1, what="zero1 ")
+    assert np.array_equal(parity.bits(o1), out1)
+    # oracle, ZeRO-2 order
+    A_ref = None
+    for k, g in enumerate(micro):
+        A_ref = oracle.accumulate_reduce(A_ref, parity.bits(g), first=(k == 0))
+    parity.assert_bit_exact_f32(A, A_ref)
+    out2, *st2 = oracle.rs_adamw_reference(A_ref[None, :], n_dp * K, parity.f32(w0), zero, zero, HP, 1)
+    parity.assert_state(s2, st2, what="zero2 ")
+    assert np.array_equal(parity.bits(o2), out2)
+    # the two orders: mean gradients agree within the fp32 summation bound
+    x = np.stack([oracle.bf16_to_f32(parity.bits(g)).astype(np.float64) for g in micro])
+    bound = (n_dp * K * 2.0 ** -24 / (1 - n_dp * K * 2.0 ** -24)) * np.abs(x).sum(axis=(0, 1))
+    assert np.all(np.abs(np.stack(acc_ref).astype(np.float64).sum(0) - A_ref) <= 2 * bound + 1e-45)
+
+
+@pytest.mark.parametrize("n_dp,S,align", [(1, 8, 8), (3, 5, 1), (8, 4096, 8), (7, 1001, 1), (65, 24, 8)])
+def test_gather_is_concatenation(zlib, cuda_device, n_dp, S, align):
+    zb = zlib
+    L = zb.zero_layout([n_dp * S], n_dp, align=align)
+    assert L.shard == S or align > 1
+    rng = np.random.default_rng(n_dp)
+    shards_np = rng.integers(0, 1 << 16, size=(n_dp, L.shard)).astype(np.uint16)
+    shards = [inputs.from_bf16_bits(shards_np[o], "cuda") for o in range(n_dp)]
+    full = torch.full((L.padded_n + 16,), 777, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    zb.zero_gather_layer(L, shards, full[: L.padded_n])
+    torch.cuda.synchronize()
+    fb = parity.bits(full)
+    assert np.array_equal(fb[: L.padded_n], np.concatenate(list(shards_np)))
+    assert np.all(fb[L.padded_n:] == 777)
+
+
+def test_zero3_units(zlib, cuda_device):
+    """The stage-3 sequence over ragged units (numel 1, 7, 4097, 33031 and a
+    4-tensor block) at n_dp = 7: gather for forward, release, gather for
+    backward, reduce-scatter the unit gradient, update the owned shards in bf16;
+    at most two units resident; every gathered buffer is the concatenation of
+    the shards; the reduce-scattered pieces equal the data-parallel gradient."""
+    zb = zlib
+    n_dp = 7
+    units_numels = [[1], [7], [4097], [33_031], [1000, 24, 3, 5000]]
+    units = []
+    for i, numels in enumerate(units_numels):
+        L = zb.zero_layout(numels, n_dp)
+        P = L.padded_n
+        w = inputs.master_weights(L.n, P, seed=100 + i).cuda()
+        shards = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+        shards.copy_(w)       # the initial bf16 weights: torch's cast (inputs only)
+        units.append(zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w,
+                                     torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")))
+    cap = max(u.layout.padded_n for u in units)
+    ring = zstep.GatherRing(cap)
+    ref_state = [[parity.f32(u.master), np.zeros(u.layout.padded_n, np.float32),
+                  np.zeros(u.layout.padded_n, np.float32)] for u in units]
+    ref_shards = [parity.bits(u.shards).copy() for u in units]
+    # forward: gather each unit, "compute", release; the next unit's gather may overlap
+    prev = None
+    for i, u in enumerate(units):
+        buf = zstep.zero3_gather(u, ring, ("fwd", i))
+        torch.cuda.synchronize()
+        assert np.array_equal(parity.bits(buf), ref_shards[i].reshape(-1))
+        if prev is not None:
+            ring.release(prev)
+        prev = ("fwd", i)
+        assert ring.resident <= 2
+    ring.release(prev)
+    # backward, in reverse: gather again, reduce-scatter the unit gradient, update
+    for i in reversed(range(len(units))):
+        u = units[i]
+        L = u.layout
+        buf = zstep.zero3_gather(u, ring, ("bwd", i))
+        torch.cuda.synchronize()
+        assert np.array_equal(parity.bits(buf), ref_shards[i].reshape(-1))
+        g = inputs.grads_bf16(n_dp, L.n, L.padded_n, seed=200 + i, step=1)
+        A = torch.empty(L.padded_n, device="cuda")
+        zstep.zero3_layer_reduce_scatter(u, [g[r].cuda() for r in range(n_dp)], A)
+        ring.release(("bwd", i))
+        zstep.zero3_update(u, A, _hp(zb, 1))
+        torch.cuda.synchronize()
+        A_ref = oracle.accumulate_reduce(None, parity.bits(g), first=True)
+        parity.assert_bit_exact_f32(A, A_ref)
+        # each owner's piece of the mean is the data-parallel mean gradient's piece
+        np.testing.assert_array_equal(A_ref / np.float32(n_dp), oracle.reduce_mean(parity.bits(g), n_dp))
+        out_ref, *st = oracle.rs_adamw_reference(A_ref[None, :], n_dp, *ref_state[i], HP, 1)
+        parity.assert_state([u.master, u.m, u.v], st, what=f"unit {i} ")
+        assert np.array_equal(parity.bits(u.shards).reshape(-1), out_ref)
+    assert ring.peak <= 2 and ring.resident == 0

@@ -1,0 +1,234 @@
+"""Thin ctypes binding for libzero_gb300.so (names as in include/zero_gb300.h).
+
+Argument marshalling only: torch tensors are checked (device, dtype,
+contiguity, extent) and turned into pointers; every step of the computation
+runs in the library's CUDA kernels.  There is no CPU fallback: if the library
+is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_PKG, "libzero_gb300.so")
+
+ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ERANGE, ZERO_ECUDA, ZERO_ETIMEOUT = 0, -1, -2, -3, -4, -5
+ZERO_BF16, ZERO_F32 = 0, 1
+ZERO_OUT_FULL, ZERO_OUT_SHARD = 0, 1
+ZERO_ACC_LOCAL, ZERO_ACC_REDUCE = 0, 1
+ZERO_MAX_SRC = 64
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {zero_strerror(code)} ({code})")
+
+
+class ZeroLayout(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("padded_n", ctypes.c_int64), ("shard", ctypes.c_int64),
+                ("align", ctypes.c_int64), ("bucket", ctypes.c_int64), ("n_buckets", ctypes.c_int64),
+                ("n_dp", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+    def __repr__(self):
+        return f"ZeroLayout({self.as_dict()})"
+
+
+class ZeroAdamW(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("reserved", ctypes.c_int32), ("step", ctypes.c_int64)]
+
+    @classmethod
+    def make(cls, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1):
+        return cls(lr, beta1, beta2, eps, weight_decay, 0, step)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(lib_path):
+            raise ImportError(
+                f"{lib_path} is missing: build it with `python -m zero_sharded_mixed_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(lib_path)
+        i32, i64, f32, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+        P = ctypes.POINTER
+        lib.zero_layout.argtypes = [P(i64), i32, i32, i64, i64, P(i64), P(ZeroLayout)]
+        lib.zero_bucket_range.argtypes = [P(ZeroLayout), i64, P(i64), P(i64)]
+        lib.zero_shard_range.argtypes = [P(ZeroLayout), i32, P(i64), P(i64), P(i64)]
+        lib.zero_reduce_scatter_adamw.argtypes = [
+            P(ZeroLayout), P(p), i32, i32, i64, f32, i32, i32, i64, i64,
+            p, p, p, p, i32, P(ZeroAdamW), p]
+        lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
+        lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
+                                        i32, p]
+        lib.zero_status_check.argtypes = [p]
+        lib.zero_strerror.argtypes = [ctypes.c_int]
+        lib.zero_strerror.restype = ctypes.c_char_p
+        lib.zero_memory_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
+                                          P(ctypes.c_double)]
+        lib.zero_comm_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
+                                        ctypes.c_double, P(ctypes.c_double)]
+        for name in ("zero_layout", "zero_bucket_range", "zero_shard_range",
+                     "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate",
+                     "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def zero_strerror(code: int) -> str:
+    return load().zero_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != ZERO_OK:
+        raise ZeroError(rc, where)
+
+
+# --------------------------------------------------------------------------
+# host-only calls
+# --------------------------------------------------------------------------
+
+def zero_layout(numels: Sequence[int], n_dp: int, align: int = 8,
+                bucket_elems: int = 500_000_000, with_offsets: bool = False):
+    arr = (ctypes.c_int64 * max(1, len(numels)))(*[int(x) for x in numels])
+    offs = (ctypes.c_int64 * max(1, len(numels)))()
+    L = ZeroLayout()
+    _check(load().zero_layout(arr, len(numels), int(n_dp), int(align), int(bucket_elems), offs,
+                              ctypes.byref(L)), "zero_layout")
+    if with_offsets:
+        return L, [offs[i] for i in range(len(numels))]
+    return L
+
+
+def zero_bucket_range(L: ZeroLayout, b: int):
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().zero_bucket_range(ctypes.byref(L), int(b), ctypes.byref(lo), ctypes.byref(hi)),
+           "zero_bucket_range")
+    return lo.value, hi.value
+
+
+def zero_shard_range(L: ZeroLayout, rank: int):
+    lo, hi, valid = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(load().zero_shard_range(ctypes.byref(L), int(rank), ctypes.byref(lo), ctypes.byref(hi),
+                                   ctypes.byref(valid)), "zero_shard_range")
+    return lo.value, hi.value, valid.value
+
+
+def zero_memory_bytes(n, n_dp, stage, k_bytes=12.0) -> float:
+    out = ctypes.c_double()
+    _check(load().zero_memory_bytes(float(n), int(n_dp), int(stage), float(k_bytes),
+                                    ctypes.byref(out)), "zero_memory_bytes")
+    return out.value
+
+
+def zero_comm_bytes(n, n_dp, stage, param_bytes=2.0, grad_bytes=2.0) -> float:
+    out = ctypes.c_double()
+    _check(load().zero_comm_bytes(float(n), int(n_dp), int(stage), float(param_bytes),
+                                  float(grad_bytes), ctypes.byref(out)), "zero_comm_bytes")
+    return out.value
+
+
+# --------------------------------------------------------------------------
+# device calls
+# --------------------------------------------------------------------------
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _tensor(t: torch.Tensor, name: str, dtype, min_numel: int) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} has {t.numel()} elements, the call reads or writes {min_numel}")
+    return t.data_ptr()
+
+
+_SRC_DT = {ZERO_BF16: torch.bfloat16, ZERO_F32: torch.float32}
+
+
+def _src_array(srcs, dtype, min_numel):
+    if len(srcs) == 0:
+        raise ValueError("need at least one source")
+    ptrs = [_tensor(s, f"src[{i}]", dtype, min_numel) for i, s in enumerate(srcs)]
+    return (ctypes.c_void_p * len(ptrs))(*ptrs), len(ptrs)
+
+
+def zero_reduce_scatter_adamw(L: ZeroLayout, srcs, src_dtype: int, src_base: int, divisor: float,
+                              rank_begin: int, rank_end: int, begin: int, end: int,
+                              master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                              out: torch.Tensor, out_mode: int, hp: ZeroAdamW, stream=None):
+    """Fused mean reduce-scatter + AdamW + bf16 cast + gather write over [begin, end)."""
+    if end <= begin:
+        src_need = state_need = out_need = 0
+    else:
+        src_need = end - src_base
+        state_need = end - rank_begin * L.shard
+        out_need = end if out_mode == ZERO_OUT_FULL else state_need
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    rc = load().zero_reduce_scatter_adamw(
+        ctypes.byref(L), arr, n, int(src_dtype), int(src_base), float(divisor),
+        int(rank_begin), int(rank_end), int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(out, "out", torch.bfloat16, out_need),
+        int(out_mode), ctypes.byref(hp), _stream_ptr(stream))
+    _check(rc, "zero_reduce_scatter_adamw")
+
+
+def zero_gather_layer(unit: ZeroLayout, shards, full_out: torch.Tensor, stream=None):
+    """Concatenate unit.n_dp bf16 shards (unit.shard elements each) into full_out."""
+    if len(shards) != unit.n_dp:
+        raise ValueError(f"need {unit.n_dp} shards, got {len(shards)}")
+    ptrs = [_tensor(s, f"shards[{i}]", torch.bfloat16, unit.shard) for i, s in enumerate(shards)]
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+    rc = load().zero_gather_layer(ctypes.byref(unit), arr,
+                                  _tensor(full_out, "full_out", torch.bfloat16, unit.padded_n),
+                                  _stream_ptr(stream))
+    _check(rc, "zero_gather_layer")
+
+
+def zero_accumulate(L: ZeroLayout, mode: int, srcs, src_dtype: int, src_base: int,
+                    dst: torch.Tensor, dst_base: int, begin: int, end: int, first: bool,
+                    stream=None):
+    """dst[i - dst_base] (+)= src[0] (LOCAL) or sum_r src[r] (REDUCE) over [begin, end)."""
+    src_need = max(0, end - src_base) if end > begin else 0
+    dst_need = max(0, end - dst_base) if end > begin else 0
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    rc = load().zero_accumulate(ctypes.byref(L), int(mode), arr, n, int(src_dtype), int(src_base),
+                                _tensor(dst, "dst", torch.float32, dst_need), int(dst_base),
+                                int(begin), int(end), int(bool(first)), _stream_ptr(stream))
+    _check(rc, "zero_accumulate")
+
+
+def zero_status_check(stream=None):
+    _check(load().zero_status_check(_stream_ptr(stream)), "zero_status_check")

@@ -1,0 +1,70 @@
+// Shared device helpers and host-side argument checks for the sm_103a kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "zero_gb300.h"
+
+namespace zgb {
+
+constexpr int kThreads = 256;   // threads per CTA for every streaming kernel
+
+// ----------------------------------------------------------------- device
+
+// bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 bits.
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+__device__ __forceinline__ float bf16_one(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+
+// Two fp32 -> packed bf16x2, round to nearest even (hardware cvt.rn);
+// `lo` lands in bits 0..15 (the lower address), `hi` in bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+    return (uint16_t)(pack_bf16x2(x, 0.0f) & 0xffffu);
+}
+
+// Streaming (evict-first) 128-bit loads and stores: every byte of this path is
+// touched once per launch, so nothing is worth keeping in L1 or L2.
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float4 ld_stream_f4(const void* p) {
+    return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+}
+__device__ __forceinline__ void st_stream_f4(void* p, float4 v) {
+    __stcs(reinterpret_cast<float4*>(p), v);
+}
+
+// ----------------------------------------------------------------- host
+
+// 0 if p is device (or managed) memory of the current device, else ZERO_EINVAL.
+int check_device_ptr(const void* p);
+// ZERO_EALIGN unless p is a multiple of `bytes`.
+inline int check_aligned(const void* p, int bytes) {
+    return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)bytes) ? ZERO_EALIGN : ZERO_OK;
+}
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// SM count of the current device (cached per device).
+int sm_count();
+// CTAs of `threads` each that fit on one SM for `kernel` (cached by the caller).
+int ctas_per_sm(const void* kernel, int threads, size_t smem);
+// ZERO_ECUDA if the last launch on this thread failed.
+int launch_status();
+// Grid for a grid-stride loop over `work` items with `per_cta` items per CTA
+// pass, capped at `resident` CTAs (so every CTA is resident at once).
+inline unsigned grid_for(int64_t work, int64_t per_cta, int64_t resident) {
+    int64_t g = (work + per_cta - 1) / per_cta;
+    if (g > resident) g = resident;
+    if (g < 1) g = 1;
+    return (unsigned)g;
+}
+
+}  // namespace zgb

@@ -1,0 +1,64 @@
+// Host-side runtime support shared by the kernels: pointer checks, device
+// properties, launch status, and zero_status_check.
+#include <atomic>
+
+#include "zero_common.cuh"
+
+namespace zgb {
+
+int check_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();   // clear the sticky-free error so later launches are not blamed
+        return ZERO_EINVAL;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return ZERO_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || a.device != dev) return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev >= kMaxDevices) {
+        int n = 1;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+int ctas_per_sm(const void* kernel, int threads, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    return n;
+}
+
+int launch_status() {
+    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+}  // namespace zgb
+
+extern "C" int zero_status_check(void* stream) {
+    const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    const cudaError_t last = cudaGetLastError();
+    return (e == cudaSuccess && last == cudaSuccess) ? ZERO_OK : ZERO_ECUDA;
+}

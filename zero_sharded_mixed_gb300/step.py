@@ -1,0 +1,160 @@
+"""Host-side orchestration of the C-ABI calls: the bucket loop of a ZeRO-1/2
+step, the two gradient-accumulation orders, and the ZeRO-3 per-unit
+gather / release / reduce-scatter / update sequence with a two-slot ring of
+gathered buffers.  No arithmetic happens here; every element is touched only
+by the library's kernels.
+
+Buffer conventions (simulated ranks in one GPU):
+* ``grads``: n_dp bf16 tensors, rank r's full local gradient of P elements.
+* ``master``, ``m``, ``v``: fp32 tensors holding the owned shards of ranks
+  ``rank_begin..rank_end-1`` back to back (all ranks: P elements).
+* ``out``: the full flat bf16 weight buffer (P elements).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import binding as zb
+
+
+def bucket_ranges(L: zb.ZeroLayout, lo: int = 0, hi: int | None = None):
+    """The non-empty intersections of [lo, hi) with the layout's buckets."""
+    hi = L.padded_n if hi is None else hi
+    out = []
+    for b in range(L.n_buckets):
+        b0, b1 = zb.zero_bucket_range(L, b)
+        s, e = max(b0, lo), min(b1, hi)
+        if s < e:
+            out.append((s, e))
+    return out
+
+
+def zero12_step(L, grads, master, m, v, out, hp, rank_begin=0, rank_end=None, stream=None,
+                grad_base=0, divisor=None):
+    """One ZeRO-1/2 step for the owners rank_begin..rank_end-1, bucket by bucket
+    ("ZeRO and FSDP": stage 2 reduce-scatters each bucket as it becomes ready;
+    stage 1 once at the end -- the arithmetic is the same)."""
+    rank_end = L.n_dp if rank_end is None else rank_end
+    lo, hi = rank_begin * L.shard, rank_end * L.shard
+    div = float(L.n_dp) if divisor is None else float(divisor)
+    for s, e in bucket_ranges(L, lo, hi):
+        zb.zero_reduce_scatter_adamw(L, grads, zb.ZERO_BF16, grad_base, div, rank_begin, rank_end,
+                                     s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
+
+
+# --------------------------------------------------------------------------
+# gradient accumulation ("ZeRO and FSDP", paragraph on accumulation)
+# --------------------------------------------------------------------------
+
+def zero1_accumulate_micro(L, grads, acc, first: bool, stream=None):
+    """Stage 1: every rank adds its full local micro-batch gradient into its own
+    full fp32 buffer acc[r]; nothing is communicated."""
+    for r in range(L.n_dp):
+        zb.zero_accumulate(L, zb.ZERO_ACC_LOCAL, [grads[r]], zb.ZERO_BF16, 0, acc[r], 0,
+                           0, L.padded_n, first, stream)
+
+
+def zero1_finish(L, acc, n_micro, master, m, v, out, hp, stream=None):
+    """Stage 1 after K micro-batches: one reduce-scatter (mean over n_dp*K) of
+    the fp32 buffers fused with the update, bucket by bucket."""
+    for s, e in bucket_ranges(L):
+        zb.zero_reduce_scatter_adamw(L, acc, zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
+                                     s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
+
+
+def zero2_accumulate_micro(L, grads, A, first: bool, stream=None):
+    """Stage 2: after every micro-batch, each bucket is reduce-scattered into the
+    owners' fp32 shard buffer A (all owners back to back, P elements)."""
+    for s, e in bucket_ranges(L):
+        zb.zero_accumulate(L, zb.ZERO_ACC_REDUCE, grads, zb.ZERO_BF16, 0, A, 0, s, e, first,
+                           stream)
+
+
+def zero2_finish(L, A, n_micro, master, m, v, out, hp, stream=None):
+    for s, e in bucket_ranges(L):
+        zb.zero_reduce_scatter_adamw(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
+                                     s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
+
+
+# --------------------------------------------------------------------------
+# ZeRO-3 ("DeepSpeed ZeRO", "Stage 3 step by step"; "ZeRO and FSDP", "FSDP,
+# ZeRO-3 inside PyTorch": per-unit flat buffers, at most two gathered at once)
+# --------------------------------------------------------------------------
+
+@dataclass
+class GatherRing:
+    """Two gathered-unit buffers reused in turn.  ``acquire`` hands out a slot
+    for a unit; ``release`` returns it.  ``peak`` counts the most units that
+    were ever resident at once."""
+    capacity: int
+    device: str = "cuda"
+    slots: int = 2
+    buffers: list = field(default_factory=list)
+    owner: list = field(default_factory=list)
+    peak: int = 0
+
+    def __post_init__(self):
+        self.buffers = [torch.empty(self.capacity, dtype=torch.bfloat16, device=self.device)
+                        for _ in range(self.slots)]
+        self.owner = [None] * self.slots
+
+    def acquire(self, unit_id, numel: int) -> torch.Tensor:
+        if numel > self.capacity:
+            raise ValueError(f"unit of {numel} elements exceeds the ring's {self.capacity}")
+        for i, o in enumerate(self.owner):
+            if o is None:
+                self.owner[i] = unit_id
+                self.peak = max(self.peak, sum(x is not None for x in self.owner))
+                return self.buffers[i][:numel]
+        raise RuntimeError("both gathered-unit slots are in use: release one first")
+
+    def release(self, unit_id):
+        for i, o in enumerate(self.owner):
+            if o == unit_id:
+                self.owner[i] = None
+                return
+        raise KeyError(unit_id)
+
+    @property
+    def resident(self) -> int:
+        return sum(x is not None for x in self.owner)
+
+
+@dataclass
+class Zero3Unit:
+    """One unit's sharded state: n_dp bf16 shards (one [n_dp, S] tensor whose row
+    o is rank o's shard) and the owners' fp32 master / m / v (P elements)."""
+    layout: zb.ZeroLayout
+    shards: torch.Tensor
+    master: torch.Tensor
+    m: torch.Tensor
+    v: torch.Tensor
+
+    def shard_list(self):
+        return [self.shards[o] for o in range(self.layout.n_dp)]
+
+
+def zero3_gather(unit: Zero3Unit, ring: GatherRing, unit_id, stream=None) -> torch.Tensor:
+    buf = ring.acquire(unit_id, unit.layout.padded_n)
+    zb.zero_gather_layer(unit.layout, unit.shard_list(), buf, stream)
+    return buf
+
+
+def zero3_layer_reduce_scatter(unit: Zero3Unit, layer_grads, A: torch.Tensor, first: bool = True,
+                               stream=None):
+    """Each owner receives the sum over ranks of its slice of the unit's
+    gradient, in fp32 (the mean's division is applied by the update)."""
+    L = unit.layout
+    zb.zero_accumulate(L, zb.ZERO_ACC_REDUCE, layer_grads, zb.ZERO_BF16, 0, A, 0, 0, L.padded_n,
+                       first, stream)
+
+
+def zero3_update(unit: Zero3Unit, A: torch.Tensor, hp, n_micro: int = 1, stream=None):
+    """Every owner updates its shard and writes bf16 into its own shard only
+    (no final all-gather at stage 3)."""
+    L = unit.layout
+    zb.zero_reduce_scatter_adamw(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
+                                 0, L.padded_n, unit.master, unit.m, unit.v,
+                                 unit.shards.view(-1), zb.ZERO_OUT_SHARD, hp, stream)
