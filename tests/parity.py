@@ -55,7 +55,8 @@ def assert_f32_close(got, ref, rtol=RTOL, atol=ATOL, what="fp32"):
     assert g.shape == r.shape, (what, g.shape, r.shape)
     gn, rn = np.isnan(g), np.isnan(r)
     assert np.array_equal(gn, rn), f"{what}: NaN positions differ"
-    ok = np.abs(g[~gn].astype(np.float64) - r[~rn]) <= atol + rtol * np.abs(r[~rn].astype(np.float64))
+    with np.errstate(invalid="ignore"):    # inf - inf: equal infinities are accepted below
+        ok = np.abs(g[~gn].astype(np.float64) - r[~rn]) <= atol + rtol * np.abs(r[~rn].astype(np.float64))
     ok |= (g[~gn] == r[~rn])   # equal infinities
     assert ok.all(), (f"{what}: {int((~ok).sum())} of {ok.size} elements outside "
                       f"{rtol} rel + {atol} abs")
