@@ -1,22 +1,29 @@
 #!/usr/bin/env python
-"""Benchmark of the fused ZeRO-2 step: mean reduce-scatter of n_dp bf16 gradient
-buffers + fp32 AdamW + bf16 cast + gather write, on one GB300 per process.
+"""Benchmark of the ZeRO step on one GB300 per process: the fused mean
+reduce-scatter of n_dp bf16 gradient buffers + fp32 AdamW + bf16 cast + gather
+write, plus the accumulation and ZeRO-3 paths.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step is one pass of the whole path over the workload: the bucket loop of
-zero_reduce_scatter_adamw launches over every owned shard.  Default workload:
-GPT-2-XL shapes (N = 1,557,611,200 parameters, 48 blocks, d 1600, ffn 6400,
-vocab 50257) flattened for n_dp = 8 simulated ranks, 5e8-element buckets.  The
-Llama-7B single-shard workload (S = 842,301,952, 8 gradient slices with 1 %
-outliers x100) is measured in the same run and reported under "workloads".
+One step is one pass of the path over the workload.  The headline workload
+(the JSON line's value) is GPT-2-XL shapes (N = 1,557,611,200 parameters, 48
+blocks, d 1600, ffn 6400, vocab 50257) flattened for n_dp = 8 simulated ranks
+with 5e8-element buckets, every owned shard updated each step.  Measured in the
+same run and reported under "workloads", with fewer steps:
+  llama7b-shard  one owned shard of Llama-7B shapes (S = 842,301,952), 8 slices
+                 with 1 % outliers x100;
+  accum-zero1/2  gradient accumulation, GPT-2-XL shapes, n_dp = 4, 4 micro-batches,
+                 in the stage-1 and stage-2 orders;
+  zero3          the per-unit gather / reduce-scatter / update path over the 34
+                 Llama-7B units at n_dp = 8.
+Every launch is timed with CUDA events on its stream; `roofline` uses the
+dominant kernel's algorithmic bytes per launch over its average launch time.
 
-Printed: one JSON line (rank 0).  `value` = parameters updated per second over
-all ranks (each rank runs its own replica: the simulated ranks live in one
-GPU's memory, nothing is exchanged between GPUs, so N GPUs are N independent
-replicas -> weak scaling).  Inputs are larger than L2 (tens of GB), so no L2
-flush is needed between steps.  --impl reference times the CPU oracle on a
-bounded sample of the same workload instead.
+`value` = parameters updated per second over all ranks.  The simulated ranks
+live in one GPU's memory and nothing is exchanged between GPUs, so N GPUs run
+N independent replicas (weak scaling).  Inputs are tens of GB, larger than L2,
+so no L2 flush is needed between steps.  --impl reference times the CPU oracle
+on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -50,7 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["gpt2xl", "llama7b-shard", "probe"], default="gpt2xl",
+    ap.add_argument("--workload", choices=["gpt2xl", "llama7b-shard", "probe", "accum-zero1",
+                                           "accum-zero2", "zero3"], default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
     ap.add_argument("--no-e2e", action="store_true")
@@ -81,6 +89,12 @@ def dist_init(world, local):
 def barrier(dist):
     if dist is not None:
         dist.barrier()
+
+
+def replica_value(elems_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job parameters updated per second: every rank updates its own
+    replica's elements; the slowest rank's step time counts."""
+    return elems_per_rank * world / (ms_per_step / 1e3)
 
 
 def max_over_ranks(dist, x: float, device) -> float:
@@ -193,98 +207,289 @@ def _traffic_per_elem(n_src):
         return None
 
 
+class Op:
+    """One timed launch of a step: kernel kind, algorithmic bytes, the call."""
+    __slots__ = ("kind", "bytes", "fn")
+
+    def __init__(self, kind, nbytes, fn):
+        self.kind, self.bytes, self.fn = kind, nbytes, fn
+
+
 class Workload:
-    """Device buffers and the step of one configuration."""
+    """Device buffers and the step (a list of Ops) of one configuration."""
+
+    n_src = 8
+    kernel_label = "zgb::rs_adamw_vec_kernel<8,true>"
+
+    def __init__(self, device):
+        from zero_sharded_mixed_gb300 import binding as zb
+        self.zb = zb
+        self.device = device
+
+    def hp(self, t):
+        return self.zb.ZeroAdamW.make(step=t, **HP)
+
+    def ops(self, t):
+        raise NotImplementedError
+
+    def free(self):
+        for k in list(vars(self)):
+            if k not in ("zb", "device", "desc", "elems", "device_bytes", "name", "bytes_per_elem",
+                         "dominant"):
+                setattr(self, k, None)
+
+
+def _master(n_real, n, device):
+    import torch
+    from zero_sharded_mixed_gb300 import inputs
+    w = torch.zeros(n, dtype=torch.float32, device=device)
+    if n_real:
+        w[:n_real].normal_(0.0, 0.02, generator=torch.Generator(device=device).manual_seed(
+            inputs.derive_seed(SEED, 1)))
+    return w
+
+
+class Zero2Workload(Workload):
+    """ZeRO-2 step: the bucketed fused update of every owned element in
+    [lo, hi) from n_dp bf16 gradient buffers."""
 
     def __init__(self, name, device):
         import torch
-        from zero_sharded_mixed_gb300 import binding as zb
         from zero_sharded_mixed_gb300 import inputs
         from zero_sharded_mixed_gb300.step import bucket_ranges
-        self.name = name
-        self.zb = zb
-        self.device = device
+        super().__init__(device)
+        zb = self.zb
         n_dp = 8
+        self.name = name
         if name == "gpt2xl":
-            numels = inputs.gpt2xl_numels()
-            L = zb.zero_layout(numels, n_dp, 8, 500_000_000)
-            self.owner = None
-            lo, hi = 0, L.padded_n
-            self.rank_begin, self.rank_end, self.src_base = 0, n_dp, 0
+            L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+            lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
             self.desc = {"workload": "gpt2xl_zero2_all_shards", "model": "GPT-2-XL shapes",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "padded_n": L.padded_n,
                          "bucket": L.bucket, "buckets": L.n_buckets}
         elif name == "probe":
             L = zb.zero_layout([1 << 26], n_dp, 8, 500_000_000)
-            self.owner = None
-            lo, hi = 0, L.padded_n
-            self.rank_begin, self.rank_end, self.src_base = 0, n_dp, 0
+            lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
             self.desc = {"workload": "probe_flat_2p26_ndp8", "model": "flat vector",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "padded_n": L.padded_n,
                          "bucket": L.bucket, "buckets": L.n_buckets}
         else:
-            numels = inputs.llama7b_numels()
-            L = zb.zero_layout(numels, n_dp, 8, 500_000_000)
+            L = zb.zero_layout(inputs.llama7b_numels(), n_dp, 8, 500_000_000)
             o = 0
-            self.owner = o
-            lo, hi = o * L.shard, (o + 1) * L.shard
-            self.rank_begin, self.rank_end, self.src_base = o, o + 1, lo
+            lo, hi, self.rank_begin, self.rank_end = o * L.shard, (o + 1) * L.shard, o, o + 1
             src_len, outlier = L.shard, 0.01
             self.desc = {"workload": "llama7b_zero2_one_shard", "model": "Llama-7B shapes",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "owner": o,
                          "bucket": L.bucket, "outliers": "1% x100"}
-        self.L = L
+        self.L, self.src_base = L, lo
         self.ranges = bucket_ranges(L, lo, hi)
         self.elems = hi - lo
-        self.n_src = n_dp
         self.bytes_per_elem = 26 + 2 * n_dp
+        self.dominant = "rs_adamw"
         g = torch.empty((n_dp, src_len), dtype=torch.bfloat16, device=device)
         n_real = max(0, min(L.n, hi) - lo)
         for r in range(n_dp):
             inputs.grad_bf16_into(g[r], n_real, SEED, step=1, rank=r, outlier_p=outlier)
         self.grads = g
         self.grad_list = [g[r] for r in range(n_dp)]
-        w = torch.zeros(self.elems, dtype=torch.float32, device=device)
-        if n_real:
-            w[:n_real].normal_(0.0, 0.02, generator=torch.Generator(device=device).manual_seed(
-                inputs.derive_seed(SEED, 1)))
-        self.master = w
-        self.m = torch.zeros_like(w)
-        self.v = torch.zeros_like(w)
+        self.master = _master(n_real, self.elems, device)
+        self.m = torch.zeros_like(self.master)
+        self.v = torch.zeros_like(self.master)
         self.out = torch.zeros(L.padded_n, dtype=torch.bfloat16, device=device)
-        self.launches_per_step = len(self.ranges)
-        self.device_bytes = (g.numel() * 2 + 3 * w.numel() * 4 + self.out.numel() * 2)
+        self.device_bytes = g.numel() * 2 + 3 * self.elems * 4 + self.out.numel() * 2
 
-    def hp(self, t):
-        return self.zb.ZeroAdamW.make(step=t, **HP)
+    def ops(self, t):
+        zb, hp = self.zb, self.hp(t)
+        out = []
+        for s, e in self.ranges:
+            def fn(s=s, e=e):
+                zb.zero_reduce_scatter_adamw(self.L, self.grad_list, zb.ZERO_BF16, self.src_base,
+                                             float(self.L.n_dp), self.rank_begin, self.rank_end,
+                                             s, e, self.master, self.m, self.v, self.out,
+                                             zb.ZERO_OUT_FULL, hp)
+            out.append(Op("rs_adamw", (e - s) * self.bytes_per_elem, fn))
+        return out
 
-    def step(self, t, events=None):
+
+class AccumWorkload(Workload):
+    """Gradient accumulation, GPT-2-XL shapes, n_dp = 4, K = 4 micro-batches.
+    zero1: each rank adds its full bf16 micro-batch gradient into its own fp32
+    buffer, then one fused update from the n_dp fp32 buffers (divisor n_dp*K).
+    zero2: each micro-batch is reduce-scattered (summed) into the owners' fp32
+    shard buffer, then one fused update from it.  The same n_dp gradient
+    buffers serve every micro-batch (each read is larger than L2, so the
+    traffic is that of fresh data)."""
+
+    n_src = 4
+
+    def __init__(self, name, device):
+        import torch
+        from zero_sharded_mixed_gb300 import inputs
+        from zero_sharded_mixed_gb300.step import bucket_ranges
+        super().__init__(device)
         zb = self.zb
-        hp = self.hp(t)
-        for j, (s, e) in enumerate(self.ranges):
-            if events is not None:
-                events[j][0].record()
-            zb.zero_reduce_scatter_adamw(self.L, self.grad_list, zb.ZERO_BF16, self.src_base,
-                                         float(self.L.n_dp), self.rank_begin, self.rank_end, s, e,
-                                         self.master, self.m, self.v, self.out, zb.ZERO_OUT_FULL, hp)
-            if events is not None:
-                events[j][1].record()
+        self.name = name
+        n_dp, K = 4, 4
+        self.K = K
+        self.order = "zero1" if name == "accum-zero1" else "zero2"
+        L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+        self.L = L
+        P = L.padded_n
+        self.ranges = bucket_ranges(L)
+        self.elems = P
+        g = torch.empty((n_dp, P), dtype=torch.bfloat16, device=device)
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=1, rank=r)
+        self.grads = [g[r] for r in range(n_dp)]
+        self._g = g
+        self.master = _master(L.n, P, device)
+        self.m = torch.zeros(P, device=device)
+        self.v = torch.zeros(P, device=device)
+        self.out = torch.zeros(P, dtype=torch.bfloat16, device=device)
+        if self.order == "zero1":
+            self.acc = [torch.empty(P, device=device) for _ in range(n_dp)]
+            per = n_dp * (6 + (K - 1) * 10) + (26 + 4 * n_dp)
+            self.kernel_label = "zgb::acc_vec_kernel<1,true,true> + zgb::rs_adamw_vec_kernel<4,false>"
+            self.dominant = "accumulate_local"
+        else:
+            self.A = torch.empty(P, device=device)
+            per = (2 * n_dp + 4) + (K - 1) * (2 * n_dp + 8) + 30
+            self.kernel_label = "zgb::acc_vec_kernel<4,true,false> + zgb::rs_adamw_vec_kernel<1,false>"
+            self.dominant = "accumulate_reduce"
+        self.bytes_per_elem = per
+        self.desc = {"workload": "gpt2xl_accumulation_%s" % self.order, "model": "GPT-2-XL shapes",
+                     "N": L.n, "n_dp": n_dp, "micro_batches": K, "bucket": L.bucket}
+        self.device_bytes = (g.numel() * 2 + 3 * P * 4 + P * 2 +
+                             (n_dp * P * 4 if self.order == "zero1" else P * 4))
 
-    def free(self):
-        for k in ("grads", "grad_list", "master", "m", "v", "out"):
-            setattr(self, k, None)
+    def ops(self, t):
+        zb, hp, L, K = self.zb, self.hp(t), self.L, self.K
+        n_dp = L.n_dp
+        out = []
+        if self.order == "zero1":
+            for k in range(K):
+                for r in range(n_dp):
+                    def fn(r=r, k=k):
+                        zb.zero_accumulate(L, zb.ZERO_ACC_LOCAL, [self.grads[r]], zb.ZERO_BF16, 0,
+                                           self.acc[r], 0, 0, L.padded_n, k == 0)
+                    out.append(Op("accumulate_local", L.padded_n * (6 if k == 0 else 10), fn))
+            for s, e in self.ranges:
+                def fn(s=s, e=e):
+                    zb.zero_reduce_scatter_adamw(L, self.acc, zb.ZERO_F32, 0, float(n_dp * K), 0, n_dp,
+                                                 s, e, self.master, self.m, self.v, self.out,
+                                                 zb.ZERO_OUT_FULL, hp)
+                out.append(Op("rs_adamw", (e - s) * (26 + 4 * n_dp), fn))
+        else:
+            for k in range(K):
+                for s, e in self.ranges:
+                    def fn(s=s, e=e, k=k):
+                        zb.zero_accumulate(L, zb.ZERO_ACC_REDUCE, self.grads, zb.ZERO_BF16, 0, self.A, 0,
+                                           s, e, k == 0)
+                    out.append(Op("accumulate_reduce", (e - s) * (2 * n_dp + (4 if k == 0 else 8)), fn))
+            for s, e in self.ranges:
+                def fn(s=s, e=e):
+                    zb.zero_reduce_scatter_adamw(L, [self.A], zb.ZERO_F32, 0, float(n_dp * K), 0, n_dp,
+                                                 s, e, self.master, self.m, self.v, self.out,
+                                                 zb.ZERO_OUT_FULL, hp)
+                out.append(Op("rs_adamw", (e - s) * 30, fn))
+        return out
+
+
+class Zero3Workload(Workload):
+    """ZeRO-3 per-unit path, Llama-7B units at n_dp = 8 (embedding, 32 blocks,
+    head).  Per unit and step: gather the bf16 shards into a ring buffer for
+    forward, release; gather again for backward; reduce-scatter the unit
+    gradient (8 bf16 buffers -> fp32 owned shards); release; update the owned
+    shards, bf16 into each rank's own shard.  One set of 8 unit-gradient
+    buffers (sized for the largest unit) serves every unit."""
+
+    def __init__(self, name, device):
+        import torch
+        from zero_sharded_mixed_gb300 import inputs
+        from zero_sharded_mixed_gb300 import step as zstep
+        super().__init__(device)
+        zb = self.zb
+        self.name = name
+        self.zstep = zstep
+        n_dp = 8
+        self.units = []
+        total = 0
+        for i, numels in enumerate(inputs.llama7b_units()):
+            L = zb.zero_layout(numels, n_dp)
+            P = L.padded_n
+            w = _master(L.n, P, device)
+            shards = w.to(torch.bfloat16)
+            self.units.append(zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w,
+                                              torch.zeros(P, device=device), torch.zeros(P, device=device)))
+            total += P
+        cap = max(u.layout.padded_n for u in self.units)
+        self.ring = zstep.GatherRing(cap, device=str(device))
+        g = torch.empty((n_dp, cap), dtype=torch.bfloat16, device=device)
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], cap, SEED, step=1, rank=r)
+        self._g = g
+        self.A = torch.empty(cap, device=device)
+        self.elems = total
+        self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
+        self.dominant = "rs_adamw"
+        self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,true,false>, rs_adamw_vec_kernel<1,false>"
+        self.desc = {"workload": "llama7b_zero3_units", "model": "Llama-7B shapes",
+                     "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
+                     "ring_slots": 2}
+        self.device_bytes = total * (12 + 2) + 2 * cap * 2 + g.numel() * 2 + cap * 4
+
+    def ops(self, t):
+        zb, hp, zs = self.zb, self.hp(t), self.zstep
+        out = []
+        for i, u in enumerate(self.units):
+            P = u.layout.padded_n
+            grads = [self._g[r, :P] for r in range(u.layout.n_dp)]
+
+            def fwd(u=u, i=i):
+                zs.zero3_gather(u, self.ring, ("fwd", i))
+                self.ring.release(("fwd", i))
+
+            def bwd_gather(u=u, i=i):
+                zs.zero3_gather(u, self.ring, ("bwd", i))
+
+            def rs(u=u, i=i, P=P, grads=grads):
+                zs.zero3_layer_reduce_scatter(u, grads, self.A[:P])
+                self.ring.release(("bwd", i))
+
+            def upd(u=u, P=P):
+                zs.zero3_update(u, self.A[:P], hp)
+
+            out.append(Op("gather", P * 4, fwd))
+            out.append(Op("gather", P * 4, bwd_gather))
+            out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
+            out.append(Op("rs_adamw", P * 30, upd))
+        return out
+
+
+def make_workload(name, device):
+    if name in ("gpt2xl", "llama7b-shard", "probe"):
+        return Zero2Workload(name, device)
+    if name in ("accum-zero1", "accum-zero2"):
+        return AccumWorkload(name, device)
+    if name == "zero3":
+        return Zero3Workload(name, device)
+    raise ValueError(name)
 
 
 def time_workload(wl, steps, warmup, dist, device, sampler=None):
+    """W untimed steps, then K timed steps with a CUDA event pair around every
+    launch (on the launching stream) and one pair around the whole region."""
     import torch
     t = 1
     for _ in range(warmup):
-        wl.step(t)
+        for op in wl.ops(t):
+            op.fn()
         t += 1
+    plan = [wl.ops(t + k) for k in range(steps)]
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in wl.ranges] for _ in range(steps)]
+           for _ in ops] for ops in plan]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -294,45 +499,49 @@ def time_workload(wl, steps, warmup, dist, device, sampler=None):
         sampler.start()
         time.sleep(0.15)
     start.record()
-    for k in range(steps):
-        wl.step(t, ev[k])
-        t += 1
+    for ops, evs in zip(plan, ev):
+        for op, (a, b) in zip(ops, evs):
+            a.record()
+            op.fn()
+            b.record()
     end.record()
     torch.cuda.synchronize()
     barrier(dist)
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
-    total_ms = start.elapsed_time(end)
-    kernel_ms = sum(a.elapsed_time(b) for step_ev in ev for a, b in step_ev)
-    return total_ms, kernel_ms, clocks, t
+    per_kind = {}
+    for ops, evs in zip(plan, ev):
+        for op, (a, b) in zip(ops, evs):
+            d = per_kind.setdefault(op.kind, {"ms": 0.0, "bytes": 0, "launches": 0})
+            d["ms"] += a.elapsed_time(b)
+            d["bytes"] += op.bytes
+            d["launches"] += 1
+    return start.elapsed_time(end), per_kind, clocks, t + steps
 
 
 def time_e2e(wl, steps, warmup, t0, dist):
-    """The same step through the public binding with host buffers: every step
-    copies the n_dp gradient buffers from pinned host memory to the device and
-    reads the updated bf16 weights back to pinned host memory."""
+    """The same step through the public API with host buffers: every step copies
+    the n_dp gradient buffers from pinned host memory to the device and reads the
+    updated bf16 weights back into pinned host memory (step.HostPipeline, which
+    overlaps bucket b's copies with bucket b-1's update)."""
     import torch
+    from zero_sharded_mixed_gb300.step import HostPipeline
     host_g = torch.empty(wl.grads.shape, dtype=wl.grads.dtype, pin_memory=True)
     host_g.copy_(wl.grads)
     host_out = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    pipe = HostPipeline(wl.L, device=wl.device)
     t = t0
-
-    def one():
-        nonlocal t
-        wl.grads.copy_(host_g, non_blocking=True)
-        wl.step(t)
-        host_out.copy_(wl.out, non_blocking=True)
-        t += 1
-
     for _ in range(warmup):
-        one()
+        pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
+        t += 1
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(dist)
     start.record()
     for _ in range(steps):
-        one()
+        pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
+        t += 1
     end.record()
     torch.cuda.synchronize()
     barrier(dist)
@@ -373,6 +582,16 @@ def time_oracle(sample, seconds, n_dp):
 # arms
 # --------------------------------------------------------------------------
 
+def _kernels_summary(per_kind, steps):
+    out = {}
+    for kind, d in per_kind.items():
+        out[kind] = {"launches_per_step": d["launches"] // steps,
+                     "ms_per_step": d["ms"] / steps,
+                     "bytes_per_step": d["bytes"] // steps,
+                     "achieved_gbs": d["bytes"] / (d["ms"] / 1e3) / 1e9 if d["ms"] > 0 else None}
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -388,44 +607,50 @@ def run_ours(args):
 
     peak, peak_kind = _peak()
     primary = args.workload
-    extra = [w for w in ("gpt2xl", "llama7b-shard") if w != primary]
-    order = [primary] + ([] if args.no_extra or primary == "probe" else extra)
+    extras = [w for w in ("gpt2xl", "llama7b-shard", "accum-zero1", "accum-zero2", "zero3")
+              if w != primary]
+    order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
-    line = None
     for name in order:
-        wl = Workload(name, device)
+        wl = make_workload(name, device)
         torch.cuda.synchronize()
-        sampler = ClockSampler(local) if name == primary else None
-        total_ms, kernel_ms, clocks, t_next = time_workload(wl, args.steps, args.warmup, dist, device, sampler)
-        ms_step = max_over_ranks(dist, total_ms / args.steps, device)
-        kern_ms = max_over_ranks(dist, kernel_ms / args.steps, device)
-        value = wl.elems * world / (ms_step / 1e3)
-        launches = wl.launches_per_step
+        is_primary = name == primary
+        steps = args.steps if is_primary else max(1, min(args.steps, 10))
+        warm = args.warmup if is_primary else max(1, min(args.warmup, 2))
+        sampler = ClockSampler(local) if is_primary else None
+        total_ms, per_kind, clocks, t_next = time_workload(wl, steps, warm, dist, device, sampler)
+        ms_step = max_over_ranks(dist, total_ms / steps, device)
+        kernels = _kernels_summary(per_kind, steps)
+        dom = per_kind[wl.dominant]
+        dom_ms = max_over_ranks(dist, dom["ms"] / dom["launches"], device)   # average launch
+        dom_bytes = dom["bytes"] / dom["launches"]                           # per launch
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         bytes_step = wl.elems * wl.bytes_per_elem
-        achieved = bytes_step / (kern_ms / 1e3) / 1e9
-        tpe = _traffic_per_elem(wl.n_src)
+        tpe = _traffic_per_elem(wl.n_src) if wl.dominant == "rs_adamw" and name != "zero3" and \
+            not name.startswith("accum") else None
         res = {
-            "value": value, "ms_per_step": ms_step,
+            "value": replica_value(wl.elems, world, ms_step), "ms_per_step": ms_step, "steps": steps,
             "hbm_gbs_step": bytes_step / (ms_step / 1e3) / 1e9,
+            "bytes_per_param_step": wl.bytes_per_elem,
             "config": dict(wl.desc, l2="inputs %.1f GB > 129 MB L2, no flush" % (wl.device_bytes / 1e9)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": (tpe * wl.elems / launches) if tpe is not None else None,
-                         "algorithmic_bytes_per_launch": bytes_step / launches,
-                         "bytes_per_param": wl.bytes_per_elem,
-                         "kernel": "zgb::rs_adamw_vec_kernel<%d,true>" % wl.n_src},
-            "gpu_launches": launches * args.steps,
+                         "traffic": (tpe * dom_bytes / wl.bytes_per_elem) if tpe is not None else None,
+                         "algorithmic_bytes_per_launch": dom_bytes,
+                         "kernel": wl.dominant, "kernel_symbols": wl.kernel_label},
+            "kernels": kernels,
+            "gpu_launches": sum(d["launches"] for d in per_kind.values()),
         }
-        if name == primary:
+        if is_primary:
             res["clocks"] = clocks
-            if not args.no_e2e:
+            if not args.no_e2e and isinstance(wl, Zero2Workload):
                 e2e_steps = max(1, min(args.steps, 10))
                 e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
                 e_ms = max_over_ranks(dist, e_ms, device)
-                res["e2e"] = {"value": wl.elems * world / (e_ms / 1e3), "unit": UNIT,
+                res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
                               "ms_per_step": e_ms, "steps": e2e_steps,
                               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-            if not args.no_cpu_baseline and world == 1 and rank == 0:
+            if not args.no_cpu_baseline and world == 1 and rank == 0 and isinstance(wl, Zero2Workload):
                 sample = cpu_sample(wl, CPU_SAMPLE)
                 rate, secs, done = time_oracle(sample, CPU_BASELINE_SECONDS, wl.n_src)
                 res["cpu_baseline"] = {
@@ -447,16 +672,16 @@ def run_ours(args):
             "dtype": "f32", "storage": "bf16 gradients and weights, fp32 master/m/v",
             "data": "synthetic (seeded normal gradients and weights, model shapes only)",
             "config": dict(p["config"], parallelism="replicas x%d (simulated n_dp=%d per GPU)"
-                           % (world, p["config"]["n_dp"])),
+                           % (world, p["config"].get("n_dp", 8))),
             "hbm_gbs_step": p["hbm_gbs_step"],
             "roofline": p["roofline"],
+            "kernels": p["kernels"],
             "gpu_launches": p["gpu_launches"],
             "clocks": p.get("clocks"),
             "e2e": p.get("e2e"),
             "cpu_baseline": p.get("cpu_baseline"),
             "impl": "ours",
-            "workloads": {k: {kk: v[kk] for kk in ("value", "ms_per_step", "hbm_gbs_step", "roofline", "config")}
-                          for k, v in results.items() if k != primary},
+            "workloads": {k: v for k, v in results.items() if k != primary},
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -493,7 +718,7 @@ def run_reference(args):
     ms = el * 1e3 / max(1, args.steps)
     value = n / (ms / 1e3)
     wl_name = {"gpt2xl": "gpt2xl_zero2_all_shards", "llama7b-shard": "llama7b_zero2_one_shard",
-               "probe": "probe_flat_2p26_ndp8"}[args.workload]
+               "probe": "probe_flat_2p26_ndp8"}.get(args.workload, args.workload)
     sample = "%d owned elements per step (a bounded sample of %s), %d gradient slices" % (n, wl_name, n_dp)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

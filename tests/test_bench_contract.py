@@ -1,0 +1,36 @@
+"""The benchmark's command line and the reference arm's JSON line (CPU only)."""
+import io
+import json
+from contextlib import redirect_stdout
+
+import bench
+
+
+def test_defaults():
+    a = bench.parse_args([])
+    assert (a.gpus, a.impl, a.workload) == (1, "ours", "gpt2xl")
+    assert a.warmup >= 3 and a.steps >= 1
+
+
+def test_reference_arm_line(monkeypatch):
+    monkeypatch.setattr(bench, "REF_SAMPLE", 1 << 12)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_reference_arm_other_ranks_are_silent(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    assert buf.getvalue() == ""

@@ -1,0 +1,229 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times.  Every element's update depends only on that element's own
+inputs, so the oracle is run on sampled elements (random positions plus every
+bucket and shard boundary, the first and last elements and the padding) and
+compared one by one; properties that hold at any size are checked on every
+element on the device (the bf16 buffer is the cast of the master weights, the
+padding stays zero, nothing became non-finite)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from zero_sharded_mixed_gb300 import inputs
+from zero_sharded_mixed_gb300 import step as zstep
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+HP = oracle.AdamW(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
+SEED = 0
+
+
+def _hp(zb, t):
+    return zb.ZeroAdamW.make(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay, t)
+
+
+def _sample_indices(lo, hi, boundaries, n_random=1 << 18, seed=0):
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(lo, hi, size=n_random)]
+    for b in boundaries:
+        idx.append(np.arange(b - 8, b + 8))
+    idx.append(np.arange(lo, lo + 64))
+    idx.append(np.arange(hi - 64, hi))
+    idx = np.unique(np.concatenate(idx))
+    return idx[(idx >= lo) & (idx < hi)]
+
+
+def _take(t, idx_dev):
+    return t.index_select(0, idx_dev)
+
+
+def _bits_at(t, idx_dev):
+    return parity.bits(_take(t, idx_dev))
+
+
+def _full_properties(master, out_slice, n_real_in_slice):
+    """On the device, over every element: out is the RNE cast of master, the
+    padding is zero and nothing is non-finite."""
+    assert torch.isfinite(master).all()
+    cast = master.to(torch.bfloat16)   # torch's own round-to-nearest-even cast
+    assert torch.equal(out_slice.view(torch.int16), cast.view(torch.int16))
+    if n_real_in_slice < master.numel():
+        assert not master[n_real_in_slice:].any()
+        assert not out_slice[n_real_in_slice:].view(torch.int16).any()
+
+
+def test_gpt2xl_zero2_all_shards(zlib, cuda_device):
+    """GPT-2-XL shapes (N = 1,557,611,200), n_dp = 8, 5e8-element buckets,
+    all eight owned shards updated per step, 2 steps."""
+    zb = zlib
+    dev = cuda_device
+    L = zb.zero_layout(inputs.gpt2xl_numels(), 8, 8, 500_000_000)
+    P, S = L.padded_n, L.shard
+    assert (L.n, P, L.n_buckets) == (1_557_611_200, 1_557_611_200, 4)
+    g = torch.empty((8, P), dtype=torch.bfloat16, device=dev)
+    master = inputs.master_weights(L.n, P, seed=SEED, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    bounds = [b * L.bucket for b in range(1, L.n_buckets)] + [o * S for o in range(1, 8)]
+    idx = _sample_indices(0, P, bounds)
+    idx_dev = torch.from_numpy(idx).to(dev)
+    ref = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
+    for t in (1, 2):
+        for r in range(8):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=t, rank=r)
+        gs = np.stack([_bits_at(g[r], idx_dev) for r in range(8)])
+        zstep.zero12_step(L, [g[r] for r in range(8)], master, m, v, out, _hp(zb, t))
+        zb.zero_status_check()
+        ref_out, *ref = oracle.rs_adamw_reference(gs, 8, *ref, HP, t)
+        parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref, what=f"t={t} ")
+        assert np.array_equal(_bits_at(out, idx_dev), ref_out)
+    _full_properties(master, out, L.n)
+
+
+def test_llama7b_one_shard(zlib, cuda_device):
+    """Llama-7B shapes (N = 6,738,415,616) at n_dp = 8: one owned shard of
+    842,301,952 elements, 8 bf16 gradient slices with 1 % outliers x100, the
+    fused update writing into the full bf16 buffer, 2 steps."""
+    zb = zlib
+    dev = cuda_device
+    L = zb.zero_layout(inputs.llama7b_numels(), 8, 8, 500_000_000)
+    S = L.shard
+    assert S == 842_301_952
+    o = 3
+    lo, hi = o * S, (o + 1) * S
+    g = torch.empty((8, S), dtype=torch.bfloat16, device=dev)
+    master = inputs.master_weights(S, S, seed=SEED, device=dev)
+    m = torch.zeros(S, device=dev)
+    v = torch.zeros(S, device=dev)
+    out = torch.full((L.padded_n,), 0x1234, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    bounds = [b * L.bucket - lo for b in range(1, L.n_buckets) if lo < b * L.bucket < hi]
+    idx = _sample_indices(0, S, bounds, seed=1)
+    idx_dev = torch.from_numpy(idx).to(dev)
+    ref = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
+    for t in (1, 2):
+        for r in range(8):
+            inputs.grad_bf16_into(g[r], S, SEED, step=t, rank=r, outlier_p=0.01)
+        gs = np.stack([_bits_at(g[r], idx_dev) for r in range(8)])
+        zstep.zero12_step(L, [g[r] for r in range(8)], master, m, v, out, _hp(zb, t),
+                          rank_begin=o, rank_end=o + 1, grad_base=lo)
+        zb.zero_status_check()
+        ref_out, *ref = oracle.rs_adamw_reference(gs, 8, *ref, HP, t)
+        parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref, what=f"t={t} ")
+        assert np.array_equal(_bits_at(out[lo:hi], idx_dev), ref_out)
+    _full_properties(master, out[lo:hi], S)
+    # nothing outside the owner's part of the full buffer was written
+    iv = out.view(torch.int16)
+    assert bool((iv[:lo] == 0x1234).all()) and bool((iv[hi:] == 0x1234).all())
+
+
+def test_gpt2xl_accumulation_both_orders(zlib, cuda_device):
+    """Gradient accumulation, GPT-2-XL shapes, n_dp = 4, K = 4 micro-batches:
+    ZeRO-1 (fp32 local accumulation per rank, one reduce-scatter) and ZeRO-2
+    (reduce-scatter per micro-batch), each against its own oracle order on
+    sampled elements, then the two against each other."""
+    zb = zlib
+    dev = cuda_device
+    n_dp, K = 4, 4
+    L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+    P = L.padded_n
+    g = torch.empty((n_dp, P), dtype=torch.bfloat16, device=dev)
+    acc = [torch.empty(P, device=dev) for _ in range(n_dp)]
+    A = torch.empty(P, device=dev)
+    w0 = inputs.master_weights(L.n, P, seed=SEED, device=dev)
+    s1 = [w0.clone(), torch.zeros(P, device=dev), torch.zeros(P, device=dev)]
+    s2 = [w0, torch.zeros(P, device=dev), torch.zeros(P, device=dev)]
+    o1 = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    o2 = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    bounds = [b * L.bucket for b in range(1, L.n_buckets)] + [o * L.shard for o in range(1, n_dp)]
+    idx = _sample_indices(0, P, bounds, seed=2)
+    idx_dev = torch.from_numpy(idx).to(dev)
+    w_s = parity.f32(_take(w0, idx_dev))
+    samples = []
+    for k in range(K):
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=1, rank=r, micro=k)
+        samples.append(np.stack([_bits_at(g[r], idx_dev) for r in range(n_dp)]))
+        zstep.zero1_accumulate_micro(L, [g[r] for r in range(n_dp)], acc, first=(k == 0))
+        zstep.zero2_accumulate_micro(L, [g[r] for r in range(n_dp)], A, first=(k == 0))
+    zstep.zero1_finish(L, acc, K, *s1, o1, _hp(zb, 1))
+    zstep.zero2_finish(L, A, K, *s2, o2, _hp(zb, 1))
+    zb.zero_status_check()
+    z = np.zeros(idx.size, np.float32)
+    acc_ref = [None] * n_dp
+    A_ref = None
+    for k, gs in enumerate(samples):
+        for r in range(n_dp):
+            acc_ref[r] = oracle.accumulate_local(acc_ref[r], gs[r], first=(k == 0))
+        A_ref = oracle.accumulate_reduce(A_ref, gs, first=(k == 0))
+    for r in range(n_dp):
+        parity.assert_bit_exact_f32(_take(acc[r], idx_dev), acc_ref[r])
+    parity.assert_bit_exact_f32(_take(A, idx_dev), A_ref)
+    out1, *st1 = oracle.rs_adamw_reference(np.stack(acc_ref), n_dp * K, w_s, z, z, HP, 1)
+    out2, *st2 = oracle.rs_adamw_reference(A_ref[None, :], n_dp * K, w_s, z, z, HP, 1)
+    parity.assert_state([_take(x, idx_dev) for x in s1], st1, what="zero1 ")
+    parity.assert_state([_take(x, idx_dev) for x in s2], st2, what="zero2 ")
+    assert np.array_equal(_bits_at(o1, idx_dev), out1)
+    assert np.array_equal(_bits_at(o2, idx_dev), out2)
+    # the two orders agree within the fp32 summation bound, on every element
+    x_abs = sum(np.abs(oracle.bf16_to_f32(gs).astype(np.float64)).sum(0) for gs in samples)
+    bound = n_dp * K * 2.0 ** -24 / (1 - n_dp * K * 2.0 ** -24) * x_abs
+    sum1 = sum(parity.f32(_take(a, idx_dev)).astype(np.float64) for a in acc)
+    assert np.all(np.abs(sum1 - parity.f32(_take(A, idx_dev))) <= 2 * bound + 1e-45)
+    _full_properties(s1[0], o1, L.n)
+    _full_properties(s2[0], o2, L.n)
+
+
+def test_llama7b_zero3_units(zlib, cuda_device):
+    """ZeRO-3 per-unit path on Llama-7B units at n_dp = 8 (embedding, 32 blocks,
+    head): per unit, gather the bf16 shards into one of two ring buffers for
+    forward and again for backward, reduce-scatter the unit gradient into fp32,
+    update the owned shards writing bf16 into each rank's own shard.  Checked on
+    sampled elements of every unit; at most two units resident."""
+    zb = zlib
+    dev = cuda_device
+    n_dp = 8
+    units_numels = inputs.llama7b_units()
+    layouts = [zb.zero_layout(u, n_dp) for u in units_numels]
+    cap = max(L.padded_n for L in layouts)
+    ring = zstep.GatherRing(cap, device=str(dev))
+    gbuf = torch.empty((n_dp, cap), dtype=torch.bfloat16, device=dev)
+    A = torch.empty(cap, device=dev)
+    rng = np.random.default_rng(5)
+    for i, L in enumerate(layouts):
+        P = L.padded_n
+        w = inputs.master_weights(L.n, P, seed=SEED + i, device=dev)
+        shards = w.to(torch.bfloat16)            # the initial bf16 shards (inputs only)
+        unit = zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w, torch.zeros(P, device=dev),
+                               torch.zeros(P, device=dev))
+        idx = np.unique(np.concatenate([rng.integers(0, P, 4096), np.arange(max(0, L.n - 8), P),
+                                        [o * L.shard for o in range(n_dp)]]))
+        idx_dev = torch.from_numpy(idx).to(dev)
+        shard_bits = _bits_at(unit.shards.view(-1), idx_dev)
+        # forward gather + release, backward gather
+        buf = zstep.zero3_gather(unit, ring, ("fwd", i))
+        assert np.array_equal(_bits_at(buf, idx_dev), shard_bits)
+        ring.release(("fwd", i))
+        buf = zstep.zero3_gather(unit, ring, ("bwd", i))
+        assert torch.equal(buf.view(torch.int16), unit.shards.view(-1).view(torch.int16))
+        for r in range(n_dp):
+            inputs.grad_bf16_into(gbuf[r, :P], L.n, SEED, step=1, rank=r, micro=i)
+        gs = np.stack([_bits_at(gbuf[r, :P], idx_dev) for r in range(n_dp)])
+        ws = parity.f32(_take(w, idx_dev))
+        zstep.zero3_layer_reduce_scatter(unit, [gbuf[r, :P] for r in range(n_dp)], A[:P])
+        ring.release(("bwd", i))
+        zstep.zero3_update(unit, A[:P], _hp(zb, 1))
+        zb.zero_status_check()
+        A_ref = oracle.accumulate_reduce(None, gs, first=True)
+        parity.assert_bit_exact_f32(_take(A[:P], idx_dev), A_ref)
+        z = np.zeros(idx.size, np.float32)
+        out_ref, *st = oracle.rs_adamw_reference(A_ref[None, :], n_dp, ws, z, z, HP, 1)
+        parity.assert_state([_take(x, idx_dev) for x in (unit.master, unit.m, unit.v)], st,
+                            what=f"unit {i} ")
+        assert np.array_equal(_bits_at(unit.shards.view(-1), idx_dev), out_ref)
+        _full_properties(unit.master, unit.shards.view(-1), L.n)
+        assert ring.peak <= 2
+        del unit, w, shards
+    assert ring.resident == 0

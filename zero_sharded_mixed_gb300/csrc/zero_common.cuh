@@ -8,7 +8,10 @@
 
 namespace zgb {
 
-constexpr int kThreads = 256;   // threads per CTA for every streaming kernel
+#ifndef ZGB_THREADS
+#define ZGB_THREADS 256
+#endif
+constexpr int kThreads = ZGB_THREADS;   // threads per CTA for every streaming kernel
 
 // ----------------------------------------------------------------- device
 

@@ -28,7 +28,10 @@
 #include "zero_common.cuh"
 
 #ifndef ZGB_RS_WAVES
-#define ZGB_RS_WAVES 1   // grid = resident CTAs x this (grid-stride loop inside)
+#define ZGB_RS_WAVES 1       // grid = resident CTAs x this (grid-stride loop inside)
+#endif
+#ifndef ZGB_RS_MINBLOCKS
+#define ZGB_RS_MINBLOCKS 1   // CTAs per SM the register allocation must allow
 #endif
 
 namespace zgb {
@@ -159,7 +162,7 @@ __device__ __forceinline__ void step_one(const RsAdamwParams& p, int64_t i) {
 }
 
 template <int NDP, bool kBf16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
 rs_adamw_vec_kernel(const __grid_constant__ RsAdamwParams p) {
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;

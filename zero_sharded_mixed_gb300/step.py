@@ -158,3 +158,47 @@ def zero3_update(unit: Zero3Unit, A: torch.Tensor, hp, n_micro: int = 1, stream=
     zb.zero_reduce_scatter_adamw(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
                                  0, L.padded_n, unit.master, unit.m, unit.v,
                                  unit.shards.view(-1), zb.ZERO_OUT_SHARD, hp, stream)
+
+
+# --------------------------------------------------------------------------
+# host-resident gradients: copies overlapped with the per-bucket update
+# --------------------------------------------------------------------------
+
+class HostPipeline:
+    """A ZeRO-1/2 step whose gradients arrive in pinned host memory and whose
+    bf16 result goes back to pinned host memory.  Bucket b's host-to-device
+    copies run on one stream, its fused update on the caller's stream once they
+    have landed, and its device-to-host copy on a third stream, so the copies of
+    one bucket overlap the update of the previous one ("ZeRO and FSDP", stage
+    2: each bucket is reduce-scattered as soon as it is ready)."""
+
+    def __init__(self, L, device=None):
+        self.L = L
+        self.ranges = bucket_ranges(L)
+        self.h2d = torch.cuda.Stream(device=device)
+        self.d2h = torch.cuda.Stream(device=device)
+        self.ev_in = [torch.cuda.Event() for _ in self.ranges]
+        self.ev_done = [torch.cuda.Event() for _ in self.ranges]
+        self.ev_out = torch.cuda.Event()
+
+    def step(self, host_grads, dev_grads, master, m, v, out, host_out, hp):
+        L = self.L
+        comp = torch.cuda.current_stream()
+        self.h2d.wait_stream(comp)       # the device gradient buffer is free to overwrite
+        with torch.cuda.stream(self.h2d):
+            for j, (s, e) in enumerate(self.ranges):
+                for r in range(L.n_dp):
+                    dev_grads[r, s:e].copy_(host_grads[r, s:e], non_blocking=True)
+                self.ev_in[j].record(self.h2d)
+        rows = [dev_grads[r] for r in range(L.n_dp)]
+        for j, (s, e) in enumerate(self.ranges):
+            comp.wait_event(self.ev_in[j])
+            zb.zero_reduce_scatter_adamw(L, rows, zb.ZERO_BF16, 0, float(L.n_dp), 0, L.n_dp, s, e,
+                                         master, m, v, out, zb.ZERO_OUT_FULL, hp, comp)
+            self.ev_done[j].record(comp)
+        with torch.cuda.stream(self.d2h):
+            for j, (s, e) in enumerate(self.ranges):
+                self.d2h.wait_event(self.ev_done[j])
+                host_out[s:e].copy_(out[s:e], non_blocking=True)
+            self.ev_out.record(self.d2h)
+        comp.wait_event(self.ev_out)     # the step ends when the result is on the host
