@@ -178,3 +178,52 @@ def test_zero3_units(zlib, cuda_device):
         parity.assert_state([u.master, u.m, u.v], st, what=f"unit {i} ")
         assert np.array_equal(parity.bits(u.shards).reshape(-1), out_ref)
     assert ring.peak <= 2 and ring.resident == 0
+
+
+@pytest.mark.parametrize("mode,n_src,dtype", [("local", 1, "bf16"), ("local", 1, "f32"),
+                                              ("reduce", 1, "bf16"), ("reduce", 2, "bf16"),
+                                              ("reduce", 4, "bf16"), ("reduce", 8, "bf16"),
+                                              ("reduce", 2, "f32"), ("reduce", 5, "bf16")])
+def test_accumulate_several_waves(zlib, cuda_device, mode, n_src, dtype):
+    """5,000,011 elements: several passes of the multi-vector loops, a partial
+    last group, a ragged tail; first and accumulating calls."""
+    zb = zlib
+    N = 5_000_011
+    L = zb.zero_layout([N], 1, align=1)
+    rng = np.random.default_rng(7 + n_src)
+    dst = torch.zeros(N, device="cuda")
+    ref = None
+    for k in range(2):
+        xf = (rng.standard_normal((n_src, N)) * 1e-3).astype(np.float32)
+        if dtype == "bf16":
+            xs = oracle.cast_bf16(xf)
+            srcs = [inputs.from_bf16_bits(xs[r], "cuda") for r in range(n_src)]
+            code = zb.ZERO_BF16
+            xr = oracle.bf16_to_f32(xs)
+        else:
+            srcs = [torch.from_numpy(xf[r].copy()).cuda() for r in range(n_src)]
+            code = zb.ZERO_F32
+            xr = xf
+        m = zb.ZERO_ACC_LOCAL if mode == "local" else zb.ZERO_ACC_REDUCE
+        zb.zero_accumulate(L, m, srcs, code, 0, dst, 0, 0, N, k == 0)
+        if mode == "local":
+            ref = xr[0].copy() if k == 0 else ref + xr[0]
+        elif dtype == "bf16":
+            ref = oracle.accumulate_reduce(ref, xs, first=(k == 0))
+        else:
+            s = oracle.reduce_mean(xr, 1.0)        # the fp32 sum over sources (division by 1 is exact)
+            ref = s if k == 0 else ref + s
+    torch.cuda.synchronize()
+    parity.assert_bit_exact_f32(dst, ref)
+
+
+def test_gather_several_waves(zlib, cuda_device):
+    zb = zlib
+    n_dp, S = 3, 4_000_000
+    L = zb.zero_layout([n_dp * S], n_dp)
+    rng = np.random.default_rng(3)
+    sh = rng.integers(0, 1 << 16, size=(n_dp, S)).astype(np.uint16)
+    full = torch.empty(L.padded_n, dtype=torch.bfloat16, device="cuda")
+    zb.zero_gather_layer(L, [inputs.from_bf16_bits(sh[o], "cuda") for o in range(n_dp)], full)
+    torch.cuda.synchronize()
+    assert np.array_equal(parity.bits(full), sh.reshape(-1))

@@ -199,3 +199,33 @@ def test_zero_length_range_is_a_no_op(zlib, cuda_device):
                                  zb.ZERO_OUT_FULL, _hp(zb, 1))
     zb.zero_status_check()
     assert all(torch.all(x == 1) for x in st) and not out.view(torch.int16).any()
+
+
+@pytest.mark.parametrize("n_src,dtype", [(1, "bf16"), (2, "bf16"), (1, "f32"), (2, "f32"), (8, "bf16")])
+def test_several_waves_with_partial_groups(zlib, cuda_device, n_src, dtype):
+    """5,000,011 elements: several grid-stride passes of the multi-vector loop,
+    a partial last group and a ragged tail."""
+    zb = zlib
+    N = 5_000_011
+    L = zb.zero_layout([N], 1, align=1)
+    rng = np.random.default_rng(n_src)
+    xf = (rng.standard_normal((n_src, N)) * 1e-3).astype(np.float32)
+    if dtype == "bf16":
+        src_np = oracle.cast_bf16(xf)
+        srcs = [inputs.from_bf16_bits(src_np[r], "cuda") for r in range(n_src)]
+        code = zb.ZERO_BF16
+    else:
+        src_np = xf
+        srcs = [torch.from_numpy(xf[r].copy()).cuda() for r in range(n_src)]
+        code = zb.ZERO_F32
+    w0 = parity.f32(inputs.master_weights(N, N, seed=n_src))
+    m0 = (np.abs(rng.standard_normal(N)) * 1e-4).astype(np.float32)
+    v0 = (np.abs(rng.standard_normal(N)) * 1e-8).astype(np.float32)
+    st = [torch.from_numpy(x.copy()).cuda() for x in (w0, m0, v0)]
+    out = torch.zeros(N, dtype=torch.bfloat16, device="cuda")
+    zb.zero_reduce_scatter_adamw(L, srcs, code, 0, float(n_src), 0, 1, 0, N, *st, out,
+                                 zb.ZERO_OUT_FULL, _hp(zb, 4))
+    torch.cuda.synchronize()
+    ref_out, w, m, v = oracle.rs_adamw_reference(src_np, n_src, w0, m0, v0, HP_ORACLE, 4)
+    parity.assert_state(st, [w, m, v])
+    assert np.array_equal(parity.bits(out), ref_out)

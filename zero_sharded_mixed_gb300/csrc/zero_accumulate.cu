@@ -15,6 +15,13 @@
 // explicit IEEE fp32 adds in ascending source order.
 #include "zero_common.cuh"
 
+#ifndef ZGB_ACC_LOCAL_U
+#define ZGB_ACC_LOCAL_U 2    // vectors per thread and iteration, LOCAL mode
+#endif
+#ifndef ZGB_ACC_REDUCE_U
+#define ZGB_ACC_REDUCE_U 4   // the same for REDUCE with at most 4 source loads per vector
+#endif
+
 namespace zgb {
 
 struct AccParams {
@@ -86,6 +93,97 @@ __device__ __forceinline__ void acc_vec(const AccParams& p, int64_t vi) {
     st_stream_f4(p.dst + e + 4, make_float4(x[4], x[5], x[6], x[7]));
 }
 
+// U vectors per thread and iteration (vi0, vi0 + stride, ...), all loads issued
+// before the first add: the accumulation kernels move few bytes per vector
+// (LOCAL: one 16-byte source load plus the 32-byte dst), so one vector per
+// thread leaves HBM short of bytes in flight.
+template <int NDP, bool kBf16, bool kLocal, int U>
+__device__ __forceinline__ void acc_vecs(const AccParams& p, int64_t vi0, int64_t stride, int64_t nv) {
+    constexpr int R = kLocal ? 1 : NDP;
+    static_assert(R > 0, "the multi-vector step needs a compile-time source count");
+    constexpr int kRaw = kBf16 ? R : 2 * R;
+    uint4 graw[U][kBf16 ? kRaw : 1];
+    float4 fraw[U][kBf16 ? 1 : kRaw];
+    float4 d[U][2];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t vi = vi0 + u * stride;
+        ok[u] = vi < nv;
+        if (ok[u]) {
+            const int64_t e = vi * 8;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if constexpr (kBf16) {
+                    graw[u][r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
+                } else {
+                    fraw[u][2 * r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
+                    fraw[u][2 * r + 1] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
+                }
+            }
+            if (!p.first) {
+                d[u][0] = ld_stream_f4(p.dst + e);
+                d[u][1] = ld_stream_f4(p.dst + e + 4);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!ok[u]) continue;
+        const int64_t e = (vi0 + u * stride) * 8;
+        float x[8];
+        if constexpr (kLocal) {
+            if constexpr (kBf16) {
+                const uint4 a = graw[u][0];
+                x[0] = bf16_lo(a.x); x[1] = bf16_hi(a.x); x[2] = bf16_lo(a.y); x[3] = bf16_hi(a.y);
+                x[4] = bf16_lo(a.z); x[5] = bf16_hi(a.z); x[6] = bf16_lo(a.w); x[7] = bf16_hi(a.w);
+            } else {
+                const float4 a = fraw[u][0], b = fraw[u][1];
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if constexpr (kBf16) {
+                    const uint4 a = graw[u][r];
+                    x[0] = __fadd_rn(x[0], bf16_lo(a.x)); x[1] = __fadd_rn(x[1], bf16_hi(a.x));
+                    x[2] = __fadd_rn(x[2], bf16_lo(a.y)); x[3] = __fadd_rn(x[3], bf16_hi(a.y));
+                    x[4] = __fadd_rn(x[4], bf16_lo(a.z)); x[5] = __fadd_rn(x[5], bf16_hi(a.z));
+                    x[6] = __fadd_rn(x[6], bf16_lo(a.w)); x[7] = __fadd_rn(x[7], bf16_hi(a.w));
+                } else {
+                    const float4 a = fraw[u][2 * r], b = fraw[u][2 * r + 1];
+                    x[0] = __fadd_rn(x[0], a.x); x[1] = __fadd_rn(x[1], a.y);
+                    x[2] = __fadd_rn(x[2], a.z); x[3] = __fadd_rn(x[3], a.w);
+                    x[4] = __fadd_rn(x[4], b.x); x[5] = __fadd_rn(x[5], b.y);
+                    x[6] = __fadd_rn(x[6], b.z); x[7] = __fadd_rn(x[7], b.w);
+                }
+            }
+        }
+        if (!p.first) {
+            const float4 a = d[u][0], b = d[u][1];
+            x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]);
+            x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
+            x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]);
+            x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
+        }
+        st_stream_f4(p.dst + e, make_float4(x[0], x[1], x[2], x[3]));
+        st_stream_f4(p.dst + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+    }
+}
+
+// Vectors per thread and iteration, chosen by measurement on GB300 (GPT-2-XL
+// shapes): LOCAL does best with two; REDUCE with four while a vector has at
+// most four source loads, one beyond that (eight bf16 sources already keep
+// ten loads per vector in flight).
+template <int NDP, bool kBf16, bool kLocal>
+__host__ __device__ constexpr int acc_vectors_per_iter() {
+    return kLocal ? ZGB_ACC_LOCAL_U
+         : (NDP > 0 && (kBf16 ? NDP : 2 * NDP) <= 4) ? ZGB_ACC_REDUCE_U : 1;
+}
+
 template <bool kBf16, bool kLocal>
 __device__ __forceinline__ void acc_one(const AccParams& p, int64_t i) {
     float x;
@@ -106,7 +204,12 @@ __global__ void __launch_bounds__(kThreads) acc_vec_kernel(const __grid_constant
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t vi = tid; vi < nv; vi += stride) acc_vec<NDP, kBf16, kLocal>(p, vi);
+    constexpr int U = acc_vectors_per_iter<NDP, kBf16, kLocal>();
+    if constexpr (U > 1) {
+        for (int64_t vi = tid; vi < nv; vi += U * stride) acc_vecs<NDP, kBf16, kLocal, U>(p, vi, stride, nv);
+    } else {
+        for (int64_t vi = tid; vi < nv; vi += stride) acc_vec<NDP, kBf16, kLocal>(p, vi);
+    }
     const int64_t tail = p.n - (nv << 3);
     if (tid < tail) acc_one<kBf16, kLocal>(p, (nv << 3) + tid);
 }

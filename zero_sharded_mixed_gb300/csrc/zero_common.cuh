@@ -31,19 +31,48 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
     return (uint16_t)(pack_bf16x2(x, 0.0f) & 0xffffu);
 }
 
-// Streaming (evict-first) 128-bit loads and stores: every byte of this path is
-// touched once per launch, so nothing is worth keeping in L1 or L2.
+// 128-bit loads and stores of the streams.  Every byte of these kernels is
+// touched once per launch, so nothing is worth keeping in L1; the cache
+// policy is a compile-time choice (measured): ZGB_LD_HINT 1 = ld.global.cs
+// (evict-first), 0 = plain ld.global, 2 = ld.global.nc (read-only path);
+// ZGB_ST_HINT 1 = st.global.cs (evict-first), 0 = plain st.global.
+#ifndef ZGB_LD_HINT
+#define ZGB_LD_HINT 1
+#endif
+#ifndef ZGB_ST_HINT
+#define ZGB_ST_HINT 1
+#endif
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+#if ZGB_LD_HINT == 1
     return __ldcs(reinterpret_cast<const uint4*>(p));
+#elif ZGB_LD_HINT == 2
+    return __ldg(reinterpret_cast<const uint4*>(p));
+#else
+    return *reinterpret_cast<const uint4*>(p);
+#endif
 }
 __device__ __forceinline__ float4 ld_stream_f4(const void* p) {
+#if ZGB_LD_HINT == 1
     return __ldcs(reinterpret_cast<const float4*>(p));
+#elif ZGB_LD_HINT == 2
+    return __ldg(reinterpret_cast<const float4*>(p));
+#else
+    return *reinterpret_cast<const float4*>(p);
+#endif
 }
 __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
+#if ZGB_ST_HINT == 1
     __stcs(reinterpret_cast<uint4*>(p), v);
+#else
+    *reinterpret_cast<uint4*>(p) = v;
+#endif
 }
 __device__ __forceinline__ void st_stream_f4(void* p, float4 v) {
+#if ZGB_ST_HINT == 1
     __stcs(reinterpret_cast<float4*>(p), v);
+#else
+    *reinterpret_cast<float4*>(p) = v;
+#endif
 }
 
 // ----------------------------------------------------------------- host

@@ -10,6 +10,10 @@
 // 2 bytes written per unit element.
 #include "zero_common.cuh"
 
+#ifndef ZGB_GATHER_U
+#define ZGB_GATHER_U 1       // 128-bit vectors per thread and iteration (1 measured best)
+#endif
+
 namespace zgb {
 
 struct GatherParams {
@@ -24,7 +28,17 @@ __global__ void __launch_bounds__(kThreads) gather_vec_kernel(const __grid_const
     const int64_t nv = p.shard_len >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t vi = tid; vi < nv; vi += stride) st_stream_u4(dst + vi * 8, ld_stream_u4(src + vi * 8));
+    // U vectors per thread and iteration, loads first
+    constexpr int U = ZGB_GATHER_U;
+    for (int64_t vi = tid; vi < nv; vi += U * stride) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (vi + u * stride < nv) x[u] = ld_stream_u4(src + (vi + u * stride) * 8);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (vi + u * stride < nv) st_stream_u4(dst + (vi + u * stride) * 8, x[u]);
+    }
     const int64_t tail = p.shard_len - (nv << 3);
     if (tid < tail) dst[(nv << 3) + tid] = src[(nv << 3) + tid];
 }

@@ -30,6 +30,9 @@
 #ifndef ZGB_RS_WAVES
 #define ZGB_RS_WAVES 1       // grid = resident CTAs x this (grid-stride loop inside)
 #endif
+#ifndef ZGB_RS_MULTI
+#define ZGB_RS_MULTI 1       // 0: one vector per thread and iteration everywhere
+#endif
 #ifndef ZGB_RS_MINBLOCKS
 #define ZGB_RS_MINBLOCKS 1   // CTAs per SM the register allocation must allow
 #endif
@@ -161,13 +164,96 @@ __device__ __forceinline__ void step_one(const RsAdamwParams& p, int64_t i) {
     p.out[i] = to_bf16(w);
 }
 
+// U vectors per thread and iteration (vectors vi0, vi0 + stride, ...): every
+// load of all U vectors is issued before the first add, so a thread keeps
+// U * (loads per vector) 128-bit loads in flight.  Used when one vector alone
+// has few loads (one or two sources), where a single vector per thread leaves
+// HBM short of bytes in flight.
+template <int NDP, bool kBf16, int U>
+__device__ __forceinline__ void step_vecs(const RsAdamwParams& p, int64_t vi0, int64_t stride,
+                                          int64_t nv) {
+    static_assert(NDP > 0, "the multi-vector step needs a compile-time source count");
+    constexpr int kRaw = kBf16 ? NDP : 2 * NDP;   // 128-bit source loads per vector
+    uint4 graw[U][kBf16 ? kRaw : 1];
+    float4 fraw[U][kBf16 ? 1 : kRaw];
+    float4 st[U][6];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t vi = vi0 + u * stride;
+        ok[u] = vi < nv;
+        if (ok[u]) {
+            const int64_t e = vi * 8;
+#pragma unroll
+            for (int r = 0; r < NDP; ++r) {
+                if constexpr (kBf16) {
+                    graw[u][r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
+                } else {
+                    fraw[u][2 * r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
+                    fraw[u][2 * r + 1] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
+                }
+            }
+            st[u][0] = ld_stream_f4(p.w + e);
+            st[u][1] = ld_stream_f4(p.w + e + 4);
+            st[u][2] = ld_stream_f4(p.m + e);
+            st[u][3] = ld_stream_f4(p.m + e + 4);
+            st[u][4] = ld_stream_f4(p.v + e);
+            st[u][5] = ld_stream_f4(p.v + e + 4);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!ok[u]) continue;
+        const int64_t e = (vi0 + u * stride) * 8;
+        float s[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < NDP; ++r) {
+            if constexpr (kBf16) add_bf16x8(s, graw[u][r]);
+            else add_f32x8(s, fraw[u][2 * r], fraw[u][2 * r + 1]);
+        }
+        float w[8] = {st[u][0].x, st[u][0].y, st[u][0].z, st[u][0].w,
+                      st[u][1].x, st[u][1].y, st[u][1].z, st[u][1].w};
+        float m[8] = {st[u][2].x, st[u][2].y, st[u][2].z, st[u][2].w,
+                      st[u][3].x, st[u][3].y, st[u][3].z, st[u][3].w};
+        float v[8] = {st[u][4].x, st[u][4].y, st[u][4].z, st[u][4].w,
+                      st[u][5].x, st[u][5].y, st[u][5].z, st[u][5].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) adamw_update(__fdiv_rn(s[j], p.divisor), w[j], m[j], v[j], p);
+        st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
+        st_stream_f4(p.w + e + 4, make_float4(w[4], w[5], w[6], w[7]));
+        st_stream_f4(p.m + e, make_float4(m[0], m[1], m[2], m[3]));
+        st_stream_f4(p.m + e + 4, make_float4(m[4], m[5], m[6], m[7]));
+        st_stream_f4(p.v + e, make_float4(v[0], v[1], v[2], v[3]));
+        st_stream_f4(p.v + e + 4, make_float4(v[4], v[5], v[6], v[7]));
+        uint4 o;
+        o.x = pack_bf16x2(w[0], w[1]);
+        o.y = pack_bf16x2(w[2], w[3]);
+        o.z = pack_bf16x2(w[4], w[5]);
+        o.w = pack_bf16x2(w[6], w[7]);
+        st_stream_u4(p.out + e, o);
+    }
+}
+
+// Vectors per thread and iteration: two when one vector has at most 8 loads.
+template <int NDP, bool kBf16>
+__host__ __device__ constexpr int vectors_per_iter() {
+    return ZGB_RS_MULTI && NDP > 0 && ((kBf16 ? NDP : 2 * NDP) + 6) <= 8 ? 2 : 1;
+}
+
 template <int NDP, bool kBf16>
 __global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
 rs_adamw_vec_kernel(const __grid_constant__ RsAdamwParams p) {
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t vi = tid; vi < nv; vi += stride) step_vec<NDP, kBf16>(p, vi);
+    constexpr int U = vectors_per_iter<NDP, kBf16>();
+    if constexpr (U > 1) {
+        for (int64_t vi = tid; vi < nv; vi += U * stride) step_vecs<NDP, kBf16, U>(p, vi, stride, nv);
+    } else {
+        for (int64_t vi = tid; vi < nv; vi += stride) step_vec<NDP, kBf16>(p, vi);
+    }
     const int64_t tail = p.n - (nv << 3);
     if (tid < tail) step_one<kBf16>(p, (nv << 3) + tid);
 }
