@@ -90,6 +90,14 @@ def _load():
         lib.oracle_accumulate_reduce.restype = None
         lib.oracle_all_gather_bf16.argtypes = [p, i32, i64, p]
         lib.oracle_all_gather_bf16.restype = None
+        lib.oracle_grad_norm_sq_bf16.argtypes = [p, i32, i64, i64, f32]
+        lib.oracle_grad_norm_sq_bf16.restype = ctypes.c_double
+        lib.oracle_grad_norm_sq_f32.argtypes = [p, i32, i64, i64, f32]
+        lib.oracle_grad_norm_sq_f32.restype = ctypes.c_double
+        lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
+        lib.oracle_clip_coef.restype = f32
+        lib.oracle_scale.argtypes = [p, i64, f32]
+        lib.oracle_scale.restype = None
         _lib = lib
         return lib
 
@@ -247,9 +255,34 @@ def all_gather(shards) -> np.ndarray:
     return full
 
 
-def rs_adamw_reference(src, divisor, w, m, v, hp: AdamW, t: int):
-    """Mean of source rows, then AdamW, then cast: the per-element definition of
-    one fused update call.  Returns (out_bf16, w, m, v)."""
+def grad_norm_sq(src, divisor) -> float:
+    """Squared L2 norm (fp64) of the mean over rows of a 2-D array."""
+    src = np.ascontiguousarray(src)
+    n_src, n = src.shape
+    d = float(np.float32(divisor))
+    if src.dtype == np.uint16:
+        return _load().oracle_grad_norm_sq_bf16(_ptr(src), n_src, n, n, d)
+    src = _f32(src)
+    return _load().oracle_grad_norm_sq_f32(_ptr(src), n_src, n, n, d)
+
+
+def clip_coef(norm_sq: float, max_norm: float) -> np.float32:
+    return np.float32(_load().oracle_clip_coef(float(norm_sq), float(np.float32(max_norm))))
+
+
+def scale(g, coef) -> np.ndarray:
+    g = _f32(g).copy()
+    _load().oracle_scale(_ptr(g), g.size, float(np.float32(coef)))
+    return g
+
+
+def rs_adamw_reference(src, divisor, w, m, v, hp: AdamW, t: int, clip=None):
+    """Mean of source rows, (optionally) the clip scale, then AdamW, then cast:
+    the per-element definition of one fused update call.  clip = (norm_sq,
+    max_norm) with norm_sq the squared norm of the whole step's mean gradient.
+    Returns (out_bf16, w, m, v)."""
     g = reduce_mean(src, divisor)
+    if clip is not None:
+        g = scale(g, clip_coef(*clip))
     w2, m2, v2 = adamw(w, m, v, g, hp, t)
     return cast_bf16(w2), w2, m2, v2

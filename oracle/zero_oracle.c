@@ -290,3 +290,53 @@ void oracle_all_gather_bf16(const uint16_t* shards, int32_t n_dp, int64_t shard,
         for (int64_t i = 0; i < shard; ++i)
             full[(int64_t)o * shard + i] = shards[(int64_t)o * shard + i];
 }
+
+/* ------------------------------------------------------------------------ */
+/* Clipping by the global gradient norm                                     */
+/* ------------------------------------------------------------------------ */
+
+/* The configurations of "DeepSpeed ZeRO" ("The configuration file") and "ZeRO
+ * Optimizer, in depth" ("Running it with DeepSpeed") set gradient_clipping to
+ * 1.0: the gradient is scaled so that its global L2 norm does not exceed it.
+ * Reading taken (the pages give no formula): the global norm is the L2 norm of
+ * the mean gradient over all elements, ||g|| = sqrt(sum g_i^2); the scale is
+ * min(1, max_norm / (||g|| + 1e-6)), applied as one fp32 multiply.  Squares
+ * and their sum are taken in fp64 (each square of an fp32 value is exact);
+ * the quotient is taken in fp64 and rounded once to fp32. */
+
+double oracle_grad_norm_sq_bf16(const uint16_t* src, int32_t n_src, int64_t ld, int64_t n,
+                                float divisor)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = 0.0f;
+        for (int32_t r = 0; r < n_src; ++r) s = s + oracle_bf16_to_f32(src[(int64_t)r * ld + i]);
+        double g = (double)(s / divisor);
+        sum = sum + g * g;
+    }
+    return sum;
+}
+
+double oracle_grad_norm_sq_f32(const float* src, int32_t n_src, int64_t ld, int64_t n,
+                               float divisor)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = 0.0f;
+        for (int32_t r = 0; r < n_src; ++r) s = s + src[(int64_t)r * ld + i];
+        double g = (double)(s / divisor);
+        sum = sum + g * g;
+    }
+    return sum;
+}
+
+float oracle_clip_coef(double norm_sq, float max_norm)
+{
+    float c = (float)((double)max_norm / (sqrt(norm_sq) + 1e-6));
+    return c < 1.0f ? c : 1.0f;
+}
+
+void oracle_scale(float* g, int64_t n, float coef)
+{
+    for (int64_t i = 0; i < n; ++i) g[i] = g[i] * coef;
+}
