@@ -147,6 +147,48 @@ int zero_reduce_scatter_adamw(const zero_layout_t* L,
                               uint16_t* out_bf16, int32_t out_mode,
                               const zero_adamw_t* hp, void* stream);
 
+/* ---- clipping by the global gradient norm --------------------------------
+ * "DeepSpeed ZeRO", "The configuration file" and "ZeRO Optimizer, in depth",
+ * "Running it with DeepSpeed": gradient_clipping 1.0 -- the mean gradient is
+ * scaled so that its global L2 norm does not exceed max_norm.
+ *
+ * zero_grad_norm_sq: for every flat i in [begin, end) forms the mean gradient
+ *   g_i exactly as zero_reduce_scatter_adamw does (same sources, base, divisor)
+ *   and adds g_i^2 (exact in fp64) into an fp64 sum; *norm_sq (DEVICE pointer,
+ *   8-byte aligned) receives the sum (accumulate = 0) or has it added
+ *   (accumulate = 1, for the second and later buckets of one step).  Nothing
+ *   is returned to the host.  The summation order is fixed for a given GPU and
+ *   range, so results repeat run to run; against a sequential fp64 sum they
+ *   differ only by fp64 rounding.
+ *   workspace: DEVICE scratch of at least zero_grad_norm_workspace() bytes,
+ *   8-byte aligned, owned by the caller; its contents on entry do not matter and
+ *   are overwritten (per-CTA partial sums).  Calls that share a workspace must
+ *   not overlap on the GPU (use one stream, or one workspace per stream).
+ *   [begin, end) inside [0, P); src_base <= begin.
+ *   Errors: ZERO_EINVAL, ZERO_ERANGE (workspace too small, n_src too large),
+ *   ZERO_EALIGN, ZERO_ECUDA. */
+int zero_grad_norm_workspace(int64_t* bytes);
+int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_src,
+                      int32_t src_dtype, int64_t src_base, float divisor, int64_t begin,
+                      int64_t end, void* workspace, int64_t workspace_bytes, double* norm_sq,
+                      int32_t accumulate, void* stream);
+
+/* zero_reduce_scatter_adamw_clip: zero_reduce_scatter_adamw with the mean
+ * gradient multiplied, before the update, by
+ *   coef = min(1, fp32(max_norm / (sqrt(*norm_sq) + 1e-6)))
+ * (the quotient in fp64, rounded once to fp32; the multiply in fp32).
+ * norm_sq is a DEVICE pointer, normally written by zero_grad_norm_sq over the
+ * whole step's gradient before the first update launch; max_norm > 0. */
+int zero_reduce_scatter_adamw_clip(const zero_layout_t* L,
+                                   const void* const* src, int32_t n_src, int32_t src_dtype,
+                                   int64_t src_base, float divisor,
+                                   int32_t rank_begin, int32_t rank_end,
+                                   int64_t begin, int64_t end,
+                                   float* master, float* m, float* v,
+                                   uint16_t* out_bf16, int32_t out_mode,
+                                   const zero_adamw_t* hp, const double* norm_sq, float max_norm,
+                                   void* stream);
+
 /* ---- stage-3 gather ------------------------------------------------------
  * "DeepSpeed ZeRO", "Stage 3 step by step" and "ZeRO and FSDP", "FSDP, ZeRO-3
  * inside PyTorch": before a unit (layer) runs, its weights are all-gathered
@@ -180,6 +222,27 @@ int zero_accumulate(const zero_layout_t* L, int32_t mode,
                     const void* const* src, int32_t n_src, int32_t src_dtype, int64_t src_base,
                     float* dst, int64_t dst_base, int64_t begin, int64_t end,
                     int32_t first, void* stream);
+
+/* ---- the last micro-batch of an accumulation window, fused with the update --
+ * The same sums as zero_accumulate on the last micro-batch followed by
+ * zero_reduce_scatter_adamw over the fp32 buffers, in the same order (so
+ * bit-identical to that sequence), without writing and re-reading the fp32
+ * buffers.  For every flat i in [begin, end):
+ *   ZERO_ACC_LOCAL  (stage 1; n_acc == n_grads == number of ranks):
+ *       g = (sum over r of (acc[r][i - acc_base] + grads[r][i - grad_base])) / divisor
+ *   ZERO_ACC_REDUCE (stage 2; n_acc == 1):
+ *       g = (acc[0][i - acc_base] + sum over r of grads[r][i - grad_base]) / divisor
+ * (sums in fp32, ranks ascending from +0.0f), then the AdamW update, cast and
+ * output exactly as zero_reduce_scatter_adamw.  acc (fp32) and grads (bf16) are
+ * host arrays of device pointers, read only.  divisor is n_dp * K for K
+ * micro-batches.  Errors as zero_reduce_scatter_adamw. */
+int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,
+                          const float* const* acc, int32_t n_acc, int64_t acc_base,
+                          const uint16_t* const* grads, int32_t n_grads, int64_t grad_base,
+                          float divisor, int32_t rank_begin, int32_t rank_end,
+                          int64_t begin, int64_t end, float* master, float* m, float* v,
+                          uint16_t* out_bf16, int32_t out_mode, const zero_adamw_t* hp,
+                          void* stream);
 
 /* ---- status ---------------------------------------------------------------
  * Synchronizes `stream` and returns ZERO_ECUDA if it (or an earlier launch on

@@ -227,3 +227,47 @@ def test_llama7b_zero3_units(zlib, cuda_device):
         assert ring.peak <= 2
         del unit, w, shards
     assert ring.resident == 0
+
+
+def test_gpt2xl_clipped_step(zlib, cuda_device):
+    """GPT-2-XL shapes, n_dp = 8, 5e8-element buckets, clipping at 1.0 with
+    gradients large enough that it is active.  The full-size norm is checked
+    against torch (fp32 sums in rank order, an fp64 sum of squares on the
+    device); updates are checked on sampled elements with the oracle, using
+    the clip coefficient the oracle derives from that norm."""
+    zb = zlib
+    dev = cuda_device
+    L = zb.zero_layout(inputs.gpt2xl_numels(), 8, 8, 500_000_000)
+    P = L.padded_n
+    g = torch.empty((8, P), dtype=torch.bfloat16, device=dev)
+    for r in range(8):
+        inputs.grad_bf16_into(g[r], L.n, SEED, step=1, rank=r, std=1e-4)
+    master = inputs.master_weights(L.n, P, seed=SEED, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    bounds = [b * L.bucket for b in range(1, L.n_buckets)] + [o * L.shard for o in range(1, 8)]
+    idx = _sample_indices(0, P, bounds, seed=3)
+    idx_dev = torch.from_numpy(idx).to(dev)
+    ws = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
+    gs = np.stack([_bits_at(g[r], idx_dev) for r in range(8)])
+    bufs = zstep.NormBuffers(dev)
+    zstep.zero12_step_clipped(L, [g[r] for r in range(8)], master, m, v, out, _hp(zb, 1), 1.0, bufs)
+    zb.zero_status_check()
+    gpu_nsq = float(bufs.norm_sq.item())
+    # the norm over all 1.56e9 elements, by torch on the device
+    ref_nsq = 0.0
+    for lo in range(0, P, 1 << 28):
+        hi = min(P, lo + (1 << 28))
+        s = torch.zeros(hi - lo, dtype=torch.float32, device=dev)
+        for r in range(8):
+            s = s + g[r, lo:hi].float()
+        gm = s / 8.0
+        ref_nsq += float((gm.double() * gm.double()).sum().item())
+    assert gpu_nsq == pytest.approx(ref_nsq, rel=1e-10)
+    coef = oracle.clip_coef(gpu_nsq, 1.0)
+    assert coef < 1.0
+    ref_out, *ref = oracle.rs_adamw_reference(gs, 8, *ws, HP, 1, clip=(gpu_nsq, 1.0))
+    parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref)
+    assert np.array_equal(_bits_at(out, idx_dev), ref_out)
+    _full_properties(master, out, L.n)

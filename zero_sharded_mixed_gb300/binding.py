@@ -75,6 +75,15 @@ def load():
         lib.zero_reduce_scatter_adamw.argtypes = [
             P(ZeroLayout), P(p), i32, i32, i64, f32, i32, i32, i64, i64,
             p, p, p, p, i32, P(ZeroAdamW), p]
+        lib.zero_reduce_scatter_adamw_clip.argtypes = [
+            P(ZeroLayout), P(p), i32, i32, i64, f32, i32, i32, i64, i64,
+            p, p, p, p, i32, P(ZeroAdamW), p, f32, p]
+        lib.zero_accumulate_adamw.argtypes = [
+            P(ZeroLayout), i32, P(p), i32, i64, P(p), i32, i64, f32, i32, i32, i64, i64,
+            p, p, p, p, i32, P(ZeroAdamW), p]
+        lib.zero_grad_norm_workspace.argtypes = [P(i64)]
+        lib.zero_grad_norm_sq.argtypes = [P(ZeroLayout), P(p), i32, i32, i64, f32, i64, i64,
+                                          p, i64, p, i32, p]
         lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
         lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
                                         i32, p]
@@ -86,7 +95,9 @@ def load():
         lib.zero_comm_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
                                         ctypes.c_double, P(ctypes.c_double)]
         for name in ("zero_layout", "zero_bucket_range", "zero_shard_range",
-                     "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate",
+                     "zero_reduce_scatter_adamw", "zero_reduce_scatter_adamw_clip",
+                     "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
+                     "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -203,6 +214,85 @@ def zero_reduce_scatter_adamw(L: ZeroLayout, srcs, src_dtype: int, src_base: int
         _tensor(out, "out", torch.bfloat16, out_need),
         int(out_mode), ctypes.byref(hp), _stream_ptr(stream))
     _check(rc, "zero_reduce_scatter_adamw")
+
+
+def zero_reduce_scatter_adamw_clip(L: ZeroLayout, srcs, src_dtype: int, src_base: int,
+                                   divisor: float, rank_begin: int, rank_end: int, begin: int,
+                                   end: int, master: torch.Tensor, m: torch.Tensor,
+                                   v: torch.Tensor, out: torch.Tensor, out_mode: int,
+                                   hp: ZeroAdamW, norm_sq: torch.Tensor, max_norm: float,
+                                   stream=None):
+    """zero_reduce_scatter_adamw with the mean gradient scaled by
+    min(1, max_norm / (sqrt(norm_sq) + 1e-6)); norm_sq is a 1-element fp64 CUDA tensor."""
+    if end <= begin:
+        src_need = state_need = out_need = 0
+    else:
+        src_need = end - src_base
+        state_need = end - rank_begin * L.shard
+        out_need = end if out_mode == ZERO_OUT_FULL else state_need
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    rc = load().zero_reduce_scatter_adamw_clip(
+        ctypes.byref(L), arr, n, int(src_dtype), int(src_base), float(divisor),
+        int(rank_begin), int(rank_end), int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(out, "out", torch.bfloat16, out_need),
+        int(out_mode), ctypes.byref(hp), _tensor(norm_sq, "norm_sq", torch.float64, 1),
+        float(max_norm), _stream_ptr(stream))
+    _check(rc, "zero_reduce_scatter_adamw_clip")
+
+
+def zero_accumulate_adamw(L: ZeroLayout, mode: int, acc, acc_base: int, grads, grad_base: int,
+                          divisor: float, rank_begin: int, rank_end: int, begin: int, end: int,
+                          master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                          out: torch.Tensor, out_mode: int, hp: ZeroAdamW, stream=None):
+    """The last micro-batch of an accumulation window fused with the update
+    (LOCAL: sum_r (acc[r] + grads[r]); REDUCE: acc[0] + sum_r grads[r])."""
+    if end <= begin:
+        acc_need = grad_need = state_need = out_need = 0
+    else:
+        acc_need, grad_need = end - acc_base, end - grad_base
+        state_need = end - rank_begin * L.shard
+        out_need = end if out_mode == ZERO_OUT_FULL else state_need
+    if len(acc) == 0 or len(grads) == 0:
+        raise ValueError("need accumulators and gradients")
+    acc_p = [_tensor(a, f"acc[{i}]", torch.float32, acc_need) for i, a in enumerate(acc)]
+    g_p = [_tensor(g, f"grads[{i}]", torch.bfloat16, grad_need) for i, g in enumerate(grads)]
+    rc = load().zero_accumulate_adamw(
+        ctypes.byref(L), int(mode), (ctypes.c_void_p * len(acc_p))(*acc_p), len(acc_p), int(acc_base),
+        (ctypes.c_void_p * len(g_p))(*g_p), len(g_p), int(grad_base), float(divisor),
+        int(rank_begin), int(rank_end), int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(out, "out", torch.bfloat16, out_need),
+        int(out_mode), ctypes.byref(hp), _stream_ptr(stream))
+    _check(rc, "zero_accumulate_adamw")
+
+
+def zero_grad_norm_workspace() -> int:
+    """Bytes of device workspace zero_grad_norm_sq needs on the current device."""
+    out = ctypes.c_int64()
+    _check(load().zero_grad_norm_workspace(ctypes.byref(out)), "zero_grad_norm_workspace")
+    return out.value
+
+
+def zero_grad_norm_sq(L: ZeroLayout, srcs, src_dtype: int, src_base: int, divisor: float,
+                      begin: int, end: int, workspace: torch.Tensor, norm_sq: torch.Tensor,
+                      accumulate: bool, stream=None):
+    """norm_sq (1-element fp64 CUDA tensor) (+)= sum over [begin, end) of the
+    squared mean gradient; workspace: a CUDA tensor of zero_grad_norm_workspace() bytes."""
+    src_need = max(0, end - src_base) if end > begin else 0
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = load().zero_grad_norm_sq(ctypes.byref(L), arr, n, int(src_dtype), int(src_base),
+                                  float(divisor), int(begin), int(end), workspace.data_ptr(),
+                                  int(ws_bytes), _tensor(norm_sq, "norm_sq", torch.float64, 1),
+                                  int(bool(accumulate)), _stream_ptr(stream))
+    _check(rc, "zero_grad_norm_sq")
 
 
 def zero_gather_layer(unit: ZeroLayout, shards, full_out: torch.Tensor, stream=None):

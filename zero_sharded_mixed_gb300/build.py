@@ -22,9 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "zero_gb300")
 LIB = os.path.join(PKG, "libzero_gb300.so")
 
-CUDA_SOURCES = ["zero_runtime.cu", "zero_rs_adamw.cu", "zero_accumulate.cu", "zero_gather.cu"]
+CUDA_SOURCES = ["zero_runtime.cu", "zero_rs_adamw.cu", "zero_accumulate.cu", "zero_gather.cu",
+                "zero_norm.cu"]
 HOST_SOURCES = ["zero_host.cpp"]
-HEADERS = ["zero_common.cuh"]
+HEADERS = ["zero_common.cuh", "zero_update.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code: no FMA contraction either (the bias corrections are formed on the host).

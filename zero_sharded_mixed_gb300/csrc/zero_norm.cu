@@ -1,0 +1,206 @@
+// Squared global norm of the mean gradient, for clipping by the global norm
+// ("DeepSpeed ZeRO", "The configuration file" and "ZeRO Optimizer, in depth",
+// "Running it with DeepSpeed": gradient_clipping 1.0), sm_103a.
+//
+// For every flat i in [begin, end) the mean gradient g_i is formed exactly as
+// the fused update forms it (fp32 sum over sources in ascending order from
+// +0.0f, one IEEE division), and g_i^2 -- exact in fp64 -- is added to an fp64
+// sum.  Pass 1 (one streaming kernel, 2 bytes per bf16 source per element):
+// each thread sums its elements in order, each CTA reduces its threads in a
+// fixed tree and writes one fp64 partial into the caller's workspace.  Pass 2
+// (one CTA): the partials are summed in a fixed tree and the total is written
+// to (or added to) *norm_sq in device memory, where the clipped update reads
+// it -- nothing returns to the host.  For a given GPU and range the grid, and
+// so the summation order, is fixed: results are reproducible run to run.
+#include "zero_common.cuh"
+
+namespace zgb {
+
+constexpr int kMaxCtasPerSm = 2048 / kThreads;   // upper bound on resident CTAs of kThreads
+
+struct NormParams {
+    const void* src[ZERO_MAX_SRC];  // offset to the first element of the range
+    int64_t n;
+    int32_t n_src;
+    float divisor;
+    double* partials;               // one per CTA
+};
+
+template <bool kBf16>
+__device__ __forceinline__ float mean_at(const NormParams& p, int64_t i) {
+    float s = 0.0f;
+    for (int r = 0; r < p.n_src; ++r)
+        s = __fadd_rn(s, kBf16 ? bf16_one(static_cast<const uint16_t*>(p.src[r])[i])
+                               : static_cast<const float*>(p.src[r])[i]);
+    return __fdiv_rn(s, p.divisor);
+}
+
+// Fixed-order CTA reduction of one fp64 value per thread; thread 0 gets the total.
+__device__ __forceinline__ double cta_sum(double x) {
+    __shared__ double warp_sums[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_down_sync(0xffffffffu, x, off);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) warp_sums[warp] = x;
+    __syncthreads();
+    double t = 0.0;
+    if (warp == 0) {
+        t = lane < kThreads / 32 ? warp_sums[lane] : 0.0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xffffffffu, t, off);
+    }
+    return t;
+}
+
+template <bool kBf16, int R>
+__global__ void __launch_bounds__(kThreads) norm_partial_kernel(const __grid_constant__ NormParams p) {
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    double acc = 0.0;
+    if constexpr (R > 0) {
+        const int64_t nv = p.n >> 3;
+        for (int64_t vi = tid; vi < nv; vi += stride) {
+            const int64_t e = vi * 8;
+            float s[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[j] = 0.0f;
+            if constexpr (kBf16) {
+                uint4 raw[R > 0 ? R : 1];
+#pragma unroll
+                for (int r = 0; r < R; ++r) raw[r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w4[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        s[2 * k] = __fadd_rn(s[2 * k], bf16_lo(w4[k]));
+                        s[2 * k + 1] = __fadd_rn(s[2 * k + 1], bf16_hi(w4[k]));
+                    }
+                }
+            } else {
+                float4 lo[R > 0 ? R : 1], hi[R > 0 ? R : 1];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    lo[r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
+                    hi[r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    s[0] = __fadd_rn(s[0], lo[r].x); s[1] = __fadd_rn(s[1], lo[r].y);
+                    s[2] = __fadd_rn(s[2], lo[r].z); s[3] = __fadd_rn(s[3], lo[r].w);
+                    s[4] = __fadd_rn(s[4], hi[r].x); s[5] = __fadd_rn(s[5], hi[r].y);
+                    s[6] = __fadd_rn(s[6], hi[r].z); s[7] = __fadd_rn(s[7], hi[r].w);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const double g = (double)__fdiv_rn(s[j], p.divisor);
+                acc = __dadd_rn(acc, __dmul_rn(g, g));
+            }
+        }
+        const int64_t tail = p.n - (nv << 3);
+        if (tid < tail) {
+            const double g = (double)mean_at<kBf16>(p, (nv << 3) + tid);
+            acc = __dadd_rn(acc, __dmul_rn(g, g));
+        }
+    } else {
+        for (int64_t i = tid; i < p.n; i += stride) {
+            const double g = (double)mean_at<kBf16>(p, i);
+            acc = __dadd_rn(acc, __dmul_rn(g, g));
+        }
+    }
+    const double total = cta_sum(acc);
+    if (threadIdx.x == 0) p.partials[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kThreads)
+norm_finalize_kernel(const double* partials, int n_partials, double* norm_sq, int accumulate) {
+    double acc = 0.0;
+    for (int i = threadIdx.x; i < n_partials; i += kThreads) acc = __dadd_rn(acc, partials[i]);
+    const double total = cta_sum(acc);
+    if (threadIdx.x == 0) *norm_sq = accumulate ? __dadd_rn(*norm_sq, total) : total;
+}
+
+// CTAs the partial kernel may launch on this device (one partial each).
+int64_t norm_partials_capacity() { return (int64_t)sm_count() * kMaxCtasPerSm; }
+
+template <bool kBf16, int R>
+int launch_norm(const NormParams& p, bool vec, double* norm_sq, int accumulate, cudaStream_t s) {
+    static int occupancy = 0;
+    if (occupancy == 0) occupancy = ctas_per_sm((const void*)norm_partial_kernel<kBf16, R>, kThreads, 0);
+    const int64_t resident = (int64_t)sm_count() * (occupancy < kMaxCtasPerSm ? occupancy : kMaxCtasPerSm);
+    const unsigned grid = grid_for(vec ? (p.n >> 3) : p.n, kThreads, resident);
+    norm_partial_kernel<kBf16, R><<<grid, kThreads, 0, s>>>(p);
+    int rc = launch_status();
+    if (rc) return rc;
+    norm_finalize_kernel<<<1, kThreads, 0, s>>>(p.partials, (int)grid, norm_sq, accumulate);
+    return launch_status();
+}
+
+template <bool kBf16>
+int dispatch_norm(const NormParams& p, bool vec, double* norm_sq, int accumulate, cudaStream_t s) {
+    if (!vec) return launch_norm<kBf16, 0>(p, false, norm_sq, accumulate, s);
+    switch (p.n_src) {
+        case 1: return launch_norm<kBf16, 1>(p, true, norm_sq, accumulate, s);
+        case 2: return launch_norm<kBf16, 2>(p, true, norm_sq, accumulate, s);
+        case 4: return launch_norm<kBf16, 4>(p, true, norm_sq, accumulate, s);
+        case 8: return launch_norm<kBf16, 8>(p, true, norm_sq, accumulate, s);
+        default: return launch_norm<kBf16, 0>(p, false, norm_sq, accumulate, s);
+    }
+}
+
+// The body of zero_grad_norm_sq: argument checks, then the two launches.
+int grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_src, int32_t src_dtype,
+                 int64_t src_base, float divisor, int64_t begin, int64_t end, double* partials,
+                 int64_t partials_len, double* norm_sq, int32_t accumulate, void* stream) {
+    if (!L || !src || !norm_sq) return ZERO_EINVAL;
+    if (n_src < 1) return ZERO_EINVAL;
+    if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
+    if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
+    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
+    if (begin < 0 || end > L->padded_n || begin > end || src_base > begin) return ZERO_EINVAL;
+    if (!(divisor > 0.0f) || !(divisor < 3.4e38f)) return ZERO_EINVAL;
+    for (int r = 0; r < n_src; ++r)
+        if (!src[r]) return ZERO_EINVAL;
+    const int esize = src_dtype == ZERO_BF16 ? 2 : 4;
+    for (int r = 0; r < n_src; ++r)
+        if (check_aligned(src[r], esize)) return ZERO_EALIGN;
+    if (check_aligned(norm_sq, 8) || check_aligned(partials, 8)) return ZERO_EALIGN;
+    for (int r = 0; r < n_src; ++r)
+        if (check_device_ptr(src[r])) return ZERO_EINVAL;
+    if (check_device_ptr(norm_sq)) return ZERO_EINVAL;
+    if (!partials || partials_len < norm_partials_capacity()) return ZERO_ERANGE;
+    if (check_device_ptr(partials)) return ZERO_EINVAL;
+    NormParams p;
+    bool vec = true;
+    for (int r = 0; r < ZERO_MAX_SRC; ++r) p.src[r] = nullptr;
+    for (int r = 0; r < n_src; ++r) {
+        p.src[r] = static_cast<const char*>(src[r]) + (begin - src_base) * esize;
+        vec = vec && aligned16(p.src[r]);
+    }
+    p.n = end - begin;
+    p.n_src = n_src;
+    p.divisor = divisor;
+    p.partials = partials;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return src_dtype == ZERO_BF16 ? dispatch_norm<true>(p, vec, norm_sq, accumulate ? 1 : 0, s)
+                                  : dispatch_norm<false>(p, vec, norm_sq, accumulate ? 1 : 0, s);
+}
+
+}  // namespace zgb
+
+extern "C" int zero_grad_norm_workspace(int64_t* bytes) {
+    if (!bytes) return ZERO_EINVAL;
+    *bytes = zgb::norm_partials_capacity() * (int64_t)sizeof(double);
+    return ZERO_OK;
+}
+
+extern "C" int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_src,
+                                 int32_t src_dtype, int64_t src_base, float divisor, int64_t begin,
+                                 int64_t end, void* workspace, int64_t workspace_bytes,
+                                 double* norm_sq, int32_t accumulate, void* stream) {
+    using namespace zgb;
+    return grad_norm_sq(L, src, n_src, src_dtype, src_base, divisor, begin, end,
+                        static_cast<double*>(workspace), workspace_bytes / (int64_t)sizeof(double),
+                        norm_sq, accumulate, stream);
+}

@@ -10,22 +10,31 @@
 // are read once, its 12 bytes of fp32 state are read and written once and its
 // bf16 weight is written once, (26 + 2*n_src) bytes for bf16 sources.
 //
+// The same kernel template serves four kinds of gradient source:
+//   kPlainBf16 / kPlainF32  sum over n_src buffers (bf16 gradients, or fp32
+//                           accumulators after gradient accumulation);
+//   kAccLocal               the last micro-batch of stage-1 accumulation fused
+//                           in: sum over ranks of (acc_r + g_r);
+//   kAccReduce              the last micro-batch of stage-2 accumulation fused
+//                           in: A + (sum over ranks of g_r).
+// Both fused kinds perform exactly the additions of the unfused sequence
+// (zero_accumulate, then the update), in the same order, so their results are
+// bit-identical to it while skipping one fp32 write and re-read per element.
+//
 // Design: a bandwidth-bound stream.  Each thread owns 8 consecutive elements
-// per iteration: one 128-bit load per bf16 source slice, two per fp32 state
-// array, the same stores, and one 128-bit bf16 store; all loads of an iteration
-// are issued before any arithmetic, so a warp keeps (2*n_src + 6) x 512 bytes
-// in flight.  Loads and stores are evict-first (each byte is touched once).
-// A grid-stride loop over 8-element vectors, with the grid sized to the CTAs
-// that are resident at once, keeps the tail to at most one partial wave.
+// per vector: one 128-bit load per bf16 source, two per fp32 array, the same
+// stores, and one 128-bit bf16 store.  All loads of an iteration are issued
+// before any arithmetic; when a vector has few loads, a thread takes two
+// vectors per iteration.  Loads and stores are evict-first.  A grid-stride loop
+// with the grid sized to the CTAs resident at once.
 //
 // Arithmetic: every fp32 operation is an explicit IEEE round-to-nearest
-// intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so nothing is fused
-// into an FMA and the result is reproducible: the sum runs over ranks in
-// ascending order from +0.0f, divides once, and the AdamW operations run in the
-// order written in the header.
+// intrinsic, so nothing is fused into an FMA: the sum runs over ranks in
+// ascending order from +0.0f, divides once, and the AdamW operations run in
+// the order written in the header (zero_update.cuh).
 #include <cmath>
 
-#include "zero_common.cuh"
+#include "zero_update.cuh"
 
 #ifndef ZGB_RS_WAVES
 #define ZGB_RS_WAVES 1       // grid = resident CTAs x this (grid-stride loop inside)
@@ -39,33 +48,19 @@
 
 namespace zgb {
 
-struct RsAdamwParams {
-    const void* src[ZERO_MAX_SRC];  // already offset to the first element of the range
+enum SrcKind { kPlainBf16 = 0, kPlainF32 = 1, kAccLocal = 2, kAccReduce = 3 };
+
+struct UpdateParams {
+    const void* src[ZERO_MAX_SRC];  // gradient sources (bf16 or fp32), offset to the range start
+    const float* acc[ZERO_MAX_SRC]; // fp32 accumulators of the fused kinds, offset likewise
     float* w;
     float* m;
     float* v;
     uint16_t* out;
     int64_t n;                      // elements in the range
-    int32_t n_src;
-    float divisor;
-    float b1, b2, omb1, omb2;       // beta1, beta2, 1-beta1, 1-beta2 (fp32)
-    float bc1, bc2;                 // bias corrections 1-beta^t (fp64 -> fp32)
-    float lr, lrwd, eps;            // lr, lr*wd (fp32), eps
+    int32_t n_src;                  // gradient sources (ranks)
+    AdamwScalars h;
 };
-
-__device__ __forceinline__ void adamw_update(float g, float& w, float& m, float& v,
-                                             const RsAdamwParams& p) {
-    const float mi = __fadd_rn(__fmul_rn(p.b1, m), __fmul_rn(p.omb1, g));
-    const float vi = __fadd_rn(__fmul_rn(p.b2, v), __fmul_rn(p.omb2, __fmul_rn(g, g)));
-    const float m_hat = __fdiv_rn(mi, p.bc1);
-    const float v_hat = __fdiv_rn(vi, p.bc2);
-    float wi = __fsub_rn(w, __fmul_rn(p.lrwd, w));                       // decoupled decay
-    const float denom = __fadd_rn(__fsqrt_rn(v_hat), p.eps);
-    wi = __fsub_rn(wi, __fmul_rn(p.lr, __fdiv_rn(m_hat, denom)));         // Adam step
-    w = wi;
-    m = mi;
-    v = vi;
-}
 
 __device__ __forceinline__ void add_bf16x8(float (&s)[8], const uint4 x) {
     s[0] = __fadd_rn(s[0], bf16_lo(x.x));
@@ -89,50 +84,108 @@ __device__ __forceinline__ void add_f32x8(float (&s)[8], const float4 a, const f
     s[7] = __fadd_rn(s[7], b.w);
 }
 
-// One 8-element vector.  NDP > 0: that many sources, fully unrolled so every
-// load is in flight before the first add; NDP == 0: p.n_src sources in a loop.
-template <int NDP, bool kBf16>
-__device__ __forceinline__ void step_vec(const RsAdamwParams& p, int64_t vi) {
-    const int64_t e = vi * 8;
-    float s[8];
+// acc (8 fp32) + g (8 bf16), elementwise, into x
+__device__ __forceinline__ void acc_plus_bf16x8(float (&x)[8], const float4 a, const float4 b,
+                                                const uint4 g) {
+    x[0] = __fadd_rn(a.x, bf16_lo(g.x));
+    x[1] = __fadd_rn(a.y, bf16_hi(g.x));
+    x[2] = __fadd_rn(a.z, bf16_lo(g.y));
+    x[3] = __fadd_rn(a.w, bf16_hi(g.y));
+    x[4] = __fadd_rn(b.x, bf16_lo(g.z));
+    x[5] = __fadd_rn(b.y, bf16_hi(g.z));
+    x[6] = __fadd_rn(b.z, bf16_lo(g.w));
+    x[7] = __fadd_rn(b.w, bf16_hi(g.w));
+}
+
+// Registers holding one vector's gradient-source loads.  R = compile-time
+// source count (> 0).
+template <int KIND, int R>
+struct SrcRegs {
+    uint4 g[(KIND == kPlainF32) ? 1 : R];                      // bf16 gradients
+    float4 f[(KIND == kPlainF32 || KIND == kAccLocal) ? 2 * R  // fp32 sources / accumulators
+             : (KIND == kAccReduce ? 2 : 1)];
+};
+
+template <int KIND, int R>
+__device__ __forceinline__ void load_src(const UpdateParams& p, int64_t e, SrcRegs<KIND, R>& s) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j] = 0.0f;
-    if constexpr (NDP > 0) {
-        if constexpr (kBf16) {
-            uint4 raw[NDP];
-#pragma unroll
-            for (int r = 0; r < NDP; ++r)
-                raw[r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
-#pragma unroll
-            for (int r = 0; r < NDP; ++r) add_bf16x8(s, raw[r]);
-        } else {
-            float4 lo[NDP], hi[NDP];
-#pragma unroll
-            for (int r = 0; r < NDP; ++r) {
-                lo[r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
-                hi[r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
-            }
-#pragma unroll
-            for (int r = 0; r < NDP; ++r) add_f32x8(s, lo[r], hi[r]);
+    for (int r = 0; r < R; ++r) {
+        if constexpr (KIND != kPlainF32)
+            s.g[r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
+        if constexpr (KIND == kPlainF32) {
+            s.f[2 * r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
+            s.f[2 * r + 1] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
         }
-    } else {
-        for (int r = 0; r < p.n_src; ++r) {
-            if constexpr (kBf16) {
-                add_bf16x8(s, ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e));
-            } else {
-                const float* q = static_cast<const float*>(p.src[r]) + e;
-                add_f32x8(s, ld_stream_f4(q), ld_stream_f4(q + 4));
-            }
+        if constexpr (KIND == kAccLocal) {
+            s.f[2 * r] = ld_stream_f4(p.acc[r] + e);
+            s.f[2 * r + 1] = ld_stream_f4(p.acc[r] + e + 4);
         }
     }
-    const float4 w0 = ld_stream_f4(p.w + e), w1 = ld_stream_f4(p.w + e + 4);
-    const float4 m0 = ld_stream_f4(p.m + e), m1 = ld_stream_f4(p.m + e + 4);
-    const float4 v0 = ld_stream_f4(p.v + e), v1 = ld_stream_f4(p.v + e + 4);
-    float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    if constexpr (KIND == kAccReduce) {
+        s.f[0] = ld_stream_f4(p.acc[0] + e);
+        s.f[1] = ld_stream_f4(p.acc[0] + e + 4);
+    }
+}
+
+// The source sum of one vector, in the order of the unfused definition.
+template <int KIND, int R>
+__device__ __forceinline__ void sum_src(const SrcRegs<KIND, R>& s, float (&x)[8]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_update(__fdiv_rn(s[j], p.divisor), w[j], m[j], v[j], p);
+    for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if constexpr (KIND == kPlainBf16 || KIND == kAccReduce) add_bf16x8(x, s.g[r]);
+        if constexpr (KIND == kPlainF32) add_f32x8(x, s.f[2 * r], s.f[2 * r + 1]);
+        if constexpr (KIND == kAccLocal) {
+            float a[8];
+            acc_plus_bf16x8(a, s.f[2 * r], s.f[2 * r + 1], s.g[r]);    // the rank's final acc
+            add_f32x8(x, make_float4(a[0], a[1], a[2], a[3]), make_float4(a[4], a[5], a[6], a[7]));
+        }
+    }
+    if constexpr (KIND == kAccReduce) {                                  // A + (sum over ranks)
+        const float4 a = s.f[0], b = s.f[1];
+        x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]);
+        x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
+        x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]);
+        x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
+    }
+}
+
+// The same source sum with a runtime source count, loads one source at a time.
+template <int KIND>
+__device__ __forceinline__ void sum_src_dyn(const UpdateParams& p, int64_t e, float (&x)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    for (int r = 0; r < p.n_src; ++r) {
+        if constexpr (KIND == kPlainBf16 || KIND == kAccReduce) {
+            add_bf16x8(x, ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e));
+        } else if constexpr (KIND == kPlainF32) {
+            const float* q = static_cast<const float*>(p.src[r]) + e;
+            add_f32x8(x, ld_stream_f4(q), ld_stream_f4(q + 4));
+        } else {
+            float a[8];
+            acc_plus_bf16x8(a, ld_stream_f4(p.acc[r] + e), ld_stream_f4(p.acc[r] + e + 4),
+                            ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e));
+            add_f32x8(x, make_float4(a[0], a[1], a[2], a[3]), make_float4(a[4], a[5], a[6], a[7]));
+        }
+    }
+    if constexpr (KIND == kAccReduce) {
+        const float4 a = ld_stream_f4(p.acc[0] + e), b = ld_stream_f4(p.acc[0] + e + 4);
+        x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]);
+        x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
+        x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]);
+        x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
+    }
+}
+
+// Update 8 elements at e from their source sums and loaded state; store.
+__device__ __forceinline__ void finish_vec(const UpdateParams& p, int64_t e, const float (&s)[8],
+                                           const float4 (&st)[6], float coef) {
+    float w[8] = {st[0].x, st[0].y, st[0].z, st[0].w, st[1].x, st[1].y, st[1].z, st[1].w};
+    float m[8] = {st[2].x, st[2].y, st[2].z, st[2].w, st[3].x, st[3].y, st[3].z, st[3].w};
+    float v[8] = {st[4].x, st[4].y, st[4].z, st[4].w, st[5].x, st[5].y, st[5].z, st[5].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_update(mean_grad(s[j], p.h, coef), w[j], m[j], v[j], p.h);
     st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
     st_stream_f4(p.w + e + 4, make_float4(w[4], w[5], w[6], w[7]));
     st_stream_f4(p.m + e, make_float4(m[0], m[1], m[2], m[3]));
@@ -147,35 +200,21 @@ __device__ __forceinline__ void step_vec(const RsAdamwParams& p, int64_t vi) {
     st_stream_u4(p.out + e, o);
 }
 
-// One element (ragged tails and pointers that are not 16-byte aligned).
-template <bool kBf16>
-__device__ __forceinline__ void step_one(const RsAdamwParams& p, int64_t i) {
-    float s = 0.0f;
-    for (int r = 0; r < p.n_src; ++r) {
-        const float x = kBf16 ? bf16_one(static_cast<const uint16_t*>(p.src[r])[i])
-                              : static_cast<const float*>(p.src[r])[i];
-        s = __fadd_rn(s, x);
-    }
-    float w = p.w[i], m = p.m[i], v = p.v[i];
-    adamw_update(__fdiv_rn(s, p.divisor), w, m, v, p);
-    p.w[i] = w;
-    p.m[i] = m;
-    p.v[i] = v;
-    p.out[i] = to_bf16(w);
+__device__ __forceinline__ void load_state(const UpdateParams& p, int64_t e, float4 (&st)[6]) {
+    st[0] = ld_stream_f4(p.w + e);
+    st[1] = ld_stream_f4(p.w + e + 4);
+    st[2] = ld_stream_f4(p.m + e);
+    st[3] = ld_stream_f4(p.m + e + 4);
+    st[4] = ld_stream_f4(p.v + e);
+    st[5] = ld_stream_f4(p.v + e + 4);
 }
 
-// U vectors per thread and iteration (vectors vi0, vi0 + stride, ...): every
-// load of all U vectors is issued before the first add, so a thread keeps
-// U * (loads per vector) 128-bit loads in flight.  Used when one vector alone
-// has few loads (one or two sources), where a single vector per thread leaves
-// HBM short of bytes in flight.
-template <int NDP, bool kBf16, int U>
-__device__ __forceinline__ void step_vecs(const RsAdamwParams& p, int64_t vi0, int64_t stride,
-                                          int64_t nv) {
-    static_assert(NDP > 0, "the multi-vector step needs a compile-time source count");
-    constexpr int kRaw = kBf16 ? NDP : 2 * NDP;   // 128-bit source loads per vector
-    uint4 graw[U][kBf16 ? kRaw : 1];
-    float4 fraw[U][kBf16 ? 1 : kRaw];
+// U vectors (vi0, vi0 + stride, ...) with a compile-time source count R:
+// every load of all U vectors is issued before the first add.
+template <int KIND, int R, int U>
+__device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, int64_t stride,
+                                          int64_t nv, float coef) {
+    SrcRegs<KIND, R> src[U];
     float4 st[U][6];
     bool ok[U];
 #pragma unroll
@@ -183,125 +222,241 @@ __device__ __forceinline__ void step_vecs(const RsAdamwParams& p, int64_t vi0, i
         const int64_t vi = vi0 + u * stride;
         ok[u] = vi < nv;
         if (ok[u]) {
-            const int64_t e = vi * 8;
-#pragma unroll
-            for (int r = 0; r < NDP; ++r) {
-                if constexpr (kBf16) {
-                    graw[u][r] = ld_stream_u4(static_cast<const uint16_t*>(p.src[r]) + e);
-                } else {
-                    fraw[u][2 * r] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e);
-                    fraw[u][2 * r + 1] = ld_stream_f4(static_cast<const float*>(p.src[r]) + e + 4);
-                }
-            }
-            st[u][0] = ld_stream_f4(p.w + e);
-            st[u][1] = ld_stream_f4(p.w + e + 4);
-            st[u][2] = ld_stream_f4(p.m + e);
-            st[u][3] = ld_stream_f4(p.m + e + 4);
-            st[u][4] = ld_stream_f4(p.v + e);
-            st[u][5] = ld_stream_f4(p.v + e + 4);
+            load_src<KIND, R>(p, vi * 8, src[u]);
+            load_state(p, vi * 8, st[u]);
         }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         if (!ok[u]) continue;
-        const int64_t e = (vi0 + u * stride) * 8;
         float s[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = 0.0f;
-#pragma unroll
-        for (int r = 0; r < NDP; ++r) {
-            if constexpr (kBf16) add_bf16x8(s, graw[u][r]);
-            else add_f32x8(s, fraw[u][2 * r], fraw[u][2 * r + 1]);
-        }
-        float w[8] = {st[u][0].x, st[u][0].y, st[u][0].z, st[u][0].w,
-                      st[u][1].x, st[u][1].y, st[u][1].z, st[u][1].w};
-        float m[8] = {st[u][2].x, st[u][2].y, st[u][2].z, st[u][2].w,
-                      st[u][3].x, st[u][3].y, st[u][3].z, st[u][3].w};
-        float v[8] = {st[u][4].x, st[u][4].y, st[u][4].z, st[u][4].w,
-                      st[u][5].x, st[u][5].y, st[u][5].z, st[u][5].w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) adamw_update(__fdiv_rn(s[j], p.divisor), w[j], m[j], v[j], p);
-        st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
-        st_stream_f4(p.w + e + 4, make_float4(w[4], w[5], w[6], w[7]));
-        st_stream_f4(p.m + e, make_float4(m[0], m[1], m[2], m[3]));
-        st_stream_f4(p.m + e + 4, make_float4(m[4], m[5], m[6], m[7]));
-        st_stream_f4(p.v + e, make_float4(v[0], v[1], v[2], v[3]));
-        st_stream_f4(p.v + e + 4, make_float4(v[4], v[5], v[6], v[7]));
-        uint4 o;
-        o.x = pack_bf16x2(w[0], w[1]);
-        o.y = pack_bf16x2(w[2], w[3]);
-        o.z = pack_bf16x2(w[4], w[5]);
-        o.w = pack_bf16x2(w[6], w[7]);
-        st_stream_u4(p.out + e, o);
+        sum_src<KIND, R>(src[u], s);
+        finish_vec(p, (vi0 + u * stride) * 8, s, st[u], coef);
     }
+}
+
+// One vector with a runtime source count.
+template <int KIND>
+__device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, float coef) {
+    const int64_t e = vi * 8;
+    float s[8];
+    sum_src_dyn<KIND>(p, e, s);
+    float4 st[6];
+    load_state(p, e, st);
+    finish_vec(p, e, s, st, coef);
+}
+
+// One element (ragged tails and ranges not on 16-byte boundaries).
+template <int KIND>
+__device__ __forceinline__ void step_one(const UpdateParams& p, int64_t i, float coef) {
+    float s = 0.0f;
+    for (int r = 0; r < p.n_src; ++r) {
+        float x;
+        if constexpr (KIND == kPlainF32) {
+            x = static_cast<const float*>(p.src[r])[i];
+        } else {
+            x = bf16_one(static_cast<const uint16_t*>(p.src[r])[i]);
+            if constexpr (KIND == kAccLocal) x = __fadd_rn(p.acc[r][i], x);
+        }
+        s = __fadd_rn(s, x);
+    }
+    if constexpr (KIND == kAccReduce) s = __fadd_rn(p.acc[0][i], s);
+    float w = p.w[i], m = p.m[i], v = p.v[i];
+    adamw_update(mean_grad(s, p.h, coef), w, m, v, p.h);
+    p.w[i] = w;
+    p.m[i] = m;
+    p.v[i] = v;
+    p.out[i] = to_bf16(w);
+}
+
+// 128-bit loads per vector of one source kind (gradient sources plus state).
+template <int KIND, int R>
+__host__ __device__ constexpr int loads_per_vec() {
+    return (KIND == kPlainBf16 ? R : KIND == kPlainF32 ? 2 * R : KIND == kAccLocal ? 3 * R : R + 2) + 6;
 }
 
 // Vectors per thread and iteration: two when one vector has at most 8 loads.
-template <int NDP, bool kBf16>
+template <int KIND, int R>
 __host__ __device__ constexpr int vectors_per_iter() {
-    return ZGB_RS_MULTI && NDP > 0 && ((kBf16 ? NDP : 2 * NDP) + 6) <= 8 ? 2 : 1;
+    return ZGB_RS_MULTI && R > 0 && loads_per_vec<KIND, R>() <= 8 ? 2 : 1;
 }
 
-template <int NDP, bool kBf16>
+template <int KIND, int R>
 __global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
-rs_adamw_vec_kernel(const __grid_constant__ RsAdamwParams p) {
+rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
+    const float coef = clip_coef(p.h);
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    constexpr int U = vectors_per_iter<NDP, kBf16>();
-    if constexpr (U > 1) {
-        for (int64_t vi = tid; vi < nv; vi += U * stride) step_vecs<NDP, kBf16, U>(p, vi, stride, nv);
+    if constexpr (R > 0) {
+        constexpr int U = vectors_per_iter<KIND, R>();
+        for (int64_t vi = tid; vi < nv; vi += U * stride) step_vecs<KIND, R, U>(p, vi, stride, nv, coef);
     } else {
-        for (int64_t vi = tid; vi < nv; vi += stride) step_vec<NDP, kBf16>(p, vi);
+        for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND>(p, vi, coef);
     }
     const int64_t tail = p.n - (nv << 3);
-    if (tid < tail) step_one<kBf16>(p, (nv << 3) + tid);
+    if (tid < tail) step_one<KIND>(p, (nv << 3) + tid, coef);
 }
 
-template <bool kBf16>
-__global__ void __launch_bounds__(kThreads)
-rs_adamw_scalar_kernel(const __grid_constant__ RsAdamwParams p) {
+template <int KIND>
+__global__ void __launch_bounds__(kThreads) rs_adamw_scalar_kernel(const __grid_constant__ UpdateParams p) {
+    const float coef = clip_coef(p.h);
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n; i += stride)
-        step_one<kBf16>(p, i);
+        step_one<KIND>(p, i, coef);
 }
 
-template <int NDP, bool kBf16>
-int launch_vec(const RsAdamwParams& p, cudaStream_t stream) {
+template <int KIND, int R>
+int launch_vec(const UpdateParams& p, cudaStream_t stream) {
     static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<NDP, kBf16>, kThreads, 0);
+    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R>, kThreads, 0);
     const int64_t resident = (int64_t)sm_count() * occupancy * ZGB_RS_WAVES;
     const unsigned grid = grid_for(p.n >> 3, kThreads, resident);
-    rs_adamw_vec_kernel<NDP, kBf16><<<grid, kThreads, 0, stream>>>(p);
+    rs_adamw_vec_kernel<KIND, R><<<grid, kThreads, 0, stream>>>(p);
     return launch_status();
 }
 
-template <bool kBf16>
-int launch_scalar(const RsAdamwParams& p, cudaStream_t stream) {
+template <int KIND>
+int launch_scalar(const UpdateParams& p, cudaStream_t stream) {
     static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_scalar_kernel<kBf16>, kThreads, 0);
+    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_scalar_kernel<KIND>, kThreads, 0);
     const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
-    rs_adamw_scalar_kernel<kBf16><<<grid, kThreads, 0, stream>>>(p);
+    rs_adamw_scalar_kernel<KIND><<<grid, kThreads, 0, stream>>>(p);
     return launch_status();
 }
 
-template <bool kBf16>
-int dispatch_vec(const RsAdamwParams& p, cudaStream_t s) {
-    switch (p.n_src) {
-        case 1: return launch_vec<1, kBf16>(p, s);
-        case 2: return launch_vec<2, kBf16>(p, s);
-        case 3: return launch_vec<3, kBf16>(p, s);
-        case 4: return launch_vec<4, kBf16>(p, s);
-        case 5: return launch_vec<5, kBf16>(p, s);
-        case 6: return launch_vec<6, kBf16>(p, s);
-        case 7: return launch_vec<7, kBf16>(p, s);
-        case 8: return launch_vec<8, kBf16>(p, s);
-        case 16: return launch_vec<16, kBf16>(p, s);
-        default: return launch_vec<0, kBf16>(p, s);
+template <int KIND>
+int dispatch(const UpdateParams& p, bool vec, cudaStream_t s) {
+    if (!vec) return launch_scalar<KIND>(p, s);
+    if constexpr (KIND == kPlainBf16 || KIND == kPlainF32) {
+        switch (p.n_src) {
+            case 1: return launch_vec<KIND, 1>(p, s);
+            case 2: return launch_vec<KIND, 2>(p, s);
+            case 3: return launch_vec<KIND, 3>(p, s);
+            case 4: return launch_vec<KIND, 4>(p, s);
+            case 5: return launch_vec<KIND, 5>(p, s);
+            case 6: return launch_vec<KIND, 6>(p, s);
+            case 7: return launch_vec<KIND, 7>(p, s);
+            case 8: return launch_vec<KIND, 8>(p, s);
+            case 16: return launch_vec<KIND, 16>(p, s);
+            default: return launch_vec<KIND, 0>(p, s);
+        }
+    } else {
+        switch (p.n_src) {
+            case 1: return launch_vec<KIND, 1>(p, s);
+            case 2: return launch_vec<KIND, 2>(p, s);
+            case 4: return launch_vec<KIND, 4>(p, s);
+            case 8: return launch_vec<KIND, 8>(p, s);
+            default: return launch_vec<KIND, 0>(p, s);
+        }
     }
 }
 
-bool finite(float x) { return std::isfinite(x); }
+// ----------------------------------------------------------------- host checks
+
+int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
+                   int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
+                   UpdateTarget* t) {
+    if (!L || !master || !m || !v || !out) return ZERO_EINVAL;
+    if (out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD) return ZERO_EINVAL;
+    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
+    if (rank_begin < 0 || rank_end > L->n_dp || rank_begin >= rank_end) return ZERO_EINVAL;
+    const int64_t own_lo = (int64_t)rank_begin * L->shard;
+    const int64_t own_hi = (int64_t)rank_end * L->shard;
+    if (begin < own_lo || end > own_hi || begin > end) return ZERO_EINVAL;
+    if (check_aligned(master, 4) || check_aligned(m, 4) || check_aligned(v, 4) || check_aligned(out, 2))
+        return ZERO_EALIGN;
+    const int64_t state_off = begin - own_lo;
+    t->w = master + state_off;
+    t->m = m + state_off;
+    t->v = v + state_off;
+    t->out = out + (out_mode == ZERO_OUT_FULL ? begin : state_off);
+    t->n = end - begin;
+    t->aligned = aligned16(t->w) && aligned16(t->m) && aligned16(t->v) && aligned16(t->out);
+    return ZERO_OK;
+}
+
+int check_target_ptrs(const UpdateTarget& t) {
+    if (check_device_ptr(t.w) || check_device_ptr(t.m) || check_device_ptr(t.v) ||
+        check_device_ptr(t.out))
+        return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h) {
+    if (!hp) return ZERO_EINVAL;
+    if (!(divisor > 0.0f) || !std::isfinite(divisor)) return ZERO_EINVAL;
+    if (hp->step < 1 || !std::isfinite(hp->lr) || !std::isfinite(hp->eps) ||
+        !std::isfinite(hp->weight_decay) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) ||
+        !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+        return ZERO_EINVAL;
+    h->divisor = divisor;
+    h->b1 = hp->beta1;
+    h->b2 = hp->beta2;
+    h->omb1 = 1.0f - hp->beta1;
+    h->omb2 = 1.0f - hp->beta2;
+    h->bc1 = (float)(1.0 - std::pow((double)hp->beta1, (double)hp->step));
+    h->bc2 = (float)(1.0 - std::pow((double)hp->beta2, (double)hp->step));
+    h->lr = hp->lr;
+    h->lrwd = hp->lr * hp->weight_decay;
+    h->eps = hp->eps;
+    h->max_norm = 0.0f;
+    h->norm_sq = nullptr;
+    if (!(h->bc1 > 0.0f) || !(h->bc2 > 0.0f)) return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+// Shared body of the plain-source entry points (optionally clipped).
+int rs_adamw_plain(const zero_layout_t* L, const void* const* src, int32_t n_src, int32_t src_dtype,
+                   int64_t src_base, float divisor, int32_t rank_begin, int32_t rank_end,
+                   int64_t begin, int64_t end, float* master, float* m, float* v, uint16_t* out,
+                   int32_t out_mode, const zero_adamw_t* hp, const double* norm_sq, float max_norm,
+                   void* stream) {
+    if (!src) return ZERO_EINVAL;
+    if (n_src < 1) return ZERO_EINVAL;
+    if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
+    if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
+    UpdateTarget t;
+    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out, out_mode, &t);
+    if (rc) return rc;
+    if (src_base > begin) return ZERO_EINVAL;
+    UpdateParams p;
+    if ((rc = make_scalars(hp, divisor, &p.h))) return rc;
+    if (norm_sq) {
+        if (!(max_norm > 0.0f) || !std::isfinite(max_norm)) return ZERO_EINVAL;
+        if (check_aligned(norm_sq, 8)) return ZERO_EALIGN;
+        p.h.norm_sq = norm_sq;
+        p.h.max_norm = max_norm;
+    }
+    for (int r = 0; r < n_src; ++r)
+        if (!src[r]) return ZERO_EINVAL;
+    const int esize = src_dtype == ZERO_BF16 ? 2 : 4;
+    for (int r = 0; r < n_src; ++r)
+        if (check_aligned(src[r], esize)) return ZERO_EALIGN;
+    if (end == begin) return ZERO_OK;
+    for (int r = 0; r < n_src; ++r)
+        if (check_device_ptr(src[r])) return ZERO_EINVAL;
+    if ((rc = check_target_ptrs(t))) return rc;
+    if (norm_sq && check_device_ptr(norm_sq)) return ZERO_EINVAL;
+
+    bool vec = t.aligned;
+    for (int r = 0; r < ZERO_MAX_SRC; ++r) {
+        p.src[r] = nullptr;
+        p.acc[r] = nullptr;
+    }
+    for (int r = 0; r < n_src; ++r) {
+        p.src[r] = static_cast<const char*>(src[r]) + (begin - src_base) * esize;
+        vec = vec && aligned16(p.src[r]);
+    }
+    p.w = t.w;
+    p.m = t.m;
+    p.v = t.v;
+    p.out = t.out;
+    p.n = t.n;
+    p.n_src = n_src;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return src_dtype == ZERO_BF16 ? dispatch<kPlainBf16>(p, vec, s) : dispatch<kPlainF32>(p, vec, s);
+}
 
 }  // namespace zgb
 
@@ -311,73 +466,77 @@ extern "C" int zero_reduce_scatter_adamw(const zero_layout_t* L, const void* con
                                          int64_t begin, int64_t end, float* master, float* m,
                                          float* v, uint16_t* out_bf16, int32_t out_mode,
                                          const zero_adamw_t* hp, void* stream) {
+    return zgb::rs_adamw_plain(L, src, n_src, src_dtype, src_base, divisor, rank_begin, rank_end,
+                               begin, end, master, m, v, out_bf16, out_mode, hp, nullptr, 0.0f,
+                               stream);
+}
+
+extern "C" int zero_reduce_scatter_adamw_clip(const zero_layout_t* L, const void* const* src,
+                                              int32_t n_src, int32_t src_dtype, int64_t src_base,
+                                              float divisor, int32_t rank_begin, int32_t rank_end,
+                                              int64_t begin, int64_t end, float* master, float* m,
+                                              float* v, uint16_t* out_bf16, int32_t out_mode,
+                                              const zero_adamw_t* hp, const double* norm_sq,
+                                              float max_norm, void* stream) {
+    if (!norm_sq) return ZERO_EINVAL;
+    return zgb::rs_adamw_plain(L, src, n_src, src_dtype, src_base, divisor, rank_begin, rank_end,
+                               begin, end, master, m, v, out_bf16, out_mode, hp, norm_sq, max_norm,
+                               stream);
+}
+
+extern "C" int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,
+                                     const float* const* acc, int32_t n_acc, int64_t acc_base,
+                                     const uint16_t* const* grads, int32_t n_grads, int64_t grad_base,
+                                     float divisor, int32_t rank_begin, int32_t rank_end,
+                                     int64_t begin, int64_t end, float* master, float* m, float* v,
+                                     uint16_t* out_bf16, int32_t out_mode, const zero_adamw_t* hp,
+                                     void* stream) {
     using namespace zgb;
-    // ---- arguments that need no CUDA call
-    if (!L || !src || !master || !m || !v || !out_bf16 || !hp) return ZERO_EINVAL;
-    if (n_src < 1) return ZERO_EINVAL;
-    if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
-    if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
-    if (out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD) return ZERO_EINVAL;
-    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp)
-        return ZERO_EINVAL;
-    if (rank_begin < 0 || rank_end > L->n_dp || rank_begin >= rank_end) return ZERO_EINVAL;
-    const int64_t own_lo = (int64_t)rank_begin * L->shard;
-    const int64_t own_hi = (int64_t)rank_end * L->shard;
-    if (begin < own_lo || end > own_hi || begin > end) return ZERO_EINVAL;
-    if (src_base > begin) return ZERO_EINVAL;
-    if (!(divisor > 0.0f) || !finite(divisor)) return ZERO_EINVAL;
-    if (hp->step < 1 || !finite(hp->lr) || !finite(hp->eps) || !finite(hp->weight_decay) ||
-        !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
-        return ZERO_EINVAL;
-    for (int r = 0; r < n_src; ++r)
-        if (!src[r]) return ZERO_EINVAL;
-    const int esize = src_dtype == ZERO_BF16 ? 2 : 4;
-    for (int r = 0; r < n_src; ++r)
-        if (check_aligned(src[r], esize)) return ZERO_EALIGN;
-    if (check_aligned(master, 4) || check_aligned(m, 4) || check_aligned(v, 4) ||
-        check_aligned(out_bf16, 2))
-        return ZERO_EALIGN;
+    if (!acc || !grads) return ZERO_EINVAL;
+    if (mode != ZERO_ACC_LOCAL && mode != ZERO_ACC_REDUCE) return ZERO_EINVAL;
+    if (n_grads < 1) return ZERO_EINVAL;
+    if (n_grads > ZERO_MAX_SRC) return ZERO_ERANGE;
+    if (mode == ZERO_ACC_LOCAL ? n_acc != n_grads : n_acc != 1) return ZERO_EINVAL;
+    UpdateTarget t;
+    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode, &t);
+    if (rc) return rc;
+    if (acc_base > begin || grad_base > begin) return ZERO_EINVAL;
+    UpdateParams p;
+    if ((rc = make_scalars(hp, divisor, &p.h))) return rc;
+    for (int r = 0; r < n_acc; ++r)
+        if (!acc[r]) return ZERO_EINVAL;
+    for (int r = 0; r < n_grads; ++r)
+        if (!grads[r]) return ZERO_EINVAL;
+    for (int r = 0; r < n_acc; ++r)
+        if (check_aligned(acc[r], 4)) return ZERO_EALIGN;
+    for (int r = 0; r < n_grads; ++r)
+        if (check_aligned(grads[r], 2)) return ZERO_EALIGN;
     if (end == begin) return ZERO_OK;
+    for (int r = 0; r < n_acc; ++r)
+        if (check_device_ptr(acc[r])) return ZERO_EINVAL;
+    for (int r = 0; r < n_grads; ++r)
+        if (check_device_ptr(grads[r])) return ZERO_EINVAL;
+    if ((rc = check_target_ptrs(t))) return rc;
 
-    // ---- pointer kinds (device memory of the current device)
-    for (int r = 0; r < n_src; ++r)
-        if (check_device_ptr(src[r])) return ZERO_EINVAL;
-    if (check_device_ptr(master) || check_device_ptr(m) || check_device_ptr(v) ||
-        check_device_ptr(out_bf16))
-        return ZERO_EINVAL;
-
-    // ---- parameters
-    RsAdamwParams p;
-    const int64_t state_off = begin - own_lo;
-    const int64_t out_off = out_mode == ZERO_OUT_FULL ? begin : state_off;
-    const int64_t src_off = begin - src_base;
-    bool vec = true;
-    for (int r = 0; r < ZERO_MAX_SRC; ++r) p.src[r] = nullptr;
-    for (int r = 0; r < n_src; ++r) {
-        p.src[r] = static_cast<const char*>(src[r]) + src_off * esize;
+    bool vec = t.aligned;
+    for (int r = 0; r < ZERO_MAX_SRC; ++r) {
+        p.src[r] = nullptr;
+        p.acc[r] = nullptr;
+    }
+    for (int r = 0; r < n_grads; ++r) {
+        p.src[r] = grads[r] + (begin - grad_base);
         vec = vec && aligned16(p.src[r]);
     }
-    p.w = master + state_off;
-    p.m = m + state_off;
-    p.v = v + state_off;
-    p.out = out_bf16 + out_off;
-    vec = vec && aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.out);
-    p.n = end - begin;
-    p.n_src = n_src;
-    p.divisor = divisor;
-    p.b1 = hp->beta1;
-    p.b2 = hp->beta2;
-    p.omb1 = 1.0f - hp->beta1;
-    p.omb2 = 1.0f - hp->beta2;
-    p.bc1 = (float)(1.0 - std::pow((double)hp->beta1, (double)hp->step));
-    p.bc2 = (float)(1.0 - std::pow((double)hp->beta2, (double)hp->step));
-    p.lr = hp->lr;
-    p.lrwd = hp->lr * hp->weight_decay;
-    p.eps = hp->eps;
-    if (!(p.bc1 > 0.0f) || !(p.bc2 > 0.0f)) return ZERO_EINVAL;   // beta == 0 at t >= 1 is fine; guards underflow
-
+    for (int r = 0; r < n_acc; ++r) {
+        p.acc[r] = acc[r] + (begin - acc_base);
+        vec = vec && aligned16(p.acc[r]);
+    }
+    p.w = t.w;
+    p.m = t.m;
+    p.v = t.v;
+    p.out = t.out;
+    p.n = t.n;
+    p.n_src = n_grads;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool bf16 = src_dtype == ZERO_BF16;
-    if (vec) return bf16 ? dispatch_vec<true>(p, s) : dispatch_vec<false>(p, s);
-    return bf16 ? launch_scalar<true>(p, s) : launch_scalar<false>(p, s);
+    return mode == ZERO_ACC_LOCAL ? dispatch<kAccLocal>(p, vec, s) : dispatch<kAccReduce>(p, vec, s);
 }

@@ -1,0 +1,83 @@
+// The AdamW element update shared by every fused update kernel, and the host
+// checks that place an update range on the owners' state.
+//
+// AdamW ("ZeRO and FSDP", exercise "A sharded Adam step": bias correction at
+// step t, eps outside the square root; decoupled weight decay per the "AdamW"
+// optimizer blocks of "DeepSpeed ZeRO", "The configuration file"):
+//   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;  mh = m/bc1;  vh = v/bc2;
+//   w = w - (lr*wd)*w;    w = w - lr*(mh/(sqrt(vh)+eps))
+// every operation one IEEE fp32 rounding (explicit _rn intrinsics, no FMA).
+//
+// Optional clipping by the global gradient norm ("DeepSpeed ZeRO", "The
+// configuration file": gradient_clipping 1.0): with ||g||^2 in device memory,
+// coef = min(1, fp32(max_norm / (sqrt(||g||^2) + 1e-6))) evaluated in fp64 and
+// rounded once, and g is multiplied by coef before the update.
+#pragma once
+
+#include "zero_common.cuh"
+
+namespace zgb {
+
+struct AdamwScalars {
+    float divisor;                  // g = sum / divisor
+    float b1, b2, omb1, omb2;       // beta1, beta2, 1-beta1, 1-beta2 (fp32)
+    float bc1, bc2;                 // 1 - beta^t in fp64, rounded to fp32
+    float lr, lrwd, eps;            // lr, lr*wd (fp32), eps
+    float max_norm;                 // clipping threshold (used when norm_sq is set)
+    const double* norm_sq;          // device: squared global gradient norm, or nullptr
+};
+
+// The clipping coefficient, or 1 when no norm is given.
+__device__ __forceinline__ float clip_coef(const AdamwScalars& h) {
+    if (h.norm_sq == nullptr) return 1.0f;
+    const double nrm = __dsqrt_rn(*h.norm_sq);
+    const float c = __double2float_rn(__ddiv_rn((double)h.max_norm, __dadd_rn(nrm, 1e-6)));
+    return c < 1.0f ? c : 1.0f;
+}
+
+// g is the mean gradient (already divided and clipped).
+__device__ __forceinline__ void adamw_update(float g, float& w, float& m, float& v,
+                                             const AdamwScalars& h) {
+    const float mi = __fadd_rn(__fmul_rn(h.b1, m), __fmul_rn(h.omb1, g));
+    const float vi = __fadd_rn(__fmul_rn(h.b2, v), __fmul_rn(h.omb2, __fmul_rn(g, g)));
+    const float m_hat = __fdiv_rn(mi, h.bc1);
+    const float v_hat = __fdiv_rn(vi, h.bc2);
+    float wi = __fsub_rn(w, __fmul_rn(h.lrwd, w));                        // decoupled decay
+    const float denom = __fadd_rn(__fsqrt_rn(v_hat), h.eps);
+    wi = __fsub_rn(wi, __fmul_rn(h.lr, __fdiv_rn(m_hat, denom)));          // Adam step
+    w = wi;
+    m = mi;
+    v = vi;
+}
+
+// The mean gradient of one element from its source sum: one IEEE division,
+// then the clip multiply (exact when coef == 1).
+__device__ __forceinline__ float mean_grad(float sum, const AdamwScalars& h, float coef) {
+    return __fmul_rn(__fdiv_rn(sum, h.divisor), coef);
+}
+
+// ----------------------------------------------------------------- host
+
+// Where an update over flat [begin, end) of the owners rank_begin..rank_end-1
+// reads and writes: state and output pointers already offset to `begin`.
+struct UpdateTarget {
+    float* w;
+    float* m;
+    float* v;
+    uint16_t* out;
+    int64_t n;
+    bool aligned;   // all four pointers 16-byte aligned
+};
+
+// Argument checks that need no CUDA call, then the offsets (zero_gb300.h,
+// zero_reduce_scatter_adamw: state of i at [i - rank_begin*S]; out at [i] for
+// ZERO_OUT_FULL, like the state for ZERO_OUT_SHARD).
+int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
+                   int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
+                   UpdateTarget* t);
+// The pointer-kind checks (CUDA calls) of a prepared target.
+int check_target_ptrs(const UpdateTarget& t);
+// Hyper-parameter checks and the fp32 scalars of the update.
+int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h);
+
+}  // namespace zgb

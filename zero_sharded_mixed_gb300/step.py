@@ -78,6 +78,55 @@ def zero2_finish(L, A, n_micro, master, m, v, out, hp, stream=None):
                                      s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
 
 
+def zero1_finish_fused(L, acc, last_grads, n_micro, master, m, v, out, hp, stream=None):
+    """Stage 1, last micro-batch fused with the update: each rank's final
+    accumulator acc[r] + g_r is formed in registers, never written back."""
+    for s, e in bucket_ranges(L):
+        zb.zero_accumulate_adamw(L, zb.ZERO_ACC_LOCAL, acc, 0, last_grads, 0,
+                                 float(L.n_dp * n_micro), 0, L.n_dp, s, e, master, m, v, out,
+                                 zb.ZERO_OUT_FULL, hp, stream)
+
+
+def zero2_finish_fused(L, A, last_grads, n_micro, master, m, v, out, hp, stream=None):
+    """Stage 2, last micro-batch fused with the update: A + sum over ranks of
+    the last micro-batch's gradients, formed in registers."""
+    for s, e in bucket_ranges(L):
+        zb.zero_accumulate_adamw(L, zb.ZERO_ACC_REDUCE, [A], 0, last_grads, 0,
+                                 float(L.n_dp * n_micro), 0, L.n_dp, s, e, master, m, v, out,
+                                 zb.ZERO_OUT_FULL, hp, stream)
+
+
+# --------------------------------------------------------------------------
+# clipping by the global gradient norm ("DeepSpeed ZeRO", "The configuration
+# file": gradient_clipping)
+# --------------------------------------------------------------------------
+
+class NormBuffers:
+    """Device workspace and the fp64 squared-norm scalar of a clipped step."""
+
+    def __init__(self, device=None):
+        nbytes = zb.zero_grad_norm_workspace()
+        self.workspace = torch.empty(nbytes // 8, dtype=torch.float64, device=device)
+        self.norm_sq = torch.zeros(1, dtype=torch.float64, device=device)
+
+
+def zero12_step_clipped(L, grads, master, m, v, out, hp, max_norm, bufs: NormBuffers,
+                        rank_begin=0, rank_end=None, stream=None, grad_base=0):
+    """A ZeRO-1/2 step with the mean gradient clipped to max_norm: first the
+    squared norm over every owned bucket (kept on the device), then the clipped
+    fused update of every bucket."""
+    rank_end = L.n_dp if rank_end is None else rank_end
+    ranges = bucket_ranges(L, rank_begin * L.shard, rank_end * L.shard)
+    div = float(L.n_dp)
+    for j, (s, e) in enumerate(ranges):
+        zb.zero_grad_norm_sq(L, grads, zb.ZERO_BF16, grad_base, div, s, e, bufs.workspace,
+                             bufs.norm_sq, j > 0, stream)
+    for s, e in ranges:
+        zb.zero_reduce_scatter_adamw_clip(L, grads, zb.ZERO_BF16, grad_base, div, rank_begin,
+                                          rank_end, s, e, master, m, v, out, zb.ZERO_OUT_FULL,
+                                          hp, bufs.norm_sq, max_norm, stream)
+
+
 # --------------------------------------------------------------------------
 # ZeRO-3 ("DeepSpeed ZeRO", "Stage 3 step by step"; "ZeRO and FSDP", "FSDP,
 # ZeRO-3 inside PyTorch": per-unit flat buffers, at most two gathered at once)
