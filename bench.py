@@ -12,6 +12,8 @@ with 5e8-element buckets, every owned shard updated each step.  Measured in the
 same run and reported under "workloads", with fewer steps:
   llama7b-shard  one owned shard of Llama-7B shapes (S = 842,301,952), 8 slices
                  with 1 % outliers x100;
+  gpt2xl-clip    the GPT-2-XL step with clipping by the global gradient norm
+                 (a norm pass, then the clipped fused update);
   accum-zero1/2  gradient accumulation, GPT-2-XL shapes, n_dp = 4, 4 micro-batches,
                  in the stage-1 and stage-2 orders;
   zero3          the per-unit gather / reduce-scatter / update path over the 34
@@ -57,8 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["gpt2xl", "llama7b-shard", "probe", "accum-zero1",
-                                           "accum-zero2", "zero3"], default="gpt2xl",
+    ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe",
+                                           "accum-zero1", "accum-zero2", "zero3"], default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
     ap.add_argument("--no-e2e", action="store_true")
@@ -261,11 +263,13 @@ class Zero2Workload(Workload):
         zb = self.zb
         n_dp = 8
         self.name = name
-        if name == "gpt2xl":
+        self.clip = name == "gpt2xl-clip"
+        if name in ("gpt2xl", "gpt2xl-clip"):
             L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
             lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
-            self.desc = {"workload": "gpt2xl_zero2_all_shards", "model": "GPT-2-XL shapes",
+            self.desc = {"workload": "gpt2xl_zero2_all_shards" + ("_clip1.0" if self.clip else ""),
+                         "model": "GPT-2-XL shapes",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "padded_n": L.padded_n,
                          "bucket": L.bucket, "buckets": L.n_buckets}
         elif name == "probe":
@@ -286,8 +290,12 @@ class Zero2Workload(Workload):
         self.L, self.src_base = L, lo
         self.ranges = bucket_ranges(L, lo, hi)
         self.elems = hi - lo
-        self.bytes_per_elem = 26 + 2 * n_dp
-        self.dominant = "rs_adamw"
+        self.bytes_per_elem = 26 + 2 * n_dp + (2 * n_dp if self.clip else 0)
+        self.dominant = "rs_adamw_clip" if self.clip else "rs_adamw"
+        if self.clip:
+            from zero_sharded_mixed_gb300.step import NormBuffers
+            self.norm = NormBuffers(device)
+            self.kernel_label = "zgb::norm_partial_kernel<true,8> + zgb::rs_adamw_vec_kernel<0,8> (clip)"
         g = torch.empty((n_dp, src_len), dtype=torch.bfloat16, device=device)
         n_real = max(0, min(L.n, hi) - lo)
         for r in range(n_dp):
@@ -302,11 +310,27 @@ class Zero2Workload(Workload):
 
     def ops(self, t):
         zb, hp = self.zb, self.hp(t)
+        n_dp = self.L.n_dp
         out = []
+        if self.clip:
+            for j, (s, e) in enumerate(self.ranges):
+                def fn(s=s, e=e, j=j):
+                    zb.zero_grad_norm_sq(self.L, self.grad_list, zb.ZERO_BF16, self.src_base,
+                                         float(n_dp), s, e, self.norm.workspace, self.norm.norm_sq,
+                                         j > 0)
+                out.append(Op("grad_norm", (e - s) * 2 * n_dp, fn))
+            for s, e in self.ranges:
+                def fn(s=s, e=e):
+                    zb.zero_reduce_scatter_adamw_clip(
+                        self.L, self.grad_list, zb.ZERO_BF16, self.src_base, float(n_dp),
+                        self.rank_begin, self.rank_end, s, e, self.master, self.m, self.v, self.out,
+                        zb.ZERO_OUT_FULL, hp, self.norm.norm_sq, 1.0)
+                out.append(Op("rs_adamw_clip", (e - s) * (26 + 2 * n_dp), fn))
+            return out
         for s, e in self.ranges:
             def fn(s=s, e=e):
                 zb.zero_reduce_scatter_adamw(self.L, self.grad_list, zb.ZERO_BF16, self.src_base,
-                                             float(self.L.n_dp), self.rank_begin, self.rank_end,
+                                             float(n_dp), self.rank_begin, self.rank_end,
                                              s, e, self.master, self.m, self.v, self.out,
                                              zb.ZERO_OUT_FULL, hp)
             out.append(Op("rs_adamw", (e - s) * self.bytes_per_elem, fn))
@@ -316,11 +340,12 @@ class Zero2Workload(Workload):
 class AccumWorkload(Workload):
     """Gradient accumulation, GPT-2-XL shapes, n_dp = 4, K = 4 micro-batches.
     zero1: each rank adds its full bf16 micro-batch gradient into its own fp32
-    buffer, then one fused update from the n_dp fp32 buffers (divisor n_dp*K).
-    zero2: each micro-batch is reduce-scattered (summed) into the owners' fp32
-    shard buffer, then one fused update from it.  The same n_dp gradient
-    buffers serve every micro-batch (each read is larger than L2, so the
-    traffic is that of fresh data)."""
+    buffer for the first K-1 micro-batches; the last one is fused with the
+    update (sum over ranks of acc_r + g_r, divisor n_dp*K).
+    zero2: the first K-1 micro-batches are reduce-scattered (summed) into the
+    owners' fp32 shard buffer; the last is fused with the update (A + sum over
+    ranks of g_r).  The same n_dp gradient buffers serve every micro-batch
+    (each read is larger than L2, so the traffic is that of fresh data)."""
 
     n_src = 4
 
@@ -350,13 +375,13 @@ class AccumWorkload(Workload):
         self.out = torch.zeros(P, dtype=torch.bfloat16, device=device)
         if self.order == "zero1":
             self.acc = [torch.empty(P, device=device) for _ in range(n_dp)]
-            per = n_dp * (6 + (K - 1) * 10) + (26 + 4 * n_dp)
-            self.kernel_label = "zgb::acc_vec_kernel<1,true,true> + zgb::rs_adamw_vec_kernel<4,false>"
+            per = n_dp * (6 + (K - 2) * 10) + (6 * n_dp + 26)
+            self.kernel_label = "zgb::acc_vec_kernel<1,true,true> + zgb::rs_adamw_vec_kernel<2,4> (fused finish)"
             self.dominant = "accumulate_local"
         else:
             self.A = torch.empty(P, device=device)
-            per = (2 * n_dp + 4) + (K - 1) * (2 * n_dp + 8) + 30
-            self.kernel_label = "zgb::acc_vec_kernel<4,true,false> + zgb::rs_adamw_vec_kernel<1,false>"
+            per = (2 * n_dp + 4) + (K - 2) * (2 * n_dp + 8) + (4 + 2 * n_dp + 26)
+            self.kernel_label = "zgb::acc_vec_kernel<4,true,false> + zgb::rs_adamw_vec_kernel<3,4> (fused finish)"
             self.dominant = "accumulate_reduce"
         self.bytes_per_elem = per
         self.desc = {"workload": "gpt2xl_accumulation_%s" % self.order, "model": "GPT-2-XL shapes",
@@ -369,7 +394,7 @@ class AccumWorkload(Workload):
         n_dp = L.n_dp
         out = []
         if self.order == "zero1":
-            for k in range(K):
+            for k in range(K - 1):
                 for r in range(n_dp):
                     def fn(r=r, k=k):
                         zb.zero_accumulate(L, zb.ZERO_ACC_LOCAL, [self.grads[r]], zb.ZERO_BF16, 0,
@@ -377,12 +402,12 @@ class AccumWorkload(Workload):
                     out.append(Op("accumulate_local", L.padded_n * (6 if k == 0 else 10), fn))
             for s, e in self.ranges:
                 def fn(s=s, e=e):
-                    zb.zero_reduce_scatter_adamw(L, self.acc, zb.ZERO_F32, 0, float(n_dp * K), 0, n_dp,
-                                                 s, e, self.master, self.m, self.v, self.out,
-                                                 zb.ZERO_OUT_FULL, hp)
-                out.append(Op("rs_adamw", (e - s) * (26 + 4 * n_dp), fn))
+                    zb.zero_accumulate_adamw(L, zb.ZERO_ACC_LOCAL, self.acc, 0, self.grads, 0,
+                                             float(n_dp * K), 0, n_dp, s, e, self.master, self.m,
+                                             self.v, self.out, zb.ZERO_OUT_FULL, hp)
+                out.append(Op("accumulate_adamw", (e - s) * (6 * n_dp + 26), fn))
         else:
-            for k in range(K):
+            for k in range(K - 1):
                 for s, e in self.ranges:
                     def fn(s=s, e=e, k=k):
                         zb.zero_accumulate(L, zb.ZERO_ACC_REDUCE, self.grads, zb.ZERO_BF16, 0, self.A, 0,
@@ -390,10 +415,10 @@ class AccumWorkload(Workload):
                     out.append(Op("accumulate_reduce", (e - s) * (2 * n_dp + (4 if k == 0 else 8)), fn))
             for s, e in self.ranges:
                 def fn(s=s, e=e):
-                    zb.zero_reduce_scatter_adamw(L, [self.A], zb.ZERO_F32, 0, float(n_dp * K), 0, n_dp,
-                                                 s, e, self.master, self.m, self.v, self.out,
-                                                 zb.ZERO_OUT_FULL, hp)
-                out.append(Op("rs_adamw", (e - s) * 30, fn))
+                    zb.zero_accumulate_adamw(L, zb.ZERO_ACC_REDUCE, [self.A], 0, self.grads, 0,
+                                             float(n_dp * K), 0, n_dp, s, e, self.master, self.m,
+                                             self.v, self.out, zb.ZERO_OUT_FULL, hp)
+                out.append(Op("accumulate_adamw", (e - s) * (4 + 2 * n_dp + 26), fn))
         return out
 
 
@@ -469,7 +494,7 @@ class Zero3Workload(Workload):
 
 
 def make_workload(name, device):
-    if name in ("gpt2xl", "llama7b-shard", "probe"):
+    if name in ("gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe"):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device)
@@ -607,8 +632,8 @@ def run_ours(args):
 
     peak, peak_kind = _peak()
     primary = args.workload
-    extras = [w for w in ("gpt2xl", "llama7b-shard", "accum-zero1", "accum-zero2", "zero3")
-              if w != primary]
+    extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "accum-zero1", "accum-zero2",
+                          "zero3") if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
     for name in order:
@@ -626,8 +651,8 @@ def run_ours(args):
         dom_bytes = dom["bytes"] / dom["launches"]                           # per launch
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         bytes_step = wl.elems * wl.bytes_per_elem
-        tpe = _traffic_per_elem(wl.n_src) if wl.dominant == "rs_adamw" and name != "zero3" and \
-            not name.startswith("accum") else None
+        tpe = _traffic_per_elem(wl.n_src) if wl.dominant == "rs_adamw" and \
+            name in ("gpt2xl", "llama7b-shard", "probe") else None
         res = {
             "value": replica_value(wl.elems, world, ms_step), "ms_per_step": ms_step, "steps": steps,
             "hbm_gbs_step": bytes_step / (ms_step / 1e3) / 1e9,

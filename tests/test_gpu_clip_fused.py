@@ -180,3 +180,27 @@ def test_clipped_step(zlib, cuda_device, std, max_norm):
             parity.assert_bit_exact_f32(a, b)
     else:
         assert coef < 1.0
+
+
+def test_grad_norm_extreme_values(zlib, cuda_device):
+    """Squares outside the fp32 pair's exact range (|g| < 2^-50 or >= 2^60)
+    take the fp64 path: tiny, huge, zero and ordinary values mixed."""
+    zb = zlib
+    N = 40_000
+    L = zb.zero_layout([N], 1, align=1)
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((2, N)) * 1e-3).astype(np.float32)
+    x[:, :1000] = 1e-20
+    x[:, 1000:1010] = 3e25
+    x[:, 1010:2000] = 0.0
+    x[0, 2000:2100] = 2.0 ** -50
+    x[1, 2000:2100] = 0.0
+    srcs = [torch.from_numpy(x[r].copy()).cuda() for r in range(2)]
+    bufs = zstep.NormBuffers("cuda")
+    zb.zero_grad_norm_sq(L, srcs, zb.ZERO_F32, 0, 2.0, 0, N, bufs.workspace, bufs.norm_sq, False)
+    assert float(bufs.norm_sq.item()) == pytest.approx(oracle.grad_norm_sq(x, 2.0), rel=1e-12)
+    # only tiny values: the answer comes from the fp64 path alone
+    t = np.full((1, 4096), 1e-25, np.float32)
+    zb.zero_grad_norm_sq(L, [torch.from_numpy(t[0].copy()).cuda()], zb.ZERO_F32, 0, 1.0, 0, 4096,
+                         bufs.workspace, bufs.norm_sq, False)
+    assert float(bufs.norm_sq.item()) == pytest.approx(oracle.grad_norm_sq(t, 1.0), rel=1e-12)

@@ -4,10 +4,18 @@
 //
 // For every flat i in [begin, end) the mean gradient g_i is formed exactly as
 // the fused update forms it (fp32 sum over sources in ascending order from
-// +0.0f, one IEEE division), and g_i^2 -- exact in fp64 -- is added to an fp64
-// sum.  Pass 1 (one streaming kernel, 2 bytes per bf16 source per element):
-// each thread sums its elements in order, each CTA reduces its threads in a
-// fixed tree and writes one fp64 partial into the caller's workspace.  Pass 2
+// +0.0f, one IEEE division), and g_i^2 is added to the thread's running sum.
+// fp64 arithmetic is slow on this GPU (a few per element would bound the pass
+// below the HBM rate), so the thread's sum is kept as an unevaluated pair of
+// fp32 values (hi, lo): the square is split exactly into p + e by the FMA
+// two-product (Dekker; Ogita, Rump and Oishi, "Accurate sum and dot product",
+// 2005) and added with Knuth's two-sum, whose rounding error goes into lo.
+// The pair carries about 48 significant bits; squares outside the range where
+// that split is exact (|g| < 2^-50 or >= 2^60) go to a plain fp64 sum instead.
+// Pass 1 (one streaming kernel, 2 bytes per bf16 source per element): each
+// thread sums its elements in order, widens its pair to fp64, each CTA reduces
+// its threads in a fixed tree and writes one fp64 partial into the caller's
+// workspace.  Pass 2
 // (one CTA): the partials are summed in a fixed tree and the total is written
 // to (or added to) *norm_sq in device memory, where the clipped update reads
 // it -- nothing returns to the host.  For a given GPU and range the grid, and
@@ -35,6 +43,33 @@ __device__ __forceinline__ float mean_at(const NormParams& p, int64_t i) {
     return __fdiv_rn(s, p.divisor);
 }
 
+// A thread's running sum of squares: (hi + lo) in fp32 pairs plus an fp64 sum
+// for squares outside the range where the fp32 split is exact.
+struct SquareSum {
+    float hi = 0.0f, lo = 0.0f;
+    double wide = 0.0;
+
+    __device__ __forceinline__ void add(float g) {
+        const float a = fabsf(g);
+        if (a >= 0x1p-50f && a < 0x1p+60f) {
+            const float p = __fmul_rn(g, g);
+            const float e = __fmaf_rn(g, g, -p);                 // g*g = p + e exactly
+            const float t = __fadd_rn(hi, p);                    // two-sum of hi and p
+            const float bp = __fsub_rn(t, hi);
+            const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+            hi = t;
+            lo = __fadd_rn(lo, __fadd_rn(err, e));
+        } else if (a != 0.0f) {
+            const double d = (double)g;
+            wide = __dadd_rn(wide, __dmul_rn(d, d));
+        }
+    }
+
+    __device__ __forceinline__ double total() const {
+        return __dadd_rn(__dadd_rn((double)hi, (double)lo), wide);
+    }
+};
+
 // Fixed-order CTA reduction of one fp64 value per thread; thread 0 gets the total.
 __device__ __forceinline__ double cta_sum(double x) {
     __shared__ double warp_sums[kThreads / 32];
@@ -56,7 +91,7 @@ template <bool kBf16, int R>
 __global__ void __launch_bounds__(kThreads) norm_partial_kernel(const __grid_constant__ NormParams p) {
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    double acc = 0.0;
+    SquareSum acc;
     if constexpr (R > 0) {
         const int64_t nv = p.n >> 3;
         for (int64_t vi = tid; vi < nv; vi += stride) {
@@ -93,23 +128,14 @@ __global__ void __launch_bounds__(kThreads) norm_partial_kernel(const __grid_con
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const double g = (double)__fdiv_rn(s[j], p.divisor);
-                acc = __dadd_rn(acc, __dmul_rn(g, g));
-            }
+            for (int j = 0; j < 8; ++j) acc.add(__fdiv_rn(s[j], p.divisor));
         }
         const int64_t tail = p.n - (nv << 3);
-        if (tid < tail) {
-            const double g = (double)mean_at<kBf16>(p, (nv << 3) + tid);
-            acc = __dadd_rn(acc, __dmul_rn(g, g));
-        }
+        if (tid < tail) acc.add(mean_at<kBf16>(p, (nv << 3) + tid));
     } else {
-        for (int64_t i = tid; i < p.n; i += stride) {
-            const double g = (double)mean_at<kBf16>(p, i);
-            acc = __dadd_rn(acc, __dmul_rn(g, g));
-        }
+        for (int64_t i = tid; i < p.n; i += stride) acc.add(mean_at<kBf16>(p, i));
     }
-    const double total = cta_sum(acc);
+    const double total = cta_sum(acc.total());
     if (threadIdx.x == 0) p.partials[blockIdx.x] = total;
 }
 

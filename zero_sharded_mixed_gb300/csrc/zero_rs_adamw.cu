@@ -43,7 +43,7 @@
 #define ZGB_RS_MULTI 1       // 0: one vector per thread and iteration everywhere
 #endif
 #ifndef ZGB_RS_MINBLOCKS
-#define ZGB_RS_MINBLOCKS 1   // CTAs per SM the register allocation must allow
+#define ZGB_RS_MINBLOCKS 2   // CTAs per SM the register allocation must allow (caps at 128)
 #endif
 
 namespace zgb {
