@@ -173,6 +173,28 @@ int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_
                       int64_t end, void* workspace, int64_t workspace_bytes, double* norm_sq,
                       int32_t accumulate, void* stream);
 
+/* zero_grad_norm_sq_static: zero_grad_norm_sq without the workspace argument,
+ * for callers that cannot allocate device memory -- for example a plugin that
+ * is handed only its input and output buffers by a host framework that owns
+ * every allocation on the device, or code that must not call cudaMalloc
+ * because of the device-wide synchronization it can imply.  The pages have no
+ * counterpart: this is an interface convenience of this library.
+ * The per-CTA partial sums live in a library-owned device array of 4096
+ * doubles (32 KiB, allocated when the library is loaded and held by every GPU
+ * that loads it until the process exits), so the call allocates nothing and
+ * calls no allocating routine.  Limits: a device needing more than 4096
+ * partials (more than 512 SMs) gets ZERO_ERANGE.  The first call on each device
+ * looks up that array's device address (cudaGetSymbolAddress, with that device
+ * current) and caches it; make the first call on a device before any stream
+ * capture begins.  Every call shares the one array and overwrites the partials
+ * it reads, so no clearing is needed between calls, but calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * the array: order them, or use zero_grad_norm_sq with one workspace each.
+ * Arguments, results and other errors as zero_grad_norm_sq. */
+int zero_grad_norm_sq_static(const zero_layout_t* L, const void* const* src, int32_t n_src,
+                             int32_t src_dtype, int64_t src_base, float divisor, int64_t begin,
+                             int64_t end, double* norm_sq, int32_t accumulate, void* stream);
+
 /* zero_reduce_scatter_adamw_clip: zero_reduce_scatter_adamw with the mean
  * gradient multiplied, before the update, by
  *   coef = min(1, fp32(max_norm / (sqrt(*norm_sq) + 1e-6)))

@@ -84,6 +84,8 @@ def load():
         lib.zero_grad_norm_workspace.argtypes = [P(i64)]
         lib.zero_grad_norm_sq.argtypes = [P(ZeroLayout), P(p), i32, i32, i64, f32, i64, i64,
                                           p, i64, p, i32, p]
+        lib.zero_grad_norm_sq_static.argtypes = [P(ZeroLayout), P(p), i32, i32, i64, f32, i64,
+                                                 i64, p, i32, p]
         lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
         lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
                                         i32, p]
@@ -97,6 +99,7 @@ def load():
         for name in ("zero_layout", "zero_bucket_range", "zero_shard_range",
                      "zero_reduce_scatter_adamw", "zero_reduce_scatter_adamw_clip",
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
+                     "zero_grad_norm_sq_static",
                      "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -293,6 +296,20 @@ def zero_grad_norm_sq(L: ZeroLayout, srcs, src_dtype: int, src_base: int, diviso
                                   int(ws_bytes), _tensor(norm_sq, "norm_sq", torch.float64, 1),
                                   int(bool(accumulate)), _stream_ptr(stream))
     _check(rc, "zero_grad_norm_sq")
+
+
+def zero_grad_norm_sq_static(L: ZeroLayout, srcs, src_dtype: int, src_base: int, divisor: float,
+                             begin: int, end: int, norm_sq: torch.Tensor, accumulate: bool,
+                             stream=None):
+    """zero_grad_norm_sq with its partial sums in the library's own device array:
+    no workspace, nothing allocated.  Calls that overlap on the GPU race."""
+    src_need = max(0, end - src_base) if end > begin else 0
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    rc = load().zero_grad_norm_sq_static(ctypes.byref(L), arr, n, int(src_dtype), int(src_base),
+                                         float(divisor), int(begin), int(end),
+                                         _tensor(norm_sq, "norm_sq", torch.float64, 1),
+                                         int(bool(accumulate)), _stream_ptr(stream))
+    _check(rc, "zero_grad_norm_sq_static")
 
 
 def zero_gather_layer(unit: ZeroLayout, shards, full_out: torch.Tensor, stream=None):

@@ -20,6 +20,8 @@
 // to (or added to) *norm_sq in device memory, where the clipped update reads
 // it -- nothing returns to the host.  For a given GPU and range the grid, and
 // so the summation order, is fixed: results are reproducible run to run.
+#include <atomic>
+
 #include "zero_common.cuh"
 
 namespace zgb {
@@ -229,4 +231,65 @@ extern "C" int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src,
     return grad_norm_sq(L, src, n_src, src_dtype, src_base, divisor, begin, end,
                         static_cast<double*>(workspace), workspace_bytes / (int64_t)sizeof(double),
                         norm_sq, accumulate, stream);
+}
+
+// ---------------------------------------------------------------------------
+// zero_grad_norm_sq_static: the same computation with its partial sums in a
+// fixed array of device memory that belongs to this library, for callers that
+// cannot hand it a workspace.
+// ---------------------------------------------------------------------------
+
+namespace zgb {
+
+// Capacity of the library-owned partials: one fp64 per CTA of the partial
+// pass, which launches at most (SMs x resident CTAs per SM) CTAs -- 4096
+// covers GPUs of up to 512 SMs.  32 KiB, held by every GPU that loads the
+// library until the process exits.
+constexpr int64_t kStaticPartials = 4096;
+static __device__ __align__(256) double g_static_partials[kStaticPartials];
+
+namespace {
+constexpr int kMaxStaticDevices = 64;
+std::atomic<double*> g_static_partials_addr[kMaxStaticDevices];
+}  // namespace
+
+// The device address of g_static_partials on the current device, looked up
+// once per device (cudaGetSymbolAddress with that device current) and cached.
+int static_partials(double** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return ZERO_ECUDA;
+    }
+    if (dev >= kMaxStaticDevices) return ZERO_ERANGE;
+    double* p = g_static_partials_addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_static_partials) != cudaSuccess || addr == nullptr) {
+            (void)cudaGetLastError();
+            return ZERO_ECUDA;
+        }
+        p = static_cast<double*>(addr);
+        g_static_partials_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
+}  // namespace zgb
+
+extern "C" int zero_grad_norm_sq_static(const zero_layout_t* L, const void* const* src,
+                                        int32_t n_src, int32_t src_dtype, int64_t src_base,
+                                        float divisor, int64_t begin, int64_t end, double* norm_sq,
+                                        int32_t accumulate, void* stream) {
+    using namespace zgb;
+    if (!L || !src || !norm_sq) return ZERO_EINVAL;
+    if (norm_partials_capacity() > kStaticPartials) return ZERO_ERANGE;   // more SMs than it holds
+    double* partials = nullptr;
+    const int rc = static_partials(&partials);
+    if (rc) return rc;
+    // Every partial the finalize pass reads is written by the partial pass of
+    // the same call, so nothing in the array needs clearing between calls.
+    return grad_norm_sq(L, src, n_src, src_dtype, src_base, divisor, begin, end, partials,
+                        kStaticPartials, norm_sq, accumulate, stream);
 }
