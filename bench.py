@@ -63,6 +63,9 @@ def parse_args(argv=None):
                                            "accum-zero1", "accum-zero2", "zero3"], default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
+    ap.add_argument("--elems", type=int, default=0,
+                    help="replace the model shape by a flat vector of this many elements "
+                         "(small cases for profiling; not a headline workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the second workload")
@@ -255,7 +258,7 @@ class Zero2Workload(Workload):
     """ZeRO-2 step: the bucketed fused update of every owned element in
     [lo, hi) from n_dp bf16 gradient buffers."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, elems=0):
         import torch
         from zero_sharded_mixed_gb300 import inputs
         from zero_sharded_mixed_gb300.step import bucket_ranges
@@ -265,11 +268,13 @@ class Zero2Workload(Workload):
         self.name = name
         self.clip = name == "gpt2xl-clip"
         if name in ("gpt2xl", "gpt2xl-clip"):
-            L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+            numels = [elems] if elems else inputs.gpt2xl_numels()
+            L = zb.zero_layout(numels, n_dp, 8, 500_000_000)
             lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
-            self.desc = {"workload": "gpt2xl_zero2_all_shards" + ("_clip1.0" if self.clip else ""),
-                         "model": "GPT-2-XL shapes",
+            self.desc = {"workload": ("flat%d_zero2" % elems if elems else "gpt2xl_zero2_all_shards")
+                         + ("_clip1.0" if self.clip else ""),
+                         "model": "flat vector" if elems else "GPT-2-XL shapes",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "padded_n": L.padded_n,
                          "bucket": L.bucket, "buckets": L.n_buckets}
         elif name == "probe":
@@ -349,7 +354,7 @@ class AccumWorkload(Workload):
 
     n_src = 4
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, elems=0):
         import torch
         from zero_sharded_mixed_gb300 import inputs
         from zero_sharded_mixed_gb300.step import bucket_ranges
@@ -359,7 +364,7 @@ class AccumWorkload(Workload):
         n_dp, K = 4, 4
         self.K = K
         self.order = "zero1" if name == "accum-zero1" else "zero2"
-        L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+        L = zb.zero_layout([elems] if elems else inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
         self.L = L
         P = L.padded_n
         self.ranges = bucket_ranges(L)
@@ -384,7 +389,8 @@ class AccumWorkload(Workload):
             self.kernel_label = "zgb::acc_vec_kernel<4,true,false> + zgb::rs_adamw_vec_kernel<3,4> (fused finish)"
             self.dominant = "accumulate_reduce"
         self.bytes_per_elem = per
-        self.desc = {"workload": "gpt2xl_accumulation_%s" % self.order, "model": "GPT-2-XL shapes",
+        self.desc = {"workload": ("flat%d" % elems if elems else "gpt2xl") + "_accumulation_%s" % self.order,
+                     "model": "flat vector" if elems else "GPT-2-XL shapes",
                      "N": L.n, "n_dp": n_dp, "micro_batches": K, "bucket": L.bucket}
         self.device_bytes = (g.numel() * 2 + 3 * P * 4 + P * 2 +
                              (n_dp * P * 4 if self.order == "zero1" else P * 4))
@@ -493,11 +499,13 @@ class Zero3Workload(Workload):
         return out
 
 
-def make_workload(name, device):
-    if name in ("gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe"):
+def make_workload(name, device, elems=0):
+    if name in ("gpt2xl", "gpt2xl-clip"):
+        return Zero2Workload(name, device, elems)
+    if name in ("llama7b-shard", "probe"):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
-        return AccumWorkload(name, device)
+        return AccumWorkload(name, device, elems)
     if name == "zero3":
         return Zero3Workload(name, device)
     raise ValueError(name)
@@ -636,8 +644,10 @@ def run_ours(args):
                           "zero3") if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
+    if args.elems:
+        order = [primary]
     for name in order:
-        wl = make_workload(name, device)
+        wl = make_workload(name, device, args.elems if name == primary else 0)
         torch.cuda.synchronize()
         is_primary = name == primary
         steps = args.steps if is_primary else max(1, min(args.steps, 10))
