@@ -224,7 +224,7 @@ class Workload:
     """Device buffers and the step (a list of Ops) of one configuration."""
 
     n_src = 8
-    kernel_label = "zgb::rs_adamw_vec_kernel<8,true>"
+    kernel_label = "zgb::rs_adamw_vec_kernel<0,8> (bf16 sources x 8)"
 
     def __init__(self, device):
         from zero_sharded_mixed_gb300 import binding as zb
