@@ -98,6 +98,10 @@ def _load():
         lib.oracle_clip_coef.restype = f32
         lib.oracle_scale.argtypes = [p, i64, f32]
         lib.oracle_scale.restype = None
+        lib.oracle_quantize_int8.argtypes = [p, i64, i32, p, p]
+        lib.oracle_quantize_int8.restype = None
+        lib.oracle_dequantize_int8.argtypes = [p, p, i64, i32, p]
+        lib.oracle_dequantize_int8.restype = None
         _lib = lib
         return lib
 
@@ -286,3 +290,21 @@ def rs_adamw_reference(src, divisor, w, m, v, hp: AdamW, t: int, clip=None):
         g = scale(g, clip_coef(*clip))
     w2, m2, v2 = adamw(w, m, v, g, hp, t)
     return cast_bf16(w2), w2, m2, v2
+
+
+def quantize_int8(w_bf16, block: int = 256):
+    """One shard's bf16 weights -> (int8 q, fp32 per-block scales)."""
+    w = _u16(w_bf16).reshape(-1)
+    nb = -(-w.size // block)
+    q = np.empty(w.size, dtype=np.int8)
+    scales = np.empty(max(nb, 1), dtype=np.float32)
+    _load().oracle_quantize_int8(_ptr(w), w.size, block, _ptr(q), _ptr(scales))
+    return q, scales[:nb]
+
+
+def dequantize_int8(q, scales, block: int = 256):
+    q = np.ascontiguousarray(q, dtype=np.int8).reshape(-1)
+    scales = _f32(scales)
+    out = np.empty(q.size, dtype=np.uint16)
+    _load().oracle_dequantize_int8(_ptr(q), _ptr(scales), q.size, block, _ptr(out))
+    return out

@@ -340,3 +340,51 @@ void oracle_scale(float* g, int64_t n, float coef)
 {
     for (int64_t i = 0; i < n; ++i) g[i] = g[i] * coef;
 }
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit quantized weight gather (ZeRO++)                                    */
+/* ------------------------------------------------------------------------ */
+
+/* "ZeRO Optimizer, in depth" ("Offload and ZeRO++": zero_quantized_weights
+ * quantises the weight all-gather) and "ZeRO and FSDP" ("Fewer bytes on the
+ * wire": the weight all-gather quantized to 8 bits).  Reading taken (the
+ * pages give no format): each owner quantizes its own bf16 shard in blocks of
+ * `block` consecutive elements (the last block of a shard may be shorter);
+ * symmetric int8 with one fp32 scale per block, scale = max|w| / 127;
+ * q = round-half-even(w / scale), clamped to [-127, 127]; an all-zero block has
+ * scale 0 and q = 0.  A receiver rebuilds bf16 weights as the RNE bf16 cast of
+ * the fp32 product q * scale.  Weights must be finite. */
+
+void oracle_quantize_int8(const uint16_t* w, int64_t n, int32_t block, int8_t* q, float* scales)
+{
+    int64_t nb = n / block;
+    if (nb * block < n) nb += 1;
+    for (int64_t b = 0; b < nb; ++b) {
+        int64_t lo = b * block;
+        int64_t hi = lo + block < n ? lo + block : n;
+        float amax = 0.0f;
+        for (int64_t i = lo; i < hi; ++i) {
+            float a = fabsf(oracle_bf16_to_f32(w[i]));
+            if (a > amax) amax = a;
+        }
+        float s = amax / 127.0f;
+        scales[b] = s;
+        for (int64_t i = lo; i < hi; ++i) {
+            if (s == 0.0f) {
+                q[i] = 0;
+                continue;
+            }
+            float r = nearbyintf(oracle_bf16_to_f32(w[i]) / s);   /* ties to even */
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            q[i] = (int8_t)r;
+        }
+    }
+}
+
+void oracle_dequantize_int8(const int8_t* q, const float* scales, int64_t n, int32_t block,
+                            uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f32_to_bf16((float)q[i] * scales[i / block]);
+}
