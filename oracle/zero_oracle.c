@@ -350,10 +350,12 @@ void oracle_scale(float* g, int64_t n, float coef)
  * wire": the weight all-gather quantized to 8 bits).  Reading taken (the
  * pages give no format): each owner quantizes its own bf16 shard in blocks of
  * `block` consecutive elements (the last block of a shard may be shorter);
- * symmetric int8 with one fp32 scale per block, scale = max|w| / 127;
- * q = round-half-even(w / scale), clamped to [-127, 127]; an all-zero block has
- * scale 0 and q = 0.  A receiver rebuilds bf16 weights as the RNE bf16 cast of
- * the fp32 product q * scale.  Weights must be finite. */
+ * symmetric int8 with one fp32 scale per block, scale = max|w| / 127; each
+ * weight is multiplied by the block's inverse scale inv = 127 / max|w| (both
+ * one fp32 division per block) and rounded to the nearest integer, ties to
+ * even, clamped to [-127, 127]; an all-zero block has scale 0 and q = 0.  A
+ * receiver rebuilds bf16 weights as the RNE bf16 cast of the fp32 product
+ * q * scale.  Weights must be finite. */
 
 void oracle_quantize_int8(const uint16_t* w, int64_t n, int32_t block, int8_t* q, float* scales)
 {
@@ -367,14 +369,14 @@ void oracle_quantize_int8(const uint16_t* w, int64_t n, int32_t block, int8_t* q
             float a = fabsf(oracle_bf16_to_f32(w[i]));
             if (a > amax) amax = a;
         }
-        float s = amax / 127.0f;
-        scales[b] = s;
+        scales[b] = amax / 127.0f;
+        if (amax == 0.0f) {
+            for (int64_t i = lo; i < hi; ++i) q[i] = 0;
+            continue;
+        }
+        float inv = 127.0f / amax;
         for (int64_t i = lo; i < hi; ++i) {
-            if (s == 0.0f) {
-                q[i] = 0;
-                continue;
-            }
-            float r = nearbyintf(oracle_bf16_to_f32(w[i]) / s);   /* ties to even */
+            float r = nearbyintf(oracle_bf16_to_f32(w[i]) * inv);   /* ties to even */
             if (r > 127.0f) r = 127.0f;
             if (r < -127.0f) r = -127.0f;
             q[i] = (int8_t)r;
