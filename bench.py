@@ -17,7 +17,9 @@ same run and reported under "workloads", with fewer steps:
   accum-zero1/2  gradient accumulation, GPT-2-XL shapes, n_dp = 4, 4 micro-batches,
                  in the stage-1 and stage-2 orders;
   zero3          the per-unit gather / reduce-scatter / update path over the 34
-                 Llama-7B units at n_dp = 8.
+                 Llama-7B units at n_dp = 8;
+  zero3-int8     the same with 8-bit weight gathers (ZeRO++): each owner
+                 re-quantizes its shard after the update.
 Every launch is timed with CUDA events on its stream; `roofline` uses the
 dominant kernel's algorithmic bytes per launch over its average launch time.
 
@@ -60,7 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe",
-                                           "accum-zero1", "accum-zero2", "zero3"], default="gpt2xl",
+                                           "accum-zero1", "accum-zero2", "zero3", "zero3-int8"],
+                    default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
     ap.add_argument("--elems", type=int, default=0,
@@ -436,7 +439,7 @@ class Zero3Workload(Workload):
     shards, bf16 into each rank's own shard.  One set of 8 unit-gradient
     buffers (sized for the largest unit) serves every unit."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, elems=0):
         import torch
         from zero_sharded_mixed_gb300 import inputs
         from zero_sharded_mixed_gb300 import step as zstep
@@ -444,10 +447,11 @@ class Zero3Workload(Workload):
         zb = self.zb
         self.name = name
         self.zstep = zstep
+        self.int8 = name == "zero3-int8"
         n_dp = 8
         self.units = []
         total = 0
-        for i, numels in enumerate(inputs.llama7b_units()):
+        for i, numels in enumerate([[elems]] if elems else inputs.llama7b_units()):
             L = zb.zero_layout(numels, n_dp)
             P = L.padded_n
             w = _master(L.n, P, device)
@@ -463,12 +467,24 @@ class Zero3Workload(Workload):
         self._g = g
         self.A = torch.empty(cap, device=device)
         self.elems = total
-        self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
+        if self.int8:
+            self.qs = [zstep.Int8Shards(u.layout, 256, device) for u in self.units]
+            for u, q in zip(self.units, self.qs):
+                zstep.zero3_quantize(u, q)
+            # two 8-bit gathers (1 B read + 2 B written), RS, update, re-quantize (2 B read + 1 B written)
+            self.bytes_per_elem = 3 + 3 + (2 * n_dp + 4) + 30 + 3
+            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_vec_kernel<1>, "
+                                 "acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>")
+        else:
+            self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
+            self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>"
         self.dominant = "rs_adamw"
-        self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,true,false>, rs_adamw_vec_kernel<1,false>"
-        self.desc = {"workload": "llama7b_zero3_units", "model": "Llama-7B shapes",
+        self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else ""),
+                     "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
                      "ring_slots": 2}
+        if self.int8:
+            self.desc["quant_block"] = 256
         self.device_bytes = total * (12 + 2) + 2 * cap * 2 + g.numel() * 2 + cap * 4
 
     def ops(self, t):
@@ -477,13 +493,20 @@ class Zero3Workload(Workload):
         for i, u in enumerate(self.units):
             P = u.layout.padded_n
             grads = [self._g[r, :P] for r in range(u.layout.n_dp)]
+            q = self.qs[i] if self.int8 else None
 
-            def fwd(u=u, i=i):
-                zs.zero3_gather(u, self.ring, ("fwd", i))
+            def fwd(u=u, i=i, q=q):
+                if q is not None:
+                    zs.zero3_gather_int8(u, q, self.ring, ("fwd", i))
+                else:
+                    zs.zero3_gather(u, self.ring, ("fwd", i))
                 self.ring.release(("fwd", i))
 
-            def bwd_gather(u=u, i=i):
-                zs.zero3_gather(u, self.ring, ("bwd", i))
+            def bwd_gather(u=u, i=i, q=q):
+                if q is not None:
+                    zs.zero3_gather_int8(u, q, self.ring, ("bwd", i))
+                else:
+                    zs.zero3_gather(u, self.ring, ("bwd", i))
 
             def rs(u=u, i=i, P=P, grads=grads):
                 zs.zero3_layer_reduce_scatter(u, grads, self.A[:P])
@@ -492,10 +515,16 @@ class Zero3Workload(Workload):
             def upd(u=u, P=P):
                 zs.zero3_update(u, self.A[:P], hp)
 
-            out.append(Op("gather", P * 4, fwd))
-            out.append(Op("gather", P * 4, bwd_gather))
+            gkind, gbytes = ("gather_int8", P * 3 + q.nb * u.layout.n_dp * 4) if q is not None \
+                else ("gather", P * 4)
+            out.append(Op(gkind, gbytes, fwd))
+            out.append(Op(gkind, gbytes, bwd_gather))
             out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
             out.append(Op("rs_adamw", P * 30, upd))
+            if q is not None:
+                def quant(u=u, q=q):
+                    zs.zero3_quantize(u, q)
+                out.append(Op("quantize_int8", P * 3 + q.nb * u.layout.n_dp * 4, quant))
         return out
 
 
@@ -506,8 +535,8 @@ def make_workload(name, device, elems=0):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
-    if name == "zero3":
-        return Zero3Workload(name, device)
+    if name in ("zero3", "zero3-int8"):
+        return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
 
@@ -641,7 +670,7 @@ def run_ours(args):
     peak, peak_kind = _peak()
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "accum-zero1", "accum-zero2",
-                          "zero3") if w != primary]
+                          "zero3", "zero3-int8") if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
     if args.elems:

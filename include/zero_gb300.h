@@ -224,6 +224,30 @@ int zero_reduce_scatter_adamw_clip(const zero_layout_t* L,
 int zero_gather_layer(const zero_layout_t* unit, const uint16_t* const* shards,
                       uint16_t* full_out, void* stream);
 
+/* ---- stage-3 gather with 8-bit weights (ZeRO++) ---------------------------
+ * "ZeRO Optimizer, in depth", "Offload and ZeRO++" (zero_quantized_weights
+ * quantises the weight all-gather) and "ZeRO and FSDP", "Fewer bytes on the
+ * wire" (the weight all-gather quantized to 8 bits).  Format: each rank's bf16
+ * shard in blocks of `block` consecutive elements (block = 256, 512, 1024 or
+ * 2048; a shard's last block may be shorter), symmetric int8 with one fp32
+ * scale per block: scale = max|w| / 127 (fp32), q = round-half-even(w / scale)
+ * clamped to [-127, 127]; an all-zero block has scale 0.  Weights must be finite.
+ *
+ * zero_quantize_int8: shards_bf16 holds the unit's n_dp shards back to back
+ *   (padded_n bf16, rank o's at [o*S]); q receives the same layout in int8 and
+ *   scales receives n_dp * ceil(S / block) fp32, rank o's at [o * ceil(S/block)].
+ * zero_gather_layer_int8: q_shards[o] (S int8) and scale_shards[o]
+ *   (ceil(S / block) fp32) are rank o's quantized shard; full_out (padded_n
+ *   bf16) receives full[o*S + k] = bf16_rne(q_o[k] * scale_o[k / block]).
+ * Vector kernels need S % 8 == 0, 16-byte aligned bf16 buffers and 8-byte
+ * aligned int8 buffers; anything else runs element by element on the GPU.
+ * Errors: ZERO_EINVAL (null, bad block, pointer kind), ZERO_EALIGN, ZERO_ECUDA. */
+int zero_quantize_int8(const zero_layout_t* unit, const uint16_t* shards_bf16, int8_t* q,
+                       float* scales, int32_t block, void* stream);
+int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* const* q_shards,
+                           const float* const* scale_shards, int32_t block, uint16_t* full_out,
+                           void* stream);
+
 /* ---- gradient accumulation / stage-3 layer reduce-scatter ----------------
  * "ZeRO and FSDP", "The idea, one stage at a time", paragraph on gradient
  * accumulation: stage 1 adds each micro-batch's full local gradient into a full

@@ -87,6 +87,8 @@ def load():
         lib.zero_grad_norm_sq_static.argtypes = [P(ZeroLayout), P(p), i32, i32, i64, f32, i64,
                                                  i64, p, i32, p]
         lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
+        lib.zero_quantize_int8.argtypes = [P(ZeroLayout), p, p, p, i32, p]
+        lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
         lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
                                         i32, p]
         lib.zero_status_check.argtypes = [p]
@@ -99,7 +101,7 @@ def load():
         for name in ("zero_layout", "zero_bucket_range", "zero_shard_range",
                      "zero_reduce_scatter_adamw", "zero_reduce_scatter_adamw_clip",
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
-                     "zero_grad_norm_sq_static",
+                     "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -339,3 +341,29 @@ def zero_accumulate(L: ZeroLayout, mode: int, srcs, src_dtype: int, src_base: in
 
 def zero_status_check(stream=None):
     _check(load().zero_status_check(_stream_ptr(stream)), "zero_status_check")
+
+
+def zero_quantize_int8(unit: ZeroLayout, shards: torch.Tensor, q: torch.Tensor, scales: torch.Tensor,
+                       block: int = 256, stream=None):
+    """Quantize the unit's n_dp bf16 shards (back to back) to int8 + fp32 block scales."""
+    nb = -(-unit.shard // block) if unit.shard else 0
+    rc = load().zero_quantize_int8(
+        ctypes.byref(unit), _tensor(shards, "shards", torch.bfloat16, unit.padded_n),
+        _tensor(q, "q", torch.int8, unit.padded_n),
+        _tensor(scales, "scales", torch.float32, nb * unit.n_dp), int(block), _stream_ptr(stream))
+    _check(rc, "zero_quantize_int8")
+
+
+def zero_gather_layer_int8(unit: ZeroLayout, q_shards, scale_shards, full_out: torch.Tensor,
+                           block: int = 256, stream=None):
+    """Rebuild the full bf16 unit from each rank's int8 shard and block scales."""
+    if len(q_shards) != unit.n_dp or len(scale_shards) != unit.n_dp:
+        raise ValueError(f"need {unit.n_dp} shards and scale arrays")
+    nb = -(-unit.shard // block) if unit.shard else 0
+    qp = [_tensor(x, f"q_shards[{i}]", torch.int8, unit.shard) for i, x in enumerate(q_shards)]
+    sp = [_tensor(x, f"scale_shards[{i}]", torch.float32, nb) for i, x in enumerate(scale_shards)]
+    rc = load().zero_gather_layer_int8(
+        ctypes.byref(unit), (ctypes.c_void_p * max(1, len(qp)))(*qp),
+        (ctypes.c_void_p * max(1, len(sp)))(*sp), int(block),
+        _tensor(full_out, "full_out", torch.bfloat16, unit.padded_n), _stream_ptr(stream))
+    _check(rc, "zero_gather_layer_int8")

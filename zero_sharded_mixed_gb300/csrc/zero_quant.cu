@@ -1,0 +1,306 @@
+// 8-bit quantized weight gather for stage 3 (ZeRO++), sm_103a.
+//
+// "ZeRO Optimizer, in depth", "Offload and ZeRO++": zero_quantized_weights
+// quantises the weight all-gather; "ZeRO and FSDP", "Fewer bytes on the wire":
+// the weight all-gather is quantized to 8 bits.  Each owner quantizes its own
+// bf16 shard in blocks of `block` consecutive elements (symmetric int8, one
+// fp32 scale per block: scale = max|w| / 127; q = round-half-even(w * inv)
+// with inv = 127 / max|w|, clamped to [-127, 127]; a zero block has scale 0),
+// and the gather rebuilds the full bf16 unit as bf16_rne(q * scale).  A
+// receiver then reads 1 byte per weight plus 4 bytes per block instead of 2.
+//
+// zero_quantize_int8: a warp quantizes whole blocks, several per iteration
+//   (loads first).  Each lane loads its 8-element vectors of a block (block /
+//   256 of them).  The block maximum of |w| is taken on the bf16 bit patterns:
+//   for finite values |w| orders as (bits & 0x7fff) does, so two elements go
+//   through one SIMD max (vmax2), and the warp finishes with one redux.sync.
+//   Each element is then one multiply by inv and one add of 1.5 * 2^23, which
+//   rounds to the nearest integer, ties to even (the sum lies in [2^23, 2^24)
+//   where fp32 spacing is 1); the low byte of the sum's bits is the int8
+//   code.  |w * inv| <= 127 * (1 + 2^-23), so no clamp is needed.  About five
+//   instructions per element; 2 bytes read + 1 byte written (+4 per block).
+// zero_gather_layer_int8: blockIdx.y picks the shard; a grid-stride loop over
+//   8-element vectors (four per thread and iteration, loads first) loads 8
+//   int8 values and their block's scale, multiplies in fp32 and stores 8 bf16
+//   (cvt.rn.bf16x2).  1 byte read + 2 written per element (+ the scales).
+#include "zero_common.cuh"
+
+namespace zgb {
+
+constexpr int kWarps = kThreads / 32;
+
+struct QuantParams {
+    const uint16_t* w;   // n_dp shards of S bf16, back to back
+    int8_t* q;           // same layout
+    float* scales;       // n_dp x blocks_per_shard
+    int64_t shard;       // S
+    int64_t blocks_per_shard;
+    int64_t total_blocks;
+    int32_t block;
+};
+
+// The int8 code of x * inv (|x * inv| <= 127.00002): add 1.5 * 2^23 in fp32,
+// which rounds to the nearest integer with ties to even; the low byte of the
+// sum's bits holds the code in two's complement.
+__device__ __forceinline__ uint32_t code_bits(float x, float inv) {
+    return __float_as_uint(__fadd_rn(__fmul_rn(x, inv), 12582912.0f));
+}
+
+// Eight codes from eight bf16 weights (one 16-byte vector) packed into 8 bytes.
+__device__ __forceinline__ uint2 quant8(const uint4 raw, float inv) {
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t c[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        c[2 * k] = code_bits(bf16_lo(w4[k]), inv);
+        c[2 * k + 1] = code_bits(bf16_hi(w4[k]), inv);
+    }
+    const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+    return make_uint2(lo, hi);
+}
+
+// max over the 8 bf16 of a vector of |w|, as a pair of 16-bit lanes
+__device__ __forceinline__ uint32_t absmax8_bits(const uint4 raw, uint32_t m) {
+    m = __vmaxu2(m, raw.x & 0x7fff7fffu);
+    m = __vmaxu2(m, raw.y & 0x7fff7fffu);
+    m = __vmaxu2(m, raw.z & 0x7fff7fffu);
+    return __vmaxu2(m, raw.w & 0x7fff7fffu);
+}
+
+__device__ __forceinline__ int8_t quant_one(float x, float amax) {
+    if (amax == 0.0f) return 0;
+    return (int8_t)(code_bits(x, __fdiv_rn(127.0f, amax)) & 0xffu);
+}
+
+// VPL = 8-element vectors per lane = block / 256; UB = quantization blocks a
+// warp takes per iteration (qb0, qb0 + nwarps, ...): every load of all UB
+// blocks is issued before the first reduction, so a warp keeps UB x VPL x 512
+// bytes in flight.
+template <int VPL, int UB>
+__global__ void __launch_bounds__(kThreads) quantize_vec_kernel(const __grid_constant__ QuantParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    for (int64_t qb0 = warp; qb0 < p.total_blocks; qb0 += UB * nwarps) {
+        uint4 raw[UB][VPL];
+        int64_t base[UB], len[UB], sidx[UB];
+        float amax[UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+            const int64_t qb = qb0 + u * nwarps;
+            amax[u] = 0.0f;
+            len[u] = 0;
+            if (qb < p.total_blocks) {
+                const int64_t o = qb / p.blocks_per_shard;
+                const int64_t b = qb - o * p.blocks_per_shard;
+                const int64_t k0 = b * p.block;                               // within the shard
+                len[u] = min((int64_t)p.block, p.shard - k0);                // multiple of 8
+                base[u] = o * p.shard + k0;
+                sidx[u] = o * p.blocks_per_shard + b;
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) {
+                    const int64_t off = (int64_t)(j * 32 + lane) * 8;
+                    if (off < len[u]) raw[u][j] = ld_stream_u4(p.w + base[u] + off);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+            uint32_t m = 0u;
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                if ((int64_t)(j * 32 + lane) * 8 < len[u]) m = absmax8_bits(raw[u][j], m);
+            m = __reduce_max_sync(0xffffffffu, (m & 0xffffu) > (m >> 16) ? (m & 0xffffu) : (m >> 16));
+            amax[u] = bf16_one((uint16_t)m);
+        }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+            if (len[u] == 0) continue;                                  // uniform across the warp
+            const float a = amax[u];
+            if (lane == 0) p.scales[sidx[u]] = __fdiv_rn(a, 127.0f);
+            const float inv = a == 0.0f ? 0.0f : __fdiv_rn(127.0f, a);  // a zero block: codes 0
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                const int64_t off = (int64_t)(j * 32 + lane) * 8;
+                if (off < len[u])
+                    *reinterpret_cast<uint2*>(p.q + base[u] + off) = quant8(raw[u][j], inv);
+            }
+        }
+    }
+}
+
+// One thread per quantization block: ragged shards and unaligned buffers.
+__global__ void __launch_bounds__(kThreads) quantize_scalar_kernel(const __grid_constant__ QuantParams p) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t qb = (int64_t)blockIdx.x * kThreads + threadIdx.x; qb < p.total_blocks; qb += stride) {
+        const int64_t o = qb / p.blocks_per_shard;
+        const int64_t b = qb - o * p.blocks_per_shard;
+        const int64_t k0 = b * p.block;
+        const int64_t len = min((int64_t)p.block, p.shard - k0);
+        const int64_t base = o * p.shard + k0;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < len; ++i) amax = fmaxf(amax, fabsf(bf16_one(p.w[base + i])));
+        p.scales[o * p.blocks_per_shard + b] = __fdiv_rn(amax, 127.0f);
+        for (int64_t i = 0; i < len; ++i) p.q[base + i] = quant_one(bf16_one(p.w[base + i]), amax);
+    }
+}
+
+struct DequantParams {
+    const int8_t* q[ZERO_MAX_SRC];
+    const float* scales[ZERO_MAX_SRC];
+    uint16_t* out;       // the first of these shards' places in the full buffer
+    int64_t shard;
+    int32_t block;
+};
+
+__device__ __forceinline__ uint4 dequant8(const uint2 raw, const float s) {
+    const uint32_t w2[2] = {raw.x, raw.y};
+    uint32_t o4[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float f0 = (float)(int8_t)(w2[h] & 0xffu);
+        const float f1 = (float)(int8_t)((w2[h] >> 8) & 0xffu);
+        const float f2 = (float)(int8_t)((w2[h] >> 16) & 0xffu);
+        const float f3 = (float)(int8_t)(w2[h] >> 24);
+        o4[2 * h] = pack_bf16x2(__fmul_rn(f0, s), __fmul_rn(f1, s));
+        o4[2 * h + 1] = pack_bf16x2(__fmul_rn(f2, s), __fmul_rn(f3, s));
+    }
+    return make_uint4(o4[0], o4[1], o4[2], o4[3]);
+}
+
+// Four 8-element vectors per thread and iteration, loads first.
+__global__ void __launch_bounds__(kThreads) dequant_gather_vec_kernel(const __grid_constant__ DequantParams p) {
+    constexpr int U = 4;
+    const int8_t* q = p.q[blockIdx.y];
+    const float* sc = p.scales[blockIdx.y];
+    uint16_t* dst = p.out + (int64_t)blockIdx.y * p.shard;
+    const int64_t nv = p.shard >> 3;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t vi = (int64_t)blockIdx.x * kThreads + threadIdx.x; vi < nv; vi += U * stride) {
+        uint2 raw[U];
+        float s[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t k = (vi + u * stride) * 8;
+            if (vi + u * stride < nv) {
+                raw[u] = __ldcs(reinterpret_cast<const uint2*>(q + k));
+                s[u] = __ldg(sc + k / p.block);                      // one block: block % 8 == 0
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (vi + u * stride < nv) st_stream_u4(dst + (vi + u * stride) * 8, dequant8(raw[u], s[u]));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_gather_scalar_kernel(const __grid_constant__ DequantParams p) {
+    const int8_t* q = p.q[blockIdx.y];
+    const float* sc = p.scales[blockIdx.y];
+    uint16_t* dst = p.out + (int64_t)blockIdx.y * p.shard;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < p.shard; k += stride)
+        dst[k] = to_bf16(__fmul_rn((float)q[k], sc[k / p.block]));
+}
+
+bool valid_block(int32_t block) {
+    return block >= 256 && block <= 2048 && block % 256 == 0 && (block & (block - 1)) == 0;
+}
+
+}  // namespace zgb
+
+extern "C" int zero_quantize_int8(const zero_layout_t* unit, const uint16_t* shards_bf16, int8_t* q,
+                                  float* scales, int32_t block, void* stream) {
+    using namespace zgb;
+    if (!unit || !shards_bf16 || !q || !scales) return ZERO_EINVAL;
+    if (!valid_block(block)) return ZERO_EINVAL;
+    if (unit->n_dp < 1 || unit->shard < 0 || unit->padded_n != unit->shard * (int64_t)unit->n_dp)
+        return ZERO_EINVAL;
+    if (check_aligned(shards_bf16, 2) || check_aligned(scales, 4)) return ZERO_EALIGN;
+    if (unit->shard == 0) return ZERO_OK;
+    if (check_device_ptr(shards_bf16) || check_device_ptr(q) || check_device_ptr(scales))
+        return ZERO_EINVAL;
+    QuantParams p;
+    p.w = shards_bf16;
+    p.q = q;
+    p.scales = scales;
+    p.shard = unit->shard;
+    p.block = block;
+    p.blocks_per_shard = (unit->shard + block - 1) / block;
+    p.total_blocks = p.blocks_per_shard * unit->n_dp;
+    const bool vec = unit->shard % 8 == 0 && aligned16(shards_bf16) &&
+                     (reinterpret_cast<uintptr_t>(q) & 7u) == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!vec) {
+        static int occ = 0;
+        if (occ == 0) occ = ctas_per_sm((const void*)quantize_scalar_kernel, kThreads, 0);
+        quantize_scalar_kernel<<<grid_for(p.total_blocks, kThreads, (int64_t)sm_count() * occ), kThreads, 0, s>>>(p);
+        return launch_status();
+    }
+    // four 256-element blocks, or two 512-element blocks, per warp iteration
+    static int occ[4] = {0, 0, 0, 0};
+    const void* fns[4] = {(const void*)quantize_vec_kernel<1, 4>, (const void*)quantize_vec_kernel<2, 2>,
+                          (const void*)quantize_vec_kernel<4, 1>, (const void*)quantize_vec_kernel<8, 1>};
+    const int which = block == 256 ? 0 : block == 512 ? 1 : block == 1024 ? 2 : 3;
+    if (occ[which] == 0) occ[which] = ctas_per_sm(fns[which], kThreads, 0);
+    const unsigned grid = grid_for(p.total_blocks, kWarps, (int64_t)sm_count() * occ[which]);
+    switch (which) {
+        case 0: quantize_vec_kernel<1, 4><<<grid, kThreads, 0, s>>>(p); break;
+        case 1: quantize_vec_kernel<2, 2><<<grid, kThreads, 0, s>>>(p); break;
+        case 2: quantize_vec_kernel<4, 1><<<grid, kThreads, 0, s>>>(p); break;
+        default: quantize_vec_kernel<8, 1><<<grid, kThreads, 0, s>>>(p); break;
+    }
+    return launch_status();
+}
+
+extern "C" int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* const* q_shards,
+                                      const float* const* scale_shards, int32_t block,
+                                      uint16_t* full_out, void* stream) {
+    using namespace zgb;
+    if (!unit || !q_shards || !scale_shards || !full_out) return ZERO_EINVAL;
+    if (!valid_block(block)) return ZERO_EINVAL;
+    if (unit->n_dp < 1 || unit->shard < 0 || unit->padded_n != unit->shard * (int64_t)unit->n_dp)
+        return ZERO_EINVAL;
+    const int n_dp = unit->n_dp;
+    for (int o = 0; o < n_dp; ++o)
+        if (!q_shards[o] || !scale_shards[o]) return ZERO_EINVAL;
+    for (int o = 0; o < n_dp; ++o)
+        if (check_aligned(scale_shards[o], 4)) return ZERO_EALIGN;
+    if (check_aligned(full_out, 2)) return ZERO_EALIGN;
+    if (unit->shard == 0) return ZERO_OK;
+    for (int o = 0; o < n_dp; ++o)
+        if (check_device_ptr(q_shards[o]) || check_device_ptr(scale_shards[o])) return ZERO_EINVAL;
+    if (check_device_ptr(full_out)) return ZERO_EINVAL;
+    static int occ_vec = 0, occ_scalar = 0;
+    if (occ_vec == 0) occ_vec = ctas_per_sm((const void*)dequant_gather_vec_kernel, kThreads, 0);
+    if (occ_scalar == 0) occ_scalar = ctas_per_sm((const void*)dequant_gather_scalar_kernel, kThreads, 0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int o0 = 0; o0 < n_dp; o0 += ZERO_MAX_SRC) {
+        const int cnt = n_dp - o0 < ZERO_MAX_SRC ? n_dp - o0 : ZERO_MAX_SRC;
+        DequantParams p;
+        bool vec = unit->shard % 8 == 0;
+        for (int k = 0; k < ZERO_MAX_SRC; ++k) {
+            p.q[k] = nullptr;
+            p.scales[k] = nullptr;
+        }
+        for (int k = 0; k < cnt; ++k) {
+            p.q[k] = q_shards[o0 + k];
+            p.scales[k] = scale_shards[o0 + k];
+            vec = vec && (reinterpret_cast<uintptr_t>(p.q[k]) & 7u) == 0;
+        }
+        p.out = full_out + (int64_t)o0 * unit->shard;
+        p.shard = unit->shard;
+        p.block = block;
+        vec = vec && aligned16(p.out);
+        const int64_t resident = (int64_t)sm_count() * (vec ? occ_vec : occ_scalar);
+        const int64_t per_shard = resident / cnt > 0 ? resident / cnt : 1;
+        dim3 grid(grid_for(vec ? unit->shard >> 3 : unit->shard, kThreads, per_shard), cnt);
+        if (vec)
+            dequant_gather_vec_kernel<<<grid, kThreads, 0, s>>>(p);
+        else
+            dequant_gather_scalar_kernel<<<grid, kThreads, 0, s>>>(p);
+        const int rc = launch_status();
+        if (rc) return rc;
+    }
+    return ZERO_OK;
+}

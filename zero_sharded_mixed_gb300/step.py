@@ -251,3 +251,38 @@ class HostPipeline:
                 host_out[s:e].copy_(out[s:e], non_blocking=True)
             self.ev_out.record(self.d2h)
         comp.wait_event(self.ev_out)     # the step ends when the result is on the host
+
+
+# --------------------------------------------------------------------------
+# ZeRO-3 with 8-bit weight gathers ("ZeRO Optimizer, in depth", "Offload and
+# ZeRO++": zero_quantized_weights)
+# --------------------------------------------------------------------------
+
+class Int8Shards:
+    """A unit's quantized shards: int8 [n_dp, S] and fp32 block scales
+    [n_dp, ceil(S / block)], what each rank would send in the all-gather."""
+
+    def __init__(self, layout, block: int = 256, device="cuda"):
+        self.layout = layout
+        self.block = block
+        self.nb = -(-layout.shard // block) if layout.shard else 0
+        self.q = torch.empty((layout.n_dp, layout.shard), dtype=torch.int8, device=device)
+        self.scales = torch.empty((layout.n_dp, max(self.nb, 1)), dtype=torch.float32, device=device)
+
+    def wire_bytes(self) -> int:
+        return self.q.numel() + self.layout.n_dp * self.nb * 4
+
+
+def zero3_quantize(unit: Zero3Unit, qs: Int8Shards, stream=None):
+    """Each owner quantizes its bf16 shard (after its update) for the next gathers."""
+    zb.zero_quantize_int8(unit.layout, unit.shards.view(-1), qs.q.view(-1), qs.scales.view(-1),
+                          qs.block, stream)
+
+
+def zero3_gather_int8(unit: Zero3Unit, qs: Int8Shards, ring: GatherRing, unit_id,
+                      stream=None) -> torch.Tensor:
+    buf = ring.acquire(unit_id, unit.layout.padded_n)
+    n = unit.layout.n_dp
+    zb.zero_gather_layer_int8(unit.layout, [qs.q[o] for o in range(n)],
+                              [qs.scales[o] for o in range(n)], buf, qs.block, stream)
+    return buf
