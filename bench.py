@@ -18,6 +18,8 @@ same run and reported under "workloads", with fewer steps:
                  in the stage-1 and stage-2 orders;
   zero3          the per-unit gather / reduce-scatter / update path over the 34
                  Llama-7B units at n_dp = 8;
+  zero3-prefetch the same with each unit's gather issued one unit ahead on a
+                 side stream (at most two units resident);
   zero3-int8     the same with 8-bit weight gathers (ZeRO++): each owner
                  re-quantizes its shard after the update.
 Every launch is timed with CUDA events on its stream; `roofline` uses the
@@ -62,7 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe",
-                                           "accum-zero1", "accum-zero2", "zero3", "zero3-int8"],
+                                           "accum-zero1", "accum-zero2", "zero3", "zero3-int8",
+                                           "zero3-prefetch"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -448,6 +451,7 @@ class Zero3Workload(Workload):
         self.name = name
         self.zstep = zstep
         self.int8 = name == "zero3-int8"
+        self.prefetch = name == "zero3-prefetch"
         n_dp = 8
         self.units = []
         total = 0
@@ -479,7 +483,12 @@ class Zero3Workload(Workload):
             self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
             self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>"
         self.dominant = "rs_adamw"
-        self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else ""),
+        if self.prefetch:
+            self.dominant = "zero3_step_prefetched"
+            self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
+            self.pf = zstep.Zero3Prefetcher(self.units, self.ring, device=device)
+        self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else "")
+                     + ("_prefetch" if self.prefetch else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
                      "ring_slots": 2}
@@ -490,6 +499,13 @@ class Zero3Workload(Workload):
     def ops(self, t):
         zb, hp, zs = self.zb, self.hp(t), self.zstep
         out = []
+        if self.prefetch:
+            def step_all():
+                zs.zero3_step_prefetched(
+                    self.pf, lambda i: [self._g[r, :self.units[i].layout.padded_n]
+                                        for r in range(self.units[i].layout.n_dp)], self.A, hp)
+            out.append(Op("zero3_step_prefetched", self.elems * self.bytes_per_elem, step_all))
+            return out
         for i, u in enumerate(self.units):
             P = u.layout.padded_n
             grads = [self._g[r, :P] for r in range(u.layout.n_dp)]
@@ -535,7 +551,7 @@ def make_workload(name, device, elems=0):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
-    if name in ("zero3", "zero3-int8"):
+    if name in ("zero3", "zero3-int8", "zero3-prefetch"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -670,7 +686,7 @@ def run_ours(args):
     peak, peak_kind = _peak()
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "accum-zero1", "accum-zero2",
-                          "zero3", "zero3-int8") if w != primary]
+                          "zero3", "zero3-prefetch", "zero3-int8") if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
     if args.elems:

@@ -47,7 +47,9 @@ enum {
     ZERO_EALIGN = -2,   /* a pointer is not aligned to its element size */
     ZERO_ERANGE = -3,   /* a size does not fit (int64 overflow, too many sources) */
     ZERO_ECUDA = -4,    /* the CUDA runtime reported an error (launch or earlier async fault) */
-    ZERO_ETIMEOUT = -5  /* reserved: a bounded device-side wait gave up */
+    ZERO_ETIMEOUT = -5, /* reserved: a bounded device-side wait gave up */
+    ZERO_EIO = -6,      /* a checkpoint file could not be opened, written or read */
+    ZERO_ECORRUPT = -7  /* a checkpoint file has a wrong magic, version or CRC */
 };
 
 /* ---- enums -------------------------------------------------------------- */
@@ -289,6 +291,42 @@ int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,
                           int64_t begin, int64_t end, float* master, float* m, float* v,
                           uint16_t* out_bf16, int32_t out_mode, const zero_adamw_t* hp,
                           void* stream);
+
+/* ---- sharded checkpoints ---------------------------------------------------
+ * "ZeRO Optimizer, in depth", "Checkpoints: sharded on the way in, consolidated
+ * on the way out": every rank writes its own shard of model and optimizer
+ * state plus a small metadata file; a consolidation step rebuilds one plain
+ * full-precision state, and a layout change (another GPU count) needs a
+ * conversion.  These calls handle one rank's shard file; HOST buffers only
+ * (the caller copies device shards to host memory and back).
+ *
+ * File: a fixed header (magic "ZGBSHARD", version 1, the header struct below,
+ * a flag for bf16 weights, the CRC-32 of the payload) followed by master[S],
+ * m[S], v[S] (fp32) and, when w_bf16 is given, the rank's bf16 weights[S].
+ * zero_ckpt_write_shard: ZERO_EINVAL (inconsistent header), ZERO_EIO.
+ * zero_ckpt_read_header: reads and checks magic and version only.
+ * zero_ckpt_read_shard: capacity = elements each output holds; checks magic,
+ *   version and the payload CRC (ZERO_ECORRUPT), the size (ZERO_ERANGE); w_bf16
+ *   may be NULL even when the file holds bf16 weights.
+ * zero_crc32: the reflected CRC-32 of IEEE 802.3 (poly 0xEDB88320). */
+typedef struct {
+    int64_t n;            /* real elements of the flat vector */
+    int64_t padded_n;     /* n_dp * shard */
+    int64_t shard;        /* S */
+    int64_t align;
+    int64_t step;         /* optimizer steps taken (t of the last update) */
+    int32_t n_dp;
+    int32_t rank;         /* whose shard this file holds */
+    float lr, beta1, beta2, eps, weight_decay;
+    int32_t reserved;
+} zero_ckpt_header_t;
+
+int zero_ckpt_write_shard(const char* path, const zero_ckpt_header_t* h, const float* master,
+                          const float* m, const float* v, const uint16_t* w_bf16);
+int zero_ckpt_read_header(const char* path, zero_ckpt_header_t* h, int32_t* has_bf16);
+int zero_ckpt_read_shard(const char* path, zero_ckpt_header_t* h, float* master, float* m,
+                         float* v, uint16_t* w_bf16, int64_t capacity);
+uint32_t zero_crc32(const void* data, int64_t n);
 
 /* ---- status ---------------------------------------------------------------
  * Synchronizes `stream` and returns ZERO_ECUDA if it (or an earlier launch on

@@ -1,0 +1,102 @@
+"""Sharded checkpoints on the host (no GPU): the shard file round trip, the
+CRC-32 against zlib's (a library routine), corruption detection, consolidation
+(padding dropped, tensors split at their offsets) and resharding to another
+number of ranks."""
+import zlib as zlib_ref
+
+import numpy as np
+import pytest
+import torch
+
+from zero_sharded_mixed_gb300 import binding as zb
+from zero_sharded_mixed_gb300 import checkpoint as ck
+
+
+def _state(P, seed):
+    rng = np.random.default_rng(seed)
+    return [torch.from_numpy((rng.standard_normal(P) * s).astype(np.float32)) for s in (0.02, 1e-4, 1e-8)]
+
+
+def test_crc32_matches_zlib(zlib):
+    for n in (0, 1, 7, 4096, 100_003):
+        data = np.random.default_rng(n).integers(0, 256, n, dtype=np.uint8)
+        assert ck.crc32(data) == (zlib_ref.crc32(data.tobytes()) & 0xFFFFFFFF)
+
+
+def test_shard_round_trip_and_corruption(zlib, tmp_path):
+    S = 1000
+    h = zb.ZeroCkptHeader(3990, 4000, S, 8, 7, 4, 2, 1e-4, 0.9, 0.999, 1e-8, 0.1, 0)
+    rng = np.random.default_rng(0)
+    a = [rng.standard_normal(S).astype(np.float32) for _ in range(3)]
+    w = rng.integers(0, 1 << 16, S).astype(np.uint16)
+    p = str(tmp_path / "r.bin")
+    ck.write_shard(p, h, *a, w)
+    h2, m, mm, v, w2 = ck.read_shard(p, with_bf16=True)
+    for x, y in zip(a + [w], [m, mm, v, w2]):
+        np.testing.assert_array_equal(x, y)
+    assert (h2.rank, h2.step, h2.n_dp, h2.shard, h2.n) == (2, 7, 4, S, 3990)
+    # reading without the bf16 part still checks the whole payload
+    assert ck.read_shard(p)[4] is None
+    # one flipped byte anywhere in the payload is caught
+    raw = bytearray(open(p, "rb").read())
+    for pos in (len(raw) - 1, len(raw) - 2 * S - 5, len(raw) // 2):
+        bad = bytearray(raw)
+        bad[pos] ^= 0x40
+        open(p, "wb").write(bad)
+        with pytest.raises(zb.ZeroError) as e:
+            ck.read_shard(p)
+        assert e.value.code == zb.ZERO_ECORRUPT
+    open(p, "wb").write(b"not a shard file at all, definitely not")
+    with pytest.raises(zb.ZeroError) as e:
+        ck.read_shard(p)
+    assert e.value.code == zb.ZERO_ECORRUPT
+    with pytest.raises(zb.ZeroError) as e:
+        ck.read_shard(str(tmp_path / "missing.bin"))
+    assert e.value.code == zb.ZERO_EIO
+
+
+def test_header_validation(zlib, tmp_path):
+    x = np.zeros(8, np.float32)
+    for bad in [dict(rank=4), dict(n_dp=0), dict(padded_n=31), dict(n=33), dict(step=-1)]:
+        kw = dict(n=30, padded_n=32, shard=8, align=8, step=1, n_dp=4, rank=0)
+        kw.update(bad)
+        h = zb.ZeroCkptHeader(kw["n"], kw["padded_n"], kw["shard"], kw["align"], kw["step"],
+                              kw["n_dp"], kw["rank"], 0, 0, 0, 0, 0, 0)
+        with pytest.raises(zb.ZeroError) as e:
+            ck.write_shard(str(tmp_path / "x.bin"), h, x, x, x)
+        assert e.value.code == zb.ZERO_EINVAL
+
+
+def test_save_consolidate_reshard(zlib, tmp_path):
+    numels = [1000, 3, 4097, 50]
+    L = zb.zero_layout(numels, 4, align=8)
+    P, N = L.padded_n, L.n
+    master, m, v = _state(P, 1)
+    for t in (master, m, v):
+        t[N:] = 0
+    hp = zb.ZeroAdamW.make(step=5)
+    meta = ck.save(str(tmp_path / "a"), L, numels, master, m, v, 5, hp)
+    assert meta["n_dp"] == 4 and len(meta["crc32"]) == 4
+    flat = ck.consolidate(str(tmp_path / "a"))
+    assert flat["step"] == 5
+    for k, t in (("master", master), ("m", m), ("v", v)):
+        np.testing.assert_array_equal(flat[k], t[:N].numpy())
+    per = ck.consolidate(str(tmp_path / "a"), split=True)
+    assert [x["master"].size for x in per["tensors"]] == numels
+    np.testing.assert_array_equal(per["tensors"][2]["m"], m[1003:1003 + 4097].numpy())
+    # another GPU count: 4 -> 3 -> 7 ranks, the consolidated state is unchanged
+    ck.reshard(str(tmp_path / "a"), str(tmp_path / "b"), 3)
+    ck.reshard(str(tmp_path / "b"), str(tmp_path / "c"), 7, align=1)
+    for d in ("b", "c"):
+        again = ck.consolidate(str(tmp_path / d))
+        for k in ("master", "m", "v"):
+            np.testing.assert_array_equal(again[k], flat[k])
+    assert ck.load_meta(str(tmp_path / "c"))["n_dp"] == 7
+    # restoring into the original layout gives back every element, padding included
+    got = [torch.empty(P) for _ in range(3)]
+    assert ck.restore(str(tmp_path / "a"), L, *got) == 5
+    for a, b in zip(got, (master, m, v)):
+        assert torch.equal(a, b)
+    # and a layout mismatch is refused
+    with pytest.raises(ValueError):
+        ck.restore(str(tmp_path / "b"), L, *got)

@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_PKG, "libzero_gb300.so")
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ERANGE, ZERO_ECUDA, ZERO_ETIMEOUT = 0, -1, -2, -3, -4, -5
+ZERO_EIO, ZERO_ECORRUPT = -6, -7
 ZERO_BF16, ZERO_F32 = 0, 1
 ZERO_OUT_FULL, ZERO_OUT_SHARD = 0, 1
 ZERO_ACC_LOCAL, ZERO_ACC_REDUCE = 0, 1
@@ -40,6 +41,14 @@ class ZeroLayout(ctypes.Structure):
 
     def __repr__(self):
         return f"ZeroLayout({self.as_dict()})"
+
+
+class ZeroCkptHeader(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("padded_n", ctypes.c_int64), ("shard", ctypes.c_int64),
+                ("align", ctypes.c_int64), ("step", ctypes.c_int64), ("n_dp", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
 
 
 class ZeroAdamW(ctypes.Structure):
@@ -88,6 +97,11 @@ def load():
                                                  i64, p, i32, p]
         lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
         lib.zero_quantize_int8.argtypes = [P(ZeroLayout), p, p, p, i32, p]
+        lib.zero_ckpt_write_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p]
+        lib.zero_ckpt_read_header.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), P(i32)]
+        lib.zero_ckpt_read_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p, i64]
+        lib.zero_crc32.argtypes = [p, i64]
+        lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
         lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
                                         i32, p]
@@ -102,6 +116,7 @@ def load():
                      "zero_reduce_scatter_adamw", "zero_reduce_scatter_adamw_clip",
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
+                     "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
                      "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int

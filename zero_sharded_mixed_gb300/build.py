@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libzero_gb300.so")
 
 CUDA_SOURCES = ["zero_runtime.cu", "zero_rs_adamw.cu", "zero_accumulate.cu", "zero_gather.cu",
                 "zero_norm.cu", "zero_quant.cu"]
-HOST_SOURCES = ["zero_host.cpp"]
+HOST_SOURCES = ["zero_host.cpp", "zero_ckpt.cpp"]
 HEADERS = ["zero_common.cuh", "zero_update.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -83,6 +83,8 @@ extern "C" const char* zero_strerror(int code) {
         case ZERO_ERANGE: return "size out of range";
         case ZERO_ECUDA: return "CUDA runtime error";
         case ZERO_ETIMEOUT: return "device-side wait timed out";
+        case ZERO_EIO: return "checkpoint file I/O error";
+        case ZERO_ECORRUPT: return "checkpoint file corrupt (magic, version or CRC)";
         default: return "unknown status code";
     }
 }

@@ -286,3 +286,83 @@ def zero3_gather_int8(unit: Zero3Unit, qs: Int8Shards, ring: GatherRing, unit_id
     zb.zero_gather_layer_int8(unit.layout, [qs.q[o] for o in range(n)],
                               [qs.scales[o] for o in range(n)], buf, qs.block, stream)
     return buf
+
+
+# --------------------------------------------------------------------------
+# ZeRO-3 prefetch ("DeepSpeed ZeRO", "Stage 3 step by step": prefetching so
+# that the gather for the next layer overlaps with the compute of the current
+# one; "ZeRO and FSDP", "FSDP, ZeRO-3 inside PyTorch": with prefetching the
+# next unit is being gathered while the current one computes, so up to two
+# units are resident)
+# --------------------------------------------------------------------------
+
+class Zero3Prefetcher:
+    """Gathers units one ahead on a side stream into a two-slot GatherRing.
+
+    prefetch(i) first makes the side stream wait for everything already queued
+    on the caller's stream -- in particular the release of the slot's previous
+    unit and the last update of unit i's shards -- then enqueues the gather
+    and records an event; get(i) makes the caller's stream wait for that event.
+    """
+
+    def __init__(self, units, ring: GatherRing, int8=None, device=None):
+        self.units = units
+        self.ring = ring
+        self.int8 = int8
+        self.side = torch.cuda.Stream(device=device)
+        self.pending = {}
+
+    def prefetch(self, i, tag):
+        main = torch.cuda.current_stream()
+        issued = torch.cuda.Event()
+        issued.record(main)
+        self.side.wait_event(issued)
+        with torch.cuda.stream(self.side):
+            if self.int8 is not None:
+                buf = zero3_gather_int8(self.units[i], self.int8[i], self.ring, (tag, i), self.side)
+            else:
+                buf = zero3_gather(self.units[i], self.ring, (tag, i), self.side)
+            ready = torch.cuda.Event()
+            ready.record(self.side)
+        self.pending[(tag, i)] = (buf, ready)
+
+    def get(self, i, tag) -> torch.Tensor:
+        buf, ready = self.pending.pop((tag, i))
+        torch.cuda.current_stream().wait_event(ready)
+        return buf
+
+    def release(self, i, tag):
+        self.ring.release((tag, i))
+
+
+def zero3_step_prefetched(pf: Zero3Prefetcher, unit_grads, A: torch.Tensor, hp, compute=None):
+    """One stage-3 step over all units with gathers one unit ahead: forward in
+    order, backward in reverse (gather, compute, reduce-scatter the unit's
+    gradient, update its owned shards).  unit_grads(i) returns unit i's n_dp
+    bf16 gradient buffers; compute(i, gathered, phase) stands in for the
+    layer's work and may be None."""
+    units = pf.units
+    n = len(units)
+    if n == 0:
+        return
+    pf.prefetch(0, "fwd")
+    for i in range(n):
+        buf = pf.get(i, "fwd")
+        if i + 1 < n:
+            pf.prefetch(i + 1, "fwd")
+        if compute is not None:
+            compute(i, buf, "fwd")
+        pf.release(i, "fwd")
+    pf.prefetch(n - 1, "bwd")
+    for i in reversed(range(n)):
+        buf = pf.get(i, "bwd")
+        if i > 0:
+            pf.prefetch(i - 1, "bwd")
+        if compute is not None:
+            compute(i, buf, "bwd")
+        P = units[i].layout.padded_n
+        zero3_layer_reduce_scatter(units[i], unit_grads(i), A[:P])
+        pf.release(i, "bwd")
+        zero3_update(units[i], A[:P], hp)
+        if pf.int8 is not None:
+            zero3_quantize(units[i], pf.int8[i])
