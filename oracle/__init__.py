@@ -59,51 +59,55 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
-        i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
-        p = ctypes.c_void_p
-        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        lib.oracle_bf16_to_f32.restype = f32
-        lib.oracle_f32_to_bf16.argtypes = [f32]
-        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
-        lib.oracle_cast_bf16.argtypes = [p, p, i64]
-        lib.oracle_cast_bf16.restype = None
-        lib.oracle_layout.argtypes = [p, i32, i32, i64, i64, p, p]
-        lib.oracle_layout.restype = ctypes.c_int
-        lib.oracle_reduce_mean_bf16.argtypes = [p, i32, i64, i64, f32, p]
-        lib.oracle_reduce_mean_bf16.restype = None
-        lib.oracle_reduce_mean_f32.argtypes = [p, i32, i64, i64, f32, p]
-        lib.oracle_reduce_mean_f32.restype = None
-        lib.oracle_bias_corrections.argtypes = [f32, f32, i64, p, p]
-        lib.oracle_bias_corrections.restype = None
-        lib.oracle_adamw.argtypes = [p, p, p, p, i64, f32, f32, f32, f32, f32, i64]
-        lib.oracle_adamw.restype = None
-        lib.oracle_zero_step.argtypes = [p, i32, i64, p, p, p, p, i32,
-                                         f32, f32, f32, f32, f32, i64]
-        lib.oracle_zero_step.restype = ctypes.c_int
-        lib.oracle_dp_step.argtypes = [p, i32, i64, p, p, p, p,
-                                       f32, f32, f32, f32, f32, i64]
-        lib.oracle_dp_step.restype = ctypes.c_int
-        lib.oracle_accumulate_local.argtypes = [p, p, i64, i32]
-        lib.oracle_accumulate_local.restype = None
-        lib.oracle_accumulate_reduce.argtypes = [p, p, i32, i64, i64, i32]
-        lib.oracle_accumulate_reduce.restype = None
-        lib.oracle_all_gather_bf16.argtypes = [p, i32, i64, p]
-        lib.oracle_all_gather_bf16.restype = None
-        lib.oracle_grad_norm_sq_bf16.argtypes = [p, i32, i64, i64, f32]
-        lib.oracle_grad_norm_sq_bf16.restype = ctypes.c_double
-        lib.oracle_grad_norm_sq_f32.argtypes = [p, i32, i64, i64, f32]
-        lib.oracle_grad_norm_sq_f32.restype = ctypes.c_double
-        lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
-        lib.oracle_clip_coef.restype = f32
-        lib.oracle_scale.argtypes = [p, i64, f32]
-        lib.oracle_scale.restype = None
-        lib.oracle_quantize_int8.argtypes = [p, i64, i32, p, p]
-        lib.oracle_quantize_int8.restype = None
-        lib.oracle_dequantize_int8.argtypes = [p, p, i64, i32, p]
-        lib.oracle_dequantize_int8.restype = None
-        _lib = lib
-        return lib
+        _lib = configure(ctypes.CDLL(build()))
+        return _lib
+
+
+def configure(lib):
+    """Declare the C signatures on a loaded oracle library and return it."""
+    i64, i32, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    p = ctypes.c_void_p
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = f32
+    lib.oracle_f32_to_bf16.argtypes = [f32]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_cast_bf16.argtypes = [p, p, i64]
+    lib.oracle_cast_bf16.restype = None
+    lib.oracle_layout.argtypes = [p, i32, i32, i64, i64, p, p]
+    lib.oracle_layout.restype = ctypes.c_int
+    lib.oracle_reduce_mean_bf16.argtypes = [p, i32, i64, i64, f32, p]
+    lib.oracle_reduce_mean_bf16.restype = None
+    lib.oracle_reduce_mean_f32.argtypes = [p, i32, i64, i64, f32, p]
+    lib.oracle_reduce_mean_f32.restype = None
+    lib.oracle_bias_corrections.argtypes = [f32, f32, i64, p, p]
+    lib.oracle_bias_corrections.restype = None
+    lib.oracle_adamw.argtypes = [p, p, p, p, i64, f32, f32, f32, f32, f32, i64]
+    lib.oracle_adamw.restype = None
+    lib.oracle_zero_step.argtypes = [p, i32, i64, p, p, p, p, i32,
+                                     f32, f32, f32, f32, f32, i64]
+    lib.oracle_zero_step.restype = ctypes.c_int
+    lib.oracle_dp_step.argtypes = [p, i32, i64, p, p, p, p,
+                                   f32, f32, f32, f32, f32, i64]
+    lib.oracle_dp_step.restype = ctypes.c_int
+    lib.oracle_accumulate_local.argtypes = [p, p, i64, i32]
+    lib.oracle_accumulate_local.restype = None
+    lib.oracle_accumulate_reduce.argtypes = [p, p, i32, i64, i64, i32]
+    lib.oracle_accumulate_reduce.restype = None
+    lib.oracle_all_gather_bf16.argtypes = [p, i32, i64, p]
+    lib.oracle_all_gather_bf16.restype = None
+    lib.oracle_grad_norm_sq_bf16.argtypes = [p, i32, i64, i64, f32]
+    lib.oracle_grad_norm_sq_bf16.restype = ctypes.c_double
+    lib.oracle_grad_norm_sq_f32.argtypes = [p, i32, i64, i64, f32]
+    lib.oracle_grad_norm_sq_f32.restype = ctypes.c_double
+    lib.oracle_clip_coef.argtypes = [ctypes.c_double, f32]
+    lib.oracle_clip_coef.restype = f32
+    lib.oracle_scale.argtypes = [p, i64, f32]
+    lib.oracle_scale.restype = None
+    lib.oracle_quantize_int8.argtypes = [p, i64, i32, p, p]
+    lib.oracle_quantize_int8.restype = None
+    lib.oracle_dequantize_int8.argtypes = [p, p, i64, i32, p]
+    lib.oracle_dequantize_int8.restype = None
+    return lib
 
 
 def _ptr(a: np.ndarray) -> int:

@@ -1,0 +1,112 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source, on the CPU:
+a dropped term, a wrong sign, index, operand or constant, a rounding rule
+changed.  The copy is compiled, swapped in for the real oracle, and the pins
+of tests/test_oracle_*.py are run against it.  At least one must fail, or the
+pins would not have noticed that mistake.  Every planted mistake stays inside
+the arrays' bounds."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_cast as pc
+from tests import test_oracle_clip as pk
+from tests import test_oracle_layout as pl
+from tests import test_oracle_quant as pq
+from tests import test_oracle_step as ps
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "zero_oracle.c")
+
+# (what, exact text in the oracle, the mistake)
+MUTATIONS = [
+    ("bias correction of m dropped", "float m_hat = mi / bc1;", "float m_hat = mi;"),
+    ("Adam step with the wrong sign", "wi = wi - lr * (m_hat", "wi = wi + lr * (m_hat"),
+    ("eps inside the square root", "(sqrtf(v_hat) + eps)", "sqrtf(v_hat + eps)"),
+    ("weight decay dropped", "wi = wi - lr_wd * wi;", ";"),
+    ("beta1 used for v", "float vi = b2 * v[i]", "float vi = b1 * v[i]"),
+    ("gradient not squared in v", "one_minus_b2 * (gi * gi)", "one_minus_b2 * gi"),
+    ("bias-correction exponent off by one", "*bc1 = (float)(1.0 - pow((double)b1, (double)t));",
+     "*bc1 = (float)(1.0 - pow((double)b1, (double)(t + 1)));"),
+    ("mean divides by n_dp + 1", "shard,\n                                (float)n_dp, g);",
+     "shard,\n                                (float)(n_dp + 1), g);"),
+    ("rank reads the next rank's shard", "oracle_reduce_mean_bf16(grads + (int64_t)o * shard,",
+     "oracle_reduce_mean_bf16(grads + (int64_t)((o + 1) % n_dp) * shard,"),
+    ("sources summed in reverse order",
+     "s = s + src[(int64_t)r * ld + i];\n        g[i] = s / divisor;",
+     "s = s + src[(int64_t)(n_src - 1 - r) * ld + i];\n        g[i] = s / divisor;"),
+    ("bf16 ties rounded away from zero", "if (kept & 1u) kept += 1u;", "kept += 1u;"),
+    ("bf16 cast truncates", "if (dropped > 0x8000u) {", "if (dropped > 0xffffu) {"),
+    ("shard length not rounded up to the alignment", "if (shard * align < per_rank) shard += 1;", ";"),
+    ("shard length floors N / n_dp", "if (per_rank * n_dp < total) per_rank += 1;", ";"),
+    ("accumulation ignores the first flag", "acc[i] = first ? x : acc[i] + x;", "acc[i] = acc[i] + x;"),
+    ("gather concatenates in reverse rank order",
+     "full[(int64_t)o * shard + i] = shards[(int64_t)o * shard + i];",
+     "full[(int64_t)o * shard + i] = shards[(int64_t)(n_dp - 1 - o) * shard + i];"),
+    ("clip divides by the squared norm", "(sqrt(norm_sq) + 1e-6)", "(norm_sq + 1e-6)"),
+    ("clip coefficient not capped at 1", "return c < 1.0f ? c : 1.0f;", "return c;"),
+    ("8-bit scale uses 126", "float inv = 127.0f / amax;", "float inv = 126.0f / amax;"),
+    ("8-bit codes truncated", "nearbyintf(oracle_bf16_to_f32(w[i]) * inv)",
+     "truncf(oracle_bf16_to_f32(w[i]) * inv)"),
+    ("8-bit dequantization uses the first block's scale", "scales[i / block]", "scales[0]"),
+]
+
+
+def _pins():
+    """The pins, as (name, callable) -- parametrized ones with representative
+    arguments."""
+    return [
+        ("torch AdamW", ps.test_single_rank_matches_torch_adamw),
+        ("first-step closed form", ps.test_first_step_closed_form),
+        ("constant-gradient closed form", ps.test_constant_gradient_closed_form),
+        ("zero gradient", ps.test_zero_gradient_is_pure_decay),
+        ("bias corrections", ps.test_bias_corrections),
+        ("DP equivalence", lambda: ps.test_zero_step_equals_data_parallel(4, 4096, 8)),
+        ("DP equivalence ragged", lambda: ps.test_zero_step_equals_data_parallel(3, 1000, 1)),
+        ("shard gets its piece", ps.test_zero_step_shard_gets_its_own_gradient_piece),
+        ("dyadic mean", lambda: ps.test_mean_is_exact_for_dyadic_power_of_two(4)),
+        ("one rounding of the sum", lambda: ps.test_mean_is_one_rounding_of_exact_sum(3)),
+        ("summation order", ps.test_mean_fp32_rows_and_order),
+        ("accumulation orders", ps.test_accumulation_orders_agree_exactly_on_dyadic_inputs),
+        ("single micro-batch", ps.test_single_micro_batch_accumulation_is_the_mean),
+        ("first micro-batch overwrites", ps.test_first_micro_batch_overwrites_the_buffer),
+        ("gather", ps.test_all_gather_is_concatenation),
+        ("cast specials", pc.test_special_values),
+        ("cast low halves", pc.test_every_low_half_for_some_upper_halves),
+        ("layout brute force", lambda: pl.test_brute_force_small(8)),
+        ("workload layouts", pl.test_workload_layouts),
+        ("clip vs torch", lambda: pk.test_clip_matches_torch(1.0, 1.0)),
+        ("clip closed forms", pk.test_closed_forms),
+        ("norm vs numpy", pk.test_norm_matches_numpy_fp64),
+        ("quant error bound", lambda: pq.test_roundtrip_error_bound(256, 4097)),
+        ("quant max and symmetry", pq.test_block_max_maps_to_127_and_symmetry),
+        ("quant ties and zeros", pq.test_ties_to_even_and_zero_blocks),
+        ("quant ragged", pq.test_ragged_last_block_and_wire_bytes),
+    ]
+
+
+@pytest.mark.parametrize("what,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_a_planted_mistake_fails_a_pin(what, old, new, tmp_path, monkeypatch):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"the mutation target for '{what}' must occur exactly once"
+    mutated = tmp_path / "mutated.c"
+    mutated.write_text(src.replace(old, new))
+    so = tmp_path / "libmutated.so"
+    subprocess.check_call(["gcc", *oracle.CFLAGS, "-o", str(so), str(mutated), "-lm"])
+    lib = oracle.configure(ctypes.CDLL(str(so)))
+    monkeypatch.setattr(oracle, "_lib", lib)
+    caught = []
+    for name, pin in _pins():
+        try:
+            pin()
+        except Exception:          # an assertion, or a ValueError from a layout check
+            caught.append(name)
+    assert caught, f"no pin noticed: {what}"
+
+
+def test_the_real_oracle_passes_every_pin():
+    for name, pin in _pins():
+        pin()

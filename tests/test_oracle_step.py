@@ -255,6 +255,23 @@ def test_accumulation_orders_within_summation_bound():
         assert np.all(np.abs(z - exact) <= bound * 1.0000001 + 1e-45)
 
 
+def test_first_micro_batch_overwrites_the_buffer():
+    # "first" starts the window: whatever the buffer held before is replaced,
+    # bit for bit, by this micro-batch's values (also the sign of zero)
+    n_dp, n = 4, 1024
+    g = _grads(n_dp, n)
+    g[:, :4] = oracle.cast_bf16(np.array([-0.0, 0.0, -0.0, 1.0], np.float32))
+    garbage = (RNG.standard_normal(n) * 1e3).astype(np.float32)
+    acc = oracle.accumulate_local(garbage, g[0], first=True)
+    np.testing.assert_array_equal(acc.view(np.uint32), oracle.bf16_to_f32(g[0]).view(np.uint32))
+    A = oracle.accumulate_reduce(garbage, g, first=True)
+    np.testing.assert_array_equal(A, oracle.accumulate_reduce(None, g, first=True))
+    np.testing.assert_array_equal(A, oracle.reduce_mean(g, 1.0))
+    # and an accumulating call adds onto what is there
+    acc2 = oracle.accumulate_local(garbage, g[1], first=False)
+    np.testing.assert_array_equal(acc2, garbage + oracle.bf16_to_f32(g[1]))
+
+
 def test_single_micro_batch_accumulation_is_the_mean():
     n_dp, P = 8, 2048
     g = _grads(n_dp, P)
