@@ -10,6 +10,9 @@
 // 2 bytes written per unit element.
 #include "zero_common.cuh"
 
+#ifndef ZGB_GATHER_WAVES
+#define ZGB_GATHER_WAVES 8   // grid = resident CTAs x this (measured best on GB300)
+#endif
 #ifndef ZGB_GATHER_U
 #define ZGB_GATHER_U 1       // 128-bit vectors per thread and iteration (1 measured best)
 #endif
@@ -87,7 +90,7 @@ extern "C" int zero_gather_layer(const zero_layout_t* unit, const uint16_t* cons
         p.out = full_out + (int64_t)o0 * unit->shard;
         p.shard_len = unit->shard;
         vec = vec && aligned16(p.out);
-        const int64_t resident = (int64_t)sm_count() * (vec ? occ_vec : occ_scalar);
+        const int64_t resident = (int64_t)sm_count() * (vec ? occ_vec : occ_scalar) * ZGB_GATHER_WAVES;
         const int64_t per_shard = resident / cnt > 0 ? resident / cnt : 1;
         dim3 grid(grid_for(vec ? unit->shard >> 3 : unit->shard, kThreads, per_shard), cnt);
         if (vec)

@@ -37,7 +37,7 @@
 #include "zero_update.cuh"
 
 #ifndef ZGB_RS_WAVES
-#define ZGB_RS_WAVES 1       // grid = resident CTAs x this (grid-stride loop inside)
+#define ZGB_RS_WAVES 0       // grid = resident CTAs x this; 0 = the measured choice per kind
 #endif
 #ifndef ZGB_RS_MULTI
 #define ZGB_RS_MULTI 1       // 0: one vector per thread and iteration everywhere
@@ -209,8 +209,9 @@ __device__ __forceinline__ void load_state(const UpdateParams& p, int64_t e, flo
     st[5] = ld_stream_f4(p.v + e + 4);
 }
 
-// U vectors (vi0, vi0 + stride, ...) with a compile-time source count R:
-// every load of all U vectors is issued before the first add.
+// U vectors (vi0, vi0 + stride, ...; the kernel passes stride = kThreads, so a
+// CTA's vectors are consecutive) with a compile-time source count R: every
+// load of all U vectors is issued before the first add.
 template <int KIND, int R, int U>
 __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, int64_t stride,
                                           int64_t nv, float coef) {
@@ -281,6 +282,19 @@ __host__ __device__ constexpr int vectors_per_iter() {
     return ZGB_RS_MULTI && R > 0 && loads_per_vec<KIND, R>() <= 8 ? 2 : 1;
 }
 
+// Grid size in resident waves.  Oversubscribing the grid (CTAs run in launch
+// order, each over its own contiguous chunk) keeps the active CTAs on one
+// stretch of each stream, which DRAM serves better than a persistent grid
+// whose every pass spans the whole range.  Measured on GB300 (GPT-2-XL and
+// Llama-7B shapes): x64 for bf16 sources and the stage-1 fused finish, x8 for
+// the stage-2 fused finish, x1 for fp32 sources (the ZeRO-3 unit update lost
+// 3 % at x64).
+template <int KIND, int R>
+__host__ __device__ constexpr int rs_waves() {
+    return ZGB_RS_WAVES > 0 ? ZGB_RS_WAVES
+         : KIND == kPlainF32 ? 1 : KIND == kAccReduce ? 8 : 64;
+}
+
 template <int KIND, int R>
 __global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
 rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
@@ -289,8 +303,13 @@ rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     if constexpr (R > 0) {
+        // a CTA takes U x kThreads consecutive vectors per pass (thread t: t,
+        // t + kThreads, ...), so the CTAs resident at any moment cover one
+        // contiguous stretch of every stream
         constexpr int U = vectors_per_iter<KIND, R>();
-        for (int64_t vi = tid; vi < nv; vi += U * stride) step_vecs<KIND, R, U>(p, vi, stride, nv, coef);
+        const int64_t chunk = (int64_t)U * kThreads;
+        for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk)
+            step_vecs<KIND, R, U>(p, v0, kThreads, nv, coef);
     } else {
         for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND>(p, vi, coef);
     }
@@ -310,8 +329,9 @@ template <int KIND, int R>
 int launch_vec(const UpdateParams& p, cudaStream_t stream) {
     static int occupancy = 0;
     if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R>, kThreads, 0);
-    const int64_t resident = (int64_t)sm_count() * occupancy * ZGB_RS_WAVES;
-    const unsigned grid = grid_for(p.n >> 3, kThreads, resident);
+    const int64_t resident = (int64_t)sm_count() * occupancy * rs_waves<KIND, R>();
+    const int64_t per_cta = (R > 0 ? vectors_per_iter<KIND, R>() : 1) * (int64_t)kThreads;
+    const unsigned grid = grid_for(p.n >> 3, per_cta, resident);
     rs_adamw_vec_kernel<KIND, R><<<grid, kThreads, 0, stream>>>(p);
     return launch_status();
 }
