@@ -330,11 +330,26 @@ uint32_t zero_crc32(const void* data, int64_t n);
 
 /* ---- status ---------------------------------------------------------------
  * Synchronizes `stream` and returns ZERO_ECUDA if it (or an earlier launch on
- * this thread) failed, else ZERO_OK.  The only call that blocks. */
+ * this thread) failed; ZERO_ETIMEOUT if a bounded device-side wait (the
+ * mbarrier waits of the TMA-staged update) gave up since the last check -- the
+ * kernel that gave up recorded it, drained its own copies and returned, so
+ * the context stays usable; the record is cleared by this call.  Else ZERO_OK.
+ * The only call that blocks. */
 int zero_status_check(void* stream);
+
+/* Launches one CTA that waits on an mbarrier nothing ever completes, bounded
+ * by limit_cycles SM cycles (1 .. 2^32): the wait gives up, records
+ * ZERO_ETIMEOUT for zero_status_check and the kernel returns.  For testing the
+ * failure path of bounded waits without faulting or hanging the GPU.
+ * ZERO_EINVAL for a limit out of range. */
+int zero_selftest_bounded_wait(int64_t limit_cycles, void* stream);
 
 /* Static string for a status code (never NULL). */
 const char* zero_strerror(int code);
+
+/* The name of the last CUDA error behind a ZERO_ECUDA on this thread
+ * ("cudaSuccess" if none), for diagnostics. */
+const char* zero_last_cuda_error(void);
 
 /* ---- accounting helpers (host-only) ---------------------------------------
  * "ZeRO and FSDP", "Memory per GPU": model-state bytes per GPU with 2-byte

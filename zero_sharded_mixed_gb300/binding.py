@@ -28,7 +28,10 @@ ZERO_MAX_SRC = 64
 class ZeroError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {zero_strerror(code)} ({code})")
+        detail = ""
+        if code == ZERO_ECUDA:
+            detail = f" [{load().zero_last_cuda_error().decode()}]"
+        super().__init__(f"{where}: {zero_strerror(code)} ({code}){detail}")
 
 
 class ZeroLayout(ctypes.Structure):
@@ -100,6 +103,7 @@ def load():
         lib.zero_ckpt_write_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p]
         lib.zero_ckpt_read_header.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), P(i32)]
         lib.zero_ckpt_read_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p, i64]
+        lib.zero_selftest_bounded_wait.argtypes = [i64, p]
         lib.zero_crc32.argtypes = [p, i64]
         lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
@@ -108,6 +112,8 @@ def load():
         lib.zero_status_check.argtypes = [p]
         lib.zero_strerror.argtypes = [ctypes.c_int]
         lib.zero_strerror.restype = ctypes.c_char_p
+        lib.zero_last_cuda_error.argtypes = []
+        lib.zero_last_cuda_error.restype = ctypes.c_char_p
         lib.zero_memory_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
                                           P(ctypes.c_double)]
         lib.zero_comm_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
@@ -117,6 +123,7 @@ def load():
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
+                     "zero_selftest_bounded_wait",
                      "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -382,3 +389,9 @@ def zero_gather_layer_int8(unit: ZeroLayout, q_shards, scale_shards, full_out: t
         (ctypes.c_void_p * max(1, len(sp)))(*sp), int(block),
         _tensor(full_out, "full_out", torch.bfloat16, unit.padded_n), _stream_ptr(stream))
     _check(rc, "zero_gather_layer_int8")
+
+
+def zero_selftest_bounded_wait(limit_cycles: int, stream=None):
+    """Run the bounded-wait self test (see zero_gb300.h); follow with zero_status_check."""
+    _check(load().zero_selftest_bounded_wait(int(limit_cycles), _stream_ptr(stream)),
+           "zero_selftest_bounded_wait")

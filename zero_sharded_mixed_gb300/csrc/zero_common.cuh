@@ -88,8 +88,11 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int sm_count();
 // CTAs of `threads` each that fit on one SM for `kernel` (cached by the caller).
 int ctas_per_sm(const void* kernel, int threads, size_t smem);
-// ZERO_ECUDA if the last launch on this thread failed.
+// ZERO_ECUDA if the last launch on this thread failed (remembered for
+// zero_last_cuda_error).
 int launch_status();
+void note_cuda_error(cudaError_t e);
+const char* last_cuda_error_name();
 // Grid for a grid-stride loop over `work` items with `per_cta` items per CTA
 // pass, capped at `resident` CTAs (so every CTA is resident at once).
 inline unsigned grid_for(int64_t work, int64_t per_cta, int64_t resident) {

@@ -42,6 +42,9 @@
 #ifndef ZGB_RS_MULTI
 #define ZGB_RS_MULTI 1       // 0: one vector per thread and iteration everywhere
 #endif
+#ifndef ZGB_RS_TMA
+#define ZGB_RS_TMA 0         // 1: bf16 sources go through the TMA-staged kernel (zero_rs_adamw_tma.cu)
+#endif
 #ifndef ZGB_RS_MINBLOCKS
 #define ZGB_RS_MINBLOCKS 2   // CTAs per SM the register allocation must allow (caps at 128)
 #endif
@@ -49,18 +52,6 @@
 namespace zgb {
 
 enum SrcKind { kPlainBf16 = 0, kPlainF32 = 1, kAccLocal = 2, kAccReduce = 3 };
-
-struct UpdateParams {
-    const void* src[ZERO_MAX_SRC];  // gradient sources (bf16 or fp32), offset to the range start
-    const float* acc[ZERO_MAX_SRC]; // fp32 accumulators of the fused kinds, offset likewise
-    float* w;
-    float* m;
-    float* v;
-    uint16_t* out;
-    int64_t n;                      // elements in the range
-    int32_t n_src;                  // gradient sources (ranks)
-    AdamwScalars h;
-};
 
 __device__ __forceinline__ void add_bf16x8(float (&s)[8], const uint4 x) {
     s[0] = __fadd_rn(s[0], bf16_lo(x.x));
@@ -348,6 +339,10 @@ int launch_scalar(const UpdateParams& p, cudaStream_t stream) {
 template <int KIND>
 int dispatch(const UpdateParams& p, bool vec, cudaStream_t s) {
     if (!vec) return launch_scalar<KIND>(p, s);
+    if constexpr (KIND == kPlainBf16 && ZGB_RS_TMA) {
+        const int rc = launch_rs_adamw_tma(p, s);
+        if (rc <= 0) return rc;                           // > 0: not applicable here
+    }
     if constexpr (KIND == kPlainBf16 || KIND == kPlainF32) {
         switch (p.n_src) {
             case 1: return launch_vec<KIND, 1>(p, s);

@@ -1,0 +1,277 @@
+// The fused update for bf16 gradient sources with TMA staging, sm_103a.
+//
+// Same computation as rs_adamw_vec_kernel<kPlainBf16, NDP> (zero_rs_adamw.cu):
+// g = (sum over ranks of the bf16 gradients, fp32, ascending) / divisor, the
+// AdamW update, the bf16 cast, the gather write -- bit-identical to it.  The
+// difference is how bytes reach the SM: instead of each thread issuing its own
+// 128-bit loads, one thread per CTA issues 1-D bulk copies (cp.async.bulk,
+// the TMA engine's linear mode) of whole tiles -- 2 KB per gradient slice and
+// 4 KB per state array for a 1024-element tile -- into a 3-stage ring of
+// shared-memory buffers, each stage completed by an mbarrier transaction
+// count.  Consumers read the tile from shared memory, compute, and store the
+// results straight to global memory.  CTA b takes tiles b, b + grid, ... so
+// the CTAs in flight work on neighbouring tiles.
+//
+// Every wait is bounded: an mbarrier wait gives up after about one second of
+// SM clock; all threads of the CTA take the same decision (__syncthreads_and),
+// record ZERO_ETIMEOUT in a device status word (read by zero_status_check),
+// wait -- bounded again -- for the copies the CTA still has in flight, and
+// return.  No path waits forever.
+#include <cmath>
+
+#include "zero_update.cuh"
+
+#ifndef ZGB_TMA_INTERLEAVE
+#define ZGB_TMA_INTERLEAVE 1   // 1: CTA b takes tiles b, b + grid, ...; 0: a contiguous run per CTA
+#endif
+#ifndef ZGB_TMA_STAGES
+#define ZGB_TMA_STAGES 3
+#endif
+#ifndef ZGB_TMA_TIMEOUT_CYCLES
+#define ZGB_TMA_TIMEOUT_CYCLES (1ll << 31)   // SM cycles before a wait gives up (~1 s)
+#endif
+
+namespace zgb {
+
+__device__ int g_device_status;   // ZERO_OK, or ZERO_ETIMEOUT once a bounded wait gave up
+
+constexpr int kTmaThreads = 256;
+constexpr int kTile = 4 * kTmaThreads;   // elements per stage: 4 per thread
+constexpr int kStages = ZGB_TMA_STAGES;
+// A 4-stage ring (112 KB per CTA at 8 sources) was built once and its launch
+// failed with a CUDA runtime error whose cause was not found; only the
+// configurations that have run are allowed.
+static_assert(kStages >= 2 && kStages <= 3, "the TMA ring runs with 2 or 3 stages");
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the barrier's phase with the given parity; false after `limit`
+// SM cycles.
+__device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - start > limit) return false;
+    return true;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes`
+// transactions on the barrier.  dst 16-byte aligned, src 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+template <int NDP>
+struct TmaTile {
+    static constexpr uint32_t kGradBytes = kTile * 2;
+    static constexpr uint32_t kStateBytes = kTile * 4;
+    static constexpr uint32_t kStageBytes = NDP * kGradBytes + 3 * kStateBytes;
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes;
+};
+
+template <int NDP>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+rs_adamw_tma_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
+    using Tile = TmaTile<NDP>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    const int tid = threadIdx.x;
+    const float coef = clip_coef(p.h);
+    const int64_t n8 = (p.n >> 3) << 3;                   // the tiles cover [0, n8)
+    // the k-th tile of this CTA
+#if ZGB_TMA_INTERLEAVE
+    const int64_t count = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto tile_of = [&](int64_t k) { return (int64_t)blockIdx.x + k * gridDim.x; };
+#else
+    const int64_t per = (n_tiles + gridDim.x - 1) / gridDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * per;
+    const int64_t count = t0 < n_tiles ? min(per, n_tiles - t0) : 0;
+    auto tile_of = [&](int64_t k) { return t0 + k; };
+#endif
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // thread 0 only: stage s <- tile t0 + k
+    auto issue = [&](int64_t k, int s) {
+        const int64_t e0 = tile_of(k) * kTile;
+        const uint32_t elems = (uint32_t)min((int64_t)kTile, n8 - e0);   // a multiple of 8
+        unsigned char* st = smem + (size_t)s * Tile::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], elems * (2u * NDP + 12u));
+#pragma unroll
+        for (int r = 0; r < NDP; ++r)
+            bulk_g2s(st + r * Tile::kGradBytes, static_cast<const uint16_t*>(p.src[r]) + e0, elems * 2,
+                     &full[s]);
+        bulk_g2s(st + NDP * Tile::kGradBytes, p.w + e0, elems * 4, &full[s]);
+        bulk_g2s(st + NDP * Tile::kGradBytes + Tile::kStateBytes, p.m + e0, elems * 4, &full[s]);
+        bulk_g2s(st + NDP * Tile::kGradBytes + 2 * Tile::kStateBytes, p.v + e0, elems * 4, &full[s]);
+    };
+
+    if (tid == 0)
+        for (int s = 0; s < kStages && s < count; ++s) issue(s, s);
+
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < count; ++k) {
+        const int s = (int)(k % kStages);
+        const uint32_t parity = (uint32_t)((k / kStages) & 1);
+        ok = __syncthreads_and(mbar_wait_bounded(&full[s], parity, ZGB_TMA_TIMEOUT_CYCLES)) != 0;
+        if (!ok) break;
+        const int64_t e0 = tile_of(k) * kTile;
+        const int64_t elems = min((int64_t)kTile, n8 - e0);
+        const int j = tid * 4;
+        if (j < elems) {
+            const unsigned char* st = smem + (size_t)s * Tile::kStageBytes;
+            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int r = 0; r < NDP; ++r) {
+                const uint2 g = *reinterpret_cast<const uint2*>(st + r * Tile::kGradBytes + j * 2);
+                sum[0] = __fadd_rn(sum[0], bf16_lo(g.x));
+                sum[1] = __fadd_rn(sum[1], bf16_hi(g.x));
+                sum[2] = __fadd_rn(sum[2], bf16_lo(g.y));
+                sum[3] = __fadd_rn(sum[3], bf16_hi(g.y));
+            }
+            const unsigned char* sb = st + NDP * Tile::kGradBytes;
+            const float4 w4 = *reinterpret_cast<const float4*>(sb + j * 4);
+            const float4 m4 = *reinterpret_cast<const float4*>(sb + Tile::kStateBytes + j * 4);
+            const float4 v4 = *reinterpret_cast<const float4*>(sb + 2 * Tile::kStateBytes + j * 4);
+            float w[4] = {w4.x, w4.y, w4.z, w4.w};
+            float m[4] = {m4.x, m4.y, m4.z, m4.w};
+            float v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) adamw_update(mean_grad(sum[q], p.h, coef), w[q], m[q], v[q], p.h);
+            st_stream_f4(p.w + e0 + j, make_float4(w[0], w[1], w[2], w[3]));
+            st_stream_f4(p.m + e0 + j, make_float4(m[0], m[1], m[2], m[3]));
+            st_stream_f4(p.v + e0 + j, make_float4(v[0], v[1], v[2], v[3]));
+            *reinterpret_cast<uint2*>(p.out + e0 + j) =
+                make_uint2(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]));
+        }
+        __syncthreads();                                   // every thread is done with stage s
+        if (tid == 0 && k + kStages < count) issue(k + kStages, s);
+    }
+    if (!ok) {
+        // A wait gave up: record it, then wait (bounded) for the copies this
+        // CTA still has in flight -- tiles k .. k + kStages - 1 -- and return.
+        if (tid == 0) {
+            atomicExch(&g_device_status, ZERO_ETIMEOUT);
+            for (int64_t q = k; q < count && q < k + kStages; ++q)
+                (void)mbar_wait_bounded(&full[q % kStages], (uint32_t)((q / kStages) & 1),
+                                        ZGB_TMA_TIMEOUT_CYCLES);
+        }
+        __syncthreads();
+        return;
+    }
+    // the last n % 8 elements, element by element, in CTA 0
+    if (blockIdx.x == 0 && tid < p.n - n8) {
+        const int64_t i = n8 + tid;
+        float sum = 0.0f;
+        for (int r = 0; r < NDP; ++r) sum = __fadd_rn(sum, bf16_one(static_cast<const uint16_t*>(p.src[r])[i]));
+        float w = p.w[i], m = p.m[i], v = p.v[i];
+        adamw_update(mean_grad(sum, p.h, coef), w, m, v, p.h);
+        p.w[i] = w;
+        p.m[i] = m;
+        p.v[i] = v;
+        p.out[i] = to_bf16(w);
+    }
+}
+
+template <int NDP>
+int launch_tma(const UpdateParams& p, cudaStream_t stream) {
+    using Tile = TmaTile<NDP>;
+    static int occupancy = 0;
+    if (occupancy == 0) {
+        const cudaError_t e = cudaFuncSetAttribute((const void*)rs_adamw_tma_kernel<NDP>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)Tile::kSmemBytes);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            note_cuda_error(e);
+            return ZERO_ECUDA;
+        }
+        occupancy = ctas_per_sm((const void*)rs_adamw_tma_kernel<NDP>, kTmaThreads, Tile::kSmemBytes);
+    }
+    const int64_t n_tiles = ((p.n >> 3) * 8 + kTile - 1) / kTile;
+    const int64_t resident = (int64_t)sm_count() * occupancy;
+    const unsigned grid = (unsigned)(n_tiles < 1 ? 1 : (n_tiles < resident ? n_tiles : resident));
+    rs_adamw_tma_kernel<NDP><<<grid, kTmaThreads, Tile::kSmemBytes, stream>>>(p, n_tiles);
+    return launch_status();
+}
+
+int launch_rs_adamw_tma(const UpdateParams& p, cudaStream_t stream) {
+    switch (p.n_src) {
+        case 1: return launch_tma<1>(p, stream);
+        case 2: return launch_tma<2>(p, stream);
+        case 4: return launch_tma<4>(p, stream);
+        case 8: return launch_tma<8>(p, stream);
+        default: return 1;   // not applicable: the caller uses the register-staged kernel
+    }
+}
+
+// One CTA waits on an mbarrier that nothing completes, with a short bound:
+// the wait must give up, record ZERO_ETIMEOUT and return.
+__global__ void bounded_wait_selftest_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const bool ok = __syncthreads_and(mbar_wait_bounded(&bar, 0, limit)) != 0;
+    if (!ok && threadIdx.x == 0) atomicExch(&g_device_status, ZERO_ETIMEOUT);
+}
+
+int take_device_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ZERO_ECUDA;
+    }
+    if (v != ZERO_OK) {
+        const int zero = ZERO_OK;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return ZERO_ECUDA;
+        }
+    }
+    return v == ZERO_OK ? ZERO_OK : ZERO_ETIMEOUT;
+}
+
+}  // namespace zgb
+
+extern "C" int zero_selftest_bounded_wait(int64_t limit_cycles, void* stream) {
+    if (limit_cycles < 1 || limit_cycles > (1ll << 32)) return ZERO_EINVAL;
+    zgb::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles);
+    return zgb::launch_status();
+}

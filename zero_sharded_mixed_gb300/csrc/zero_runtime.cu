@@ -2,7 +2,7 @@
 // properties, launch status, and zero_status_check.
 #include <atomic>
 
-#include "zero_common.cuh"
+#include "zero_update.cuh"
 
 namespace zgb {
 
@@ -51,14 +51,34 @@ int ctas_per_sm(const void* kernel, int threads, size_t smem) {
     return n;
 }
 
+namespace {
+thread_local cudaError_t g_last_error = cudaSuccess;
+}  // namespace
+
 int launch_status() {
-    return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return ZERO_OK;
+    g_last_error = e;
+    return ZERO_ECUDA;
+}
+
+void note_cuda_error(cudaError_t e) {
+    if (e != cudaSuccess) g_last_error = e;
+}
+
+const char* last_cuda_error_name() {
+    return g_last_error == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(g_last_error);
 }
 
 }  // namespace zgb
 
+extern "C" const char* zero_last_cuda_error(void) { return zgb::last_cuda_error_name(); }
+
 extern "C" int zero_status_check(void* stream) {
     const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     const cudaError_t last = cudaGetLastError();
-    return (e == cudaSuccess && last == cudaSuccess) ? ZERO_OK : ZERO_ECUDA;
+    zgb::note_cuda_error(e);
+    zgb::note_cuda_error(last);
+    if (e != cudaSuccess || last != cudaSuccess) return ZERO_ECUDA;
+    return zgb::take_device_status();   // ZERO_ETIMEOUT if a bounded device wait gave up
 }

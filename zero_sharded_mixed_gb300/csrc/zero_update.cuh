@@ -56,7 +56,28 @@ __device__ __forceinline__ float mean_grad(float sum, const AdamwScalars& h, flo
     return __fmul_rn(__fdiv_rn(sum, h.divisor), coef);
 }
 
+// The launch parameters of the fused update kernels.
+struct UpdateParams {
+    const void* src[ZERO_MAX_SRC];  // gradient sources (bf16 or fp32), offset to the range start
+    const float* acc[ZERO_MAX_SRC]; // fp32 accumulators of the fused kinds, offset likewise
+    float* w;
+    float* m;
+    float* v;
+    uint16_t* out;
+    int64_t n;                      // elements in the range
+    int32_t n_src;                  // gradient sources (ranks)
+    AdamwScalars h;
+};
+
 // ----------------------------------------------------------------- host
+
+// The TMA-staged variant for bf16 sources (zero_rs_adamw_tma.cu): returns
+// ZERO_EINVAL when it does not apply (source count or alignment), so that the
+// caller falls back to the register-staged kernel.
+int launch_rs_adamw_tma(const UpdateParams& p, cudaStream_t stream);
+// Reads and clears the device status word of the bounded waits (ZERO_OK or
+// ZERO_ETIMEOUT); synchronizes the device.
+int take_device_status();
 
 // Where an update over flat [begin, end) of the owners rank_begin..rank_end-1
 // reads and writes: state and output pointers already offset to `begin`.
