@@ -198,7 +198,7 @@ def _peak():
 
 def _kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("zero_rs_adamw.cu", "zero_common.cuh"):
+    for name in ("zero_rs_adamw.cu", "zero_common.cuh", "zero_update.cuh"):
         with open(os.path.join(ROOT, "zero_sharded_mixed_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
