@@ -107,6 +107,8 @@ def configure(lib):
     lib.oracle_quantize_int8.restype = None
     lib.oracle_dequantize_int8.argtypes = [p, p, i64, i32, p]
     lib.oracle_dequantize_int8.restype = None
+    lib.oracle_dequantize_grad_int8.argtypes = [p, p, i64, i32, p]
+    lib.oracle_dequantize_grad_int8.restype = None
     return lib
 
 
@@ -312,3 +314,57 @@ def dequantize_int8(q, scales, block: int = 256):
     out = np.empty(q.size, dtype=np.uint16)
     _load().oracle_dequantize_int8(_ptr(q), _ptr(scales), q.size, block, _ptr(out))
     return out
+
+
+# ---------------------------------------------------------------------------
+# 8-bit quantized gradient reduce-scatter (ZeRO++): "ZeRO Optimizer, in depth",
+# "Offload and ZeRO++" (zero_quantized_gradients); "ZeRO and FSDP", "Fewer
+# bytes on the wire".  Each rank's gradient slice for owner o is quantized in
+# the weight format; the owner dequantizes to fp32 and takes the fp32 mean.
+# ---------------------------------------------------------------------------
+
+def quantize_grad_int8(g_rows, n_dp: int, block: int = 256):
+    """Rows of bf16 gradients (n_src, P = n_dp*S), every row quantized slice by
+    slice (slice o = [o*S, (o+1)*S)) -> q (n_src, P) int8 and scales
+    (n_src, n_dp*nb) fp32 with nb = ceil(S / block), slice o's at [o*nb]."""
+    g = _u16(g_rows)
+    assert g.ndim == 2 and g.shape[1] % n_dp == 0
+    n_src, P = g.shape
+    S = P // n_dp
+    nb = -(-S // block)
+    q = np.empty((n_src, P), dtype=np.int8)
+    scales = np.empty((n_src, n_dp * nb), dtype=np.float32)
+    for r in range(n_src):
+        for o in range(n_dp):
+            q[r, o * S:(o + 1) * S], scales[r, o * nb:(o + 1) * nb] = \
+                quantize_int8(g[r, o * S:(o + 1) * S], block)
+    return q, scales
+
+
+def dequantize_grad_int8(q_rows, scale_rows, n_dp: int, block: int = 256) -> np.ndarray:
+    """The owners' fp32 view of quantized gradient rows: (n_src, P) float32,
+    element k of slice o = code * (slice o's scale of block k // block)."""
+    q = np.ascontiguousarray(q_rows, dtype=np.int8)
+    sc = _f32(scale_rows)
+    n_src, P = q.shape
+    S = P // n_dp
+    nb = -(-S // block)
+    assert sc.shape == (n_src, n_dp * nb)
+    out = np.empty((n_src, P), dtype=np.float32)
+    for r in range(n_src):
+        for o in range(n_dp):
+            qs = np.ascontiguousarray(q[r, o * S:(o + 1) * S])
+            ss = np.ascontiguousarray(sc[r, o * nb:(o + 1) * nb])
+            part = np.empty(S, dtype=np.float32)
+            _load().oracle_dequantize_grad_int8(_ptr(qs), _ptr(ss), S, block, _ptr(part))
+            out[r, o * S:(o + 1) * S] = part
+    return out
+
+
+def qgrad_rs_adamw_reference(q_rows, scale_rows, n_dp: int, block: int, divisor, w, m, v,
+                             hp: AdamW, t: int):
+    """One step over the whole padded vector from 8-bit gradients: dequantize,
+    fp32 mean over ranks, AdamW, bf16 cast.  Returns (out_bf16, w, m, v)."""
+    g = reduce_mean(dequantize_grad_int8(q_rows, scale_rows, n_dp, block), divisor)
+    w2, m2, v2 = adamw(w, m, v, g, hp, t)
+    return cast_bf16(w2), w2, m2, v2

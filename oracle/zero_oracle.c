@@ -390,3 +390,24 @@ void oracle_dequantize_int8(const int8_t* q, const float* scales, int64_t n, int
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_f32_to_bf16((float)q[i] * scales[i / block]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* 8-bit quantized gradient reduce-scatter (ZeRO++)                          */
+/* ------------------------------------------------------------------------ */
+
+/* "ZeRO Optimizer, in depth" ("Offload and ZeRO++": zero_quantized_gradients
+ * quantises the gradient reduce-scatter) and "ZeRO and FSDP" ("Fewer bytes on
+ * the wire": gradients quantized during the reduce-scatter).  Reading taken
+ * (the pages give neither the format nor the bit width): each rank quantizes
+ * the slice of its bf16 gradient that goes to owner o -- the elements
+ * [o*S, (o+1)*S) -- in the 8-bit block format of the weight gather above
+ * (oracle_quantize_int8 over that slice).  The owner turns every received
+ * code back into an fp32 gradient value, the code times its block's scale
+ * rounded once to fp32 (no bf16 rounding in between), and then takes the same
+ * fp32 mean over ranks as for bf16 gradients (oracle_reduce_mean_f32). */
+void oracle_dequantize_grad_int8(const int8_t* codes, const float* block_scales, int64_t n,
+                                 int32_t block, float* out)
+{
+    for (int64_t k = 0; k < n; ++k)
+        out[k] = (float)codes[k] * block_scales[k / block];
+}

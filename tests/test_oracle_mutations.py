@@ -16,6 +16,7 @@ import oracle
 from tests import test_oracle_cast as pc
 from tests import test_oracle_clip as pk
 from tests import test_oracle_layout as pl
+from tests import test_oracle_qgrad as pg
 from tests import test_oracle_quant as pq
 from tests import test_oracle_step as ps
 
@@ -52,6 +53,12 @@ MUTATIONS = [
     ("8-bit codes truncated", "nearbyintf(oracle_bf16_to_f32(w[i]) * inv)",
      "truncf(oracle_bf16_to_f32(w[i]) * inv)"),
     ("8-bit dequantization uses the first block's scale", "scales[i / block]", "scales[0]"),
+    ("8-bit gradient uses the previous block's scale", "block_scales[k / block];",
+     "block_scales[k / block > 0 ? k / block - 1 : 0];"),
+    ("8-bit gradient rounded to bf16 before the mean",
+     "out[k] = (float)codes[k] * block_scales[k / block];",
+     "out[k] = oracle_bf16_to_f32(oracle_f32_to_bf16((float)codes[k] * block_scales[k / block]));"),
+    ("8-bit gradient loses the code's sign", "out[k] = (float)codes[k] *", "out[k] = fabsf((float)codes[k]) *"),
 ]
 
 
@@ -85,6 +92,10 @@ def _pins():
         ("quant max and symmetry", pq.test_block_max_maps_to_127_and_symmetry),
         ("quant ties and zeros", pq.test_ties_to_even_and_zero_blocks),
         ("quant ragged", pq.test_ragged_last_block_and_wire_bytes),
+        ("8-bit gradient exact codes",
+         lambda: pg.test_exact_gradients_quantize_to_their_codes_and_step_like_bf16(4, 1000, 256)),
+        ("8-bit gradient error bound", lambda: pg.test_error_within_half_a_step(4, 5000, 256)),
+        ("8-bit gradient slices", pg.test_blocks_restart_at_every_slice),
     ]
 
 
