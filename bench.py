@@ -51,6 +51,7 @@ METRIC = "params updated/s for fused reduce+AdamW+cast+gather; HBM GB/s vs GB300
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
 SEED = 0
+QGRAD_BLOCK = 256        # block of the 8-bit gradient format in the ZeRO++ workloads
 HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
 CPU_SAMPLE = 1 << 25          # elements of the cpu_baseline sample
 CPU_BASELINE_SECONDS = 10.0   # CPU work for the cpu_baseline leg
@@ -63,9 +64,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "llama7b-shard", "probe",
-                                           "accum-zero1", "accum-zero2", "zero3", "zero3-int8",
-                                           "zero3-prefetch"],
+    ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
+                                           "probe", "accum-zero1", "accum-zero2", "zero3",
+                                           "zero3-int8", "zero3-prefetch", "zero3-zeropp"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -273,13 +274,14 @@ class Zero2Workload(Workload):
         n_dp = 8
         self.name = name
         self.clip = name == "gpt2xl-clip"
-        if name in ("gpt2xl", "gpt2xl-clip"):
+        self.qgrad = name == "gpt2xl-qgrad"
+        if name in ("gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad"):
             numels = [elems] if elems else inputs.gpt2xl_numels()
             L = zb.zero_layout(numels, n_dp, 8, 500_000_000)
             lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
             self.desc = {"workload": ("flat%d_zero2" % elems if elems else "gpt2xl_zero2_all_shards")
-                         + ("_clip1.0" if self.clip else ""),
+                         + ("_clip1.0" if self.clip else "") + ("_int8_grads" if self.qgrad else ""),
                          "model": "flat vector" if elems else "GPT-2-XL shapes",
                          "N": L.n, "n_dp": n_dp, "shard": L.shard, "padded_n": L.padded_n,
                          "bucket": L.bucket, "buckets": L.n_buckets}
@@ -318,11 +320,38 @@ class Zero2Workload(Workload):
         self.v = torch.zeros_like(self.master)
         self.out = torch.zeros(L.padded_n, dtype=torch.bfloat16, device=device)
         self.device_bytes = g.numel() * 2 + 3 * self.elems * 4 + self.out.numel() * 2
+        if self.qgrad:
+            from zero_sharded_mixed_gb300.step import Int8Grads
+            self.qg = Int8Grads(L, n_dp, QGRAD_BLOCK, device)
+            self.desc["quant_block"] = QGRAD_BLOCK
+            sb = n_dp * 4 / QGRAD_BLOCK            # scale bytes per element of all sources
+            # every rank quantizes its gradient (2 B read + 1 B written + scales),
+            # then the fused update reads 1 B per source plus its scale
+            self.bytes_per_elem = n_dp * 3 + sb + 26 + n_dp + sb
+            self.dominant = "rs_adamw_int8"
+            self.kernel_label = "zgb::qgrad_vec_kernel<8,true> + zgb::quantize_vec_kernel<1,4> x 8 ranks"
+            self.device_bytes += self.qg.q.numel() + self.qg.scales.numel() * 4
 
     def ops(self, t):
         zb, hp = self.zb, self.hp(t)
         n_dp = self.L.n_dp
         out = []
+        if self.qgrad:
+            P = self.L.padded_n
+            sb = n_dp * 4 / QGRAD_BLOCK
+            for r in range(n_dp):
+                def quant(r=r):
+                    zb.zero_quantize_int8(self.L, self.grad_list[r], self.qg.q[r], self.qg.scales[r],
+                                          QGRAD_BLOCK)
+                out.append(Op("quantize_grad", int(P * (3 + 4 / QGRAD_BLOCK)), quant))
+            qs, ss = self.qg.sources()
+            for s, e in self.ranges:
+                def fn(s=s, e=e):
+                    zb.zero_reduce_scatter_adamw_int8(self.L, qs, ss, QGRAD_BLOCK, float(n_dp), 0,
+                                                      n_dp, s, e, self.master, self.m, self.v,
+                                                      self.out, zb.ZERO_OUT_FULL, hp)
+                out.append(Op("rs_adamw_int8", int((e - s) * (26 + n_dp + sb)), fn))
+            return out
         if self.clip:
             for j, (s, e) in enumerate(self.ranges):
                 def fn(s=s, e=e, j=j):
@@ -450,7 +479,8 @@ class Zero3Workload(Workload):
         zb = self.zb
         self.name = name
         self.zstep = zstep
-        self.int8 = name == "zero3-int8"
+        self.zeropp = name == "zero3-zeropp"
+        self.int8 = name in ("zero3-int8", "zero3-zeropp")
         self.prefetch = name == "zero3-prefetch"
         n_dp = 8
         self.units = []
@@ -483,11 +513,19 @@ class Zero3Workload(Workload):
             self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
             self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>"
         self.dominant = "rs_adamw"
+        if self.zeropp:
+            self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp), n_dp, QGRAD_BLOCK, device)
+            sb = n_dp * 4 / QGRAD_BLOCK
+            # + every rank quantizes its unit gradient; the RS reads 1 B per source (+ scales)
+            self.bytes_per_elem = 3 + 3 + (n_dp * 3 + sb) + (n_dp + sb + 4) + 30 + 3
+            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_vec_kernel<1,4>, "
+                                 "qgrad_vec_kernel<8,false>, rs_adamw_vec_kernel<1,1>")
         if self.prefetch:
             self.dominant = "zero3_step_prefetched"
             self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
             self.pf = zstep.Zero3Prefetcher(self.units, self.ring, device=device)
         self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else "")
+                     + ("_int8_grads" if self.zeropp else "")
                      + ("_prefetch" if self.prefetch else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
@@ -495,6 +533,8 @@ class Zero3Workload(Workload):
         if self.int8:
             self.desc["quant_block"] = 256
         self.device_bytes = total * (12 + 2) + 2 * cap * 2 + g.numel() * 2 + cap * 4
+        if self.zeropp:
+            self.device_bytes += self.qg.q.numel() + self.qg.scales.numel() * 4
 
     def ops(self, t):
         zb, hp, zs = self.zb, self.hp(t), self.zstep
@@ -528,6 +568,17 @@ class Zero3Workload(Workload):
                 zs.zero3_layer_reduce_scatter(u, grads, self.A[:P])
                 self.ring.release(("bwd", i))
 
+            def quant_grads(u=u, P=P, grads=grads):
+                for r in range(u.layout.n_dp):
+                    zb.zero_quantize_int8(u.layout, grads[r], self.qg.q[r, :P],
+                                          self.qg.scales[r], QGRAD_BLOCK)
+
+            def rs_int8(u=u, i=i, P=P):
+                zb.zero_accumulate_int8(u.layout, [self.qg.q[r, :P] for r in range(u.layout.n_dp)],
+                                        [self.qg.scales[r] for r in range(u.layout.n_dp)],
+                                        QGRAD_BLOCK, self.A[:P], 0, 0, P, True)
+                self.ring.release(("bwd", i))
+
             def upd(u=u, P=P):
                 zs.zero3_update(u, self.A[:P], hp)
 
@@ -535,7 +586,13 @@ class Zero3Workload(Workload):
                 else ("gather", P * 4)
             out.append(Op(gkind, gbytes, fwd))
             out.append(Op(gkind, gbytes, bwd_gather))
-            out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
+            if self.zeropp:
+                n = u.layout.n_dp
+                sbytes = n * (-(-u.layout.shard // QGRAD_BLOCK)) * 4
+                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads))
+                out.append(Op("accumulate_int8", P * (n + 4) + n * sbytes, rs_int8))
+            else:
+                out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
             out.append(Op("rs_adamw", P * 30, upd))
             if q is not None:
                 def quant(u=u, q=q):
@@ -545,13 +602,13 @@ class Zero3Workload(Workload):
 
 
 def make_workload(name, device, elems=0):
-    if name in ("gpt2xl", "gpt2xl-clip"):
+    if name in ("gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad"):
         return Zero2Workload(name, device, elems)
     if name in ("llama7b-shard", "probe"):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
-    if name in ("zero3", "zero3-int8", "zero3-prefetch"):
+    if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -685,8 +742,9 @@ def run_ours(args):
 
     peak, peak_kind = _peak()
     primary = args.workload
-    extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "accum-zero1", "accum-zero2",
-                          "zero3", "zero3-prefetch", "zero3-int8") if w != primary]
+    extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
+                          "accum-zero2", "zero3", "zero3-prefetch", "zero3-int8", "zero3-zeropp")
+              if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}
     if args.elems:

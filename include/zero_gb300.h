@@ -136,10 +136,15 @@ int zero_shard_range(const zero_layout_t* L, int32_t rank, int64_t* begin, int64
  *   src_dtype ZERO_BF16 (per-rank bf16 gradients) or ZERO_F32 (accumulated
  *   fp32 gradients).  src_base <= begin.  divisor > 0 and finite (n_dp for a
  *   mean over ranks, n_dp*K after K accumulated micro-batches).
+ * Memory: master, m, v and out are device memory of the current device.  Each
+ *   src[r] is device memory or pinned host memory that the device addresses
+ *   at the same pointer (page-locked, mapped; the kernel then reads it over the
+ *   host link, with no staging copy -- on Grace-Blackwell the NVLink-C2C).
+ *   Pageable host memory is refused.
  * Sources are read only; master, m, v and out are updated in place.
  * Errors: ZERO_EINVAL (null, range outside the owned shards, bad mode/dtype,
- *   hp->step < 1, non-finite hyper-parameter, divisor <= 0, pointer not device
- *   memory), ZERO_ERANGE (n_src > ZERO_MAX_SRC), ZERO_EALIGN, ZERO_ECUDA. */
+ *   hp->step < 1, non-finite hyper-parameter, divisor <= 0, pointer of the
+ *   wrong kind), ZERO_ERANGE (n_src > ZERO_MAX_SRC), ZERO_EALIGN, ZERO_ECUDA. */
 int zero_reduce_scatter_adamw(const zero_layout_t* L,
                               const void* const* src, int32_t n_src, int32_t src_dtype,
                               int64_t src_base, float divisor,
@@ -249,6 +254,46 @@ int zero_quantize_int8(const zero_layout_t* unit, const uint16_t* shards_bf16, i
 int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* const* q_shards,
                            const float* const* scale_shards, int32_t block, uint16_t* full_out,
                            void* stream);
+
+/* ---- reduce-scatter of 8-bit gradients (ZeRO++) ---------------------------
+ * "ZeRO Optimizer, in depth", "Offload and ZeRO++" (zero_quantized_gradients
+ * quantises the gradient reduce-scatter) and "ZeRO and FSDP", "Fewer bytes on
+ * the wire" (gradients quantized during the reduce-scatter).  The pages give
+ * no format; the one taken is the 8-bit block format above, applied by each
+ * rank to its bf16 gradient slice for every owner: rank r calls
+ * zero_quantize_int8 with its whole gradient (padded_n bf16) as the "shards",
+ * giving codes q_r (padded_n int8, slice o at [o*S]) and scales s_r
+ * (n_dp * nb fp32, nb = ceil(S / block), slice o's at [o*nb]).
+ *
+ * For flat i in [begin, end), owned by o = i / S, with k = i - o*S:
+ *   g_r = fp32(q_r[i]) * s_r[o*nb + k/block]      (one fp32 rounding)
+ *   x   = +0 + g_0 + g_1 + ... + g_{n_src-1}      (fp32, ascending r)
+ * zero_reduce_scatter_adamw_int8: g = x / divisor, then AdamW, the bf16 cast
+ *   and the write exactly as zero_reduce_scatter_adamw (state of i at
+ *   [i - rank_begin*S]; out at [i] for ZERO_OUT_FULL, like the state for
+ *   ZERO_OUT_SHARD); [begin, end) must lie in the owned range of ranks
+ *   rank_begin..rank_end-1.
+ * zero_accumulate_int8: dst[i - dst_base] = x (first != 0) or
+ *   dst[i - dst_base] + x (first == 0) -- the stage-3 layer reduce-scatter
+ *   (first = 1, divisor applied by the update) or stage-2 accumulation.
+ * q_src and scale_src are host arrays of n_src device pointers; the codes are
+ * read at flat offsets [begin, end), the scales of the owners met.  A call runs
+ * one launch per owner met, in order, on `stream`.  Vector kernels need the
+ * slice-local start k a multiple of 8, 8-byte aligned codes at `begin` and
+ * 16-byte aligned state, output and dst; anything else runs element by element
+ * on the GPU.  Gradients must be finite.
+ * Errors: ZERO_EINVAL (null, block not 256/512/1024/2048, range, pointer kind,
+ * hyper-parameters), ZERO_ERANGE (n_src > ZERO_MAX_SRC), ZERO_EALIGN (scales
+ * not 4-byte aligned, state or dst not element-aligned), ZERO_ECUDA. */
+int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8_t* const* q_src,
+                                   const float* const* scale_src, int32_t n_src, int32_t block,
+                                   float divisor, int32_t rank_begin, int32_t rank_end,
+                                   int64_t begin, int64_t end, float* master, float* m, float* v,
+                                   uint16_t* out_bf16, int32_t out_mode, const zero_adamw_t* hp,
+                                   void* stream);
+int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const* q_src,
+                         const float* const* scale_src, int32_t n_src, int32_t block, float* dst,
+                         int64_t dst_base, int64_t begin, int64_t end, int32_t first, void* stream);
 
 /* ---- gradient accumulation / stage-3 layer reduce-scatter ----------------
  * "ZeRO and FSDP", "The idea, one stage at a time", paragraph on gradient

@@ -368,3 +368,13 @@ def qgrad_rs_adamw_reference(q_rows, scale_rows, n_dp: int, block: int, divisor,
     g = reduce_mean(dequantize_grad_int8(q_rows, scale_rows, n_dp, block), divisor)
     w2, m2, v2 = adamw(w, m, v, g, hp, t)
     return cast_bf16(w2), w2, m2, v2
+
+
+def accumulate_reduce_int8(acc, q_rows, scale_rows, n_dp: int, block: int, first: bool) -> np.ndarray:
+    """The owner's fp32 accumulation of 8-bit gradients over the whole padded
+    vector: x = +0 + sum over ranks of the dequantized values (ascending), then
+    acc = x (first) or acc + x (one fp32 addition)."""
+    x = reduce_mean(dequantize_grad_int8(q_rows, scale_rows, n_dp, block), 1.0)   # sum / 1 is exact
+    if first:
+        return x
+    return (_f32(acc) + x).astype(np.float32)

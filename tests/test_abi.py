@@ -186,6 +186,46 @@ def test_accumulate_and_gather_argument_checks(zlib):
     assert g(ctypes.byref(empty), src, FAKE, None) == 0
 
 
+def test_int8_gradient_argument_checks(zlib):
+    """zero_reduce_scatter_adamw_int8 and zero_accumulate_int8 refuse bad
+    arguments before touching any pointer."""
+    lib = zlib.load()
+    L = zlib.zero_layout([4096], 4)
+    Lp = ctypes.byref(L)
+    q = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    s = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    hp = zlib.ZeroAdamW.make(step=1)
+    hpp = ctypes.byref(hp)
+
+    def rs(q=q, s=s, n=4, block=256, div=4.0, rb=0, re=4, b=0, e=4096, w=FAKE, mode=0, h=hpp):
+        return lib.zero_reduce_scatter_adamw_int8(Lp, q, s, n, block, div, rb, re, b, e,
+                                                  w, FAKE, FAKE, FAKE, mode, h, None)
+
+    assert rs(q=None) == -1
+    assert rs(n=0) == -1
+    assert rs(n=65) == -3
+    for block in (0, 128, 384, 4096):
+        assert rs(block=block) == -1
+    assert rs(s=(ctypes.c_void_p * 4)(FAKE, FAKE + 2, FAKE, FAKE)) == -2     # scales 4-byte aligned
+    assert rs(q=(ctypes.c_void_p * 4)(FAKE, 0, FAKE, FAKE)) == -1
+    assert rs(div=0.0) == -1
+    assert rs(rb=1, b=0) == -1                                               # begin below the owners
+    assert rs(e=4097) == -1
+    assert rs(mode=7) == -1
+    assert rs(w=FAKE + 2) == -2
+    assert rs(h=None) == -1
+    assert rs(b=64, e=64) == 0                                               # empty
+    acc = lib.zero_accumulate_int8
+    assert acc(None, q, s, 4, 256, FAKE, 0, 0, 4096, 1, None) == -1
+    assert acc(Lp, q, s, 4, 256, None, 0, 0, 4096, 1, None) == -1
+    assert acc(Lp, q, s, 4, 100, FAKE, 0, 0, 4096, 1, None) == -1           # block
+    assert acc(Lp, q, s, 65, 256, FAKE, 0, 0, 4096, 1, None) == -3
+    assert acc(Lp, q, s, 4, 256, FAKE, 8, 0, 4096, 1, None) == -1           # dst_base > begin
+    assert acc(Lp, q, s, 4, 256, FAKE, 0, 0, 4097, 1, None) == -1           # past P
+    assert acc(Lp, q, s, 4, 256, FAKE + 2, 0, 0, 4096, 1, None) == -2       # dst alignment
+    assert acc(Lp, q, s, 4, 256, FAKE, 0, 64, 64, 1, None) == 0             # empty
+
+
 def test_missing_library_fails_loudly(zlib, monkeypatch, tmp_path):
     from zero_sharded_mixed_gb300 import binding
     monkeypatch.setattr(binding, "lib_path", str(tmp_path / "nope.so"))

@@ -271,3 +271,62 @@ def test_gpt2xl_clipped_step(zlib, cuda_device):
     parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref)
     assert np.array_equal(_bits_at(out, idx_dev), ref_out)
     _full_properties(master, out, L.n)
+
+
+def test_gpt2xl_int8_gradients(zlib, cuda_device):
+    """GPT-2-XL shapes at n_dp = 8 with 8-bit gradients (block 256): every rank
+    quantizes its whole gradient, then the fused update over all buckets,
+    2 steps.  A code's scale depends on its whole block, so the oracle runs on
+    sampled blocks (random ones plus those at every bucket and slice boundary
+    and the ends): codes and scales of every rank, then the state and bf16
+    output of every element of those blocks."""
+    zb = zlib
+    dev = cuda_device
+    block, n_dp = 256, 8
+    L = zb.zero_layout(inputs.gpt2xl_numels(), n_dp, 8, 500_000_000)
+    P, S = L.padded_n, L.shard
+    nb = -(-S // block)
+    g = torch.empty((n_dp, P), dtype=torch.bfloat16, device=dev)
+    qg = zstep.Int8Grads(L, n_dp, block, dev)
+    master = inputs.master_weights(L.n, P, seed=SEED, device=dev)
+    m = torch.zeros(P, device=dev)
+    v = torch.zeros(P, device=dev)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=dev)
+    # sampled blocks, as (owner, block index within the slice)
+    rng = np.random.default_rng(4)
+    flat = set(int(x) for x in rng.integers(0, n_dp * nb, size=2048))
+    for e in [b * L.bucket for b in range(1, L.n_buckets)] + [o * S for o in range(n_dp + 1)]:
+        for i in (e - 1, e):
+            if 0 <= i < P:
+                flat.add((i // S) * nb + (i % S) // block)
+    blocks = sorted(flat)
+    spans = [(o * S + j * block, o * S + min((j + 1) * block, S)) for o, j in
+             (divmod(b, nb) for b in blocks)]
+    idx = np.concatenate([np.arange(a, c) for a, c in spans])
+    idx_dev = torch.from_numpy(idx).to(dev)
+    sidx_dev = torch.tensor(blocks, device=dev)
+    ref = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
+    for t in (1, 2):
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=t, rank=r, outlier_p=0.01)
+        qg.quantize([g[r] for r in range(n_dp)])
+        zstep.zero12_step_int8(L, qg, master, m, v, out, _hp(zb, t))
+        zb.zero_status_check()
+        gs = [_bits_at(g[r], idx_dev) for r in range(n_dp)]
+        deq = np.empty((n_dp, idx.size), np.float32)
+        for r in range(n_dp):
+            q_got = qg.q[r].index_select(0, idx_dev).cpu().numpy()
+            s_got = qg.scales[r].index_select(0, sidx_dev).cpu().numpy()
+            pos = 0
+            for k, (a, c) in enumerate(spans):
+                q, s = oracle.quantize_int8(gs[r][pos:pos + c - a], block)
+                assert np.array_equal(q_got[pos:pos + c - a], q), (t, r, a)
+                assert s_got[k] == s[0], (t, r, a)
+                deq[r, pos:pos + c - a] = oracle.dequantize_grad_int8(q[None, :], s[None, :], 1, block)[0]
+                pos += c - a
+        gm = oracle.reduce_mean(deq, n_dp)
+        w2, m2, v2 = oracle.adamw(*ref, gm, HP, t)
+        ref = [w2, m2, v2]
+        parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref, what=f"t={t} ")
+        assert np.array_equal(_bits_at(out, idx_dev), oracle.cast_bf16(w2))
+    _full_properties(master, out, L.n)

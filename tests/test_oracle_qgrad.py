@@ -112,3 +112,19 @@ def test_blocks_restart_at_every_slice():
         last = np.abs(x[o * S + block:(o + 1) * S]).max()
         assert scales[0, 2 * o] == np.float32(first) / np.float32(127)
         assert scales[0, 2 * o + 1] == np.float32(last) / np.float32(127)
+
+
+def test_exact_gradients_accumulate_like_bf16():
+    """With exactly representable gradients the 8-bit accumulation equals the
+    pinned bf16 accumulation (stage 2 and the stage-3 layer reduce-scatter),
+    overwrite and add alike."""
+    n_dp, S, block = 4, 600, 256
+    g1, _, _ = _exact_grads(n_dp, n_dp, S, block, seed=11)
+    g2, _, _ = _exact_grads(n_dp, n_dp, S, block, seed=12)
+    q1, s1 = oracle.quantize_grad_int8(g1, n_dp, block)
+    q2, s2 = oracle.quantize_grad_int8(g2, n_dp, block)
+    a = oracle.accumulate_reduce_int8(None, q1, s1, n_dp, block, True)
+    assert np.array_equal(a, oracle.accumulate_reduce(None, g1, True))
+    a = oracle.accumulate_reduce_int8(a, q2, s2, n_dp, block, False)
+    ref = oracle.accumulate_reduce(oracle.accumulate_reduce(None, g1, True), g2, False)
+    assert np.array_equal(a, ref)

@@ -107,6 +107,11 @@ def load():
         lib.zero_crc32.argtypes = [p, i64]
         lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
+        lib.zero_reduce_scatter_adamw_int8.argtypes = [
+            P(ZeroLayout), P(p), P(p), i32, i32, f32, i32, i32, i64, i64,
+            p, p, p, p, i32, P(ZeroAdamW), p]
+        lib.zero_accumulate_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, i32, p, i64, i64, i64,
+                                             i32, p]
         lib.zero_accumulate.argtypes = [P(ZeroLayout), i32, P(p), i32, i32, i64, p, i64, i64, i64,
                                         i32, p]
         lib.zero_status_check.argtypes = [p]
@@ -196,10 +201,14 @@ def _stream_ptr(stream) -> int | None:
     return stream.cuda_stream or None
 
 
-def _tensor(t: torch.Tensor, name: str, dtype, min_numel: int) -> int:
+def _tensor(t: torch.Tensor, name: str, dtype, min_numel: int, pinned_ok: bool = False) -> int:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if pinned_ok and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name} is host memory but not pinned; the kernels read only "
+                             "device memory or pinned host memory")
+    elif t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -213,10 +222,10 @@ def _tensor(t: torch.Tensor, name: str, dtype, min_numel: int) -> int:
 _SRC_DT = {ZERO_BF16: torch.bfloat16, ZERO_F32: torch.float32}
 
 
-def _src_array(srcs, dtype, min_numel):
+def _src_array(srcs, dtype, min_numel, pinned_ok=False):
     if len(srcs) == 0:
         raise ValueError("need at least one source")
-    ptrs = [_tensor(s, f"src[{i}]", dtype, min_numel) for i, s in enumerate(srcs)]
+    ptrs = [_tensor(s, f"src[{i}]", dtype, min_numel, pinned_ok) for i, s in enumerate(srcs)]
     return (ctypes.c_void_p * len(ptrs))(*ptrs), len(ptrs)
 
 
@@ -224,14 +233,16 @@ def zero_reduce_scatter_adamw(L: ZeroLayout, srcs, src_dtype: int, src_base: int
                               rank_begin: int, rank_end: int, begin: int, end: int,
                               master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
                               out: torch.Tensor, out_mode: int, hp: ZeroAdamW, stream=None):
-    """Fused mean reduce-scatter + AdamW + bf16 cast + gather write over [begin, end)."""
+    """Fused mean reduce-scatter + AdamW + bf16 cast + gather write over [begin, end).
+    The sources may be pinned host tensors: the kernel then reads them over the
+    host link."""
     if end <= begin:
         src_need = state_need = out_need = 0
     else:
         src_need = end - src_base
         state_need = end - rank_begin * L.shard
         out_need = end if out_mode == ZERO_OUT_FULL else state_need
-    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need, pinned_ok=True)
     rc = load().zero_reduce_scatter_adamw(
         ctypes.byref(L), arr, n, int(src_dtype), int(src_base), float(divisor),
         int(rank_begin), int(rank_end), int(begin), int(end),
@@ -257,7 +268,7 @@ def zero_reduce_scatter_adamw_clip(L: ZeroLayout, srcs, src_dtype: int, src_base
         src_need = end - src_base
         state_need = end - rank_begin * L.shard
         out_need = end if out_mode == ZERO_OUT_FULL else state_need
-    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need, pinned_ok=True)
     rc = load().zero_reduce_scatter_adamw_clip(
         ctypes.byref(L), arr, n, int(src_dtype), int(src_base), float(divisor),
         int(rank_begin), int(rank_end), int(begin), int(end),
@@ -389,6 +400,54 @@ def zero_gather_layer_int8(unit: ZeroLayout, q_shards, scale_shards, full_out: t
         (ctypes.c_void_p * max(1, len(sp)))(*sp), int(block),
         _tensor(full_out, "full_out", torch.bfloat16, unit.padded_n), _stream_ptr(stream))
     _check(rc, "zero_gather_layer_int8")
+
+
+def _qgrad_sources(L: ZeroLayout, q_src, scale_src, block: int, need: int):
+    """Host arrays of the codes and scales of 8-bit gradient sources."""
+    if len(q_src) == 0 or len(q_src) != len(scale_src):
+        raise ValueError("need the same nonzero number of code and scale sources")
+    nb = -(-L.shard // block) if L.shard else 0
+    qp = [_tensor(x, f"q_src[{i}]", torch.int8, need) for i, x in enumerate(q_src)]
+    sp = [_tensor(x, f"scale_src[{i}]", torch.float32, nb * L.n_dp if need else 0)
+          for i, x in enumerate(scale_src)]
+    n = len(qp)
+    return (ctypes.c_void_p * n)(*qp), (ctypes.c_void_p * n)(*sp), n
+
+
+def zero_reduce_scatter_adamw_int8(L: ZeroLayout, q_src, scale_src, block: int, divisor: float,
+                                   rank_begin: int, rank_end: int, begin: int, end: int,
+                                   master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                                   out: torch.Tensor, out_mode: int, hp: ZeroAdamW, stream=None):
+    """The fused update over [begin, end) from 8-bit gradients: each rank's
+    codes (padded_n int8) and block scales (n_dp * ceil(S / block) fp32)."""
+    if end <= begin:
+        src_need = state_need = out_need = 0
+    else:
+        src_need = end
+        state_need = end - rank_begin * L.shard
+        out_need = end if out_mode == ZERO_OUT_FULL else state_need
+    qa, sa, n = _qgrad_sources(L, q_src, scale_src, block, src_need)
+    rc = load().zero_reduce_scatter_adamw_int8(
+        ctypes.byref(L), qa, sa, n, int(block), float(divisor), int(rank_begin), int(rank_end),
+        int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(out, "out", torch.bfloat16, out_need),
+        int(out_mode), ctypes.byref(hp), _stream_ptr(stream))
+    _check(rc, "zero_reduce_scatter_adamw_int8")
+
+
+def zero_accumulate_int8(L: ZeroLayout, q_src, scale_src, block: int, dst: torch.Tensor,
+                         dst_base: int, begin: int, end: int, first: bool, stream=None):
+    """dst[i - dst_base] (+)= sum over ranks of the dequantized 8-bit gradients."""
+    src_need = end if end > begin else 0
+    dst_need = max(0, end - dst_base) if end > begin else 0
+    qa, sa, n = _qgrad_sources(L, q_src, scale_src, block, src_need)
+    rc = load().zero_accumulate_int8(ctypes.byref(L), qa, sa, n, int(block),
+                                     _tensor(dst, "dst", torch.float32, dst_need), int(dst_base),
+                                     int(begin), int(end), int(bool(first)), _stream_ptr(stream))
+    _check(rc, "zero_accumulate_int8")
 
 
 def zero_selftest_bounded_wait(limit_cycles: int, stream=None):

@@ -60,6 +60,15 @@ __device__ __forceinline__ float4 ld_stream_f4(const void* p) {
     return *reinterpret_cast<const float4*>(p);
 #endif
 }
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
+#if ZGB_LD_HINT == 1
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+#elif ZGB_LD_HINT == 2
+    return __ldg(reinterpret_cast<const uint2*>(p));
+#else
+    return *reinterpret_cast<const uint2*>(p);
+#endif
+}
 __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
 #if ZGB_ST_HINT == 1
     __stcs(reinterpret_cast<uint4*>(p), v);
@@ -79,6 +88,9 @@ __device__ __forceinline__ void st_stream_f4(void* p, float4 v) {
 
 // 0 if p is device (or managed) memory of the current device, else ZERO_EINVAL.
 int check_device_ptr(const void* p);
+// Also 0 for pinned host memory that the device addresses at the same pointer
+// (read by the kernels over the host link).
+int check_source_ptr(const void* p);
 // ZERO_EALIGN unless p is a multiple of `bytes`.
 inline int check_aligned(const void* p, int bytes) {
     return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)bytes) ? ZERO_EALIGN : ZERO_OK;

@@ -1,0 +1,408 @@
+// The 8-bit gradient reduce-scatter (ZeRO++ quantized gradients), sm_103a.
+//
+// "ZeRO Optimizer, in depth", "Offload and ZeRO++" (zero_quantized_gradients
+// quantises the gradient reduce-scatter) and "ZeRO and FSDP", "Fewer bytes on
+// the wire".  Every rank has quantized its bf16 gradient slice for owner o in
+// the block format of the weight gather (zero_quantize_int8 over the rank's
+// whole gradient: slice o's codes at [o*S], its scales at [o*nb]).  For each
+// owned element the owner reads the n_src codes (1 byte each) and their block
+// scales, forms g_r = code * scale (one fp32 rounding), sums over ranks in
+// ascending order from +0, and then
+//   zero_reduce_scatter_adamw_int8  divides once, AdamW, bf16 cast, gather write
+//                                   (what zero_reduce_scatter_adamw does with
+//                                   the sum of bf16 gradients);
+//   zero_accumulate_int8            adds the sum into an fp32 buffer (the
+//                                   stage-3 layer reduce-scatter, or stage-2
+//                                   accumulation).
+// Bytes per element: n_src * (1 + 4/block) + 26 for the update, + 4 (+ 4 when
+// adding) for the accumulation -- against 2 * n_src bytes of bf16 gradients.
+//
+// Design: the register-staged stream of the bf16 update.  A thread takes 8
+// consecutive elements per vector: one 64-bit code load per source (a warp
+// reads 256 consecutive bytes of each source), the source's block scale
+// through the read-only path (blocks are >= 256 elements, so the 32 lanes of a
+// warp share one scale), the fp32 state as 128-bit loads; every load of a
+// vector is issued before the first add.  The host splits a call at owner
+// boundaries into one launch per owner, so that all elements of a launch lie
+// in one slice and the scale index is (k0 + i) >> log2(block).
+#include <cmath>
+
+#include "zero_update.cuh"
+
+#ifndef ZGB_QGRAD_WAVES
+#define ZGB_QGRAD_WAVES 1    // update: grid = resident CTAs x this (measured: x1 +5 % over x64)
+#endif
+#ifndef ZGB_QACC_WAVES
+#define ZGB_QACC_WAVES 1     // accumulation: the same (measured: 5.7 TB/s at x1, 5.2 at x64)
+#endif
+#ifndef ZGB_QGRAD_PREFETCH
+#define ZGB_QGRAD_PREFETCH 0 // grid-stride passes ahead whose chunk a CTA prefetches into L2
+                             // (0: off; measured: 1 or 2 ahead cost the update 2-3 %)
+#endif
+#ifndef ZGB_QGRAD_U
+#define ZGB_QGRAD_U 0        // vectors per thread and iteration; 0 = the measured choice
+#endif
+
+namespace zgb {
+
+struct QGradParams {
+    const int8_t* q[ZERO_MAX_SRC];     // rank r's codes, offset to the launch's first element
+    const float* scale[ZERO_MAX_SRC];  // rank r's block scales of this owner's slice
+    float* w;                          // update: state, offset like q
+    float* m;
+    float* v;
+    uint16_t* out;                     // update: bf16 output, offset like q
+    float* dst;                        // accumulation: fp32 destination, offset like q
+    int64_t n;                         // elements of the launch, all in one owner's slice
+    int64_t k0;                        // slice-local index of the launch's first element
+    int32_t n_src;
+    int32_t block_shift;               // log2(block)
+    int32_t first;                     // accumulation: 1 overwrites dst, 0 adds to it
+    AdamwScalars h;
+};
+
+// Code j (0..3) of a 32-bit word as an fp32 value (exact: |code| <= 127).
+__device__ __forceinline__ float code_f32(uint32_t word, int j) {
+    return (float)(int)(int8_t)(word >> (8 * j));
+}
+
+// x[j] = x[j] + code_j * scale for the 8 codes of c; each product and each
+// sum one IEEE rounding.
+__device__ __forceinline__ void add_codes8(float (&x)[8], const uint2 c, const float s) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = __fadd_rn(x[j], __fmul_rn(code_f32(c.x, j), s));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[4 + j] = __fadd_rn(x[4 + j], __fmul_rn(code_f32(c.y, j), s));
+}
+
+// One vector's loads: R sources' codes and scales, then the state (update) or
+// the destination (accumulation that adds).
+template <int R, bool kUpdate>
+struct QVec {
+    uint2 c[R];
+    float s[R];
+    float4 st[kUpdate ? 6 : 2];
+};
+
+template <int R, bool kUpdate>
+__device__ __forceinline__ void load_qvec(const QGradParams& p, int64_t e, QVec<R, kUpdate>& x) {
+    const int64_t b = (p.k0 + e) >> p.block_shift;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        x.c[r] = ld_stream_u2(p.q[r] + e);
+        x.s[r] = __ldg(p.scale[r] + b);
+    }
+    if constexpr (kUpdate) {
+        load_state(p, e, x.st);
+    } else if (!p.first) {
+        x.st[0] = ld_stream_f4(p.dst + e);
+        x.st[1] = ld_stream_f4(p.dst + e + 4);
+    }
+}
+
+// The accumulation's result of one vector: (dst +) the source sum.
+__device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float (&x)[8],
+                                          const float4 (&d)[2]) {
+    if (!p.first) {
+        const float4 a = d[0], b = d[1];
+        x[0] = __fadd_rn(a.x, x[0]); x[1] = __fadd_rn(a.y, x[1]);
+        x[2] = __fadd_rn(a.z, x[2]); x[3] = __fadd_rn(a.w, x[3]);
+        x[4] = __fadd_rn(b.x, x[4]); x[5] = __fadd_rn(b.y, x[5]);
+        x[6] = __fadd_rn(b.z, x[6]); x[7] = __fadd_rn(b.w, x[7]);
+    }
+    st_stream_f4(p.dst + e, make_float4(x[0], x[1], x[2], x[3]));
+    st_stream_f4(p.dst + e + 4, make_float4(x[4], x[5], x[6], x[7]));
+}
+
+// U vectors (vi0, vi0 + kThreads, ...) with a compile-time source count.
+template <int R, bool kUpdate, int U>
+__device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, int64_t nv) {
+    QVec<R, kUpdate> x[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t vi = vi0 + u * kThreads;
+        ok[u] = vi < nv;
+        if (ok[u]) load_qvec<R, kUpdate>(p, vi * 8, x[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!ok[u]) continue;
+        const int64_t e = (vi0 + u * kThreads) * 8;
+        float s[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) add_codes8(s, x[u].c[r], x[u].s[r]);
+        if constexpr (kUpdate) {
+            finish_vec(p, e, s, x[u].st, 1.0f);
+        } else {
+            const float4 d[2] = {x[u].st[0], x[u].st[1]};
+            store_acc(p, e, s, d);
+        }
+    }
+}
+
+// One vector with a runtime source count, one source at a time.
+template <bool kUpdate>
+__device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) {
+    const int64_t e = vi * 8;
+    const int64_t b = (p.k0 + e) >> p.block_shift;
+    float s[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = 0.0f;
+    for (int r = 0; r < p.n_src; ++r) add_codes8(s, ld_stream_u2(p.q[r] + e), __ldg(p.scale[r] + b));
+    if constexpr (kUpdate) {
+        float4 st[6];
+        load_state(p, e, st);
+        finish_vec(p, e, s, st, 1.0f);
+    } else {
+        float4 d[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        if (!p.first) {
+            d[0] = ld_stream_f4(p.dst + e);
+            d[1] = ld_stream_f4(p.dst + e + 4);
+        }
+        store_acc(p, e, s, d);
+    }
+}
+
+// One element (ragged tails, ranges off the 8-element grid).
+template <bool kUpdate>
+__device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i) {
+    const int64_t b = (p.k0 + i) >> p.block_shift;
+    float s = 0.0f;
+    for (int r = 0; r < p.n_src; ++r) s = __fadd_rn(s, __fmul_rn((float)p.q[r][i], __ldg(p.scale[r] + b)));
+    if constexpr (kUpdate) {
+        float w = p.w[i], m = p.m[i], v = p.v[i];
+        adamw_update(mean_grad(s, p.h, 1.0f), w, m, v, p.h);
+        p.w[i] = w;
+        p.m[i] = m;
+        p.v[i] = v;
+        p.out[i] = to_bf16(w);
+    } else {
+        p.dst[i] = p.first ? s : __fadd_rn(p.dst[i], s);
+    }
+}
+
+// Asks the TMA engine to bring [p, p + bytes) into L2: no registers, nothing to
+// wait for.  The range is shrunk to the whole 16-byte units inside it, so the
+// prefetch never leaves the bytes the launch itself reads.
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15);
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo))
+                     : "memory");
+}
+
+// Threads 0 .. R+2 of a CTA prefetch one array each of the CTA's chunk
+// [c0, c0 + chunk) (in vectors): the R code arrays, then w, m, v (update) or
+// dst (accumulation that adds).
+template <int R, bool kUpdate>
+__device__ __forceinline__ void prefetch_chunk(const QGradParams& p, int64_t c0, int64_t chunk,
+                                               int64_t nv) {
+    const int t = threadIdx.x;
+    if (t >= R + 3 || c0 >= nv) return;
+    const int64_t e0 = c0 * 8;
+    const int64_t n = ((c0 + chunk < nv ? c0 + chunk : nv) - c0) * 8;
+    if (t < R) {
+        prefetch_l2(p.q[t] + e0, n);
+    } else if constexpr (kUpdate) {
+        const float* a = t == R ? p.w : t == R + 1 ? p.m : p.v;
+        prefetch_l2(a + e0, n * 4);
+    } else if (t == R && !p.first) {
+        prefetch_l2(p.dst + e0, n * 4);
+    }
+}
+
+// Vectors per thread and iteration: the code loads are 8 bytes, so a vector
+// with few sources leaves HBM short of bytes in flight unless a thread takes
+// several.
+template <int R, bool kUpdate>
+__host__ __device__ constexpr int qgrad_vectors_per_iter() {
+    return R == 0 ? 1 : ZGB_QGRAD_U > 0 ? ZGB_QGRAD_U
+         : kUpdate ? (R <= 2 ? 2 : 1) : (R <= 4 ? 4 : R <= 8 ? 2 : 1);
+}
+
+template <int R, bool kUpdate>
+__global__ void __launch_bounds__(kThreads, 2) qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
+    const int64_t nv = p.n >> 3;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if constexpr (R > 0) {
+        constexpr int U = qgrad_vectors_per_iter<R, kUpdate>();
+        const int64_t chunk = (int64_t)U * kThreads;
+        for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk) {
+            if constexpr (ZGB_QGRAD_PREFETCH > 0)
+                prefetch_chunk<R, kUpdate>(p, v0 - threadIdx.x + ZGB_QGRAD_PREFETCH * (int64_t)gridDim.x * chunk,
+                                           chunk, nv);
+            qgrad_vecs<R, kUpdate, U>(p, v0, nv);
+        }
+    } else {
+        const int64_t stride = (int64_t)gridDim.x * kThreads;
+        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate>(p, vi);
+    }
+    const int64_t tail = p.n - (nv << 3);
+    if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid);
+}
+
+template <bool kUpdate>
+__global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_constant__ QGradParams p) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n; i += stride)
+        qgrad_one<kUpdate>(p, i);
+}
+
+template <int R, bool kUpdate>
+int launch_qgrad_vec(const QGradParams& p, cudaStream_t s) {
+    static int occupancy = 0;
+    if (occupancy == 0) occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate>, kThreads, 0);
+    const int64_t per_cta = (int64_t)qgrad_vectors_per_iter<R, kUpdate>() * kThreads;
+    const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
+    const unsigned grid = grid_for(p.n >> 3, per_cta, (int64_t)sm_count() * occupancy * waves);
+    qgrad_vec_kernel<R, kUpdate><<<grid, kThreads, 0, s>>>(p);
+    return launch_status();
+}
+
+template <bool kUpdate>
+int launch_qgrad(const QGradParams& p, bool vec, cudaStream_t s) {
+    if (!vec) {
+        static int occupancy = 0;
+        if (occupancy == 0) occupancy = ctas_per_sm((const void*)qgrad_scalar_kernel<kUpdate>, kThreads, 0);
+        const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
+        qgrad_scalar_kernel<kUpdate><<<grid, kThreads, 0, s>>>(p);
+        return launch_status();
+    }
+    switch (p.n_src) {
+        case 1: return launch_qgrad_vec<1, kUpdate>(p, s);
+        case 2: return launch_qgrad_vec<2, kUpdate>(p, s);
+        case 4: return launch_qgrad_vec<4, kUpdate>(p, s);
+        case 8: return launch_qgrad_vec<8, kUpdate>(p, s);
+        case 16: return launch_qgrad_vec<16, kUpdate>(p, s);
+        default: return launch_qgrad_vec<0, kUpdate>(p, s);
+    }
+}
+
+// log2 of a block size the format allows (256, 512, 1024, 2048), else -1.
+int qgrad_block_shift(int32_t block) {
+    for (int sh = 8; sh <= 11; ++sh)
+        if (block == (1 << sh)) return sh;
+    return -1;
+}
+
+// The source checks shared by both entry points (no CUDA call).
+int check_qsources(const int8_t* const* q_src, const float* const* scale_src, int32_t n_src,
+                   int32_t block) {
+    if (!q_src || !scale_src) return ZERO_EINVAL;
+    if (n_src < 1) return ZERO_EINVAL;
+    if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
+    if (qgrad_block_shift(block) < 0) return ZERO_EINVAL;
+    for (int r = 0; r < n_src; ++r)
+        if (!q_src[r] || !scale_src[r]) return ZERO_EINVAL;
+    for (int r = 0; r < n_src; ++r)
+        if (check_aligned(scale_src[r], 4)) return ZERO_EALIGN;
+    return ZERO_OK;
+}
+
+int check_qsource_ptrs(const int8_t* const* q_src, const float* const* scale_src, int32_t n_src) {
+    for (int r = 0; r < n_src; ++r)
+        if (check_device_ptr(q_src[r]) || check_device_ptr(scale_src[r])) return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+// One launch per owner o whose slice meets [begin, end).  `place` sets the
+// target pointers of a launch covering flat [lo, hi) and returns whether they
+// allow the vector kernel.
+template <bool kUpdate, class Place>
+int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* const* scale_src,
+              int32_t n_src, int32_t block, int64_t begin, int64_t end, QGradParams base,
+              Place place, cudaStream_t s) {
+    const int64_t S = L->shard;
+    const int64_t nb = (S + block - 1) / block;
+    base.n_src = n_src;
+    base.block_shift = qgrad_block_shift(block);
+    for (int r = n_src; r < ZERO_MAX_SRC; ++r) {
+        base.q[r] = nullptr;
+        base.scale[r] = nullptr;
+    }
+    for (int64_t o = begin / S; o < L->n_dp; ++o) {
+        const int64_t lo = begin > o * S ? begin : o * S;
+        const int64_t hi = end < (o + 1) * S ? end : (o + 1) * S;
+        if (lo >= hi) break;
+        QGradParams p = base;
+        p.n = hi - lo;
+        p.k0 = lo - o * S;
+        bool vec = (p.k0 & 7) == 0;
+        for (int r = 0; r < n_src; ++r) {
+            p.q[r] = q_src[r] + lo;
+            p.scale[r] = scale_src[r] + o * nb;
+            vec = vec && (reinterpret_cast<uintptr_t>(p.q[r]) & 7u) == 0;
+        }
+        vec = place(p, lo) && vec;
+        const int rc = launch_qgrad<kUpdate>(p, vec, s);
+        if (rc) return rc;
+    }
+    return ZERO_OK;
+}
+
+}  // namespace zgb
+
+extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8_t* const* q_src,
+                                              const float* const* scale_src, int32_t n_src,
+                                              int32_t block, float divisor, int32_t rank_begin,
+                                              int32_t rank_end, int64_t begin, int64_t end,
+                                              float* master, float* m, float* v, uint16_t* out_bf16,
+                                              int32_t out_mode, const zero_adamw_t* hp, void* stream) {
+    using namespace zgb;
+    int rc = check_qsources(q_src, scale_src, n_src, block);
+    if (rc) return rc;
+    UpdateTarget t;
+    if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode, &t)))
+        return rc;
+    QGradParams base;
+    if ((rc = make_scalars(hp, divisor, &base.h))) return rc;
+    if (end == begin) return ZERO_OK;
+    if ((rc = check_qsource_ptrs(q_src, scale_src, n_src))) return rc;
+    if ((rc = check_target_ptrs(t))) return rc;
+    base.dst = nullptr;
+    base.first = 0;
+    auto place = [&](QGradParams& p, int64_t lo) {
+        const int64_t off = lo - begin;
+        p.w = t.w + off;
+        p.m = t.m + off;
+        p.v = t.v + off;
+        p.out = t.out + off;
+        return aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.out);
+    };
+    return qgrad_run<true>(L, q_src, scale_src, n_src, block, begin, end, base, place,
+                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const* q_src,
+                                    const float* const* scale_src, int32_t n_src, int32_t block,
+                                    float* dst, int64_t dst_base, int64_t begin, int64_t end,
+                                    int32_t first, void* stream) {
+    using namespace zgb;
+    if (!L || !dst) return ZERO_EINVAL;
+    int rc = check_qsources(q_src, scale_src, n_src, block);
+    if (rc) return rc;
+    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp)
+        return ZERO_EINVAL;
+    if (begin < 0 || end > L->padded_n || begin > end) return ZERO_EINVAL;
+    if (dst_base > begin) return ZERO_EINVAL;
+    if (check_aligned(dst, 4)) return ZERO_EALIGN;
+    if (end == begin) return ZERO_OK;
+    if ((rc = check_qsource_ptrs(q_src, scale_src, n_src))) return rc;
+    if (check_device_ptr(dst)) return ZERO_EINVAL;
+    QGradParams base;
+    base.w = base.m = base.v = nullptr;
+    base.out = nullptr;
+    base.first = first ? 1 : 0;
+    base.h = AdamwScalars{};
+    auto place = [&](QGradParams& p, int64_t lo) {
+        p.dst = dst + (lo - dst_base);
+        return aligned16(p.dst);
+    };
+    return qgrad_run<false>(L, q_src, scale_src, n_src, block, begin, end, base, place,
+                            static_cast<cudaStream_t>(stream));
+}

@@ -19,6 +19,17 @@ int check_device_ptr(const void* p) {
     return ZERO_OK;
 }
 
+int check_source_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ZERO_EINVAL;
+    }
+    if (a.type == cudaMemoryTypeHost)                       // pinned, mapped at the same address
+        return a.devicePointer == p ? ZERO_OK : ZERO_EINVAL;
+    return check_device_ptr(p);
+}
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];

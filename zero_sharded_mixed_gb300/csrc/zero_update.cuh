@@ -56,6 +56,40 @@ __device__ __forceinline__ float mean_grad(float sum, const AdamwScalars& h, flo
     return __fmul_rn(__fdiv_rn(sum, h.divisor), coef);
 }
 
+// Update 8 elements at e from their source sums and loaded state; store.
+// P is a parameter block with the update target w, m, v, out and scalars h.
+template <class P>
+__device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&s)[8],
+                                           const float4 (&st)[6], float coef) {
+    float w[8] = {st[0].x, st[0].y, st[0].z, st[0].w, st[1].x, st[1].y, st[1].z, st[1].w};
+    float m[8] = {st[2].x, st[2].y, st[2].z, st[2].w, st[3].x, st[3].y, st[3].z, st[3].w};
+    float v[8] = {st[4].x, st[4].y, st[4].z, st[4].w, st[5].x, st[5].y, st[5].z, st[5].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_update(mean_grad(s[j], p.h, coef), w[j], m[j], v[j], p.h);
+    st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
+    st_stream_f4(p.w + e + 4, make_float4(w[4], w[5], w[6], w[7]));
+    st_stream_f4(p.m + e, make_float4(m[0], m[1], m[2], m[3]));
+    st_stream_f4(p.m + e + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_stream_f4(p.v + e, make_float4(v[0], v[1], v[2], v[3]));
+    st_stream_f4(p.v + e + 4, make_float4(v[4], v[5], v[6], v[7]));
+    uint4 o;
+    o.x = pack_bf16x2(w[0], w[1]);
+    o.y = pack_bf16x2(w[2], w[3]);
+    o.z = pack_bf16x2(w[4], w[5]);
+    o.w = pack_bf16x2(w[6], w[7]);
+    st_stream_u4(p.out + e, o);
+}
+
+template <class P>
+__device__ __forceinline__ void load_state(const P& p, int64_t e, float4 (&st)[6]) {
+    st[0] = ld_stream_f4(p.w + e);
+    st[1] = ld_stream_f4(p.w + e + 4);
+    st[2] = ld_stream_f4(p.m + e);
+    st[3] = ld_stream_f4(p.m + e + 4);
+    st[4] = ld_stream_f4(p.v + e);
+    st[5] = ld_stream_f4(p.v + e + 4);
+}
+
 // The launch parameters of the fused update kernels.
 struct UpdateParams {
     const void* src[ZERO_MAX_SRC];  // gradient sources (bf16 or fp32), offset to the range start

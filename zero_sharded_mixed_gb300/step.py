@@ -253,6 +253,36 @@ class HostPipeline:
         comp.wait_event(self.ev_out)     # the step ends when the result is on the host
 
 
+class HostDirect:
+    """A ZeRO-1/2 step whose gradients stay in pinned host memory: the fused
+    kernel reads the n_dp gradient rows over the host link itself (on
+    Grace-Blackwell the NVLink-C2C), bucket by bucket, with no staging copy;
+    each bucket's bf16 result is copied back to pinned host memory on a second
+    stream while the next bucket updates."""
+
+    def __init__(self, L, device=None):
+        self.L = L
+        self.ranges = bucket_ranges(L)
+        self.d2h = torch.cuda.Stream(device=device)
+        self.ev_done = [torch.cuda.Event() for _ in self.ranges]
+        self.ev_out = torch.cuda.Event()
+
+    def step(self, host_grads, master, m, v, out, host_out, hp):
+        L = self.L
+        comp = torch.cuda.current_stream()
+        rows = [host_grads[r] for r in range(L.n_dp)]
+        for j, (s, e) in enumerate(self.ranges):
+            zb.zero_reduce_scatter_adamw(L, rows, zb.ZERO_BF16, 0, float(L.n_dp), 0, L.n_dp, s, e,
+                                         master, m, v, out, zb.ZERO_OUT_FULL, hp, comp)
+            self.ev_done[j].record(comp)
+        with torch.cuda.stream(self.d2h):
+            for j, (s, e) in enumerate(self.ranges):
+                self.d2h.wait_event(self.ev_done[j])
+                host_out[s:e].copy_(out[s:e], non_blocking=True)
+            self.ev_out.record(self.d2h)
+        comp.wait_event(self.ev_out)     # the step ends when the result is on the host
+
+
 # --------------------------------------------------------------------------
 # ZeRO-3 with 8-bit weight gathers ("ZeRO Optimizer, in depth", "Offload and
 # ZeRO++": zero_quantized_weights)
@@ -286,6 +316,61 @@ def zero3_gather_int8(unit: Zero3Unit, qs: Int8Shards, ring: GatherRing, unit_id
     zb.zero_gather_layer_int8(unit.layout, [qs.q[o] for o in range(n)],
                               [qs.scales[o] for o in range(n)], buf, qs.block, stream)
     return buf
+
+
+# --------------------------------------------------------------------------
+# 8-bit gradient reduce-scatter ("ZeRO Optimizer, in depth", "Offload and
+# ZeRO++": zero_quantized_gradients; "ZeRO and FSDP", "Fewer bytes on the
+# wire": gradients quantized during the reduce-scatter)
+# --------------------------------------------------------------------------
+
+class Int8Grads:
+    """Every simulated rank's quantized gradient: codes [n_src, P] int8 and
+    block scales [n_src, n_dp * ceil(S / block)] fp32.  Row r is what rank r
+    sends in the reduce-scatter: its slice o (codes [o*S, (o+1)*S), scales
+    [o*nb, (o+1)*nb)) to owner o."""
+
+    def __init__(self, layout, n_src: int | None = None, block: int = 256, device="cuda"):
+        self.layout = layout
+        self.block = block
+        self.n_src = layout.n_dp if n_src is None else n_src
+        self.nb = -(-layout.shard // block) if layout.shard else 0
+        self.q = torch.empty((self.n_src, layout.padded_n), dtype=torch.int8, device=device)
+        self.scales = torch.empty((self.n_src, max(layout.n_dp * self.nb, 1)), dtype=torch.float32,
+                                  device=device)
+
+    def quantize(self, grads, stream=None):
+        """Each rank quantizes its bf16 gradient (P elements), slice by slice."""
+        for r in range(self.n_src):
+            zb.zero_quantize_int8(self.layout, grads[r], self.q[r], self.scales[r], self.block, stream)
+
+    def sources(self):
+        return [self.q[r] for r in range(self.n_src)], [self.scales[r] for r in range(self.n_src)]
+
+    def wire_bytes(self) -> int:
+        """Bytes one rank sends: its slices for the n_dp - 1 other owners."""
+        L = self.layout
+        return (L.n_dp - 1) * (L.shard + self.nb * 4)
+
+
+def zero12_step_int8(L, qg: Int8Grads, master, m, v, out, hp, rank_begin=0, rank_end=None,
+                     stream=None):
+    """A ZeRO-1/2 step from 8-bit gradients, bucket by bucket: every owner
+    dequantizes the ranks' slices, takes the fp32 mean and updates."""
+    rank_end = L.n_dp if rank_end is None else rank_end
+    qs, ss = qg.sources()
+    for s, e in bucket_ranges(L, rank_begin * L.shard, rank_end * L.shard):
+        zb.zero_reduce_scatter_adamw_int8(L, qs, ss, qg.block, float(L.n_dp), rank_begin, rank_end,
+                                          s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
+
+
+def zero3_layer_reduce_scatter_int8(unit: Zero3Unit, qg: Int8Grads, A: torch.Tensor,
+                                    first: bool = True, stream=None):
+    """The stage-3 layer reduce-scatter from 8-bit unit gradients: each owner
+    receives the fp32 sum over ranks of its dequantized slice."""
+    L = unit.layout
+    qs, ss = qg.sources()
+    zb.zero_accumulate_int8(L, qs, ss, qg.block, A, 0, 0, L.padded_n, first, stream)
 
 
 # --------------------------------------------------------------------------
