@@ -329,7 +329,7 @@ class Zero2Workload(Workload):
             # then the fused update reads 1 B per source plus its scale
             self.bytes_per_elem = n_dp * 3 + sb + 26 + n_dp + sb
             self.dominant = "rs_adamw_int8"
-            self.kernel_label = "zgb::qgrad_vec_kernel<8,true> + zgb::quantize_vec_kernel<1,4> x 8 ranks"
+            self.kernel_label = "zgb::qgrad_vec_kernel<8,true> + zgb::quantize_group_kernel<8,4> x 8 ranks"
             self.device_bytes += self.qg.q.numel() + self.qg.scales.numel() * 4
 
     def ops(self, t):
@@ -507,7 +507,7 @@ class Zero3Workload(Workload):
                 zstep.zero3_quantize(u, q)
             # two 8-bit gathers (1 B read + 2 B written), RS, update, re-quantize (2 B read + 1 B written)
             self.bytes_per_elem = 3 + 3 + (2 * n_dp + 4) + 30 + 3
-            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_vec_kernel<1>, "
+            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_group_kernel<8,4>, "
                                  "acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>")
         else:
             self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
@@ -518,7 +518,7 @@ class Zero3Workload(Workload):
             sb = n_dp * 4 / QGRAD_BLOCK
             # + every rank quantizes its unit gradient; the RS reads 1 B per source (+ scales)
             self.bytes_per_elem = 3 + 3 + (n_dp * 3 + sb) + (n_dp + sb + 4) + 30 + 3
-            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_vec_kernel<1,4>, "
+            self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_group_kernel<8,4>, "
                                  "qgrad_vec_kernel<8,false>, rs_adamw_vec_kernel<1,1>")
         if self.prefetch:
             self.dominant = "zero3_step_prefetched"
