@@ -39,8 +39,19 @@
 #define ZGB_QGRAD_PREFETCH 0 // grid-stride passes ahead whose chunk a CTA prefetches into L2
                              // (0: off; measured: 1 or 2 ahead cost the update 2-3 %)
 #endif
+#ifndef ZGB_QGRAD_MINBLOCKS
+#define ZGB_QGRAD_MINBLOCKS 3 // update with one vector per thread: CTAs per SM the register
+                              // allocation must allow (3: 80 registers, no spills); the others keep
+                              // 2 (they spill below 128)
+#endif
+#ifndef ZGB_QACC_MINBLOCKS
+#define ZGB_QACC_MINBLOCKS 2  // the same for the accumulation
+#endif
 #ifndef ZGB_QGRAD_U
 #define ZGB_QGRAD_U 0        // vectors per thread and iteration; 0 = the measured choice
+#endif
+#ifndef ZGB_QACC_U
+#define ZGB_QACC_U 0         // the same for the accumulation
 #endif
 
 namespace zgb {
@@ -221,12 +232,15 @@ __device__ __forceinline__ void prefetch_chunk(const QGradParams& p, int64_t c0,
 // several.
 template <int R, bool kUpdate>
 __host__ __device__ constexpr int qgrad_vectors_per_iter() {
-    return R == 0 ? 1 : ZGB_QGRAD_U > 0 ? ZGB_QGRAD_U
-         : kUpdate ? (R <= 2 ? 2 : 1) : (R <= 4 ? 4 : R <= 8 ? 2 : 1);
+    return R == 0 ? 1
+         : kUpdate ? (ZGB_QGRAD_U > 0 ? ZGB_QGRAD_U : R <= 2 ? 2 : 1)
+                   : (ZGB_QACC_U > 0 ? ZGB_QACC_U : R <= 4 ? 4 : R <= 8 ? 2 : 1);
 }
 
 template <int R, bool kUpdate>
-__global__ void __launch_bounds__(kThreads, 2) qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
+__global__ void __launch_bounds__(kThreads, !kUpdate ? ZGB_QACC_MINBLOCKS
+                                           : qgrad_vectors_per_iter<R, kUpdate>() == 1 ? ZGB_QGRAD_MINBLOCKS : 2)
+qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if constexpr (R > 0) {
