@@ -330,3 +330,90 @@ def test_gpt2xl_int8_gradients(zlib, cuda_device):
         parity.assert_state([_take(x, idx_dev) for x in (master, m, v)], ref, what=f"t={t} ")
         assert np.array_equal(_bits_at(out, idx_dev), oracle.cast_bf16(w2))
     _full_properties(master, out, L.n)
+
+
+def _block_spans(S, n_dp, block, rng, n_random):
+    """Sampled quantization blocks of the n_dp slices, as flat (start, end):
+    random ones plus the first and last block of every slice."""
+    nb = -(-S // block)
+    picks = set(int(x) for x in rng.integers(0, n_dp * nb, size=n_random))
+    for o in range(n_dp):
+        picks.update((o * nb, o * nb + nb - 1))
+    blocks = sorted(picks)
+    spans = [(o * S + j * block, o * S + min((j + 1) * block, S)) for o, j in (divmod(b, nb) for b in blocks)]
+    return blocks, spans
+
+
+def test_llama7b_zero3_zeropp_units(zlib, cuda_device):
+    """ZeRO-3 with both ZeRO++ 8-bit paths on Llama-7B units at n_dp = 8 (the
+    embedding, the first and last blocks, the head), block 256: each owner
+    quantizes its bf16 shard and the 8-bit gather rebuilds the unit; every rank
+    quantizes its unit gradient, the owners accumulate the dequantized slices
+    in fp32 and update.  Checked on sampled whole blocks of every unit: codes,
+    scales, the gathered weights, the fp32 accumulation, the state and the bf16
+    shards."""
+    zb = zlib
+    dev = cuda_device
+    n_dp, block = 8, 256
+    all_units = inputs.llama7b_units()
+    picked = [0, 1, len(all_units) - 2, len(all_units) - 1]
+    layouts = [zb.zero_layout(all_units[k], n_dp) for k in picked]
+    cap = max(L.padded_n for L in layouts)
+    ring = zstep.GatherRing(cap, device=str(dev))
+    gbuf = torch.empty((n_dp, cap), dtype=torch.bfloat16, device=dev)
+    A = torch.empty(cap, device=dev)
+    rng = np.random.default_rng(6)
+    for i, L in enumerate(layouts):
+        P, S = L.padded_n, L.shard
+        w = inputs.master_weights(L.n, P, seed=SEED + 40 + i, device=dev)
+        shards = w.to(torch.bfloat16)
+        unit = zstep.Zero3Unit(L, shards.view(n_dp, S), w, torch.zeros(P, device=dev),
+                               torch.zeros(P, device=dev))
+        blocks, spans = _block_spans(S, n_dp, block, rng, 1024)
+        idx = np.concatenate([np.arange(a, c) for a, c in spans])
+        idx_dev = torch.from_numpy(idx).to(dev)
+        bidx_dev = torch.tensor(blocks, device=dev)
+        # 8-bit weights: quantize every shard, gather
+        qs = zstep.Int8Shards(L, block, dev)
+        zstep.zero3_quantize(unit, qs)
+        buf = zstep.zero3_gather_int8(unit, qs, ring, ("bwd", i))
+        sb = _bits_at(unit.shards.view(-1), idx_dev)
+        qw = qs.q.view(-1).index_select(0, idx_dev).cpu().numpy()
+        sw = qs.scales[:, :qs.nb].reshape(-1).index_select(0, bidx_dev).cpu().numpy()
+        gathered = _bits_at(buf, idx_dev)
+        pos = 0
+        for k, (a, c) in enumerate(spans):
+            q, s = oracle.quantize_int8(sb[pos:pos + c - a], block)
+            assert np.array_equal(qw[pos:pos + c - a], q) and sw[k] == s[0], (i, a)
+            assert np.array_equal(gathered[pos:pos + c - a], oracle.dequantize_int8(q, s, block)), (i, a)
+            pos += c - a
+        # 8-bit gradients: quantize every rank's unit gradient, accumulate, update
+        for r in range(n_dp):
+            inputs.grad_bf16_into(gbuf[r, :P], L.n, SEED, step=1, rank=r, micro=i)
+        qg = zstep.Int8Grads(L, n_dp, block, dev)
+        qg.quantize([gbuf[r, :P] for r in range(n_dp)])
+        ws = parity.f32(_take(w, idx_dev))
+        zstep.zero3_layer_reduce_scatter_int8(unit, qg, A[:P])
+        ring.release(("bwd", i))
+        zstep.zero3_update(unit, A[:P], _hp(zb, 1))
+        zb.zero_status_check()
+        deq = np.empty((n_dp, idx.size), np.float32)
+        for r in range(n_dp):
+            g_r = _bits_at(gbuf[r, :P], idx_dev)
+            q_got = qg.q[r].index_select(0, idx_dev).cpu().numpy()
+            s_got = qg.scales[r].index_select(0, bidx_dev).cpu().numpy()
+            pos = 0
+            for k, (a, c) in enumerate(spans):
+                q, s = oracle.quantize_int8(g_r[pos:pos + c - a], block)
+                assert np.array_equal(q_got[pos:pos + c - a], q) and s_got[k] == s[0], (i, r, a)
+                deq[r, pos:pos + c - a] = oracle.dequantize_grad_int8(q[None, :], s[None, :], 1, block)[0]
+                pos += c - a
+        A_ref = oracle.reduce_mean(deq, 1.0)
+        parity.assert_bit_exact_f32(_take(A[:P], idx_dev), A_ref)
+        z = np.zeros(idx.size, np.float32)
+        out_ref, *st = oracle.rs_adamw_reference(A_ref[None, :], n_dp, ws, z, z, HP, 1)
+        parity.assert_state([_take(x, idx_dev) for x in (unit.master, unit.m, unit.v)], st, what=f"unit {i} ")
+        assert np.array_equal(_bits_at(unit.shards.view(-1), idx_dev), out_ref)
+        _full_properties(unit.master, unit.shards.view(-1), L.n)
+        del unit, w, shards, qs, qg
+    assert ring.resident == 0
