@@ -645,12 +645,15 @@ def time_workload(wl, steps, warmup, dist, device, sampler=None):
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     per_kind = {}
+    step_ms = []
     for ops, evs in zip(plan, ev):
+        step_ms.append(evs[0][0].elapsed_time(evs[-1][1]))     # first launch's start to last's end
         for op, (a, b) in zip(ops, evs):
             d = per_kind.setdefault(op.kind, {"ms": 0.0, "bytes": 0, "launches": 0})
             d["ms"] += a.elapsed_time(b)
             d["bytes"] += op.bytes
             d["launches"] += 1
+    per_kind["_steps"] = step_ms
     return start.elapsed_time(end), per_kind, clocks, t + steps
 
 
@@ -757,6 +760,7 @@ def run_ours(args):
         warm = args.warmup if is_primary else max(1, min(args.warmup, 2))
         sampler = ClockSampler(local) if is_primary else None
         total_ms, per_kind, clocks, t_next = time_workload(wl, steps, warm, dist, device, sampler)
+        step_list = sorted(per_kind.pop("_steps"))
         ms_step = max_over_ranks(dist, total_ms / steps, device)
         kernels = _kernels_summary(per_kind, steps)
         dom = per_kind[wl.dominant]
@@ -768,6 +772,7 @@ def run_ours(args):
             name in ("gpt2xl", "llama7b-shard", "probe") else None
         res = {
             "value": replica_value(wl.elems, world, ms_step), "ms_per_step": ms_step, "steps": steps,
+            "step_ms_median": step_list[len(step_list) // 2], "step_ms_min": step_list[0],
             "hbm_gbs_step": bytes_step / (ms_step / 1e3) / 1e9,
             "bytes_per_param_step": wl.bytes_per_elem,
             "config": dict(wl.desc, l2="inputs %.1f GB > 129 MB L2, no flush" % (wl.device_bytes / 1e9)),
@@ -806,6 +811,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": p["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": p["ms_per_step"],
+            "step_ms_median": p["step_ms_median"], "step_ms_min": p["step_ms_min"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "storage": "bf16 gradients and weights, fp32 master/m/v",
             "data": "synthetic (seeded normal gradients and weights, model shapes only)",

@@ -41,6 +41,7 @@ def _quantized(zb, L, g_cpu, block):
     (4097, 5, 1, 1000, 256),                # S = 820: slices off the 8-element grid
     (7, 2, 1, 500_000_000, 256),            # fewer elements than one vector
     (50_000, 6, 8, 500_000_000, 1024),      # 6 sources: the runtime-count kernel
+    (64_005, 64, 8, 500_000_000, 256),      # the most sources a call takes
 ])
 def test_step_matches_oracle(zlib, cuda_device, N, n_dp, align, bucket, block):
     """Two steps of quantize + fused update against the oracle: codes, scales,

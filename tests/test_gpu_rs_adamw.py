@@ -229,3 +229,38 @@ def test_several_waves_with_partial_groups(zlib, cuda_device, n_src, dtype):
     ref_out, w, m, v = oracle.rs_adamw_reference(src_np, n_src, w0, m0, v0, HP_ORACLE, 4)
     parity.assert_state(st, [w, m, v])
     assert np.array_equal(parity.bits(out), ref_out)
+
+
+@pytest.mark.parametrize("n_src,dtype", [(6, "bf16"), (32, "bf16"), (64, "bf16"), (3, "f32"),
+                                         (64, "f32")])
+def test_source_counts_up_to_the_limit(zlib, cuda_device, n_src, dtype):
+    """Every source count the kernels take, up to ZERO_MAX_SRC = 64: the
+    compile-time counts and the runtime-count kernel, bf16 and fp32 sources,
+    a ragged tail; two steps against the oracle, bit for bit."""
+    zb = zlib
+    assert zb.ZERO_MAX_SRC == 64
+    N = 1000 * n_src + 7
+    L = zb.zero_layout([N], n_src)
+    P = L.padded_n
+    w0 = inputs.master_weights(N, P, seed=n_src)
+    st = [w0.cuda(), torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")]
+    out = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    ref = [parity.f32(w0), np.zeros(P, np.float32), np.zeros(P, np.float32)]
+    for t in (1, 2):
+        g = inputs.grads_bf16(n_src, N, P, seed=n_src, step=t)
+        if dtype == "bf16":
+            srcs, dt, rows = [g[r].cuda() for r in range(n_src)], zb.ZERO_BF16, parity.bits(g)
+        else:
+            gf = (g.float() * 3.0).contiguous()            # fp32 sources not on the bf16 grid
+            srcs, dt, rows = [gf[r].cuda() for r in range(n_src)], zb.ZERO_F32, gf.numpy()
+        zb.zero_reduce_scatter_adamw(L, srcs, dt, 0, float(n_src), 0, n_src, 0, P, *st, out,
+                                     zb.ZERO_OUT_FULL, _hp(zb, t))
+        torch.cuda.synchronize()
+        out_ref, *ref = oracle.rs_adamw_reference(rows, n_src, *ref, HP_ORACLE, t)
+        parity.assert_state(st, ref, what=f"t={t} ")
+        assert np.array_equal(parity.bits(out), out_ref)
+    too_many = [srcs[0]] * 65
+    with pytest.raises(zb.ZeroError) as e:
+        zb.zero_reduce_scatter_adamw(L, too_many, dt, 0, 65.0, 0, n_src, 0, P, *st, out,
+                                     zb.ZERO_OUT_FULL, _hp(zb, 3))
+    assert e.value.code == -3
