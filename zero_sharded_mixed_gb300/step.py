@@ -44,6 +44,18 @@ def zero12_step(L, grads, master, m, v, out, hp, rank_begin=0, rank_end=None, st
                                      s, e, master, m, v, out, zb.ZERO_OUT_FULL, hp, stream)
 
 
+def split_ranges(ranges, chunk_elems: int | None):
+    """The ranges cut into pieces of at most chunk_elems elements (a multiple
+    of 8, so every piece but a range's last keeps the 8-element grid); None
+    keeps them whole.  The pieces change no number, only the granularity at
+    which host copies and updates overlap."""
+    if not chunk_elems:
+        return list(ranges)
+    if chunk_elems % 8:
+        raise ValueError("chunk_elems must be a multiple of 8")
+    return [(a, min(a + chunk_elems, e)) for s, e in ranges for a in range(s, e, chunk_elems)]
+
+
 # --------------------------------------------------------------------------
 # gradient accumulation ("ZeRO and FSDP", paragraph on accumulation)
 # --------------------------------------------------------------------------
@@ -221,9 +233,9 @@ class HostPipeline:
     one bucket overlap the update of the previous one ("ZeRO and FSDP", stage
     2: each bucket is reduce-scattered as soon as it is ready)."""
 
-    def __init__(self, L, device=None):
+    def __init__(self, L, device=None, chunk_elems: int | None = None):
         self.L = L
-        self.ranges = bucket_ranges(L)
+        self.ranges = split_ranges(bucket_ranges(L), chunk_elems)
         self.h2d = torch.cuda.Stream(device=device)
         self.d2h = torch.cuda.Stream(device=device)
         self.ev_in = [torch.cuda.Event() for _ in self.ranges]
