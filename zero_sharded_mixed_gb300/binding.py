@@ -128,8 +128,8 @@ def load():
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
-                     "zero_selftest_bounded_wait",
-                     "zero_gather_layer", "zero_accumulate",
+                     "zero_selftest_bounded_wait", "zero_reduce_scatter_adamw_int8",
+                     "zero_accumulate_int8", "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib

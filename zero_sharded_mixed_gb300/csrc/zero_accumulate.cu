@@ -231,9 +231,7 @@ __global__ void __launch_bounds__(kThreads) acc_scalar_kernel(const __grid_const
 
 template <int NDP, bool kBf16, bool kLocal>
 int launch_acc_vec(const AccParams& p, cudaStream_t s) {
-    static int occupancy = 0;
-    if (occupancy == 0)
-        occupancy = ctas_per_sm((const void*)acc_vec_kernel<NDP, kBf16, kLocal>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)acc_vec_kernel<NDP, kBf16, kLocal>, kThreads, 0);
     const int64_t per_cta = (int64_t)acc_vectors_per_iter<NDP, kBf16, kLocal>() * kThreads;
     const unsigned grid = grid_for(p.n >> 3, per_cta, (int64_t)sm_count() * occupancy * ZGB_ACC_WAVES);
     acc_vec_kernel<NDP, kBf16, kLocal><<<grid, kThreads, 0, s>>>(p);
@@ -242,9 +240,7 @@ int launch_acc_vec(const AccParams& p, cudaStream_t s) {
 
 template <bool kBf16, bool kLocal>
 int launch_acc_scalar(const AccParams& p, cudaStream_t s) {
-    static int occupancy = 0;
-    if (occupancy == 0)
-        occupancy = ctas_per_sm((const void*)acc_scalar_kernel<kBf16, kLocal>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)acc_scalar_kernel<kBf16, kLocal>, kThreads, 0);
     const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
     acc_scalar_kernel<kBf16, kLocal><<<grid, kThreads, 0, s>>>(p);
     return launch_status();

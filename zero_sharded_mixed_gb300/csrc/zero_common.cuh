@@ -98,7 +98,8 @@ inline int check_aligned(const void* p, int bytes) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // SM count of the current device (cached per device).
 int sm_count();
-// CTAs of `threads` each that fit on one SM for `kernel` (cached by the caller).
+// CTAs of `threads` each that fit on one SM for `kernel` with `smem` bytes of
+// dynamic shared memory on the current device; cached, safe from any thread.
 int ctas_per_sm(const void* kernel, int threads, size_t smem);
 // ZERO_ECUDA if the last launch on this thread failed (remembered for
 // zero_last_cuda_error).

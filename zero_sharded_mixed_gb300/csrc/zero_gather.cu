@@ -73,9 +73,8 @@ extern "C" int zero_gather_layer(const zero_layout_t* unit, const uint16_t* cons
         if (check_device_ptr(shards[o])) return ZERO_EINVAL;
     if (check_device_ptr(full_out)) return ZERO_EINVAL;
 
-    static int occ_vec = 0, occ_scalar = 0;
-    if (occ_vec == 0) occ_vec = ctas_per_sm((const void*)gather_vec_kernel, kThreads, 0);
-    if (occ_scalar == 0) occ_scalar = ctas_per_sm((const void*)gather_scalar_kernel, kThreads, 0);
+    const int occ_vec = ctas_per_sm((const void*)gather_vec_kernel, kThreads, 0);
+    const int occ_scalar = ctas_per_sm((const void*)gather_scalar_kernel, kThreads, 0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // shards go in groups of at most ZERO_MAX_SRC per launch (kernel parameter space)
     for (int o0 = 0; o0 < n_dp; o0 += ZERO_MAX_SRC) {

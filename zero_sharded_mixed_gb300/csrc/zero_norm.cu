@@ -154,8 +154,7 @@ int64_t norm_partials_capacity() { return (int64_t)sm_count() * kMaxCtasPerSm; }
 
 template <bool kBf16, int R>
 int launch_norm(const NormParams& p, bool vec, double* norm_sq, int accumulate, cudaStream_t s) {
-    static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)norm_partial_kernel<kBf16, R>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)norm_partial_kernel<kBf16, R>, kThreads, 0);
     const int64_t resident = (int64_t)sm_count() * (occupancy < kMaxCtasPerSm ? occupancy : kMaxCtasPerSm);
     const unsigned grid = grid_for(vec ? (p.n >> 3) : p.n, kThreads, resident);
     norm_partial_kernel<kBf16, R><<<grid, kThreads, 0, s>>>(p);

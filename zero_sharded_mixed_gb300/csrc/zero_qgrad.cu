@@ -269,8 +269,7 @@ __global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_con
 
 template <int R, bool kUpdate>
 int launch_qgrad_vec(const QGradParams& p, cudaStream_t s) {
-    static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate>, kThreads, 0);
     const int64_t per_cta = (int64_t)qgrad_vectors_per_iter<R, kUpdate>() * kThreads;
     const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
     const unsigned grid = grid_for(p.n >> 3, per_cta, (int64_t)sm_count() * occupancy * waves);
@@ -281,8 +280,7 @@ int launch_qgrad_vec(const QGradParams& p, cudaStream_t s) {
 template <bool kUpdate>
 int launch_qgrad(const QGradParams& p, bool vec, cudaStream_t s) {
     if (!vec) {
-        static int occupancy = 0;
-        if (occupancy == 0) occupancy = ctas_per_sm((const void*)qgrad_scalar_kernel<kUpdate>, kThreads, 0);
+        const int occupancy = ctas_per_sm((const void*)qgrad_scalar_kernel<kUpdate>, kThreads, 0);
         const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
         qgrad_scalar_kernel<kUpdate><<<grid, kThreads, 0, s>>>(p);
         return launch_status();

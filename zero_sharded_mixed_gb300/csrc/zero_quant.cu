@@ -234,20 +234,18 @@ extern "C" int zero_quantize_int8(const zero_layout_t* unit, const uint16_t* sha
                      (reinterpret_cast<uintptr_t>(q) & 7u) == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!vec) {
-        static int occ = 0;
-        if (occ == 0) occ = ctas_per_sm((const void*)quantize_scalar_kernel, kThreads, 0);
+        const int occ = ctas_per_sm((const void*)quantize_scalar_kernel, kThreads, 0);
         quantize_scalar_kernel<<<grid_for(p.total_blocks, kThreads, (int64_t)sm_count() * occ), kThreads, 0, s>>>(p);
         return launch_status();
     }
     // 8 lanes per 256-element block (four blocks per warp), 16 per 512, 32 per
     // 1024 and 2048; four (2048: eight) vectors per lane
-    static int occ[4] = {0, 0, 0, 0};
     const void* fns[4] = {(const void*)quantize_group_kernel<8, 4>, (const void*)quantize_group_kernel<16, 4>,
                           (const void*)quantize_group_kernel<32, 4>, (const void*)quantize_group_kernel<32, 8>};
     const int which = block == 256 ? 0 : block == 512 ? 1 : block == 1024 ? 2 : 3;
-    if (occ[which] == 0) occ[which] = ctas_per_sm(fns[which], kThreads, 0);
+    const int occ = ctas_per_sm(fns[which], kThreads, 0);
     const int64_t per_cta = (int64_t)kWarps * (which == 0 ? 4 : which == 1 ? 2 : 1);
-    const int64_t resident = (int64_t)sm_count() * occ[which] * ZGB_QUANT_WAVES;
+    const int64_t resident = (int64_t)sm_count() * occ * ZGB_QUANT_WAVES;
     for (int64_t o0 = 0; o0 < unit->n_dp; o0 += 65535) {
         const int cnt = (int)(unit->n_dp - o0 < 65535 ? unit->n_dp - o0 : 65535);
         const int64_t per_shard = resident / cnt > 0 ? resident / cnt : 1;
@@ -282,9 +280,8 @@ extern "C" int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* c
     for (int o = 0; o < n_dp; ++o)
         if (check_device_ptr(q_shards[o]) || check_device_ptr(scale_shards[o])) return ZERO_EINVAL;
     if (check_device_ptr(full_out)) return ZERO_EINVAL;
-    static int occ_vec = 0, occ_scalar = 0;
-    if (occ_vec == 0) occ_vec = ctas_per_sm((const void*)dequant_gather_vec_kernel, kThreads, 0);
-    if (occ_scalar == 0) occ_scalar = ctas_per_sm((const void*)dequant_gather_scalar_kernel, kThreads, 0);
+    const int occ_vec = ctas_per_sm((const void*)dequant_gather_vec_kernel, kThreads, 0);
+    const int occ_scalar = ctas_per_sm((const void*)dequant_gather_scalar_kernel, kThreads, 0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int o0 = 0; o0 < n_dp; o0 += ZERO_MAX_SRC) {
         const int cnt = n_dp - o0 < ZERO_MAX_SRC ? n_dp - o0 : ZERO_MAX_SRC;

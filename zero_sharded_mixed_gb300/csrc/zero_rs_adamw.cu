@@ -287,8 +287,7 @@ __global__ void __launch_bounds__(kThreads) rs_adamw_scalar_kernel(const __grid_
 
 template <int KIND, int R>
 int launch_vec(const UpdateParams& p, cudaStream_t stream) {
-    static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R>, kThreads, 0);
     const int64_t resident = (int64_t)sm_count() * occupancy * rs_waves<KIND, R>();
     const int64_t per_cta = (R > 0 ? vectors_per_iter<KIND, R>() : 1) * (int64_t)kThreads;
     const unsigned grid = grid_for(p.n >> 3, per_cta, resident);
@@ -298,8 +297,7 @@ int launch_vec(const UpdateParams& p, cudaStream_t stream) {
 
 template <int KIND>
 int launch_scalar(const UpdateParams& p, cudaStream_t stream) {
-    static int occupancy = 0;
-    if (occupancy == 0) occupancy = ctas_per_sm((const void*)rs_adamw_scalar_kernel<KIND>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)rs_adamw_scalar_kernel<KIND>, kThreads, 0);
     const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
     rs_adamw_scalar_kernel<KIND><<<grid, kThreads, 0, stream>>>(p);
     return launch_status();

@@ -210,18 +210,18 @@ rs_adamw_tma_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
 template <int NDP>
 int launch_tma(const UpdateParams& p, cudaStream_t stream) {
     using Tile = TmaTile<NDP>;
-    static int occupancy = 0;
-    if (occupancy == 0) {
-        const cudaError_t e = cudaFuncSetAttribute((const void*)rs_adamw_tma_kernel<NDP>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)Tile::kSmemBytes);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            note_cuda_error(e);
-            return ZERO_ECUDA;
-        }
-        occupancy = ctas_per_sm((const void*)rs_adamw_tma_kernel<NDP>, kTmaThreads, Tile::kSmemBytes);
+    // the opt-in above the default 48 KB of dynamic shared memory, per device:
+    // set before every launch (cheap next to the launch) so that any thread and
+    // any current device is covered
+    const cudaError_t e = cudaFuncSetAttribute((const void*)rs_adamw_tma_kernel<NDP>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)Tile::kSmemBytes);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return ZERO_ECUDA;
     }
+    const int occupancy = ctas_per_sm((const void*)rs_adamw_tma_kernel<NDP>, kTmaThreads, Tile::kSmemBytes);
     const int64_t n_tiles = ((p.n >> 3) * 8 + kTile - 1) / kTile;
     const int64_t resident = (int64_t)sm_count() * occupancy;
     const unsigned grid = (unsigned)(n_tiles < 1 ? 1 : (n_tiles < resident ? n_tiles : resident));

@@ -1,6 +1,9 @@
 // Host-side runtime support shared by the kernels: pointer checks, device
 // properties, launch status, and zero_status_check.
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "zero_update.cuh"
 
@@ -53,12 +56,26 @@ int sm_count() {
 }
 
 int ctas_per_sm(const void* kernel, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, size_t, int>, int> cache;
+    const auto key = std::make_tuple(kernel, threads, smem, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
-        n < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = 1;
     }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
     return n;
 }
 

@@ -105,9 +105,10 @@ struct UpdateParams {
 
 // ----------------------------------------------------------------- host
 
-// The TMA-staged variant for bf16 sources (zero_rs_adamw_tma.cu): returns
-// ZERO_EINVAL when it does not apply (source count or alignment), so that the
-// caller falls back to the register-staged kernel.
+// The TMA-staged variant for bf16 sources (zero_rs_adamw_tma.cu): a status
+// code, or 1 when it does not apply (a source count other than 1, 2, 4 or 8),
+// so that the caller falls back to the register-staged kernel.  The caller
+// only dispatches aligned ranges to it.
 int launch_rs_adamw_tma(const UpdateParams& p, cudaStream_t stream);
 // Reads and clears the device status word of the bounded waits (ZERO_OK or
 // ZERO_ETIMEOUT); synchronizes the device.
