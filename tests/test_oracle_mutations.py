@@ -10,6 +10,8 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
+
 import pytest
 
 import oracle
@@ -96,6 +98,8 @@ def _pins():
          lambda: pg.test_exact_gradients_quantize_to_their_codes_and_step_like_bf16(4, 1000, 256)),
         ("8-bit gradient error bound", lambda: pg.test_error_within_half_a_step(4, 5000, 256)),
         ("8-bit gradient slices", pg.test_blocks_restart_at_every_slice),
+        ("8-bit gradient accumulation", pg.test_exact_gradients_accumulate_like_bf16),
+        ("8-bit first micro-batch overwrites", pg.test_first_micro_batch_overwrites_the_buffer),
     ]
 
 
@@ -121,3 +125,67 @@ def test_a_planted_mistake_fails_a_pin(what, old, new, tmp_path, monkeypatch):
 def test_the_real_oracle_passes_every_pin():
     for name, pin in _pins():
         pin()
+
+
+# Mistakes in the oracle's Python composition of the C routines (the 8-bit
+# gradient functions slice, offset and combine them).  Each mutant replaces one
+# function of the oracle module.
+
+def _q_whole_rows(g_rows, n_dp, block=256):
+    """Blocks that do not restart at slice boundaries: each row quantized whole."""
+    g = oracle._u16(g_rows)
+    n_src, P = g.shape
+    S = P // n_dp
+    nb = -(-S // block)
+    q = np.empty((n_src, P), dtype=np.int8)
+    scales = np.zeros((n_src, n_dp * nb), dtype=np.float32)
+    for r in range(n_src):
+        q[r], s = oracle.quantize_int8(g[r], block)
+        scales[r, :s.size] = s[:n_dp * nb]
+    return q, scales
+
+
+def _deq_first_slice_scales(q_rows, scale_rows, n_dp, block=256):
+    """Every slice dequantized with slice 0's scales."""
+    q = np.ascontiguousarray(q_rows, dtype=np.int8)
+    sc = oracle._f32(scale_rows)
+    n_src, P = q.shape
+    S = P // n_dp
+    nb = -(-S // block)
+    out = np.empty((n_src, P), dtype=np.float32)
+    for r in range(n_src):
+        for o in range(n_dp):
+            k = np.arange(S)
+            out[r, o * S:(o + 1) * S] = q[r, o * S:(o + 1) * S].astype(np.float32) * sc[r, k // block]
+    return out
+
+
+def _acc_int8_ignores_first(acc, q_rows, scale_rows, n_dp, block, first):
+    x = oracle.reduce_mean(oracle.dequantize_grad_int8(q_rows, scale_rows, n_dp, block), 1.0)
+    return x if acc is None else (oracle._f32(acc) + x).astype(np.float32)
+
+
+def _qgrad_ref_wrong_divisor(q_rows, scale_rows, n_dp, block, divisor, w, m, v, hp, t):
+    g = oracle.reduce_mean(oracle.dequantize_grad_int8(q_rows, scale_rows, n_dp, block), divisor * 2)
+    w2, m2, v2 = oracle.adamw(w, m, v, g, hp, t)
+    return oracle.cast_bf16(w2), w2, m2, v2
+
+
+PY_MUTATIONS = [
+    ("8-bit gradient blocks do not restart at slices", "quantize_grad_int8", _q_whole_rows),
+    ("8-bit gradient slices use slice 0's scales", "dequantize_grad_int8", _deq_first_slice_scales),
+    ("8-bit accumulation ignores the first flag", "accumulate_reduce_int8", _acc_int8_ignores_first),
+    ("8-bit step divides twice", "qgrad_rs_adamw_reference", _qgrad_ref_wrong_divisor),
+]
+
+
+@pytest.mark.parametrize("what,name,fn", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_a_planted_composition_mistake_fails_a_pin(what, name, fn, monkeypatch):
+    monkeypatch.setattr(oracle, name, fn)
+    caught = []
+    for pin_name, pin in _pins():
+        try:
+            pin()
+        except Exception:
+            caught.append(pin_name)
+    assert caught, f"no pin noticed: {what}"

@@ -128,3 +128,17 @@ def test_exact_gradients_accumulate_like_bf16():
     a = oracle.accumulate_reduce_int8(a, q2, s2, n_dp, block, False)
     ref = oracle.accumulate_reduce(oracle.accumulate_reduce(None, g1, True), g2, False)
     assert np.array_equal(a, ref)
+
+
+def test_first_micro_batch_overwrites_the_buffer():
+    """With first set, a stale buffer is ignored: the result is the sum of the
+    dequantized gradients alone, as for a fresh buffer and as the bf16
+    accumulation (each window starts a new sum: "ZeRO and FSDP", the paragraph
+    on gradient accumulation)."""
+    n_dp, S, block = 3, 512, 256
+    g, _, _ = _exact_grads(n_dp, n_dp, S, block, seed=21)
+    q, s = oracle.quantize_grad_int8(g, n_dp, block)
+    stale = np.random.default_rng(0).standard_normal(n_dp * S).astype(np.float32)
+    fresh = oracle.accumulate_reduce_int8(None, q, s, n_dp, block, True)
+    assert np.array_equal(oracle.accumulate_reduce_int8(stale, q, s, n_dp, block, True), fresh)
+    assert np.array_equal(fresh, oracle.accumulate_reduce(stale, g, True))
