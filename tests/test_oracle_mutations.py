@@ -117,7 +117,7 @@ def test_a_planted_mistake_fails_a_pin(what, old, new, tmp_path, monkeypatch):
     for name, pin in _pins():
         try:
             pin()
-        except Exception:          # an assertion, or a ValueError from a layout check
+        except (Exception, pytest.fail.Exception):   # an assertion, a failed pytest.raises, a ValueError
             caught.append(name)
     assert caught, f"no pin noticed: {what}"
 
@@ -186,6 +186,52 @@ def test_a_planted_composition_mistake_fails_a_pin(what, name, fn, monkeypatch):
     for pin_name, pin in _pins():
         try:
             pin()
-        except Exception:
+        except (Exception, pytest.fail.Exception):
             caught.append(pin_name)
+    assert caught, f"no pin noticed: {what}"
+
+
+# Mistakes in the memory and communication formulas (oracle/formulas.py):
+# each mutant is loaded as a module in place of the real one, and the pins of
+# tests/test_oracle_formulas.py (the pages' printed numbers, the ring factor,
+# the invalid-stage rule) run against it.
+FORMULA_SRC = os.path.join(os.path.dirname(oracle.__file__), "formulas.py")
+FORMULA_MUTATIONS = [
+    ("stage 2 keeps the full gradients", "grads = grads / n_dp ", "grads = grads * 1 "),
+    ("stage 1 shards the optimizer over n_dp - 1", "optimizer = optimizer / n_dp ",
+     "optimizer = optimizer / (n_dp - 1) "),
+    ("stage 3 keeps the full weights", "weights = weights / n_dp ", "weights = weights * 1 "),
+    ("16 bytes per parameter become 18", "weights = 2 * N", "weights = 4 * N"),
+    ("ring factor dropped", "one_pass = (n_dp - 1) / n_dp * N", "one_pass = N"),
+    ("stage 3 gathers the weights once", "return one_pass * grad_bytes + 2 * one_pass * param_bytes",
+     "return one_pass * grad_bytes + one_pass * param_bytes"),
+    ("stage 0 reduce-scatters only", "return 2 * one_pass * grad_bytes", "return one_pass * grad_bytes"),
+    ("stage 4 accepted", "if stage not in (0, 1, 2, 3):\n        raise ValueError(f\"ZeRO stage must be 0, 1, 2 or 3, got {stage!r}\")\n    weights",
+     "if stage not in (0, 1, 2, 3, 4):\n        raise ValueError(f\"ZeRO stage must be 0, 1, 2 or 3, got {stage!r}\")\n    weights"),
+]
+
+
+@pytest.mark.parametrize("what,old,new", FORMULA_MUTATIONS, ids=[m[0] for m in FORMULA_MUTATIONS])
+def test_a_planted_formula_mistake_fails_a_pin(what, old, new, monkeypatch):
+    import importlib.util
+    import types
+
+    from tests import test_oracle_formulas as pf
+    src = open(FORMULA_SRC).read()
+    assert src.count(old) == 1, f"the mutation target for '{what}' must occur exactly once"
+    mutant = types.ModuleType("formulas_mutant")
+    exec(compile(src.replace(old, new), "formulas_mutant", "exec"), mutant.__dict__)
+    monkeypatch.setattr(pf, "formulas", mutant)
+    pins = [lambda c=c: pf.test_memory_matches_printed_numbers(c) for c in pf._golden()["memory"]]
+    pins += [pf.test_free_memory_after_states, pf.test_sixteen_bytes_per_parameter,
+             pf.test_per_gpu_formulas_are_the_table, pf.test_stage_limits,
+             pf.test_comm_stage12_equals_dp_and_stage3_is_one_and_a_half, pf.test_comm_exact_ring_factor,
+             pf.test_comm_fp32_gradients_double_the_gradient_term, pf.test_comm_llama3_70b_printed]
+    pins += [lambda s=s: pf.test_invalid_stage_raises(s) for s in (-1, 4, 5, "1", None, 1.5)]
+    caught = 0
+    for pin in pins:
+        try:
+            pin()
+        except (Exception, pytest.fail.Exception):
+            caught += 1
     assert caught, f"no pin noticed: {what}"
