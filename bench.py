@@ -657,6 +657,33 @@ def time_workload(wl, steps, warmup, dist, device, sampler=None):
     return start.elapsed_time(end), per_kind, clocks, t + steps
 
 
+def e2e_host_bytes(wl):
+    """Pinned host bytes the e2e leg holds: every rank's gradients and the result."""
+    return wl.grads.numel() * wl.grads.element_size() + wl.out.numel() * wl.out.element_size()
+
+
+def host_fits(nbytes) -> bool:
+    """Whether nbytes fit in 85 % of the host memory available now."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return nbytes <= 0.85 * int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return True
+
+
+def all_ranks_agree(dist, flag: bool, device) -> bool:
+    """True when the flag is true on every rank."""
+    if dist is None:
+        return flag
+    import torch
+    t = torch.tensor([1 if flag else 0], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
 def time_e2e(wl, steps, warmup, t0, dist):
     """The same step through the public API with host buffers: every step copies
     the n_dp gradient buffers from pinned host memory to the device and reads the
@@ -787,12 +814,20 @@ def run_ours(args):
         if is_primary:
             res["clocks"] = clocks
             if not args.no_e2e and isinstance(wl, Zero2Workload):
-                e2e_steps = max(1, min(args.steps, 10))
-                e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
-                e_ms = max_over_ranks(dist, e_ms, device)
-                res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
-                              "ms_per_step": e_ms, "steps": e2e_steps,
-                              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                need = e2e_host_bytes(wl)
+                fits = host_fits(need * int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
+                if all_ranks_agree(dist, fits, device):
+                    e2e_steps = max(1, min(args.steps, 10))
+                    e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
+                    e_ms = max_over_ranks(dist, e_ms, device)
+                    res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
+                                  "ms_per_step": e_ms, "steps": e2e_steps,
+                                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                else:
+                    res["e2e"] = {"value": None, "unit": UNIT,
+                                  "unavailable": "host memory: %s local ranks x %.1f GB of pinned "
+                                  "step inputs and results exceed 85%% of the available host memory"
+                                  % (os.environ.get("LOCAL_WORLD_SIZE", "1"), need / 1e9)}
             if not args.no_cpu_baseline and world == 1 and rank == 0 and isinstance(wl, Zero2Workload):
                 sample = cpu_sample(wl, CPU_SAMPLE)
                 rate, secs, done = time_oracle(sample, CPU_BASELINE_SECONDS, wl.n_src)

@@ -24,6 +24,9 @@ def _worker(rank, world, port, out):
         local_ms = 10.0 + 5.0 * rank          # rank 1 is the slow one
         ms = bench.max_over_ranks(dist, local_ms, torch.device("cpu"))
         out[rank] = (ms, bench.replica_value(1_000_000, world, ms))
+        # the e2e leg runs only when every rank's host buffers fit
+        out[f"agree{rank}"] = (bench.all_ranks_agree(dist, True, torch.device("cpu")),
+                               bench.all_ranks_agree(dist, rank == 0, torch.device("cpu")))
         bench.barrier(dist)
     finally:
         dist.destroy_process_group()
@@ -42,3 +45,11 @@ def test_two_gloo_replicas():
         assert p.exitcode == 0
     # both ranks see the slowest rank's time; the value counts both replicas
     assert out[0] == out[1] == (15.0, pytest.approx(2 * 1_000_000 / 0.015))
+    # one rank without room turns the e2e leg off on all of them
+    assert out["agree0"] == out["agree1"] == (True, False)
+
+
+def test_host_fits_reads_available_memory():
+    import bench
+    assert bench.host_fits(0)
+    assert not bench.host_fits(1 << 62)
