@@ -1,9 +1,9 @@
 """Parity of the TMA-staged build of the fused update against the oracle.
 
 The library built with ZGB_RS_TMA=1 sends bf16-source updates with 1, 2, 4 or
-8 sources through rs_adamw_tma_kernel (1-D bulk copies into a 3-stage
-shared-memory ring, mbarrier completion) instead of the register-staged
-kernel.  It is an opt-in build, so this test compiles it into a temporary
+8 sources through the bulk-copy kernels instead of the register-staged one:
+the warp-specialized pipeline (rs_adamw_ws_kernel, the default) and, with
+ZGB_TMA_WS=0, the CTA-synchronous ring (rs_adamw_tma_kernel).  It is an opt-in build, so this test compiles it into a temporary
 library and checks it in a child process of its own (one library per
 process), bit for bit against the oracle: several steps, several buckets,
 ranges that span many 1024-element tiles with a ragged last tile, a range
@@ -20,9 +20,11 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_tma_build_matches_the_oracle(tmp_path, cuda_device):
+@pytest.mark.parametrize("defines", [["ZGB_RS_TMA=1"], ["ZGB_RS_TMA=1", "ZGB_TMA_WS=0"]],
+                         ids=["warp-specialized", "cta-synchronous"])
+def test_tma_build_matches_the_oracle(tmp_path, cuda_device, defines):
     from zero_sharded_mixed_gb300 import build as zbuild
-    lib = zbuild.build(defines=["ZGB_RS_TMA=1"], out=str(tmp_path / "libzero_gb300_tma.so"))
+    lib = zbuild.build(defines=defines, out=str(tmp_path / "libzero_gb300_tma.so"))
     r = subprocess.run([sys.executable, os.path.abspath(__file__), lib], cwd=ROOT,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout + r.stderr
