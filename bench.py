@@ -66,7 +66,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
                                            "probe", "accum-zero1", "accum-zero2", "zero3",
-                                           "zero3-int8", "zero3-prefetch", "zero3-zeropp"],
+                                           "zero3-int8", "zero3-prefetch", "zero3-zeropp",
+                                           "zero3-fused"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -480,6 +481,7 @@ class Zero3Workload(Workload):
         self.name = name
         self.zstep = zstep
         self.zeropp = name == "zero3-zeropp"
+        self.fused = name == "zero3-fused"
         self.int8 = name in ("zero3-int8", "zero3-zeropp")
         self.prefetch = name == "zero3-prefetch"
         n_dp = 8
@@ -513,6 +515,11 @@ class Zero3Workload(Workload):
             self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
             self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>"
         self.dominant = "rs_adamw"
+        if self.fused:
+            # two gathers, then the reduce-scatter and the update in one pass (42 B)
+            self.bytes_per_elem = 4 + 4 + 26 + 2 * n_dp
+            self.dominant = "rs_adamw_fused"
+            self.kernel_label = "zgb::gather_vec_kernel, rs_adamw_vec_kernel<0,8> (own-shard output)"
         if self.zeropp:
             self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp), n_dp, QGRAD_BLOCK, device)
             sb = n_dp * 4 / QGRAD_BLOCK
@@ -526,6 +533,7 @@ class Zero3Workload(Workload):
             self.pf = zstep.Zero3Prefetcher(self.units, self.ring, device=device)
         self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else "")
                      + ("_int8_grads" if self.zeropp else "")
+                     + ("_fused_rs_update" if self.fused else "")
                      + ("_prefetch" if self.prefetch else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
@@ -586,6 +594,12 @@ class Zero3Workload(Workload):
                 else ("gather", P * 4)
             out.append(Op(gkind, gbytes, fwd))
             out.append(Op(gkind, gbytes, bwd_gather))
+            if self.fused:
+                def rs_upd(u=u, i=i, grads=grads):
+                    zs.zero3_reduce_scatter_update(u, grads, hp)
+                    self.ring.release(("bwd", i))
+                out.append(Op("rs_adamw_fused", P * (26 + 2 * u.layout.n_dp), rs_upd))
+                continue
             if self.zeropp:
                 n = u.layout.n_dp
                 sbytes = n * (-(-u.layout.shard // QGRAD_BLOCK)) * 4
@@ -608,7 +622,7 @@ def make_workload(name, device, elems=0):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
-    if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp"):
+    if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -773,7 +787,8 @@ def run_ours(args):
     peak, peak_kind = _peak()
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
-                          "accum-zero2", "zero3", "zero3-prefetch", "zero3-int8", "zero3-zeropp")
+                          "accum-zero2", "zero3", "zero3-fused", "zero3-prefetch", "zero3-int8",
+                          "zero3-zeropp")
               if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}

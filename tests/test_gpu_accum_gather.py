@@ -227,3 +227,32 @@ def test_gather_several_waves(zlib, cuda_device):
     zb.zero_gather_layer(L, [inputs.from_bf16_bits(sh[o], "cuda") for o in range(n_dp)], full)
     torch.cuda.synchronize()
     assert np.array_equal(parity.bits(full), sh.reshape(-1))
+
+
+def test_zero3_fused_reduce_scatter_update_equals_the_pair(zlib, cuda_device):
+    """One micro-batch, no clipping: the fused per-unit reduce-scatter + update
+    equals the layer reduce-scatter into fp32 followed by the update, bit for
+    bit, on ragged units at n_dp = 7, over two steps."""
+    zb = zlib
+    n_dp = 7
+    for i, numels in enumerate([[1], [4097], [33_031], [1000, 24, 3, 5000]]):
+        L = zb.zero_layout(numels, n_dp)
+        P = L.padded_n
+        w = inputs.master_weights(L.n, P, seed=500 + i).cuda()
+        units = []
+        for _ in range(2):
+            shards = w.to(torch.bfloat16)
+            units.append(zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w.clone(),
+                                         torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")))
+        A = torch.empty(P, device="cuda")
+        for t in (1, 2):
+            g = inputs.grads_bf16(n_dp, L.n, P, seed=600 + i, step=t)
+            gd = [g[r].cuda() for r in range(n_dp)]
+            zstep.zero3_layer_reduce_scatter(units[0], gd, A)
+            zstep.zero3_update(units[0], A, _hp(zb, t))
+            zstep.zero3_reduce_scatter_update(units[1], gd, _hp(zb, t))
+            torch.cuda.synchronize()
+            for a, b in ((units[0].master, units[1].master), (units[0].m, units[1].m),
+                         (units[0].v, units[1].v)):
+                parity.assert_bit_exact_f32(a, parity.f32(b))
+            assert torch.equal(units[0].shards.view(torch.int16), units[1].shards.view(torch.int16))

@@ -417,3 +417,32 @@ def test_llama7b_zero3_zeropp_units(zlib, cuda_device):
         _full_properties(unit.master, unit.shards.view(-1), L.n)
         del unit, w, shards, qs, qg
     assert ring.resident == 0
+
+
+def test_llama7b_zero3_fused_reduce_scatter_update(zlib, cuda_device):
+    """The fused per-unit reduce-scatter + update on a full Llama-7B block unit
+    (202,383,360 elements, n_dp = 8), as the benchmark's fused ZeRO-3 workload
+    launches it, equals the layer reduce-scatter into fp32 followed by the
+    update on every element (compared on the device), two steps."""
+    zb = zlib
+    dev = cuda_device
+    n_dp = 8
+    L = zb.zero_layout(inputs.llama7b_units()[1], n_dp)
+    P = L.padded_n
+    w = inputs.master_weights(L.n, P, seed=SEED + 70, device=dev)
+    units = [zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w.clone(),
+                             torch.zeros(P, device=dev), torch.zeros(P, device=dev)) for _ in range(2)]
+    g = torch.empty((n_dp, P), dtype=torch.bfloat16, device=dev)
+    A = torch.empty(P, device=dev)
+    for t in (1, 2):
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=t, rank=r)
+        rows = [g[r] for r in range(n_dp)]
+        zstep.zero3_layer_reduce_scatter(units[0], rows, A)
+        zstep.zero3_update(units[0], A, _hp(zb, t))
+        zstep.zero3_reduce_scatter_update(units[1], rows, _hp(zb, t))
+        zb.zero_status_check()
+        for a, b in ((units[0].master, units[1].master), (units[0].m, units[1].m), (units[0].v, units[1].v)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.equal(units[0].shards.view(torch.int16), units[1].shards.view(torch.int16))
+    _full_properties(units[1].master, units[1].shards.view(-1), L.n)

@@ -221,6 +221,21 @@ def zero3_update(unit: Zero3Unit, A: torch.Tensor, hp, n_micro: int = 1, stream=
                                  unit.shards.view(-1), zb.ZERO_OUT_SHARD, hp, stream)
 
 
+def zero3_reduce_scatter_update(unit: Zero3Unit, layer_grads, hp, stream=None):
+    """The layer reduce-scatter and the update of the unit's owned shards in one
+    pass, with bf16 into each rank's own shard.  Valid when the step has one
+    micro-batch and no global-norm clipping: each element's update then needs
+    only its own gradient, so a unit can be updated as soon as its gradient is
+    reduced (the units still to run backward keep their weights).  The sum
+    starts from +0 and is divided once, as in zero3_layer_reduce_scatter
+    followed by zero3_update, so the result is bit-identical to that pair;
+    it skips the fp32 buffer's write and re-read (8 bytes per element)."""
+    L = unit.layout
+    zb.zero_reduce_scatter_adamw(L, layer_grads, zb.ZERO_BF16, 0, float(L.n_dp), 0, L.n_dp,
+                                 0, L.padded_n, unit.master, unit.m, unit.v,
+                                 unit.shards.view(-1), zb.ZERO_OUT_SHARD, hp, stream)
+
+
 # --------------------------------------------------------------------------
 # host-resident gradients: copies overlapped with the per-bucket update
 # --------------------------------------------------------------------------
