@@ -67,7 +67,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
                                            "probe", "accum-zero1", "accum-zero2", "zero3",
                                            "zero3-int8", "zero3-prefetch", "zero3-zeropp",
-                                           "zero3-fused"],
+                                           "zero3-fused", "zero3-int8-fused"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -481,14 +481,16 @@ class Zero3Workload(Workload):
         self.name = name
         self.zstep = zstep
         self.zeropp = name == "zero3-zeropp"
-        self.fused = name == "zero3-fused"
-        self.int8 = name in ("zero3-int8", "zero3-zeropp")
+        self.fused = name in ("zero3-fused", "zero3-int8-fused")
+        self.int8 = name in ("zero3-int8", "zero3-zeropp", "zero3-int8-fused")
         self.prefetch = name == "zero3-prefetch"
         n_dp = 8
         self.units = []
         total = 0
+        # the update that writes 8-bit shards itself needs 256-element slices
+        align = 256 if name == "zero3-int8-fused" else 8
         for i, numels in enumerate([[elems]] if elems else inputs.llama7b_units()):
-            L = zb.zero_layout(numels, n_dp)
+            L = zb.zero_layout(numels, n_dp, align=align)
             P = L.padded_n
             w = _master(L.n, P, device)
             shards = w.to(torch.bfloat16)
@@ -515,11 +517,16 @@ class Zero3Workload(Workload):
             self.bytes_per_elem = 4 + 4 + (2 * n_dp + 4) + 30
             self.kernel_label = "zgb::gather_vec_kernel, acc_vec_kernel<8,1,0>, rs_adamw_vec_kernel<1,1>"
         self.dominant = "rs_adamw"
-        if self.fused:
+        if self.fused and not self.int8:
             # two gathers, then the reduce-scatter and the update in one pass (42 B)
             self.bytes_per_elem = 4 + 4 + 26 + 2 * n_dp
             self.dominant = "rs_adamw_fused"
             self.kernel_label = "zgb::gather_vec_kernel, rs_adamw_vec_kernel<0,8> (own-shard output)"
+        if self.fused and self.int8:
+            # two 8-bit gathers, then reduce-scatter + update + quantization in one pass
+            self.bytes_per_elem = 3 + 3 + 2 * n_dp + 24 + 1 + 3 * 4 / 256
+            self.dominant = "rs_adamw_fused_q8"
+            self.kernel_label = "zgb::dequant_gather_vec_kernel, rs_adamw_vec_kernel<0,8,q8>"
         if self.zeropp:
             self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp), n_dp, QGRAD_BLOCK, device)
             sb = n_dp * 4 / QGRAD_BLOCK
@@ -534,6 +541,7 @@ class Zero3Workload(Workload):
         self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else "")
                      + ("_int8_grads" if self.zeropp else "")
                      + ("_fused_rs_update" if self.fused else "")
+                     + ("_align256" if align == 256 else "")
                      + ("_prefetch" if self.prefetch else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
@@ -594,6 +602,12 @@ class Zero3Workload(Workload):
                 else ("gather", P * 4)
             out.append(Op(gkind, gbytes, fwd))
             out.append(Op(gkind, gbytes, bwd_gather))
+            if self.fused and q is not None:
+                def rs_upd_q8(u=u, i=i, grads=grads, q=q):
+                    zs.zero3_reduce_scatter_update_q8(u, grads, q, hp)
+                    self.ring.release(("bwd", i))
+                out.append(Op("rs_adamw_fused_q8", P * (2 * u.layout.n_dp + 25) + (P // 256) * 4, rs_upd_q8))
+                continue
             if self.fused:
                 def rs_upd(u=u, i=i, grads=grads):
                     zs.zero3_reduce_scatter_update(u, grads, hp)
@@ -622,7 +636,8 @@ def make_workload(name, device, elems=0):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
-    if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused"):
+    if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused",
+                "zero3-int8-fused"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -788,7 +803,7 @@ def run_ours(args):
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
                           "accum-zero2", "zero3", "zero3-fused", "zero3-prefetch", "zero3-int8",
-                          "zero3-zeropp")
+                          "zero3-int8-fused", "zero3-zeropp")
               if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}

@@ -154,6 +154,30 @@ int zero_reduce_scatter_adamw(const zero_layout_t* L,
                               uint16_t* out_bf16, int32_t out_mode,
                               const zero_adamw_t* hp, void* stream);
 
+/* ---- the fused update with an 8-bit output (ZeRO++) -----------------------
+ * Stage 3 with 8-bit weight gathers ("ZeRO Optimizer, in depth", "Offload and
+ * ZeRO++": zero_quantized_weights quantises the weight all-gather): the
+ * owner's update writes its shard straight in the 8-bit block format, instead
+ * of bf16 that zero_quantize_int8 would read back.
+ *
+ * Computes exactly zero_reduce_scatter_adamw with ZERO_OUT_SHARD followed by
+ * zero_quantize_int8 of the bf16 results with block 256: master/m/v are
+ * updated as there; q_out (int8, laid out like master: [i - rank_begin*S])
+ * receives the codes of bf16_rne(w), and scales_out one fp32 scale per 256
+ * elements of that layout ([(i - rank_begin*S) / 256]); no bf16 is written.
+ * Requirements: block == 256; S, begin and end multiples of 256 (lay the unit
+ * out with align = 256); master, m, v, q_out and the sources 16-byte aligned
+ * at begin (there is no element-wise fallback); scales_out 4-byte aligned.
+ * Sources as for zero_reduce_scatter_adamw (bf16 gradients or fp32 buffers).
+ * Errors: ZERO_EINVAL (as zero_reduce_scatter_adamw, block, a range or shard
+ * off the 256-element grid), ZERO_EALIGN, ZERO_ERANGE, ZERO_ECUDA. */
+int zero_reduce_scatter_adamw_q8(const zero_layout_t* L, const void* const* src, int32_t n_src,
+                                 int32_t src_dtype, int64_t src_base, float divisor,
+                                 int32_t rank_begin, int32_t rank_end, int64_t begin, int64_t end,
+                                 float* master, float* m, float* v, int8_t* q_out,
+                                 float* scales_out, int32_t block, const zero_adamw_t* hp,
+                                 void* stream);
+
 /* ---- clipping by the global gradient norm --------------------------------
  * "DeepSpeed ZeRO", "The configuration file" and "ZeRO Optimizer, in depth",
  * "Running it with DeepSpeed": gradient_clipping 1.0 -- the mean gradient is

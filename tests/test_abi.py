@@ -226,6 +226,28 @@ def test_int8_gradient_argument_checks(zlib):
     assert acc(Lp, q, s, 4, 256, FAKE, 0, 64, 64, 1, None) == 0             # empty
 
 
+def test_q8_update_argument_checks(zlib):
+    """zero_reduce_scatter_adamw_q8 refuses a block other than 256 and ranges or
+    shards off the 256-element grid before touching any pointer."""
+    lib = zlib.load()
+    L = zlib.zero_layout([4096], 4, align=256)
+    L8 = zlib.zero_layout([4000], 4, align=8)                # S = 1000: off the grid
+    src = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    hp = zlib.ZeroAdamW.make(step=1)
+
+    def q8(Lx=L, block=256, b=0, e=4096, q=FAKE, sc=FAKE, dt=0):
+        return lib.zero_reduce_scatter_adamw_q8(ctypes.byref(Lx), src, 4, dt, 0, 4.0, 0, 4, b, e,
+                                                FAKE, FAKE, FAKE, q, sc, block, ctypes.byref(hp), None)
+
+    assert q8(block=512) == -1
+    assert q8(Lx=L8, e=4000) == -1
+    assert q8(b=8) == -1 and q8(e=4088) == -1
+    assert q8(q=None) == -1 and q8(sc=None) == -1
+    assert q8(sc=FAKE + 2) == -2
+    assert q8(dt=5) == -1
+    assert q8(b=512, e=512) == 0                                # empty
+
+
 def test_missing_library_fails_loudly(zlib, monkeypatch, tmp_path):
     from zero_sharded_mixed_gb300 import binding
     monkeypatch.setattr(binding, "lib_path", str(tmp_path / "nope.so"))

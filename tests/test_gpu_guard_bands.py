@@ -185,3 +185,22 @@ def test_gathers_and_8bit_paths(zlib, cuda_device, align, shift, block):
             **{f"g[{r}]": x for r, x in enumerate(g_in)}, **{f"qg_in[{r}]": x for r, x in enumerate(qg_in)},
             **{f"sg_in[{r}]": x for r, x in enumerate(sg_in)}})
     zb.zero_status_check()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_q8_update(zlib, cuda_device, dtype):
+    """The update with the 8-bit output, owners 1..3 of 5, a range on block
+    boundaries inside them."""
+    zb = zlib
+    N, n_dp, block = 40_000, 5, 256
+    L = zb.zero_layout([N], n_dp, align=block)
+    S = L.shard
+    lo, hi = S + 2 * block, 4 * S - block
+    src = _grads(n_dp, hi - lo, 0, dtype)
+    w, m, v = _state(3 * S, 0)
+    q = Guarded(3 * S, torch.int8)
+    sc = Guarded(3 * S // block, torch.float32)
+    dt = zb.ZERO_BF16 if dtype == torch.bfloat16 else zb.ZERO_F32
+    zb.zero_reduce_scatter_adamw_q8(L, [g.t for g in src], dt, lo, float(n_dp), 1, 4, lo, hi, w.t, m.t,
+                                    v.t, q.t, sc.t, block, zb.ZeroAdamW.make(step=1))
+    _check({"w": w, "m": m, "v": v, "q": q, "scales": sc}, {f"src[{r}]": g for r, g in enumerate(src)})

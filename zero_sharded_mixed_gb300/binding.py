@@ -107,6 +107,9 @@ def load():
         lib.zero_crc32.argtypes = [p, i64]
         lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
+        lib.zero_reduce_scatter_adamw_q8.argtypes = [
+            P(ZeroLayout), P(p), i32, i32, i64, f32, i32, i32, i64, i64,
+            p, p, p, p, p, i32, P(ZeroAdamW), p]
         lib.zero_reduce_scatter_adamw_int8.argtypes = [
             P(ZeroLayout), P(p), P(p), i32, i32, f32, i32, i32, i64, i64,
             p, p, p, p, i32, P(ZeroAdamW), p]
@@ -129,6 +132,7 @@ def load():
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
                      "zero_selftest_bounded_wait", "zero_reduce_scatter_adamw_int8",
+                     "zero_reduce_scatter_adamw_q8",
                      "zero_accumulate_int8", "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -279,6 +283,31 @@ def zero_reduce_scatter_adamw_clip(L: ZeroLayout, srcs, src_dtype: int, src_base
         int(out_mode), ctypes.byref(hp), _tensor(norm_sq, "norm_sq", torch.float64, 1),
         float(max_norm), _stream_ptr(stream))
     _check(rc, "zero_reduce_scatter_adamw_clip")
+
+
+def zero_reduce_scatter_adamw_q8(L: ZeroLayout, srcs, src_dtype: int, src_base: int,
+                                 divisor: float, rank_begin: int, rank_end: int, begin: int,
+                                 end: int, master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                                 q_out: torch.Tensor, scales_out: torch.Tensor, block: int,
+                                 hp: ZeroAdamW, stream=None):
+    """The fused update with its result in the 8-bit block format (codes laid
+    out like the state, one scale per 256 of them) instead of bf16."""
+    if end <= begin:
+        src_need = state_need = 0
+    else:
+        src_need = end - src_base
+        state_need = end - rank_begin * L.shard
+    arr, n = _src_array(srcs, _SRC_DT.get(src_dtype, None), src_need)
+    rc = load().zero_reduce_scatter_adamw_q8(
+        ctypes.byref(L), arr, n, int(src_dtype), int(src_base), float(divisor),
+        int(rank_begin), int(rank_end), int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(q_out, "q_out", torch.int8, state_need),
+        _tensor(scales_out, "scales_out", torch.float32, -(-state_need // 256)),
+        int(block), ctypes.byref(hp), _stream_ptr(stream))
+    _check(rc, "zero_reduce_scatter_adamw_q8")
 
 
 def zero_accumulate_adamw(L: ZeroLayout, mode: int, acc, acc_base: int, grads, grad_base: int,

@@ -24,7 +24,7 @@
 //   8-element vectors (four per thread and iteration, loads first) loads 8
 //   int8 values and their block's scale, multiplies in fp32 and stores 8 bf16
 //   (cvt.rn.bf16x2).  1 byte read + 2 written per element (+ the scales).
-#include "zero_common.cuh"
+#include "zero_quant.cuh"
 
 #ifndef ZGB_QUANT_WAVES
 #define ZGB_QUANT_WAVES 512  // grid = resident CTAs x this, quantize: in effect one pass per
@@ -47,35 +47,6 @@ struct QuantParams {
     int64_t total_blocks;
     int32_t block;
 };
-
-// The int8 code of x * inv (|x * inv| <= 127.00002): add 1.5 * 2^23 in fp32,
-// which rounds to the nearest integer with ties to even; the low byte of the
-// sum's bits holds the code in two's complement.
-__device__ __forceinline__ uint32_t code_bits(float x, float inv) {
-    return __float_as_uint(__fadd_rn(__fmul_rn(x, inv), 12582912.0f));
-}
-
-// Eight codes from eight bf16 weights (one 16-byte vector) packed into 8 bytes.
-__device__ __forceinline__ uint2 quant8(const uint4 raw, float inv) {
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t c[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        c[2 * k] = code_bits(bf16_lo(w4[k]), inv);
-        c[2 * k + 1] = code_bits(bf16_hi(w4[k]), inv);
-    }
-    const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
-    const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
-    return make_uint2(lo, hi);
-}
-
-// max over the 8 bf16 of a vector of |w|, as a pair of 16-bit lanes
-__device__ __forceinline__ uint32_t absmax8_bits(const uint4 raw, uint32_t m) {
-    m = __vmaxu2(m, raw.x & 0x7fff7fffu);
-    m = __vmaxu2(m, raw.y & 0x7fff7fffu);
-    m = __vmaxu2(m, raw.z & 0x7fff7fffu);
-    return __vmaxu2(m, raw.w & 0x7fff7fffu);
-}
 
 __device__ __forceinline__ int8_t quant_one(float x, float amax) {
     if (amax == 0.0f) return 0;

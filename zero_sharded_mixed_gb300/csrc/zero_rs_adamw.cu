@@ -34,6 +34,7 @@
 // the order written in the header (zero_update.cuh).
 #include <cmath>
 
+#include "zero_quant.cuh"
 #include "zero_update.cuh"
 
 #ifndef ZGB_RS_WAVES
@@ -169,10 +170,25 @@ __device__ __forceinline__ void sum_src_dyn(const UpdateParams& p, int64_t e, fl
     }
 }
 
+// The 8-bit output of one vector (kQ8): the update, then its bf16 results in
+// the 8-bit block format of zero_quantize_int8 instead of bf16 stores.  The 32
+// lanes of a warp hold the 256 consecutive elements of one quantization block
+// (a warp's vectors are consecutive, and the host makes every launch start on a
+// block boundary and cover whole blocks), so the block maximum is one warp
+// reduction; codes and scale are computed exactly as by the quantizer.
+__device__ __forceinline__ void finish_vec_q8(const UpdateParams& p, int64_t e, const float (&s)[8],
+                                              const float4 (&st)[6], float coef) {
+    const uint4 o = update_vec(p, e, s, st, coef);
+    const float a = warp_block_absmax(absmax8_bits(o, 0u));
+    const float inv = a == 0.0f ? 0.0f : __fdiv_rn(127.0f, a);          // a zero block: codes 0
+    *reinterpret_cast<uint2*>(p.q + e) = quant8(o, inv);
+    if ((threadIdx.x & 31) == 0) p.qscale[e >> 8] = __fdiv_rn(a, 127.0f);
+}
+
 // U vectors (vi0, vi0 + stride, ...; the kernel passes stride = kThreads, so a
 // CTA's vectors are consecutive) with a compile-time source count R: every
 // load of all U vectors is issued before the first add.
-template <int KIND, int R, int U>
+template <int KIND, int R, int U, bool kQ8>
 __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, int64_t stride,
                                           int64_t nv, float coef) {
     SrcRegs<KIND, R> src[U];
@@ -192,19 +208,25 @@ __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, in
         if (!ok[u]) continue;
         float s[8];
         sum_src<KIND, R>(src[u], s);
-        finish_vec(p, (vi0 + u * stride) * 8, s, st[u], coef);
+        if constexpr (kQ8)
+            finish_vec_q8(p, (vi0 + u * stride) * 8, s, st[u], coef);
+        else
+            finish_vec(p, (vi0 + u * stride) * 8, s, st[u], coef);
     }
 }
 
 // One vector with a runtime source count.
-template <int KIND>
+template <int KIND, bool kQ8>
 __device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, float coef) {
     const int64_t e = vi * 8;
     float s[8];
     sum_src_dyn<KIND>(p, e, s);
     float4 st[6];
     load_state(p, e, st);
-    finish_vec(p, e, s, st, coef);
+    if constexpr (kQ8)
+        finish_vec_q8(p, e, s, st, coef);
+    else
+        finish_vec(p, e, s, st, coef);
 }
 
 // One element (ragged tails and ranges not on 16-byte boundaries).
@@ -255,7 +277,9 @@ __host__ __device__ constexpr int rs_waves() {
          : KIND == kPlainF32 ? 1 : KIND == kAccReduce ? 8 : 64;
 }
 
-template <int KIND, int R>
+// kQ8: the output is 8-bit codes and block scales (p.q, p.qscale) instead of
+// bf16; the host guarantees whole 256-element blocks (no tail).
+template <int KIND, int R, bool kQ8 = false>
 __global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
 rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
     const float coef = clip_coef(p.h);
@@ -269,12 +293,14 @@ rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
         constexpr int U = vectors_per_iter<KIND, R>();
         const int64_t chunk = (int64_t)U * kThreads;
         for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk)
-            step_vecs<KIND, R, U>(p, v0, kThreads, nv, coef);
+            step_vecs<KIND, R, U, kQ8>(p, v0, kThreads, nv, coef);
     } else {
-        for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND>(p, vi, coef);
+        for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND, kQ8>(p, vi, coef);
     }
-    const int64_t tail = p.n - (nv << 3);
-    if (tid < tail) step_one<KIND>(p, (nv << 3) + tid, coef);
+    if constexpr (!kQ8) {
+        const int64_t tail = p.n - (nv << 3);
+        if (tid < tail) step_one<KIND>(p, (nv << 3) + tid, coef);
+    }
 }
 
 template <int KIND>
@@ -285,14 +311,28 @@ __global__ void __launch_bounds__(kThreads) rs_adamw_scalar_kernel(const __grid_
         step_one<KIND>(p, i, coef);
 }
 
-template <int KIND, int R>
+template <int KIND, int R, bool kQ8 = false>
 int launch_vec(const UpdateParams& p, cudaStream_t stream) {
-    const int occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)rs_adamw_vec_kernel<KIND, R, kQ8>, kThreads, 0);
     const int64_t resident = (int64_t)sm_count() * occupancy * rs_waves<KIND, R>();
     const int64_t per_cta = (R > 0 ? vectors_per_iter<KIND, R>() : 1) * (int64_t)kThreads;
     const unsigned grid = grid_for(p.n >> 3, per_cta, resident);
-    rs_adamw_vec_kernel<KIND, R><<<grid, kThreads, 0, stream>>>(p);
+    rs_adamw_vec_kernel<KIND, R, kQ8><<<grid, kThreads, 0, stream>>>(p);
     return launch_status();
+}
+
+// The 8-bit-output kernels (vector path only): the source counts of the
+// stage-3 workloads (1: the fp32 buffer; 8: the ranks' bf16 gradients) and a
+// few more, the rest through the runtime-count kernel.
+template <int KIND>
+int dispatch_q8(const UpdateParams& p, cudaStream_t s) {
+    switch (p.n_src) {
+        case 1: return launch_vec<KIND, 1, true>(p, s);
+        case 2: return launch_vec<KIND, 2, true>(p, s);
+        case 4: return launch_vec<KIND, 4, true>(p, s);
+        case 8: return launch_vec<KIND, 8, true>(p, s);
+        default: return launch_vec<KIND, 0, true>(p, s);
+    }
 }
 
 template <int KIND>
@@ -339,28 +379,31 @@ int dispatch(const UpdateParams& p, bool vec, cudaStream_t s) {
 int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
                    int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
                    UpdateTarget* t) {
-    if (!L || !master || !m || !v || !out) return ZERO_EINVAL;
-    if (out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD) return ZERO_EINVAL;
+    if (!L || !master || !m || !v) return ZERO_EINVAL;
+    if (out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD && out_mode != ZERO_OUT_NONE)
+        return ZERO_EINVAL;
+    if ((out_mode == ZERO_OUT_NONE) != (out == nullptr)) return ZERO_EINVAL;
     if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
     if (rank_begin < 0 || rank_end > L->n_dp || rank_begin >= rank_end) return ZERO_EINVAL;
     const int64_t own_lo = (int64_t)rank_begin * L->shard;
     const int64_t own_hi = (int64_t)rank_end * L->shard;
     if (begin < own_lo || end > own_hi || begin > end) return ZERO_EINVAL;
-    if (check_aligned(master, 4) || check_aligned(m, 4) || check_aligned(v, 4) || check_aligned(out, 2))
+    if (check_aligned(master, 4) || check_aligned(m, 4) || check_aligned(v, 4) ||
+        (out && check_aligned(out, 2)))
         return ZERO_EALIGN;
     const int64_t state_off = begin - own_lo;
     t->w = master + state_off;
     t->m = m + state_off;
     t->v = v + state_off;
-    t->out = out + (out_mode == ZERO_OUT_FULL ? begin : state_off);
+    t->out = out ? out + (out_mode == ZERO_OUT_FULL ? begin : state_off) : nullptr;
     t->n = end - begin;
-    t->aligned = aligned16(t->w) && aligned16(t->m) && aligned16(t->v) && aligned16(t->out);
+    t->aligned = aligned16(t->w) && aligned16(t->m) && aligned16(t->v) && (!t->out || aligned16(t->out));
     return ZERO_OK;
 }
 
 int check_target_ptrs(const UpdateTarget& t) {
     if (check_device_ptr(t.w) || check_device_ptr(t.m) || check_device_ptr(t.v) ||
-        check_device_ptr(t.out))
+        (t.out && check_device_ptr(t.out)))
         return ZERO_EINVAL;
     return ZERO_OK;
 }
@@ -389,11 +432,18 @@ int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h) {
 }
 
 // Shared body of the plain-source entry points (optionally clipped).
+// q8 (optional): the 8-bit output -- codes laid out like the state and one
+// scale per 256 elements of it -- in place of out (out_mode ZERO_OUT_NONE).
+struct Q8Out {
+    int8_t* q;
+    float* scales;
+};
+
 int rs_adamw_plain(const zero_layout_t* L, const void* const* src, int32_t n_src, int32_t src_dtype,
                    int64_t src_base, float divisor, int32_t rank_begin, int32_t rank_end,
                    int64_t begin, int64_t end, float* master, float* m, float* v, uint16_t* out,
                    int32_t out_mode, const zero_adamw_t* hp, const double* norm_sq, float max_norm,
-                   void* stream) {
+                   void* stream, const Q8Out* q8 = nullptr) {
     if (!src) return ZERO_EINVAL;
     if (n_src < 1) return ZERO_EINVAL;
     if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
@@ -434,9 +484,18 @@ int rs_adamw_plain(const zero_layout_t* L, const void* const* src, int32_t n_src
     p.m = t.m;
     p.v = t.v;
     p.out = t.out;
+    p.q = nullptr;
+    p.qscale = nullptr;
     p.n = t.n;
     p.n_src = n_src;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (q8) {
+        const int64_t state_off = begin - (int64_t)rank_begin * L->shard;   // a multiple of 256
+        p.q = q8->q + state_off;
+        p.qscale = q8->scales + state_off / 256;
+        if (!vec || !aligned16(p.q)) return ZERO_EALIGN;
+        return src_dtype == ZERO_BF16 ? dispatch_q8<kPlainBf16>(p, s) : dispatch_q8<kPlainF32>(p, s);
+    }
     return src_dtype == ZERO_BF16 ? dispatch<kPlainBf16>(p, vec, s) : dispatch<kPlainF32>(p, vec, s);
 }
 
@@ -464,6 +523,23 @@ extern "C" int zero_reduce_scatter_adamw_clip(const zero_layout_t* L, const void
     return zgb::rs_adamw_plain(L, src, n_src, src_dtype, src_base, divisor, rank_begin, rank_end,
                                begin, end, master, m, v, out_bf16, out_mode, hp, norm_sq, max_norm,
                                stream);
+}
+
+extern "C" int zero_reduce_scatter_adamw_q8(const zero_layout_t* L, const void* const* src,
+                                            int32_t n_src, int32_t src_dtype, int64_t src_base,
+                                            float divisor, int32_t rank_begin, int32_t rank_end,
+                                            int64_t begin, int64_t end, float* master, float* m,
+                                            float* v, int8_t* q_out, float* scales_out, int32_t block,
+                                            const zero_adamw_t* hp, void* stream) {
+    using namespace zgb;
+    if (!L || !q_out || !scales_out) return ZERO_EINVAL;
+    if (block != 256) return ZERO_EINVAL;
+    if (L->shard % 256 != 0 || begin % 256 != 0 || end % 256 != 0) return ZERO_EINVAL;
+    if (check_aligned(scales_out, 4)) return ZERO_EALIGN;
+    if (end > begin && (check_device_ptr(q_out) || check_device_ptr(scales_out))) return ZERO_EINVAL;
+    const Q8Out q8{q_out, scales_out};
+    return rs_adamw_plain(L, src, n_src, src_dtype, src_base, divisor, rank_begin, rank_end, begin,
+                          end, master, m, v, nullptr, ZERO_OUT_NONE, hp, nullptr, 0.0f, stream, &q8);
 }
 
 extern "C" int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,

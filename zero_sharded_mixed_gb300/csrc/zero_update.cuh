@@ -56,11 +56,12 @@ __device__ __forceinline__ float mean_grad(float sum, const AdamwScalars& h, flo
     return __fmul_rn(__fdiv_rn(sum, h.divisor), coef);
 }
 
-// Update 8 elements at e from their source sums and loaded state; store.
-// P is a parameter block with the update target w, m, v, out and scalars h.
+// Update 8 elements at e from their source sums and loaded state; store the
+// state and return the 8 bf16 results packed in a 16-byte vector.  P is a
+// parameter block with the update target w, m, v and scalars h.
 template <class P>
-__device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&s)[8],
-                                           const float4 (&st)[6], float coef) {
+__device__ __forceinline__ uint4 update_vec(const P& p, int64_t e, const float (&s)[8],
+                                            const float4 (&st)[6], float coef) {
     float w[8] = {st[0].x, st[0].y, st[0].z, st[0].w, st[1].x, st[1].y, st[1].z, st[1].w};
     float m[8] = {st[2].x, st[2].y, st[2].z, st[2].w, st[3].x, st[3].y, st[3].z, st[3].w};
     float v[8] = {st[4].x, st[4].y, st[4].z, st[4].w, st[5].x, st[5].y, st[5].z, st[5].w};
@@ -77,7 +78,14 @@ __device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&
     o.y = pack_bf16x2(w[2], w[3]);
     o.z = pack_bf16x2(w[4], w[5]);
     o.w = pack_bf16x2(w[6], w[7]);
-    st_stream_u4(p.out + e, o);
+    return o;
+}
+
+// The same, storing the bf16 results at out + e.
+template <class P>
+__device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&s)[8],
+                                           const float4 (&st)[6], float coef) {
+    st_stream_u4(p.out + e, update_vec(p, e, s, st, coef));
 }
 
 template <class P>
@@ -97,7 +105,9 @@ struct UpdateParams {
     float* w;
     float* m;
     float* v;
-    uint16_t* out;
+    uint16_t* out;                  // bf16 output, or nullptr when q is set
+    int8_t* q;                      // 8-bit output (block 256) instead of bf16, or nullptr
+    float* qscale;                  // its block scales, one per 256 elements
     int64_t n;                      // elements in the range
     int32_t n_src;                  // gradient sources (ranks)
     AdamwScalars h;
@@ -120,14 +130,17 @@ struct UpdateTarget {
     float* w;
     float* m;
     float* v;
-    uint16_t* out;
+    uint16_t* out;  // nullptr for ZERO_OUT_NONE
     int64_t n;
-    bool aligned;   // all four pointers 16-byte aligned
+    bool aligned;   // all pointers 16-byte aligned
 };
+
+// out_mode of an update whose output is not bf16 (internal: the 8-bit output).
+constexpr int32_t ZERO_OUT_NONE = -1;
 
 // Argument checks that need no CUDA call, then the offsets (zero_gb300.h,
 // zero_reduce_scatter_adamw: state of i at [i - rank_begin*S]; out at [i] for
-// ZERO_OUT_FULL, like the state for ZERO_OUT_SHARD).
+// ZERO_OUT_FULL, like the state for ZERO_OUT_SHARD; no out for ZERO_OUT_NONE).
 int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
                    int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
                    UpdateTarget* t);

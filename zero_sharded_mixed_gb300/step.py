@@ -336,6 +336,27 @@ def zero3_quantize(unit: Zero3Unit, qs: Int8Shards, stream=None):
                           qs.block, stream)
 
 
+def zero3_update_q8(unit: Zero3Unit, A: torch.Tensor, qs: Int8Shards, hp, n_micro: int = 1,
+                    stream=None):
+    """zero3_update followed by zero3_quantize in one pass: the owners' update
+    writes their shards straight in the 8-bit format (block 256; the unit laid
+    out with align 256).  The bf16 shards are not written."""
+    L = unit.layout
+    zb.zero_reduce_scatter_adamw_q8(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
+                                    0, L.padded_n, unit.master, unit.m, unit.v, qs.q.view(-1),
+                                    qs.scales.view(-1), qs.block, hp, stream)
+
+
+def zero3_reduce_scatter_update_q8(unit: Zero3Unit, layer_grads, qs: Int8Shards, hp, stream=None):
+    """zero3_reduce_scatter_update with the 8-bit output of zero3_update_q8:
+    the unit's gradient reduce-scatter, update and quantization in one pass
+    (one micro-batch, no clipping)."""
+    L = unit.layout
+    zb.zero_reduce_scatter_adamw_q8(L, layer_grads, zb.ZERO_BF16, 0, float(L.n_dp), 0, L.n_dp,
+                                    0, L.padded_n, unit.master, unit.m, unit.v, qs.q.view(-1),
+                                    qs.scales.view(-1), qs.block, hp, stream)
+
+
 def zero3_gather_int8(unit: Zero3Unit, qs: Int8Shards, ring: GatherRing, unit_id,
                       stream=None) -> torch.Tensor:
     buf = ring.acquire(unit_id, unit.layout.padded_n)
