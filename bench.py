@@ -67,7 +67,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
                                            "probe", "accum-zero1", "accum-zero2", "zero3",
                                            "zero3-int8", "zero3-prefetch", "zero3-zeropp",
-                                           "zero3-fused", "zero3-int8-fused"],
+                                           "zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -480,15 +480,15 @@ class Zero3Workload(Workload):
         zb = self.zb
         self.name = name
         self.zstep = zstep
-        self.zeropp = name == "zero3-zeropp"
-        self.fused = name in ("zero3-fused", "zero3-int8-fused")
-        self.int8 = name in ("zero3-int8", "zero3-zeropp", "zero3-int8-fused")
+        self.zeropp = name in ("zero3-zeropp", "zero3-zeropp-fused")
+        self.fused = name in ("zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused")
+        self.int8 = name in ("zero3-int8", "zero3-zeropp", "zero3-int8-fused", "zero3-zeropp-fused")
         self.prefetch = name == "zero3-prefetch"
         n_dp = 8
         self.units = []
         total = 0
         # the update that writes 8-bit shards itself needs 256-element slices
-        align = 256 if name == "zero3-int8-fused" else 8
+        align = 256 if name in ("zero3-int8-fused", "zero3-zeropp-fused") else 8
         for i, numels in enumerate([[elems]] if elems else inputs.llama7b_units()):
             L = zb.zero_layout(numels, n_dp, align=align)
             P = L.padded_n
@@ -522,18 +522,25 @@ class Zero3Workload(Workload):
             self.bytes_per_elem = 4 + 4 + 26 + 2 * n_dp
             self.dominant = "rs_adamw_fused"
             self.kernel_label = "zgb::gather_vec_kernel, rs_adamw_vec_kernel<0,8> (own-shard output)"
-        if self.fused and self.int8:
+        if self.fused and self.int8 and not self.zeropp:
             # two 8-bit gathers, then reduce-scatter + update + quantization in one pass
             self.bytes_per_elem = 3 + 3 + 2 * n_dp + 24 + 1 + 3 * 4 / 256
             self.dominant = "rs_adamw_fused_q8"
             self.kernel_label = "zgb::dequant_gather_vec_kernel, rs_adamw_vec_kernel<0,8,q8>"
         if self.zeropp:
-            self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp), n_dp, QGRAD_BLOCK, device)
+            self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp, align=align), n_dp, QGRAD_BLOCK, device)
             sb = n_dp * 4 / QGRAD_BLOCK
             # + every rank quantizes its unit gradient; the RS reads 1 B per source (+ scales)
             self.bytes_per_elem = 3 + 3 + (n_dp * 3 + sb) + (n_dp + sb + 4) + 30 + 3
             self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_group_kernel<8,4>, "
                                  "qgrad_vec_kernel<8,false>, rs_adamw_vec_kernel<1,1>")
+            if self.fused:
+                # two 8-bit gathers, every rank quantizes its gradient, then one pass:
+                # 8-bit gradients in, AdamW, 8-bit shards out
+                self.bytes_per_elem = 3 + 3 + (n_dp * 3 + sb) + (n_dp + sb) + 24 + 1 + 4 / 256
+                self.dominant = "rs_adamw_int8_q8"
+                self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_group_kernel<8,4>, "
+                                     "qgrad_vec_kernel<8,true,q8>")
         if self.prefetch:
             self.dominant = "zero3_step_prefetched"
             self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
@@ -602,6 +609,19 @@ class Zero3Workload(Workload):
                 else ("gather", P * 4)
             out.append(Op(gkind, gbytes, fwd))
             out.append(Op(gkind, gbytes, bwd_gather))
+            if self.fused and self.zeropp:
+                n = u.layout.n_dp
+                sbytes = n * (-(-u.layout.shard // QGRAD_BLOCK)) * 4
+
+                def rs_upd_int8_q8(u=u, i=i, P=P, q=q, n=n):
+                    zb.zero_reduce_scatter_adamw_int8_q8(
+                        u.layout, [self.qg.q[r, :P] for r in range(n)], [self.qg.scales[r] for r in range(n)],
+                        QGRAD_BLOCK, float(n), 0, n, 0, P, u.master, u.m, u.v, q.q.view(-1),
+                        q.scales.view(-1), 256, hp)
+                    self.ring.release(("bwd", i))
+                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads))
+                out.append(Op("rs_adamw_int8_q8", P * (n + 25) + n * sbytes + (P // 256) * 4, rs_upd_int8_q8))
+                continue
             if self.fused and q is not None:
                 def rs_upd_q8(u=u, i=i, grads=grads, q=q):
                     zs.zero3_reduce_scatter_update_q8(u, grads, q, hp)
@@ -637,7 +657,7 @@ def make_workload(name, device, elems=0):
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
     if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused",
-                "zero3-int8-fused"):
+                "zero3-int8-fused", "zero3-zeropp-fused"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -803,7 +823,7 @@ def run_ours(args):
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
                           "accum-zero2", "zero3", "zero3-fused", "zero3-prefetch", "zero3-int8",
-                          "zero3-int8-fused", "zero3-zeropp")
+                          "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused")
               if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
     results = {}

@@ -315,6 +315,19 @@ int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8_t* const* 
                                    int64_t begin, int64_t end, float* master, float* m, float* v,
                                    uint16_t* out_bf16, int32_t out_mode, const zero_adamw_t* hp,
                                    void* stream);
+/* zero_reduce_scatter_adamw_int8_q8: zero_reduce_scatter_adamw_int8 with the
+ * 8-bit output of zero_reduce_scatter_adamw_q8 -- the owners' update from
+ * 8-bit gradients writes their shards straight in the 8-bit block format
+ * (out_block == 256): q_out laid out like master, scales_out one per 256
+ * elements of it; no bf16 is written.  Same requirements as
+ * zero_reduce_scatter_adamw_q8 (S, begin, end on the 256-element grid,
+ * aligned buffers, the vector path only). */
+int zero_reduce_scatter_adamw_int8_q8(const zero_layout_t* L, const int8_t* const* q_src,
+                                      const float* const* scale_src, int32_t n_src, int32_t block,
+                                      float divisor, int32_t rank_begin, int32_t rank_end,
+                                      int64_t begin, int64_t end, float* master, float* m, float* v,
+                                      int8_t* q_out, float* scales_out, int32_t out_block,
+                                      const zero_adamw_t* hp, void* stream);
 int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const* q_src,
                          const float* const* scale_src, int32_t n_src, int32_t block, float* dst,
                          int64_t dst_base, int64_t begin, int64_t end, int32_t first, void* stream);

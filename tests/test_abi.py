@@ -246,6 +246,17 @@ def test_q8_update_argument_checks(zlib):
     assert q8(sc=FAKE + 2) == -2
     assert q8(dt=5) == -1
     assert q8(b=512, e=512) == 0                                # empty
+    s8 = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+
+    def iq8(Lx=L, out_block=256, b=0, e=4096, q=FAKE, block=256):
+        return lib.zero_reduce_scatter_adamw_int8_q8(ctypes.byref(Lx), src, s8, 4, block, 4.0, 0, 4, b, e,
+                                                     FAKE, FAKE, FAKE, q, FAKE, out_block,
+                                                     ctypes.byref(hp), None)
+
+    assert iq8(out_block=512) == -1 and iq8(block=100) == -1
+    assert iq8(Lx=L8, e=4000) == -1 and iq8(b=8) == -1
+    assert iq8(q=None) == -1
+    assert iq8(b=256, e=256) == 0
 
 
 def test_missing_library_fails_loudly(zlib, monkeypatch, tmp_path):

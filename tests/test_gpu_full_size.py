@@ -478,3 +478,36 @@ def test_llama7b_zero3_fused_q8_update(zlib, cuda_device):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
         assert torch.equal(qs[0].q, qs[1].q)
         assert torch.equal(qs[0].scales.view(torch.int32), qs[1].scales.view(torch.int32))
+
+
+def test_llama7b_zero3_fused_int8_gradients_q8(zlib, cuda_device):
+    """Both ZeRO++ 8-bit paths fused on a full Llama-7B block unit laid out with
+    align 256 (n_dp = 8), as the benchmark's fused ZeRO++ workload launches it:
+    from the ranks' 8-bit gradients straight to 8-bit shards, equal on every
+    element and scale to the 8-bit accumulation into fp32, the update into bf16
+    and the quantizer (compared on the device), two steps."""
+    zb = zlib
+    dev = cuda_device
+    n_dp = 8
+    L = zb.zero_layout(inputs.llama7b_units()[1], n_dp, align=256)
+    P = L.padded_n
+    w = inputs.master_weights(L.n, P, seed=SEED + 90, device=dev)
+    units = [zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w.clone(),
+                             torch.zeros(P, device=dev), torch.zeros(P, device=dev)) for _ in range(2)]
+    qs = [zstep.Int8Shards(L, 256, dev) for _ in range(2)]
+    qg = zstep.Int8Grads(L, n_dp, 256, dev)
+    g = torch.empty((n_dp, P), dtype=torch.bfloat16, device=dev)
+    A = torch.empty(P, device=dev)
+    for t in (1, 2):
+        for r in range(n_dp):
+            inputs.grad_bf16_into(g[r], L.n, SEED, step=t, rank=r, outlier_p=0.01)
+        qg.quantize([g[r] for r in range(n_dp)])
+        zstep.zero3_layer_reduce_scatter_int8(units[0], qg, A)
+        zstep.zero3_update(units[0], A, _hp(zb, t))
+        zstep.zero3_quantize(units[0], qs[0])
+        zstep.zero3_reduce_scatter_update_int8_q8(units[1], qg, qs[1], _hp(zb, t))
+        zb.zero_status_check()
+        for a, b in ((units[0].master, units[1].master), (units[0].m, units[1].m), (units[0].v, units[1].v)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.equal(qs[0].q, qs[1].q)
+        assert torch.equal(qs[0].scales.view(torch.int32), qs[1].scales.view(torch.int32))

@@ -204,3 +204,27 @@ def test_q8_update(zlib, cuda_device, dtype):
     zb.zero_reduce_scatter_adamw_q8(L, [g.t for g in src], dt, lo, float(n_dp), 1, 4, lo, hi, w.t, m.t,
                                     v.t, q.t, sc.t, block, zb.ZeroAdamW.make(step=1))
     _check({"w": w, "m": m, "v": v, "q": q, "scales": sc}, {f"src[{r}]": g for r, g in enumerate(src)})
+
+
+def test_int8_gradient_update_with_8bit_output(zlib, cuda_device):
+    zb = zlib
+    N, n_dp, block = 40_000, 5, 256
+    L = zb.zero_layout([N], n_dp, align=block)
+    S, P = L.shard, L.padded_n
+    g = inputs.grads_bf16(n_dp, N, P, seed=6, step=1)
+    qg = [Guarded(P, torch.int8) for _ in range(n_dp)]
+    sg = [Guarded(P // block, torch.float32) for _ in range(n_dp)]
+    for r in range(n_dp):
+        zb.zero_quantize_int8(L, g[r].cuda(), qg[r].t, sg[r].t, block)
+    torch.cuda.synchronize()
+    qg_in = [Guarded(P, torch.int8, 0, x.t) for x in qg]
+    sg_in = [Guarded(P // block, torch.float32, 0, x.t) for x in sg]
+    w, m, v = _state(3 * S, 0)
+    q = Guarded(3 * S, torch.int8)
+    sc = Guarded(3 * S // block, torch.float32)
+    lo, hi = S + block, 4 * S - 2 * block
+    zb.zero_reduce_scatter_adamw_int8_q8(L, [x.t for x in qg_in], [x.t for x in sg_in], block, float(n_dp),
+                                         1, 4, lo, hi, w.t, m.t, v.t, q.t, sc.t, block,
+                                         zb.ZeroAdamW.make(step=1))
+    _check({"w": w, "m": m, "v": v, "q": q, "scales": sc},
+           {**{f"qg[{r}]": x for r, x in enumerate(qg_in)}, **{f"sg[{r}]": x for r, x in enumerate(sg_in)}})

@@ -115,3 +115,36 @@ def test_q8_update_partial_owner_range(zlib, cuda_device):
     assert np.all(qn[:a] == 77) and np.all(qn[b:] == 77)
     assert np.all(sn[:a // BLOCK] == 5.0) and np.all(sn[b // BLOCK:] == 5.0)
     assert torch.equal(w[:a], u.master[rb * S:rb * S + a]) and torch.equal(w[b:], u.master[rb * S + b:re * S])
+
+
+@pytest.mark.parametrize("numels,n_dp", [([4097], 7), ([33_031], 8), ([1000, 24, 3, 5000], 3)])
+def test_int8_gradient_update_with_8bit_output(zlib, cuda_device, numels, n_dp):
+    """Both ZeRO++ 8-bit paths in one pass: from the ranks' 8-bit gradients
+    straight to 8-bit shards.  Equal to the 8-bit accumulation into fp32, the
+    update into bf16 and the quantizer, bit for bit, and to the oracle."""
+    zb = zlib
+    a = _unit(zb, numels, n_dp, seed=20 + n_dp)
+    b = _clone(a)
+    L = a.layout
+    P, S = L.padded_n, L.shard
+    qa, qb = zstep.Int8Shards(L, BLOCK), zstep.Int8Shards(L, BLOCK)
+    A = torch.empty(P, device="cuda")
+    ref = [parity.f32(a.master), np.zeros(P, np.float32), np.zeros(P, np.float32)]
+    for t in (1, 2):
+        g = inputs.grads_bf16(n_dp, L.n, P, seed=70 + t, step=t, outlier_p=0.01)
+        qg = zstep.Int8Grads(L, n_dp, BLOCK)
+        qg.quantize([g[r].cuda() for r in range(n_dp)])
+        zstep.zero3_layer_reduce_scatter_int8(a, qg, A)
+        zstep.zero3_update(a, A, _hp(zb, t))
+        zstep.zero3_quantize(a, qa)
+        zstep.zero3_reduce_scatter_update_int8_q8(b, qg, qb, _hp(zb, t))
+        torch.cuda.synchronize()
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            parity.assert_bit_exact_f32(y, parity.f32(x))
+        assert torch.equal(qa.q, qb.q) and torch.equal(qa.scales, qb.scales)
+        q_ref, s_ref = oracle.quantize_grad_int8(parity.bits(g), n_dp, BLOCK)
+        out_ref, *ref = oracle.qgrad_rs_adamw_reference(q_ref, s_ref, n_dp, BLOCK, n_dp, *ref, HP, t)
+        parity.assert_state([b.master, b.m, b.v], ref, what=f"t={t} ")
+        cq, cs = _oracle_codes(out_ref, n_dp, S)
+        np.testing.assert_array_equal(qb.q.cpu().numpy().reshape(-1), cq)
+        np.testing.assert_array_equal(qb.scales[:, :qb.nb].cpu().numpy().reshape(-1), cs)

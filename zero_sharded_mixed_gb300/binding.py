@@ -110,6 +110,9 @@ def load():
         lib.zero_reduce_scatter_adamw_q8.argtypes = [
             P(ZeroLayout), P(p), i32, i32, i64, f32, i32, i32, i64, i64,
             p, p, p, p, p, i32, P(ZeroAdamW), p]
+        lib.zero_reduce_scatter_adamw_int8_q8.argtypes = [
+            P(ZeroLayout), P(p), P(p), i32, i32, f32, i32, i32, i64, i64,
+            p, p, p, p, p, i32, P(ZeroAdamW), p]
         lib.zero_reduce_scatter_adamw_int8.argtypes = [
             P(ZeroLayout), P(p), P(p), i32, i32, f32, i32, i32, i64, i64,
             p, p, p, p, i32, P(ZeroAdamW), p]
@@ -132,7 +135,7 @@ def load():
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
                      "zero_selftest_bounded_wait", "zero_reduce_scatter_adamw_int8",
-                     "zero_reduce_scatter_adamw_q8",
+                     "zero_reduce_scatter_adamw_q8", "zero_reduce_scatter_adamw_int8_q8",
                      "zero_accumulate_int8", "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -465,6 +468,30 @@ def zero_reduce_scatter_adamw_int8(L: ZeroLayout, q_src, scale_src, block: int, 
         _tensor(out, "out", torch.bfloat16, out_need),
         int(out_mode), ctypes.byref(hp), _stream_ptr(stream))
     _check(rc, "zero_reduce_scatter_adamw_int8")
+
+
+def zero_reduce_scatter_adamw_int8_q8(L: ZeroLayout, q_src, scale_src, block: int, divisor: float,
+                                      rank_begin: int, rank_end: int, begin: int, end: int,
+                                      master: torch.Tensor, m: torch.Tensor, v: torch.Tensor,
+                                      q_out: torch.Tensor, scales_out: torch.Tensor, out_block: int,
+                                      hp: ZeroAdamW, stream=None):
+    """The update from 8-bit gradients with its result in the 8-bit block format."""
+    if end <= begin:
+        src_need = state_need = 0
+    else:
+        src_need = end
+        state_need = end - rank_begin * L.shard
+    qa, sa, n = _qgrad_sources(L, q_src, scale_src, block, src_need)
+    rc = load().zero_reduce_scatter_adamw_int8_q8(
+        ctypes.byref(L), qa, sa, n, int(block), float(divisor), int(rank_begin), int(rank_end),
+        int(begin), int(end),
+        _tensor(master, "master", torch.float32, state_need),
+        _tensor(m, "m", torch.float32, state_need),
+        _tensor(v, "v", torch.float32, state_need),
+        _tensor(q_out, "q_out", torch.int8, state_need),
+        _tensor(scales_out, "scales_out", torch.float32, -(-state_need // 256)),
+        int(out_block), ctypes.byref(hp), _stream_ptr(stream))
+    _check(rc, "zero_reduce_scatter_adamw_int8_q8")
 
 
 def zero_accumulate_int8(L: ZeroLayout, q_src, scale_src, block: int, dst: torch.Tensor,

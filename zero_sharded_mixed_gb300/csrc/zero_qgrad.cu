@@ -64,6 +64,8 @@ struct QGradParams {
     float* v;
     uint16_t* out;                     // update: bf16 output, offset like q
     float* dst;                        // accumulation: fp32 destination, offset like q
+    int8_t* qout;                      // update with 8-bit output: codes, offset like w
+    float* qoscale;                    // and their block scales (one per 256 elements)
     int64_t n;                         // elements of the launch, all in one owner's slice
     int64_t k0;                        // slice-local index of the launch's first element
     int32_t n_src;
@@ -126,7 +128,7 @@ __device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float
 }
 
 // U vectors (vi0, vi0 + kThreads, ...) with a compile-time source count.
-template <int R, bool kUpdate, int U>
+template <int R, bool kUpdate, int U, bool kQ8>
 __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, int64_t nv) {
     QVec<R, kUpdate> x[U];
     bool ok[U];
@@ -145,7 +147,9 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
         for (int j = 0; j < 8; ++j) s[j] = 0.0f;
 #pragma unroll
         for (int r = 0; r < R; ++r) add_codes8(s, x[u].c[r], x[u].s[r]);
-        if constexpr (kUpdate) {
+        if constexpr (kQ8) {
+            finish_vec_q8(p, e, s, x[u].st, 1.0f, p.qout, p.qoscale);
+        } else if constexpr (kUpdate) {
             finish_vec(p, e, s, x[u].st, 1.0f);
         } else {
             const float4 d[2] = {x[u].st[0], x[u].st[1]};
@@ -155,7 +159,7 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
 }
 
 // One vector with a runtime source count, one source at a time.
-template <bool kUpdate>
+template <bool kUpdate, bool kQ8>
 __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) {
     const int64_t e = vi * 8;
     const int64_t b = (p.k0 + e) >> p.block_shift;
@@ -166,7 +170,10 @@ __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) 
     if constexpr (kUpdate) {
         float4 st[6];
         load_state(p, e, st);
-        finish_vec(p, e, s, st, 1.0f);
+        if constexpr (kQ8)
+            finish_vec_q8(p, e, s, st, 1.0f, p.qout, p.qoscale);
+        else
+            finish_vec(p, e, s, st, 1.0f);
     } else {
         float4 d[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
         if (!p.first) {
@@ -237,7 +244,9 @@ __host__ __device__ constexpr int qgrad_vectors_per_iter() {
                    : (ZGB_QACC_U > 0 ? ZGB_QACC_U : R <= 4 ? 4 : R <= 8 ? 2 : 1);
 }
 
-template <int R, bool kUpdate>
+// kQ8 (with kUpdate): the output is 8-bit codes and block scales (p.qout,
+// p.qoscale) instead of bf16; the host guarantees whole 256-element blocks.
+template <int R, bool kUpdate, bool kQ8 = false>
 __global__ void __launch_bounds__(kThreads, !kUpdate ? ZGB_QACC_MINBLOCKS
                                            : qgrad_vectors_per_iter<R, kUpdate>() == 1 ? ZGB_QGRAD_MINBLOCKS : 2)
 qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
@@ -250,14 +259,16 @@ qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
             if constexpr (ZGB_QGRAD_PREFETCH > 0)
                 prefetch_chunk<R, kUpdate>(p, v0 - threadIdx.x + ZGB_QGRAD_PREFETCH * (int64_t)gridDim.x * chunk,
                                            chunk, nv);
-            qgrad_vecs<R, kUpdate, U>(p, v0, nv);
+            qgrad_vecs<R, kUpdate, U, kQ8>(p, v0, nv);
         }
     } else {
         const int64_t stride = (int64_t)gridDim.x * kThreads;
-        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate>(p, vi);
+        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, vi);
     }
-    const int64_t tail = p.n - (nv << 3);
-    if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid);
+    if constexpr (!kQ8) {
+        const int64_t tail = p.n - (nv << 3);
+        if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid);
+    }
 }
 
 template <bool kUpdate>
@@ -267,18 +278,28 @@ __global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_con
         qgrad_one<kUpdate>(p, i);
 }
 
-template <int R, bool kUpdate>
+template <int R, bool kUpdate, bool kQ8 = false>
 int launch_qgrad_vec(const QGradParams& p, cudaStream_t s) {
-    const int occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate>, kThreads, 0);
+    const int occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate, kQ8>, kThreads, 0);
     const int64_t per_cta = (int64_t)qgrad_vectors_per_iter<R, kUpdate>() * kThreads;
     const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
     const unsigned grid = grid_for(p.n >> 3, per_cta, (int64_t)sm_count() * occupancy * waves);
-    qgrad_vec_kernel<R, kUpdate><<<grid, kThreads, 0, s>>>(p);
+    qgrad_vec_kernel<R, kUpdate, kQ8><<<grid, kThreads, 0, s>>>(p);
     return launch_status();
 }
 
-template <bool kUpdate>
+template <bool kUpdate, bool kQ8 = false>
 int launch_qgrad(const QGradParams& p, bool vec, cudaStream_t s) {
+    if constexpr (kQ8) {                 // vector kernels only: whole 256-element blocks per warp
+        if (!vec) return ZERO_EALIGN;
+        switch (p.n_src) {
+            case 1: return launch_qgrad_vec<1, kUpdate, true>(p, s);
+            case 2: return launch_qgrad_vec<2, kUpdate, true>(p, s);
+            case 4: return launch_qgrad_vec<4, kUpdate, true>(p, s);
+            case 8: return launch_qgrad_vec<8, kUpdate, true>(p, s);
+            default: return launch_qgrad_vec<0, kUpdate, true>(p, s);
+        }
+    }
     if (!vec) {
         const int occupancy = ctas_per_sm((const void*)qgrad_scalar_kernel<kUpdate>, kThreads, 0);
         const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
@@ -325,7 +346,7 @@ int check_qsource_ptrs(const int8_t* const* q_src, const float* const* scale_src
 // One launch per owner o whose slice meets [begin, end).  `place` sets the
 // target pointers of a launch covering flat [lo, hi) and returns whether they
 // allow the vector kernel.
-template <bool kUpdate, class Place>
+template <bool kUpdate, bool kQ8, class Place>
 int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* const* scale_src,
               int32_t n_src, int32_t block, int64_t begin, int64_t end, QGradParams base,
               Place place, cudaStream_t s) {
@@ -351,7 +372,7 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
             vec = vec && (reinterpret_cast<uintptr_t>(p.q[r]) & 7u) == 0;
         }
         vec = place(p, lo) && vec;
-        const int rc = launch_qgrad<kUpdate>(p, vec, s);
+        const int rc = launch_qgrad<kUpdate, kQ8>(p, vec, s);
         if (rc) return rc;
     }
     return ZERO_OK;
@@ -378,6 +399,8 @@ extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8
     if ((rc = check_target_ptrs(t))) return rc;
     base.dst = nullptr;
     base.first = 0;
+    base.qout = nullptr;
+    base.qoscale = nullptr;
     auto place = [&](QGradParams& p, int64_t lo) {
         const int64_t off = lo - begin;
         p.w = t.w + off;
@@ -386,7 +409,7 @@ extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8
         p.out = t.out + off;
         return aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.out);
     };
-    return qgrad_run<true>(L, q_src, scale_src, n_src, block, begin, end, base, place,
+    return qgrad_run<true, false>(L, q_src, scale_src, n_src, block, begin, end, base, place,
                            static_cast<cudaStream_t>(stream));
 }
 
@@ -409,12 +432,55 @@ extern "C" int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const*
     QGradParams base;
     base.w = base.m = base.v = nullptr;
     base.out = nullptr;
+    base.qout = nullptr;
+    base.qoscale = nullptr;
     base.first = first ? 1 : 0;
     base.h = AdamwScalars{};
     auto place = [&](QGradParams& p, int64_t lo) {
         p.dst = dst + (lo - dst_base);
         return aligned16(p.dst);
     };
-    return qgrad_run<false>(L, q_src, scale_src, n_src, block, begin, end, base, place,
+    return qgrad_run<false, false>(L, q_src, scale_src, n_src, block, begin, end, base, place,
                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int zero_reduce_scatter_adamw_int8_q8(const zero_layout_t* L, const int8_t* const* q_src,
+                                                 const float* const* scale_src, int32_t n_src,
+                                                 int32_t block, float divisor, int32_t rank_begin,
+                                                 int32_t rank_end, int64_t begin, int64_t end,
+                                                 float* master, float* m, float* v, int8_t* q_out,
+                                                 float* scales_out, int32_t out_block,
+                                                 const zero_adamw_t* hp, void* stream) {
+    using namespace zgb;
+    int rc = check_qsources(q_src, scale_src, n_src, block);
+    if (rc) return rc;
+    if (!L || !q_out || !scales_out) return ZERO_EINVAL;
+    if (out_block != 256) return ZERO_EINVAL;
+    if (L->shard % 256 != 0 || begin % 256 != 0 || end % 256 != 0) return ZERO_EINVAL;
+    if (check_aligned(scales_out, 4)) return ZERO_EALIGN;
+    UpdateTarget t;
+    if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, nullptr, ZERO_OUT_NONE, &t)))
+        return rc;
+    QGradParams base;
+    if ((rc = make_scalars(hp, divisor, &base.h))) return rc;
+    if (end == begin) return ZERO_OK;
+    if ((rc = check_qsource_ptrs(q_src, scale_src, n_src))) return rc;
+    if ((rc = check_target_ptrs(t))) return rc;
+    if (check_device_ptr(q_out) || check_device_ptr(scales_out)) return ZERO_EINVAL;
+    base.dst = nullptr;
+    base.first = 0;
+    base.out = nullptr;
+    const int64_t own_lo = (int64_t)rank_begin * L->shard;
+    auto place = [&](QGradParams& p, int64_t lo) {
+        const int64_t off = lo - begin;
+        p.w = t.w + off;
+        p.m = t.m + off;
+        p.v = t.v + off;
+        p.out = nullptr;
+        p.qout = q_out + (lo - own_lo);                  // lo - own_lo is a multiple of 256
+        p.qoscale = scales_out + (lo - own_lo) / 256;
+        return aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.qout);
+    };
+    return qgrad_run<true, true>(L, q_src, scale_src, n_src, block, begin, end, base, place,
+                                 static_cast<cudaStream_t>(stream));
 }

@@ -34,7 +34,6 @@
 // the order written in the header (zero_update.cuh).
 #include <cmath>
 
-#include "zero_quant.cuh"
 #include "zero_update.cuh"
 
 #ifndef ZGB_RS_WAVES
@@ -170,21 +169,6 @@ __device__ __forceinline__ void sum_src_dyn(const UpdateParams& p, int64_t e, fl
     }
 }
 
-// The 8-bit output of one vector (kQ8): the update, then its bf16 results in
-// the 8-bit block format of zero_quantize_int8 instead of bf16 stores.  The 32
-// lanes of a warp hold the 256 consecutive elements of one quantization block
-// (a warp's vectors are consecutive, and the host makes every launch start on a
-// block boundary and cover whole blocks), so the block maximum is one warp
-// reduction; codes and scale are computed exactly as by the quantizer.
-__device__ __forceinline__ void finish_vec_q8(const UpdateParams& p, int64_t e, const float (&s)[8],
-                                              const float4 (&st)[6], float coef) {
-    const uint4 o = update_vec(p, e, s, st, coef);
-    const float a = warp_block_absmax(absmax8_bits(o, 0u));
-    const float inv = a == 0.0f ? 0.0f : __fdiv_rn(127.0f, a);          // a zero block: codes 0
-    *reinterpret_cast<uint2*>(p.q + e) = quant8(o, inv);
-    if ((threadIdx.x & 31) == 0) p.qscale[e >> 8] = __fdiv_rn(a, 127.0f);
-}
-
 // U vectors (vi0, vi0 + stride, ...; the kernel passes stride = kThreads, so a
 // CTA's vectors are consecutive) with a compile-time source count R: every
 // load of all U vectors is issued before the first add.
@@ -209,7 +193,7 @@ __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, in
         float s[8];
         sum_src<KIND, R>(src[u], s);
         if constexpr (kQ8)
-            finish_vec_q8(p, (vi0 + u * stride) * 8, s, st[u], coef);
+            finish_vec_q8(p, (vi0 + u * stride) * 8, s, st[u], coef, p.q, p.qscale);
         else
             finish_vec(p, (vi0 + u * stride) * 8, s, st[u], coef);
     }
@@ -224,7 +208,7 @@ __device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, 
     float4 st[6];
     load_state(p, e, st);
     if constexpr (kQ8)
-        finish_vec_q8(p, e, s, st, coef);
+        finish_vec_q8(p, e, s, st, coef, p.q, p.qscale);
     else
         finish_vec(p, e, s, st, coef);
 }

@@ -14,7 +14,7 @@
 // rounded once, and g is multiplied by coef before the update.
 #pragma once
 
-#include "zero_common.cuh"
+#include "zero_quant.cuh"
 
 namespace zgb {
 
@@ -86,6 +86,22 @@ template <class P>
 __device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&s)[8],
                                            const float4 (&st)[6], float coef) {
     st_stream_u4(p.out + e, update_vec(p, e, s, st, coef));
+}
+
+// The same with the 8-bit output: the bf16 results in the 8-bit block format
+// (block 256) at qout + e, the block's scale at qscale[e / 256].  The 32 lanes
+// of the calling warp must hold the 256 consecutive elements of one block
+// (consecutive 8-element vectors, the first on a block boundary); codes and
+// scale are computed exactly as by the quantizer (zero_quantize_int8).
+template <class P>
+__device__ __forceinline__ void finish_vec_q8(const P& p, int64_t e, const float (&s)[8],
+                                              const float4 (&st)[6], float coef, int8_t* qout,
+                                              float* qscale) {
+    const uint4 o = update_vec(p, e, s, st, coef);
+    const float a = warp_block_absmax(absmax8_bits(o, 0u));
+    const float inv = a == 0.0f ? 0.0f : __fdiv_rn(127.0f, a);          // a zero block: codes 0
+    *reinterpret_cast<uint2*>(qout + e) = quant8(o, inv);
+    if ((threadIdx.x & 31) == 0) qscale[e >> 8] = __fdiv_rn(a, 127.0f);
 }
 
 template <class P>

@@ -421,6 +421,18 @@ def zero3_layer_reduce_scatter_int8(unit: Zero3Unit, qg: Int8Grads, A: torch.Ten
     zb.zero_accumulate_int8(L, qs, ss, qg.block, A, 0, 0, L.padded_n, first, stream)
 
 
+def zero3_reduce_scatter_update_int8_q8(unit: Zero3Unit, qg: Int8Grads, qs: Int8Shards, hp,
+                                        stream=None):
+    """Both ZeRO++ 8-bit paths in one pass per unit (one micro-batch, no
+    clipping): the owners dequantize the ranks' 8-bit gradient slices, update,
+    and write their shards straight in the 8-bit format (block 256)."""
+    L = unit.layout
+    q_src, s_src = qg.sources()
+    zb.zero_reduce_scatter_adamw_int8_q8(L, q_src, s_src, qg.block, float(L.n_dp), 0, L.n_dp, 0,
+                                         L.padded_n, unit.master, unit.m, unit.v, qs.q.view(-1),
+                                         qs.scales.view(-1), qs.block, hp, stream)
+
+
 # --------------------------------------------------------------------------
 # ZeRO-3 prefetch ("DeepSpeed ZeRO", "Stage 3 step by step": prefetching so
 # that the gather for the next layer overlaps with the compute of the current
