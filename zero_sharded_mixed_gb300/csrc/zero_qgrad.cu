@@ -380,15 +380,22 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
 
 }  // namespace zgb
 
-extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8_t* const* q_src,
-                                              const float* const* scale_src, int32_t n_src,
-                                              int32_t block, float divisor, int32_t rank_begin,
-                                              int32_t rank_end, int64_t begin, int64_t end,
-                                              float* master, float* m, float* v, uint16_t* out_bf16,
-                                              int32_t out_mode, const zero_adamw_t* hp, void* stream) {
-    using namespace zgb;
+namespace zgb {
+
+// The update from 8-bit gradients, with a bf16 output (out_bf16, out_mode) or
+// the 8-bit output (q8: codes like the state, a scale per 256 elements).
+int qgrad_update(const zero_layout_t* L, const int8_t* const* q_src, const float* const* scale_src,
+                 int32_t n_src, int32_t block, float divisor, int32_t rank_begin, int32_t rank_end,
+                 int64_t begin, int64_t end, float* master, float* m, float* v, uint16_t* out_bf16,
+                 int32_t out_mode, int8_t* q_out, float* scales_out, const zero_adamw_t* hp,
+                 void* stream) {
     int rc = check_qsources(q_src, scale_src, n_src, block);
     if (rc) return rc;
+    if (q_out) {
+        if (!L || !scales_out) return ZERO_EINVAL;
+        if (L->shard % 256 != 0 || begin % 256 != 0 || end % 256 != 0) return ZERO_EINVAL;
+        if (check_aligned(scales_out, 4)) return ZERO_EALIGN;
+    }
     UpdateTarget t;
     if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode, &t)))
         return rc;
@@ -397,20 +404,58 @@ extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8
     if (end == begin) return ZERO_OK;
     if ((rc = check_qsource_ptrs(q_src, scale_src, n_src))) return rc;
     if ((rc = check_target_ptrs(t))) return rc;
+    if (q_out && (check_device_ptr(q_out) || check_device_ptr(scales_out))) return ZERO_EINVAL;
     base.dst = nullptr;
     base.first = 0;
+    base.out = nullptr;
     base.qout = nullptr;
     base.qoscale = nullptr;
+    const int64_t own_lo = (int64_t)rank_begin * L->shard;
     auto place = [&](QGradParams& p, int64_t lo) {
         const int64_t off = lo - begin;
         p.w = t.w + off;
         p.m = t.m + off;
         p.v = t.v + off;
-        p.out = t.out + off;
-        return aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.out);
+        bool ok = aligned16(p.w) && aligned16(p.m) && aligned16(p.v);
+        if (q_out) {
+            p.qout = q_out + (lo - own_lo);              // lo - own_lo is a multiple of 256
+            p.qoscale = scales_out + (lo - own_lo) / 256;
+            ok = ok && aligned16(p.qout);
+        } else {
+            p.out = t.out + off;
+            ok = ok && aligned16(p.out);
+        }
+        return ok;
     };
-    return qgrad_run<true, false>(L, q_src, scale_src, n_src, block, begin, end, base, place,
-                           static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return q_out ? qgrad_run<true, true>(L, q_src, scale_src, n_src, block, begin, end, base, place, s)
+                 : qgrad_run<true, false>(L, q_src, scale_src, n_src, block, begin, end, base, place, s);
+}
+
+}  // namespace zgb
+
+extern "C" int zero_reduce_scatter_adamw_int8(const zero_layout_t* L, const int8_t* const* q_src,
+                                              const float* const* scale_src, int32_t n_src,
+                                              int32_t block, float divisor, int32_t rank_begin,
+                                              int32_t rank_end, int64_t begin, int64_t end,
+                                              float* master, float* m, float* v, uint16_t* out_bf16,
+                                              int32_t out_mode, const zero_adamw_t* hp, void* stream) {
+    if (out_mode == zgb::ZERO_OUT_NONE) return ZERO_EINVAL;
+    return zgb::qgrad_update(L, q_src, scale_src, n_src, block, divisor, rank_begin, rank_end, begin,
+                             end, master, m, v, out_bf16, out_mode, nullptr, nullptr, hp, stream);
+}
+
+extern "C" int zero_reduce_scatter_adamw_int8_q8(const zero_layout_t* L, const int8_t* const* q_src,
+                                                 const float* const* scale_src, int32_t n_src,
+                                                 int32_t block, float divisor, int32_t rank_begin,
+                                                 int32_t rank_end, int64_t begin, int64_t end,
+                                                 float* master, float* m, float* v, int8_t* q_out,
+                                                 float* scales_out, int32_t out_block,
+                                                 const zero_adamw_t* hp, void* stream) {
+    if (!q_out || out_block != 256) return ZERO_EINVAL;
+    return zgb::qgrad_update(L, q_src, scale_src, n_src, block, divisor, rank_begin, rank_end, begin,
+                             end, master, m, v, nullptr, zgb::ZERO_OUT_NONE, q_out, scales_out, hp,
+                             stream);
 }
 
 extern "C" int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const* q_src,
@@ -444,43 +489,3 @@ extern "C" int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const*
                             static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int zero_reduce_scatter_adamw_int8_q8(const zero_layout_t* L, const int8_t* const* q_src,
-                                                 const float* const* scale_src, int32_t n_src,
-                                                 int32_t block, float divisor, int32_t rank_begin,
-                                                 int32_t rank_end, int64_t begin, int64_t end,
-                                                 float* master, float* m, float* v, int8_t* q_out,
-                                                 float* scales_out, int32_t out_block,
-                                                 const zero_adamw_t* hp, void* stream) {
-    using namespace zgb;
-    int rc = check_qsources(q_src, scale_src, n_src, block);
-    if (rc) return rc;
-    if (!L || !q_out || !scales_out) return ZERO_EINVAL;
-    if (out_block != 256) return ZERO_EINVAL;
-    if (L->shard % 256 != 0 || begin % 256 != 0 || end % 256 != 0) return ZERO_EINVAL;
-    if (check_aligned(scales_out, 4)) return ZERO_EALIGN;
-    UpdateTarget t;
-    if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, nullptr, ZERO_OUT_NONE, &t)))
-        return rc;
-    QGradParams base;
-    if ((rc = make_scalars(hp, divisor, &base.h))) return rc;
-    if (end == begin) return ZERO_OK;
-    if ((rc = check_qsource_ptrs(q_src, scale_src, n_src))) return rc;
-    if ((rc = check_target_ptrs(t))) return rc;
-    if (check_device_ptr(q_out) || check_device_ptr(scales_out)) return ZERO_EINVAL;
-    base.dst = nullptr;
-    base.first = 0;
-    base.out = nullptr;
-    const int64_t own_lo = (int64_t)rank_begin * L->shard;
-    auto place = [&](QGradParams& p, int64_t lo) {
-        const int64_t off = lo - begin;
-        p.w = t.w + off;
-        p.m = t.m + off;
-        p.v = t.v + off;
-        p.out = nullptr;
-        p.qout = q_out + (lo - own_lo);                  // lo - own_lo is a multiple of 256
-        p.qoscale = scales_out + (lo - own_lo) / 256;
-        return aligned16(p.w) && aligned16(p.m) && aligned16(p.v) && aligned16(p.qout);
-    };
-    return qgrad_run<true, true>(L, q_src, scale_src, n_src, block, begin, end, base, place,
-                                 static_cast<cudaStream_t>(stream));
-}
