@@ -204,3 +204,43 @@ def test_grad_norm_extreme_values(zlib, cuda_device):
     zb.zero_grad_norm_sq(L, [torch.from_numpy(t[0].copy()).cuda()], zb.ZERO_F32, 0, 1.0, 0, 4096,
                          bufs.workspace, bufs.norm_sq, False)
     assert float(bufs.norm_sq.item()) == pytest.approx(oracle.grad_norm_sq(t, 1.0), rel=1e-12)
+
+
+@pytest.mark.parametrize("std,max_norm", [(1.0, 1.0), (1e-3, 1.0)])
+def test_zero3_clipped_units(zlib, cuda_device, std, max_norm):
+    """Stage 3 with clipping: every unit's gradient is reduce-scattered into
+    fp32, the squared norm of the mean gradient accumulates over all units on
+    the device, then every unit updates with the clipped gradient (ragged units,
+    n_dp = 7; active clipping at std 1, coefficient 1 at std 1e-3)."""
+    zb = zlib
+    n_dp = 7
+    units, As, gs, refs = [], [], [], []
+    for i, numels in enumerate([[1], [4097], [33_031], [1000, 24, 3, 5000]]):
+        L = zb.zero_layout(numels, n_dp)
+        P = L.padded_n
+        w = inputs.master_weights(L.n, P, seed=800 + i).cuda()
+        u = zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w,
+                            torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda"))
+        g = inputs.grads_bf16(n_dp, L.n, P, seed=900 + i, step=1, std=std)
+        A = torch.empty(P, device="cuda")
+        zstep.zero3_layer_reduce_scatter(u, [g[r].cuda() for r in range(n_dp)], A)
+        units.append(u)
+        As.append(A)
+        gs.append(g)
+        refs.append(parity.f32(w))
+    bufs = zstep.NormBuffers("cuda")
+    zstep.zero3_clipped_updates(units, As, _hp(zb, 1), max_norm, bufs)
+    torch.cuda.synchronize()
+    A_refs = [oracle.accumulate_reduce(None, parity.bits(g), True) for g in gs]
+    nsq_ref = sum(oracle.grad_norm_sq(A[None, :], n_dp) for A in A_refs)
+    gpu_nsq = float(bufs.norm_sq.item())
+    assert gpu_nsq == pytest.approx(nsq_ref, rel=1e-12)
+    coef = oracle.clip_coef(nsq_ref, max_norm)
+    assert oracle.clip_coef(gpu_nsq, max_norm) == coef
+    assert (coef < 1.0) == (std == 1.0)
+    for u, A_ref, w0 in zip(units, A_refs, refs):
+        z = np.zeros(A_ref.size, np.float32)
+        out_ref, *st = oracle.rs_adamw_reference(A_ref[None, :], n_dp, w0, z, z, HP, 1,
+                                                 clip=(nsq_ref, max_norm))
+        parity.assert_state([u.master, u.m, u.v], st)
+        assert np.array_equal(parity.bits(u.shards).reshape(-1), out_ref)

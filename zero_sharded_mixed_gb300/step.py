@@ -221,6 +221,24 @@ def zero3_update(unit: Zero3Unit, A: torch.Tensor, hp, n_micro: int = 1, stream=
                                  unit.shards.view(-1), zb.ZERO_OUT_SHARD, hp, stream)
 
 
+def zero3_clipped_updates(units, grads_fp32, hp, max_norm: float, bufs: "NormBuffers",
+                          n_micro: int = 1, stream=None):
+    """Stage 3 with clipping by the global gradient norm: the norm covers every
+    unit's reduced gradient, so the updates wait for the whole backward.
+    grads_fp32[i] is unit i's fp32 owned-shard sums (zero3_layer_reduce_scatter);
+    the squared norm of the mean gradient accumulates over the units on the
+    device, then every unit updates with the clipped gradient."""
+    for j, (u, A) in enumerate(zip(units, grads_fp32)):
+        L = u.layout
+        zb.zero_grad_norm_sq(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.padded_n,
+                             bufs.workspace, bufs.norm_sq, j > 0, stream)
+    for u, A in zip(units, grads_fp32):
+        L = u.layout
+        zb.zero_reduce_scatter_adamw_clip(L, [A], zb.ZERO_F32, 0, float(L.n_dp * n_micro), 0, L.n_dp,
+                                          0, L.padded_n, u.master, u.m, u.v, u.shards.view(-1),
+                                          zb.ZERO_OUT_SHARD, hp, bufs.norm_sq, max_norm, stream)
+
+
 def zero3_reduce_scatter_update(unit: Zero3Unit, layer_grads, hp, stream=None):
     """The layer reduce-scatter and the update of the unit's owned shards in one
     pass, with bf16 into each rank's own shard.  Valid when the step has one
