@@ -100,3 +100,40 @@ def test_save_consolidate_reshard(zlib, tmp_path):
     # and a layout mismatch is refused
     with pytest.raises(ValueError):
         ck.restore(str(tmp_path / "b"), L, *got)
+
+
+def test_stage3_units_save_consolidate_reshard_restore(zlib, tmp_path):
+    """Stage-3 units, each its own layout: one checkpoint per unit; the
+    consolidated model state is every unit's real elements in order; resharding
+    to another rank count keeps it; a restore gives back every element."""
+    from zero_sharded_mixed_gb300.step import Zero3Unit
+    n_dp = 5
+    numels_per_unit = [[1], [4097], [1000, 24, 3, 5000]]
+    units = []
+    for i, numels in enumerate(numels_per_unit):
+        L = zb.zero_layout(numels, n_dp)
+        master, m, v = _state(L.padded_n, 10 + i)
+        for t in (master, m, v):
+            t[L.n:] = 0
+        shards = master.to(torch.bfloat16).view(n_dp, L.shard)
+        units.append(Zero3Unit(L, shards, master, m, v))
+    hp = zb.ZeroAdamW.make(step=3)
+    ck.save_units(str(tmp_path / "u"), units, numels_per_unit, 3, hp, with_bf16=True)
+    flat = ck.consolidate_units(str(tmp_path / "u"))
+    assert flat["step"] == 3
+    for k in ("master", "m", "v"):
+        want = np.concatenate([getattr(u, k)[:u.layout.n].numpy() for u in units])
+        np.testing.assert_array_equal(flat[k], want)
+    ck.reshard_units(str(tmp_path / "u"), str(tmp_path / "u3"), 3, align=1)
+    again = ck.consolidate_units(str(tmp_path / "u3"))
+    for k in ("master", "m", "v"):
+        np.testing.assert_array_equal(again[k], flat[k])
+    fresh = [Zero3Unit(u.layout, torch.zeros_like(u.shards), torch.empty_like(u.master),
+                       torch.empty_like(u.m), torch.empty_like(u.v)) for u in units]
+    assert ck.restore_units(str(tmp_path / "u"), fresh, with_bf16=True) == 3
+    for a, b in zip(fresh, units):
+        for k in ("master", "m", "v"):
+            assert torch.equal(getattr(a, k), getattr(b, k))
+        assert torch.equal(a.shards.view(torch.int16), b.shards.view(torch.int16))
+    with pytest.raises(ValueError):
+        ck.restore_units(str(tmp_path / "u"), fresh[:2])

@@ -187,3 +187,69 @@ def reshard(dir_in, dir_out, n_dp: int, align: int | None = None, bucket: int | 
                            max(1, meta["step"]))
     return save(dir_out, L, numels, *(torch.from_numpy(padded[k]) for k in ("master", "m", "v")),
                 meta["step"], hp)
+
+
+# --------------------------------------------------------------------------
+# stage 3: one checkpoint per unit ("ZeRO and FSDP", "FSDP, ZeRO-3 inside
+# PyTorch": every unit is flattened, padded and sharded on its own)
+# --------------------------------------------------------------------------
+
+UNITS = "units.json"
+
+
+def _unit_dir(dirpath, i: int) -> str:
+    return os.path.join(dirpath, f"unit_{i:05d}")
+
+
+def save_units(dirpath, units, numels_per_unit, step: int, hp: zb.ZeroAdamW, with_bf16: bool = False):
+    """Save every stage-3 unit (step.Zero3Unit: its layout, fp32 master / m / v
+    over all owners, and the owners' bf16 shards) as its own sharded
+    checkpoint in unit_00000/, unit_00001/, ...; units.json lists them."""
+    os.makedirs(dirpath, exist_ok=True)
+    for i, (u, numels) in enumerate(zip(units, numels_per_unit)):
+        save(_unit_dir(dirpath, i), u.layout, numels, u.master, u.m, u.v, step, hp,
+             out_bf16=u.shards.reshape(-1) if with_bf16 else None)
+    with open(os.path.join(dirpath, UNITS), "w") as f:
+        json.dump({"format": FORMAT, "units": len(units), "step": int(step)}, f, indent=1)
+
+
+def _n_units(dirpath) -> int:
+    with open(os.path.join(dirpath, UNITS)) as f:
+        meta = json.load(f)
+    if meta.get("format") != FORMAT:
+        raise ValueError(f"{dirpath}: not a {FORMAT}")
+    return int(meta["units"])
+
+
+def restore_units(dirpath, units, with_bf16: bool = False) -> int:
+    """Load every unit's shards back (the layouts must match); returns the step."""
+    n = _n_units(dirpath)
+    if n != len(units):
+        raise ValueError(f"the checkpoint holds {n} units, not {len(units)}")
+    steps = {restore(_unit_dir(dirpath, i), u.layout, u.master, u.m, u.v,
+                     out_bf16=u.shards.reshape(-1) if with_bf16 else None)
+             for i, u in enumerate(units)}
+    if len(steps) != 1:
+        raise ValueError("the units were saved at different steps")
+    return steps.pop()
+
+
+def consolidate_units(dirpath):
+    """The plain full-precision state of the whole model: every unit's real
+    elements (padding dropped), units in order, as flat fp32 vectors."""
+    parts = [consolidate(_unit_dir(dirpath, i)) for i in range(_n_units(dirpath))]
+    out = {k: np.concatenate([p[k] for p in parts]) if parts else np.empty(0, np.float32)
+           for k in ("master", "m", "v")}
+    out["step"] = parts[0]["step"] if parts else 0
+    return out
+
+
+def reshard_units(dir_in, dir_out, n_dp: int, align: int | None = None):
+    """Every unit laid out for another number of ranks."""
+    n = _n_units(dir_in)
+    for i in range(n):
+        reshard(_unit_dir(dir_in, i), _unit_dir(dir_out, i), n_dp, align)
+    with open(os.path.join(dir_in, UNITS)) as f:
+        meta = json.load(f)
+    with open(os.path.join(dir_out, UNITS), "w") as f:
+        json.dump(meta, f, indent=1)
