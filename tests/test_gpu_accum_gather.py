@@ -256,3 +256,40 @@ def test_zero3_fused_reduce_scatter_update_equals_the_pair(zlib, cuda_device):
                          (units[0].v, units[1].v)):
                 parity.assert_bit_exact_f32(a, parity.f32(b))
             assert torch.equal(units[0].shards.view(torch.int16), units[1].shards.view(torch.int16))
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16-gradients", "8-bit-gradients"])
+def test_zero3_units_with_gradient_accumulation(zlib, cuda_device, int8):
+    """Stage 3 with K = 3 micro-batches: each unit's layer reduce-scatter adds
+    into its fp32 buffer (the first overwrites), and the update divides by
+    n_dp * K -- bf16 gradients, or 8-bit gradients through the dequantizing
+    reduce-scatter -- against the oracle on ragged units at n_dp = 5."""
+    zb = zlib
+    n_dp, K, block = 5, 3, 256
+    for i, numels in enumerate([[7], [4097], [1000, 24, 3, 5000]]):
+        L = zb.zero_layout(numels, n_dp)
+        P = L.padded_n
+        w = inputs.master_weights(L.n, P, seed=1100 + i).cuda()
+        unit = zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w,
+                               torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda"))
+        w0 = parity.f32(w)
+        A = torch.empty(P, device="cuda")
+        A_ref = None
+        for k in range(K):
+            g = inputs.grads_bf16(n_dp, L.n, P, seed=1200 + i, step=1, micro=k)
+            if int8:
+                qg = zstep.Int8Grads(L, n_dp, block)
+                qg.quantize([g[r].cuda() for r in range(n_dp)])
+                zstep.zero3_layer_reduce_scatter_int8(unit, qg, A, first=(k == 0))
+                q_ref, s_ref = oracle.quantize_grad_int8(parity.bits(g), n_dp, block)
+                A_ref = oracle.accumulate_reduce_int8(A_ref, q_ref, s_ref, n_dp, block, k == 0)
+            else:
+                zstep.zero3_layer_reduce_scatter(unit, [g[r].cuda() for r in range(n_dp)], A, first=(k == 0))
+                A_ref = oracle.accumulate_reduce(A_ref, parity.bits(g), first=(k == 0))
+        zstep.zero3_update(unit, A, _hp(zb, 1), n_micro=K)
+        torch.cuda.synchronize()
+        parity.assert_bit_exact_f32(A, A_ref)
+        z = np.zeros(P, np.float32)
+        out_ref, *st = oracle.rs_adamw_reference(A_ref[None, :], n_dp * K, w0, z, z, HP, 1)
+        parity.assert_state([unit.master, unit.m, unit.v], st, what=f"unit {i} ")
+        assert np.array_equal(parity.bits(unit.shards).reshape(-1), out_ref)
