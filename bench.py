@@ -814,9 +814,15 @@ def run_ours(args):
     dist = dist_init(world, local)
     from zero_sharded_mixed_gb300 import binding as zb
     from zero_sharded_mixed_gb300 import build as zbuild
-    if rank == 0 or not os.path.exists(zb.lib_path):
-        zbuild.build()
-    barrier(dist)
+    # one builder per node (ranks share the tree); every rank learns whether it worked
+    err = None
+    if local == 0:
+        try:
+            zbuild.build()
+        except Exception as e:        # reported on every rank below
+            err = e
+    if not all_ranks_agree(dist, err is None, device):
+        raise RuntimeError("building libzero_gb300.so failed on a node's first rank") from err
     zb.load()
 
     peak, peak_kind = _peak()
