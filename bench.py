@@ -199,10 +199,16 @@ def _peak():
 
 
 def _kernel_source_hash():
+    """Hash of the fused update's code: its sources with // comments and blank
+    lines removed, so that an edit of a comment keeps a traffic record valid."""
+    import re
     h = hashlib.sha256()
-    for name in ("zero_rs_adamw.cu", "zero_common.cuh", "zero_update.cuh"):
-        with open(os.path.join(ROOT, "zero_sharded_mixed_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    for name in ("zero_rs_adamw.cu", "zero_common.cuh", "zero_update.cuh", "zero_quant.cuh"):
+        with open(os.path.join(ROOT, "zero_sharded_mixed_gb300", "csrc", name)) as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -8,12 +8,15 @@
 // owned element the owner reads the n_src codes (1 byte each) and their block
 // scales, forms g_r = code * scale (one fp32 rounding), sums over ranks in
 // ascending order from +0, and then
-//   zero_reduce_scatter_adamw_int8  divides once, AdamW, bf16 cast, gather write
-//                                   (what zero_reduce_scatter_adamw does with
-//                                   the sum of bf16 gradients);
-//   zero_accumulate_int8            adds the sum into an fp32 buffer (the
-//                                   stage-3 layer reduce-scatter, or stage-2
-//                                   accumulation).
+//   zero_reduce_scatter_adamw_int8     divides once, AdamW, bf16 cast, gather
+//                                      write (what zero_reduce_scatter_adamw
+//                                      does with the sum of bf16 gradients);
+//   zero_reduce_scatter_adamw_int8_q8  the same with the owners' shards written
+//                                      in the 8-bit block format instead of
+//                                      bf16 (both ZeRO++ paths in one pass);
+//   zero_accumulate_int8               adds the sum into an fp32 buffer (the
+//                                      stage-3 layer reduce-scatter, or stage-2
+//                                      accumulation).
 // Bytes per element: n_src * (1 + 4/block) + 26 for the update, + 4 (+ 4 when
 // adding) for the accumulation -- against 2 * n_src bytes of bf16 gradients.
 //

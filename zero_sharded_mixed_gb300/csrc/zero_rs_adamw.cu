@@ -21,12 +21,17 @@
 // (zero_accumulate, then the update), in the same order, so their results are
 // bit-identical to it while skipping one fp32 write and re-read per element.
 //
+// The output is the bf16 weights, or (zero_reduce_scatter_adamw_q8, kQ8) the
+// same weights in the 8-bit block format: a warp's 256 consecutive elements are
+// one quantization block, quantized in the epilogue.
+//
 // Design: a bandwidth-bound stream.  Each thread owns 8 consecutive elements
 // per vector: one 128-bit load per bf16 source, two per fp32 array, the same
 // stores, and one 128-bit bf16 store.  All loads of an iteration are issued
 // before any arithmetic; when a vector has few loads, a thread takes two
-// vectors per iteration.  Loads and stores are evict-first.  A grid-stride loop
-// with the grid sized to the CTAs resident at once.
+// vectors per iteration.  Loads and stores are evict-first.  The grid is a
+// measured number of resident waves (rs_waves), each CTA over one contiguous
+// chunk of vectors, the consecutive vectors of a chunk on consecutive lanes.
 //
 // Arithmetic: every fp32 operation is an explicit IEEE round-to-nearest
 // intrinsic, so nothing is fused into an FMA: the sum runs over ranks in
