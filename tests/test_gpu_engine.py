@@ -1,0 +1,139 @@
+"""The configuration-driven engines against the oracle: every branch the
+engines choose (fused, accumulating, clipped, 8-bit) gives the oracle's step."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from zero_sharded_mixed_gb300 import inputs
+from zero_sharded_mixed_gb300.config import ZeroConfig
+from zero_sharded_mixed_gb300.engine import Zero3Engine, ZeroEngine
+
+pytestmark = pytest.mark.gpu
+
+HP = oracle.AdamW(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+def _cfg(**kw):
+    base = {"gradient_accumulation_steps": kw.pop("K", 1), "gradient_clipping": kw.pop("clip", 0.0),
+            "optimizer": {"type": "AdamW", "params": {"lr": HP.lr, "betas": [HP.beta1, HP.beta2],
+                                                      "eps": HP.eps, "weight_decay": HP.weight_decay}},
+            "zero_optimization": {"stage": kw.pop("stage"), "reduce_bucket_size": kw.pop("bucket", 30_000),
+                                  "zero_quantized_weights": kw.pop("qw", False),
+                                  "zero_quantized_gradients": kw.pop("qg", False)}}
+    assert not kw
+    return ZeroConfig.from_dict(base)
+
+
+def _oracle_step(rows_per_micro, n_dp, state, t, clip, qg, stage):
+    """The oracle's step for K micro-batches of bf16 rows: the accumulation
+    order of the stage, the optional 8-bit gradients, clipping, the update."""
+    K = len(rows_per_micro)
+    if qg:
+        A = None
+        for k, rows in enumerate(rows_per_micro):
+            q, s = oracle.quantize_grad_int8(rows, n_dp, 256)
+            A = oracle.accumulate_reduce_int8(A, q, s, n_dp, 256, k == 0)
+        src = A[None, :]
+    elif stage == 1:
+        acc = [None] * n_dp
+        for k, rows in enumerate(rows_per_micro):
+            acc = [oracle.accumulate_local(acc[r], rows[r], k == 0) for r in range(n_dp)]
+        src = np.stack(acc)
+    else:
+        A = None
+        for k, rows in enumerate(rows_per_micro):
+            A = oracle.accumulate_reduce(A, rows, k == 0)
+        src = A[None, :]
+    if K == 1 and not qg:
+        src = rows_per_micro[0]
+    clip_arg = None
+    if clip:
+        clip_arg = (oracle.grad_norm_sq(src, n_dp * K), clip)
+    return oracle.rs_adamw_reference(src, n_dp * K, *state, HP, t, clip=clip_arg)
+
+
+@pytest.mark.parametrize("stage,K,clip,qg", [
+    (2, 1, 0.0, False), (1, 3, 0.0, False), (2, 3, 0.0, False), (1, 1, 1.0, False),
+    (2, 3, 1.0, False), (1, 3, 1.0, False), (2, 1, 0.0, True), (2, 2, 0.0, True), (1, 1, 0.5, True),
+])
+def test_zero12_engine(zlib, cuda_device, stage, K, clip, qg):
+    n_dp, N = 4, 100_003
+    eng = ZeroEngine([N], n_dp, _cfg(stage=stage, K=K, clip=clip, qg=qg),
+                     master=inputs.master_weights(N, 100_032, seed=1).cuda())
+    P = eng.L.padded_n
+    state = [parity.f32(eng.master), np.zeros(P, np.float32), np.zeros(P, np.float32)]
+    std = 1.0 if clip else 1e-3
+    for t in (1, 2):
+        micro = []
+        for k in range(K):
+            g = inputs.grads_bf16(n_dp, N, P, seed=t, step=t, micro=k, std=std)
+            micro.append(parity.bits(g))
+            eng.backward(g.cuda())
+        eng.step()
+        torch.cuda.synchronize()
+        out_ref, *state = _oracle_step(micro, n_dp, state, t, clip, qg, stage)
+        parity.assert_state([eng.master, eng.m, eng.v], state, exact=not clip, what=f"t={t} ")
+        if clip:
+            parity.assert_bf16_close(eng.weights, out_ref)
+        else:
+            assert np.array_equal(parity.bits(eng.weights), out_ref)
+    with pytest.raises(RuntimeError):
+        eng.step()                                           # no micro-batch given
+
+
+@pytest.mark.parametrize("K,clip,qw,qg", [
+    (1, 0.0, False, False), (1, 0.0, True, False), (1, 0.0, False, True), (1, 0.0, True, True),
+    (2, 0.0, False, False), (2, 0.0, True, True), (1, 1.0, True, False), (2, 1.0, False, False),
+])
+def test_zero3_engine(zlib, cuda_device, K, clip, qw, qg):
+    n_dp = 5
+    units = [[4097], [33_031], [1000, 24, 3, 5000]]
+    eng = Zero3Engine(units, n_dp, _cfg(stage=3, K=K, clip=clip, qw=qw, qg=qg))
+    for i, u in enumerate(eng.units):                        # start from seeded weights
+        u.master.copy_(inputs.master_weights(u.layout.n, u.layout.padded_n, seed=10 + i).cuda())
+    std = 1.0 if clip else 1e-3
+    states = [[parity.f32(u.master), np.zeros(u.layout.padded_n, np.float32),
+               np.zeros(u.layout.padded_n, np.float32)] for u in eng.units]
+    micro_rows = [[] for _ in eng.units]
+    for k in range(K):
+        for i in reversed(range(len(eng.units))):            # backward order
+            u = eng.units[i]
+            buf = eng.gather(i)
+            assert buf.numel() == u.layout.padded_n
+            eng.release(i)
+            g = inputs.grads_bf16(n_dp, u.layout.n, u.layout.padded_n, seed=20 + i, step=1, micro=k, std=std)
+            micro_rows[i].append(parity.bits(g))
+            eng.backward(i, g.cuda(), micro=k)
+    eng.step()
+    torch.cuda.synchronize()
+    # the oracle: per unit the reduced gradient, the global norm over all units, the update
+    srcs = []
+    for i in range(len(eng.units)):
+        if qg:
+            A = None
+            for k, rows in enumerate(micro_rows[i]):
+                q, s = oracle.quantize_grad_int8(rows, n_dp, 256)
+                A = oracle.accumulate_reduce_int8(A, q, s, n_dp, 256, k == 0)
+        else:
+            A = None
+            for k, rows in enumerate(micro_rows[i]):
+                A = oracle.accumulate_reduce(A, rows, k == 0)
+        srcs.append(A[None, :])
+    clip_arg = None
+    if clip:
+        clip_arg = (sum(oracle.grad_norm_sq(s, n_dp * K) for s in srcs), clip)
+    for i, u in enumerate(eng.units):
+        out_ref, *st = oracle.rs_adamw_reference(srcs[i], n_dp * K, *states[i], HP, 1, clip=clip_arg)
+        parity.assert_state([u.master, u.m, u.v], st, what=f"unit {i} ")
+        S = u.layout.shard
+        if qw:
+            q = eng.q8[i]
+            for o in range(n_dp):
+                qo, so = oracle.quantize_int8(out_ref[o * S:(o + 1) * S], 256)
+                assert np.array_equal(q.q[o].cpu().numpy(), qo)
+                assert np.array_equal(q.scales[o, :q.nb].cpu().numpy(), so)
+        else:
+            assert np.array_equal(parity.bits(u.shards).reshape(-1), out_ref)
+    assert eng.ring.resident == 0 and eng.ring.peak <= 2

@@ -23,8 +23,17 @@ _BINDING_NAMES = {
 }
 
 
+_ENGINE_NAMES = {"ZeroEngine", "Zero3Engine"}
+
+
 def __getattr__(name):
     if name in _BINDING_NAMES:
         from . import binding
         return getattr(binding, name)
+    if name in _ENGINE_NAMES:
+        from . import engine
+        return getattr(engine, name)
+    if name == "ZeroConfig":
+        from .config import ZeroConfig
+        return ZeroConfig
     raise AttributeError(name)

@@ -1,0 +1,80 @@
+"""The subset of a DeepSpeed configuration that the ZeRO step reads.
+
+"DeepSpeed ZeRO", "The configuration file" and "ZeRO Optimizer, in depth",
+"Running it with DeepSpeed": a JSON configuration names the ZeRO stage, the
+reduce bucket size, the number of gradient-accumulation steps, the clipping
+threshold, the optimizer (AdamW with lr, betas, eps, weight_decay) and the
+precision (bf16); "Offload and ZeRO++" adds zero_quantized_weights and
+zero_quantized_gradients.  ``ZeroConfig.from_dict`` reads those keys, refuses
+what this build does not do (fp16 loss scaling, offload, another optimizer),
+and lists the keys it did not use instead of failing on them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+_USED_TOP = {"zero_optimization", "optimizer", "gradient_accumulation_steps", "gradient_clipping",
+             "bf16", "fp16"}
+_USED_ZERO = {"stage", "reduce_bucket_size", "zero_quantized_weights", "zero_quantized_gradients",
+              "offload_optimizer", "offload_param"}
+
+
+@dataclass
+class ZeroConfig:
+    stage: int = 2
+    reduce_bucket_size: int = 500_000_000
+    gradient_accumulation_steps: int = 1
+    gradient_clipping: float = 0.0            # 0: no clipping
+    lr: float = 1e-4
+    betas: tuple = (0.9, 0.999)
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    zero_quantized_weights: bool = False      # stage 3: 8-bit weight gathers
+    zero_quantized_gradients: bool = False    # 8-bit gradient reduce-scatter
+    quant_block: int = 256
+    ignored: list = field(default_factory=list)
+
+    def __post_init__(self):
+        if self.stage not in (1, 2, 3):
+            raise ValueError(f"zero_optimization.stage must be 1, 2 or 3, got {self.stage!r}")
+        if self.reduce_bucket_size < 1:
+            raise ValueError("reduce_bucket_size must be positive")
+        if self.gradient_accumulation_steps < 1:
+            raise ValueError("gradient_accumulation_steps must be at least 1")
+        if self.gradient_clipping < 0:
+            raise ValueError("gradient_clipping must be 0 (off) or positive")
+        if self.zero_quantized_weights and self.stage != 3:
+            raise ValueError("zero_quantized_weights applies to stage 3 (the weight all-gather)")
+        if not (0.0 <= self.betas[0] < 1.0 and 0.0 <= self.betas[1] < 1.0):
+            raise ValueError(f"betas must lie in [0, 1), got {self.betas!r}")
+
+    @classmethod
+    def from_dict(cls, cfg: dict) -> "ZeroConfig":
+        zo = dict(cfg.get("zero_optimization", {}))
+        for key in ("offload_optimizer", "offload_param"):
+            dev = (zo.get(key) or {}).get("device", "none")
+            if dev not in ("none", None):
+                raise ValueError(f"zero_optimization.{key} to {dev!r}: offload is not part of this build")
+        if (cfg.get("fp16") or {}).get("enabled", False):
+            raise ValueError("fp16 with loss scaling is not part of this build: use bf16")
+        if not (cfg.get("bf16") or {"enabled": True}).get("enabled", True):
+            raise ValueError("this build keeps weights and gradients in bf16: bf16.enabled must be true")
+        opt = cfg.get("optimizer") or {"type": "AdamW", "params": {}}
+        if str(opt.get("type", "AdamW")).lower() != "adamw":
+            raise ValueError(f"optimizer {opt.get('type')!r}: this build implements AdamW")
+        p = opt.get("params", {})
+        ignored = sorted([k for k in cfg if k not in _USED_TOP] +
+                         [f"zero_optimization.{k}" for k in zo if k not in _USED_ZERO])
+        return cls(
+            stage=int(zo.get("stage", 2)),
+            reduce_bucket_size=int(float(zo.get("reduce_bucket_size", 5e8))),
+            gradient_accumulation_steps=int(cfg.get("gradient_accumulation_steps", 1)),
+            gradient_clipping=float(cfg.get("gradient_clipping", 0.0)),
+            lr=float(p.get("lr", 1e-4)),
+            betas=tuple(float(b) for b in p.get("betas", (0.9, 0.999))),
+            eps=float(p.get("eps", 1e-8)),
+            weight_decay=float(p.get("weight_decay", 0.0)),
+            zero_quantized_weights=bool(zo.get("zero_quantized_weights", False)),
+            zero_quantized_gradients=bool(zo.get("zero_quantized_gradients", False)),
+            ignored=ignored,
+        )
