@@ -92,7 +92,10 @@ void oracle_cast_bf16(const float* x, uint16_t* y, int64_t n)
 /* Layout: flatten, pad, shard, bucket                                       */
 /* ------------------------------------------------------------------------ */
 
-/* out[0] = N (real elements), out[1] = S (shard length), out[2] = P = n_dp*S
+/* "ZeRO and FSDP", "The idea, one stage at a time": all parameters are
+ * flattened into one vector cut into n_dp equal contiguous shards, rank r
+ * owning shard r (equal shards with tail padding: the reading taken above).
+ * out[0] = N (real elements), out[1] = S (shard length), out[2] = P = n_dp*S
  * (padded length), out[3] = bucket length rounded up to a multiple of a,
  * out[4] = number of buckets covering [0, P).  offsets (may be NULL) receives
  * each tensor's start in the flat vector: the tensors are laid end to end in
@@ -136,7 +139,10 @@ int oracle_layout(const int64_t* numel, int32_t n_tensors, int32_t n_dp,
 /* Reduce-scatter as a mean                                                  */
 /* ------------------------------------------------------------------------ */
 
-/* g[i] = (sum over r = 0..n_src-1 of src[r*ld + i]) / divisor, fp32, ranks in
+/* "ZeRO and FSDP", "The idea, one stage at a time" (stage 1: rank r receives
+ * the average over ranks of shard r of the gradients) and exercise "A sharded
+ * Adam step", step (1).
+ * g[i] = (sum over r = 0..n_src-1 of src[r*ld + i]) / divisor, fp32, ranks in
  * ascending order.  src rows are bf16 bit patterns. */
 void oracle_reduce_mean_bf16(const uint16_t* src, int32_t n_src, int64_t ld, int64_t n,
                              float divisor, float* g)
@@ -163,13 +169,19 @@ void oracle_reduce_mean_f32(const float* src, int32_t n_src, int64_t ld, int64_t
 /* AdamW on one shard                                                        */
 /* ------------------------------------------------------------------------ */
 
+/* "ZeRO and FSDP", exercise "A sharded Adam step", step (2): the bias
+ * corrections 1 - beta1^t and 1 - beta2^t at step t >= 1 (fp64 from the fp32
+ * betas, rounded once to fp32: the reading taken above). */
 void oracle_bias_corrections(float b1, float b2, int64_t t, float* bc1, float* bc2)
 {
     *bc1 = (float)(1.0 - pow((double)b1, (double)t));
     *bc2 = (float)(1.0 - pow((double)b2, (double)t));
 }
 
-/* One AdamW step at step t (t >= 1) on n elements, in place on w, m, v. */
+/* One AdamW step at step t (t >= 1) on n elements, in place on w, m, v:
+ * Adam as in "ZeRO and FSDP", exercise "A sharded Adam step", step (2), with
+ * the decoupled weight decay of the "AdamW" optimizer blocks ("DeepSpeed
+ * ZeRO", "The configuration file"). */
 void oracle_adamw(float* w, float* m, float* v, const float* g, int64_t n,
                   float lr, float b1, float b2, float eps, float wd, int64_t t)
 {
@@ -203,8 +215,9 @@ void oracle_adamw(float* w, float* m, float* v, const float* g, int64_t n,
  * full_w:  n_copies rows of P bf16; after the all-gather every rank holds the
  *          full bf16 weights, so every row is written with the same vector
  *          (n_copies = n_dp reproduces every rank's copy; 1 keeps one).
- * Steps: (1) reduce-scatter: rank o receives the mean over ranks of shard o;
- * (2) AdamW on rank o's own shard only; (3) cast to bf16 and all-gather. */
+ * Steps ("ZeRO and FSDP", exercise "A sharded Adam step"): (1) reduce-scatter:
+ * rank o receives the mean over ranks of shard o; (2) AdamW on rank o's own
+ * shard only; (3) cast to bf16 and all-gather. */
 int oracle_zero_step(const uint16_t* grads, int32_t n_dp, int64_t shard,
                      float* w, float* m, float* v, uint16_t* full_w, int32_t n_copies,
                      float lr, float b1, float b2, float eps, float wd, int64_t t)
@@ -231,7 +244,10 @@ int oracle_zero_step(const uint16_t* grads, int32_t n_dp, int64_t shard,
     return 0;
 }
 
-/* Plain data parallelism, for the invariant that a ZeRO-1/2 step equals it:
+/* Plain data parallelism ("ZeRO and FSDP", "The idea, one stage at a time":
+ * stages 1 and 2 compute exactly what data parallelism computes, a ring
+ * all-reduce being a reduce-scatter followed by an all-gather), for the
+ * invariant that a ZeRO-1/2 step equals it:
  * all-reduce the gradients as a mean (same order), then every rank runs the
  * full AdamW step on its own full copy of the state (n_dp rows of P fp32) and
  * casts its full weights (n_dp rows of P bf16). */
@@ -256,7 +272,9 @@ int oracle_dp_step(const uint16_t* grads, int32_t n_dp, int64_t padded,
 /* Gradient accumulation                                                     */
 /* ------------------------------------------------------------------------ */
 
-/* Stage 1: a rank adds one micro-batch's full local bf16 gradient into its
+/* "ZeRO and FSDP", "The idea, one stage at a time", paragraph on gradient
+ * accumulation.
+ * Stage 1: a rank adds one micro-batch's full local bf16 gradient into its
  * full fp32 buffer (first = 1 starts the buffer with this micro-batch). */
 void oracle_accumulate_local(float* acc, const uint16_t* g, int64_t n, int32_t first)
 {
@@ -283,7 +301,9 @@ void oracle_accumulate_reduce(float* acc, const uint16_t* src, int32_t n_src, in
 /* All-gather (stage 3 per-unit gather, and the stage-1/2 weight gather)      */
 /* ------------------------------------------------------------------------ */
 
-/* full[o*S + i] = shards[o*S + i]: the concatenation of the n_dp shards. */
+/* "ZeRO and FSDP", stage 1's all-gather and "FSDP, ZeRO-3 inside PyTorch"
+ * (gathering a unit is one all-gather of its flat buffer):
+ * full[o*S + i] = shards[o*S + i], the concatenation of the n_dp shards. */
 void oracle_all_gather_bf16(const uint16_t* shards, int32_t n_dp, int64_t shard, uint16_t* full)
 {
     for (int32_t o = 0; o < n_dp; ++o)
