@@ -67,7 +67,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
                                            "probe", "accum-zero1", "accum-zero2", "zero3",
                                            "zero3-int8", "zero3-prefetch", "zero3-zeropp",
-                                           "zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused"],
+                                           "zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused",
+                                           "zero3-fused-graph"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -227,11 +228,12 @@ def _traffic_per_elem(n_src):
 
 
 class Op:
-    """One timed launch of a step: kernel kind, algorithmic bytes, the call."""
-    __slots__ = ("kind", "bytes", "fn")
+    """One timed call of a step: kernel kind, algorithmic bytes, the call, and
+    how many of the library's kernels the call launches."""
+    __slots__ = ("kind", "bytes", "fn", "kernels")
 
-    def __init__(self, kind, nbytes, fn):
-        self.kind, self.bytes, self.fn = kind, nbytes, fn
+    def __init__(self, kind, nbytes, fn, kernels=1):
+        self.kind, self.bytes, self.fn, self.kernels = kind, nbytes, fn, kernels
 
 
 class Workload:
@@ -256,6 +258,12 @@ class Workload:
             if k not in ("zb", "device", "desc", "elems", "device_bytes", "name", "bytes_per_elem",
                          "dominant"):
                 setattr(self, k, None)
+
+
+def _owners(L, begin, end):
+    """Owners whose shards [begin, end) overlaps: the 8-bit gradient kernels
+    launch once per owner."""
+    return (end - 1) // L.shard - begin // L.shard + 1 if end > begin else 0
 
 
 def _master(n_real, n, device):
@@ -357,7 +365,8 @@ class Zero2Workload(Workload):
                     zb.zero_reduce_scatter_adamw_int8(self.L, qs, ss, QGRAD_BLOCK, float(n_dp), 0,
                                                       n_dp, s, e, self.master, self.m, self.v,
                                                       self.out, zb.ZERO_OUT_FULL, hp)
-                out.append(Op("rs_adamw_int8", int((e - s) * (26 + n_dp + sb)), fn))
+                out.append(Op("rs_adamw_int8", int((e - s) * (26 + n_dp + sb)), fn,
+                              kernels=_owners(self.L, s, e)))
             return out
         if self.clip:
             for j, (s, e) in enumerate(self.ranges):
@@ -487,7 +496,8 @@ class Zero3Workload(Workload):
         self.name = name
         self.zstep = zstep
         self.zeropp = name in ("zero3-zeropp", "zero3-zeropp-fused")
-        self.fused = name in ("zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused")
+        self.graph = name == "zero3-fused-graph"
+        self.fused = name in ("zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph")
         self.int8 = name in ("zero3-int8", "zero3-zeropp", "zero3-int8-fused", "zero3-zeropp-fused")
         self.prefetch = name == "zero3-prefetch"
         n_dp = 8
@@ -547,6 +557,23 @@ class Zero3Workload(Workload):
                 self.dominant = "rs_adamw_int8_q8"
                 self.kernel_label = ("zgb::dequant_gather_vec_kernel, quantize_group_kernel<8,4>, "
                                      "qgrad_vec_kernel<8,true,q8>")
+        if self.graph:
+            # the fused step captured once in a CUDA graph: the schedule's advance
+            # kernel, then every unit's two gathers and its fused reduce-scatter +
+            # update, replayed as one launch per step (lr and the bias corrections
+            # read from device memory)
+            self.sched = zstep.StepSchedule(n_steps=1 << 16, **HP)
+            unit_ops = self._step_ops(self.sched.hp())
+
+            def step_fn():
+                self.sched.advance()
+                for op in unit_ops:
+                    op.fn()
+            self.gs = zstep.GraphStep(step_fn)
+            self.graph_kernels = 1 + sum(op.kernels for op in unit_ops)
+            self.dominant = "zero3_graph_step"
+            self.kernel_label = ("one CUDA graph: zgb::schedule_advance_kernel, gather_vec_kernel, "
+                                 "rs_adamw_vec_kernel<0,8> (own-shard output)")
         if self.prefetch:
             self.dominant = "zero3_step_prefetched"
             self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
@@ -555,7 +582,8 @@ class Zero3Workload(Workload):
                      + ("_int8_grads" if self.zeropp else "")
                      + ("_fused_rs_update" if self.fused else "")
                      + ("_align256" if align == 256 else "")
-                     + ("_prefetch" if self.prefetch else ""),
+                     + ("_prefetch" if self.prefetch else "")
+                     + ("_cuda_graph" if self.graph else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
                      "ring_slots": 2}
@@ -566,14 +594,21 @@ class Zero3Workload(Workload):
             self.device_bytes += self.qg.q.numel() + self.qg.scales.numel() * 4
 
     def ops(self, t):
-        zb, hp, zs = self.zb, self.hp(t), self.zstep
+        if self.graph:
+            return [Op("zero3_graph_step", self.elems * self.bytes_per_elem, self.gs.replay,
+                       kernels=self.graph_kernels)]
+        return self._step_ops(self.hp(t))
+
+    def _step_ops(self, hp):
+        zb, zs = self.zb, self.zstep
         out = []
         if self.prefetch:
             def step_all():
                 zs.zero3_step_prefetched(
                     self.pf, lambda i: [self._g[r, :self.units[i].layout.padded_n]
                                         for r in range(self.units[i].layout.n_dp)], self.A, hp)
-            out.append(Op("zero3_step_prefetched", self.elems * self.bytes_per_elem, step_all))
+            out.append(Op("zero3_step_prefetched", self.elems * self.bytes_per_elem, step_all,
+                          kernels=4 * len(self.units)))
             return out
         for i, u in enumerate(self.units):
             P = u.layout.padded_n
@@ -625,8 +660,9 @@ class Zero3Workload(Workload):
                         QGRAD_BLOCK, float(n), 0, n, 0, P, u.master, u.m, u.v, q.q.view(-1),
                         q.scales.view(-1), 256, hp)
                     self.ring.release(("bwd", i))
-                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads))
-                out.append(Op("rs_adamw_int8_q8", P * (n + 25) + n * sbytes + (P // 256) * 4, rs_upd_int8_q8))
+                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads, kernels=n))
+                out.append(Op("rs_adamw_int8_q8", P * (n + 25) + n * sbytes + (P // 256) * 4, rs_upd_int8_q8,
+                              kernels=n))
                 continue
             if self.fused and q is not None:
                 def rs_upd_q8(u=u, i=i, grads=grads, q=q):
@@ -643,8 +679,8 @@ class Zero3Workload(Workload):
             if self.zeropp:
                 n = u.layout.n_dp
                 sbytes = n * (-(-u.layout.shard // QGRAD_BLOCK)) * 4
-                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads))
-                out.append(Op("accumulate_int8", P * (n + 4) + n * sbytes, rs_int8))
+                out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads, kernels=n))
+                out.append(Op("accumulate_int8", P * (n + 4) + n * sbytes, rs_int8, kernels=n))
             else:
                 out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
             out.append(Op("rs_adamw", P * 30, upd))
@@ -663,7 +699,7 @@ def make_workload(name, device, elems=0):
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
     if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused",
-                "zero3-int8-fused", "zero3-zeropp-fused"):
+                "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -704,10 +740,11 @@ def time_workload(wl, steps, warmup, dist, device, sampler=None):
     for ops, evs in zip(plan, ev):
         step_ms.append(evs[0][0].elapsed_time(evs[-1][1]))     # first launch's start to last's end
         for op, (a, b) in zip(ops, evs):
-            d = per_kind.setdefault(op.kind, {"ms": 0.0, "bytes": 0, "launches": 0})
+            d = per_kind.setdefault(op.kind, {"ms": 0.0, "bytes": 0, "launches": 0, "kernels": 0})
             d["ms"] += a.elapsed_time(b)
             d["bytes"] += op.bytes
             d["launches"] += 1
+            d["kernels"] += op.kernels
     per_kind["_steps"] = step_ms
     return start.elapsed_time(end), per_kind, clocks, t + steps
 
@@ -805,7 +842,7 @@ def time_oracle(sample, seconds, n_dp):
 def _kernels_summary(per_kind, steps):
     out = {}
     for kind, d in per_kind.items():
-        out[kind] = {"launches_per_step": d["launches"] // steps,
+        out[kind] = {"launches_per_step": d["kernels"] // steps,
                      "ms_per_step": d["ms"] / steps,
                      "bytes_per_step": d["bytes"] // steps,
                      "achieved_gbs": d["bytes"] / (d["ms"] / 1e3) / 1e9 if d["ms"] > 0 else None}
@@ -834,7 +871,8 @@ def run_ours(args):
     peak, peak_kind = _peak()
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
-                          "accum-zero2", "zero3", "zero3-fused", "zero3-prefetch", "zero3-int8",
+                          "accum-zero2", "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch",
+                          "zero3-int8",
                           "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused")
               if w != primary]
     order = [primary] + ([] if args.no_extra or primary == "probe" else extras)
@@ -871,7 +909,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": dom_bytes,
                          "kernel": wl.dominant, "kernel_symbols": wl.kernel_label},
             "kernels": kernels,
-            "gpu_launches": sum(d["launches"] for d in per_kind.values()),
+            "gpu_launches": sum(d["kernels"] for d in per_kind.values()),
         }
         if is_primary:
             res["clocks"] = clocks

@@ -82,6 +82,12 @@ typedef struct {
     float weight_decay;
     int32_t reserved;   /* zero */
     int64_t step;       /* t, starting at 1 */
+    /* NULL, or a DEVICE pointer to 3 floats {lr, 1 - beta1^t, 1 - beta2^t} of the
+     * current step, read by the kernels in place of lr and step (written by
+     * zero_schedule_advance from a table of zero_schedule_fill): the step's
+     * scalars then live in device memory, so that a captured CUDA graph of a
+     * step can be replayed step after step.  4-byte aligned. */
+    const float* sched;
 } zero_adamw_t;
 
 /* ---- layout --------------------------------------------------------------
@@ -241,6 +247,29 @@ int zero_reduce_scatter_adamw_clip(const zero_layout_t* L,
                                    uint16_t* out_bf16, int32_t out_mode,
                                    const zero_adamw_t* hp, const double* norm_sq, float max_norm,
                                    void* stream);
+
+/* ---- per-step scalars in device memory ----------------------------------
+ * For CUDA-graph replay of steps (and per-step learning-rate schedules): the
+ * scalars that change from step to step -- lr and the bias corrections of
+ * "ZeRO and FSDP", exercise "A sharded Adam step" -- come from device memory.
+ *
+ * zero_schedule_fill (host only): table (host, 3 * n_steps floats) receives,
+ *   for k = 0..n_steps-1, {lr_k, bc1, bc2} of step t = first_step + k, with
+ *   bc1 = 1 - beta1^t and bc2 = 1 - beta2^t computed exactly as for a
+ *   by-value step (fp64 from the fp32 betas, rounded once to fp32); lr_k =
+ *   lrs[k] (host array of n_steps finite floats), or hp->lr when lrs is NULL.
+ *   Errors: ZERO_EINVAL (null, first_step < 1, n_steps < 1, a bad value).
+ * zero_schedule_advance (device, one thread, on `stream`): k = *step_index;
+ *   sched[0..2] = table[3k .. 3k+2]; *step_index = k + 1.  table (device,
+ *   3 * n_steps floats), step_index (device int64, 8-byte aligned) and sched
+ *   (device, 3 floats) are the caller's; launching it before a step's updates
+ *   (inside the same captured graph) moves them to the next row.  When k is
+ *   outside [0, n_steps) nothing is written and zero_status_check reports
+ *   ZERO_ERANGE.  Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+int zero_schedule_fill(const zero_adamw_t* hp, int64_t first_step, int64_t n_steps,
+                       const float* lrs, float* table);
+int zero_schedule_advance(const float* table, int64_t n_steps, int64_t* step_index, float* sched,
+                          void* stream);
 
 /* ---- stage-3 gather ------------------------------------------------------
  * "DeepSpeed ZeRO", "Stage 3 step by step" and "ZeRO and FSDP", "FSDP, ZeRO-3

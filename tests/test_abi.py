@@ -265,3 +265,25 @@ def test_missing_library_fails_loudly(zlib, monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(ImportError):
         binding.load()
+
+
+def test_schedule_fill_matches_the_oracle_bias_corrections(zlib):
+    """The device-schedule table holds exactly the by-value scalars: lr and the
+    oracle's bias corrections of every step."""
+    import oracle
+    hp = zlib.ZeroAdamW.make(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    table = zlib.zero_schedule_fill(hp, 5, 20)
+    o = oracle.AdamW(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    for k in range(20):
+        bc1, bc2 = oracle.bias_corrections(o, 5 + k)
+        assert table[k].tolist() == [float(np.float32(3e-4)), float(bc1), float(bc2)]
+    lrs = [1e-3 * (k + 1) for k in range(4)]
+    t2 = zlib.zero_schedule_fill(hp, 1, 4, lrs)
+    assert t2[:, 0].tolist() == [float(np.float32(x)) for x in lrs]
+    lib = zlib.load()
+    assert lib.zero_schedule_fill(None, 1, 4, None, FAKE) == -1
+    assert lib.zero_schedule_fill(ctypes.byref(hp), 0, 4, None, FAKE) == -1
+    assert lib.zero_schedule_fill(ctypes.byref(hp), 1, 0, None, FAKE) == -1
+    assert lib.zero_schedule_advance(None, 4, FAKE, FAKE, None) == -1
+    assert lib.zero_schedule_advance(FAKE, 0, FAKE, FAKE, None) == -1
+    assert lib.zero_schedule_advance(FAKE, 4, FAKE + 4, FAKE, None) == -2      # index 8-byte aligned

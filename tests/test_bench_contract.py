@@ -34,3 +34,15 @@ def test_reference_arm_other_ranks_are_silent(monkeypatch):
     with redirect_stdout(buf):
         bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
     assert buf.getvalue() == ""
+
+
+def test_owner_count_of_a_range():
+    """The 8-bit gradient kernels launch once per owner a range overlaps."""
+    import bench
+
+    class L:
+        shard = 100
+    assert bench._owners(L, 0, 100) == 1
+    assert bench._owners(L, 0, 101) == 2
+    assert bench._owners(L, 99, 201) == 3
+    assert bench._owners(L, 150, 150) == 0

@@ -15,7 +15,7 @@ _BINDING_NAMES = {
     "zero_reduce_scatter_adamw_clip", "zero_accumulate_adamw", "zero_grad_norm_workspace",
     "zero_grad_norm_sq", "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
     "zero_reduce_scatter_adamw_int8", "zero_accumulate_int8", "zero_reduce_scatter_adamw_q8",
-    "zero_reduce_scatter_adamw_int8_q8",
+    "zero_reduce_scatter_adamw_int8_q8", "zero_schedule_fill", "zero_schedule_advance",
     "zero_status_check", "zero_strerror", "zero_memory_bytes", "zero_comm_bytes",
     "zero_bucket_range", "zero_shard_range", "zero_selftest_bounded_wait", "ZERO_ETIMEOUT",
     "ZERO_BF16", "ZERO_F32", "ZERO_OUT_FULL", "ZERO_OUT_SHARD",

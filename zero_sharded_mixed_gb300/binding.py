@@ -57,11 +57,17 @@ class ZeroCkptHeader(ctypes.Structure):
 class ZeroAdamW(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
-                ("reserved", ctypes.c_int32), ("step", ctypes.c_int64)]
+                ("reserved", ctypes.c_int32), ("step", ctypes.c_int64),
+                ("sched", ctypes.c_void_p)]
 
     @classmethod
-    def make(cls, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1):
-        return cls(lr, beta1, beta2, eps, weight_decay, 0, step)
+    def make(cls, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1, sched=None):
+        """sched: None, or a CUDA float32 tensor of 3 elements {lr, bc1, bc2}
+        that the kernels read in place of lr and step."""
+        ptr = None
+        if sched is not None:
+            ptr = _tensor(sched, "sched", torch.float32, 3)
+        return cls(lr, beta1, beta2, eps, weight_decay, 0, step, ptr)
 
 
 _lock = threading.Lock()
@@ -104,6 +110,8 @@ def load():
         lib.zero_ckpt_read_header.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), P(i32)]
         lib.zero_ckpt_read_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p, i64]
         lib.zero_selftest_bounded_wait.argtypes = [i64, p]
+        lib.zero_schedule_fill.argtypes = [P(ZeroAdamW), i64, i64, p, p]
+        lib.zero_schedule_advance.argtypes = [p, i64, p, p, p]
         lib.zero_crc32.argtypes = [p, i64]
         lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
@@ -136,6 +144,7 @@ def load():
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
                      "zero_selftest_bounded_wait", "zero_reduce_scatter_adamw_int8",
                      "zero_reduce_scatter_adamw_q8", "zero_reduce_scatter_adamw_int8_q8",
+                     "zero_schedule_fill", "zero_schedule_advance",
                      "zero_accumulate_int8", "zero_gather_layer", "zero_accumulate",
                      "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -504,6 +513,32 @@ def zero_accumulate_int8(L: ZeroLayout, q_src, scale_src, block: int, dst: torch
                                      _tensor(dst, "dst", torch.float32, dst_need), int(dst_base),
                                      int(begin), int(end), int(bool(first)), _stream_ptr(stream))
     _check(rc, "zero_accumulate_int8")
+
+
+def zero_schedule_fill(hp: ZeroAdamW, first_step: int, n_steps: int, lrs=None) -> torch.Tensor:
+    """Host table [n_steps, 3] of {lr, bc1, bc2} for steps first_step..; lrs: a
+    sequence of n_steps learning rates, or None for hp.lr."""
+    table = torch.empty((int(n_steps), 3), dtype=torch.float32)
+    lr_arr = None
+    if lrs is not None:
+        lr_t = torch.tensor([float(x) for x in lrs], dtype=torch.float32)
+        if lr_t.numel() != n_steps:
+            raise ValueError(f"need {n_steps} learning rates, got {lr_t.numel()}")
+        lr_arr = lr_t
+    rc = load().zero_schedule_fill(ctypes.byref(hp), int(first_step), int(n_steps),
+                                   lr_arr.data_ptr() if lr_arr is not None else None, table.data_ptr())
+    _check(rc, "zero_schedule_fill")
+    return table
+
+
+def zero_schedule_advance(table: torch.Tensor, step_index: torch.Tensor, sched: torch.Tensor,
+                          stream=None):
+    """On the device: sched = table[step_index]; step_index += 1."""
+    rc = load().zero_schedule_advance(_tensor(table, "table", torch.float32, 3),
+                                      table.numel() // 3,
+                                      _tensor(step_index, "step_index", torch.int64, 1),
+                                      _tensor(sched, "sched", torch.float32, 3), _stream_ptr(stream))
+    _check(rc, "zero_schedule_advance")
 
 
 def zero_selftest_bounded_wait(limit_cycles: int, stream=None):

@@ -195,7 +195,7 @@ __device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i) {
     for (int r = 0; r < p.n_src; ++r) s = __fadd_rn(s, __fmul_rn((float)p.q[r][i], __ldg(p.scale[r] + b)));
     if constexpr (kUpdate) {
         float w = p.w[i], m = p.m[i], v = p.v[i];
-        adamw_update(mean_grad(s, p.h, 1.0f), w, m, v, p.h);
+        adamw_update(mean_grad(s, p.h, 1.0f), w, m, v, p.h, step_scalars(p.h));
         p.w[i] = w;
         p.m[i] = m;
         p.v[i] = v;

@@ -234,7 +234,7 @@ __device__ __forceinline__ void step_one(const UpdateParams& p, int64_t i, float
     }
     if constexpr (KIND == kAccReduce) s = __fadd_rn(p.acc[0][i], s);
     float w = p.w[i], m = p.m[i], v = p.v[i];
-    adamw_update(mean_grad(s, p.h, coef), w, m, v, p.h);
+    adamw_update(mean_grad(s, p.h, coef), w, m, v, p.h, step_scalars(p.h));
     p.w[i] = w;
     p.m[i] = m;
     p.v[i] = v;
@@ -397,25 +397,38 @@ int check_target_ptrs(const UpdateTarget& t) {
     return ZERO_OK;
 }
 
+void bias_corrections(float b1, float b2, int64_t t, float* bc1, float* bc2) {
+    *bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
+    *bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
+}
+
 int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h) {
     if (!hp) return ZERO_EINVAL;
     if (!(divisor > 0.0f) || !std::isfinite(divisor)) return ZERO_EINVAL;
-    if (hp->step < 1 || !std::isfinite(hp->lr) || !std::isfinite(hp->eps) ||
-        !std::isfinite(hp->weight_decay) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) ||
-        !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+    if (!std::isfinite(hp->eps) || !std::isfinite(hp->weight_decay) ||
+        !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
         return ZERO_EINVAL;
     h->divisor = divisor;
     h->b1 = hp->beta1;
     h->b2 = hp->beta2;
     h->omb1 = 1.0f - hp->beta1;
     h->omb2 = 1.0f - hp->beta2;
-    h->bc1 = (float)(1.0 - std::pow((double)hp->beta1, (double)hp->step));
-    h->bc2 = (float)(1.0 - std::pow((double)hp->beta2, (double)hp->step));
-    h->lr = hp->lr;
-    h->lrwd = hp->lr * hp->weight_decay;
     h->eps = hp->eps;
+    h->wd = hp->weight_decay;
     h->max_norm = 0.0f;
     h->norm_sq = nullptr;
+    h->sched = hp->sched;
+    if (hp->sched) {                        // lr and the bias corrections come from the device
+        if (check_aligned(hp->sched, 4)) return ZERO_EALIGN;
+        if (check_device_ptr(hp->sched)) return ZERO_EINVAL;
+        h->lr = h->lrwd = 0.0f;
+        h->bc1 = h->bc2 = 1.0f;
+        return ZERO_OK;
+    }
+    if (hp->step < 1 || !std::isfinite(hp->lr)) return ZERO_EINVAL;
+    bias_corrections(hp->beta1, hp->beta2, hp->step, &h->bc1, &h->bc2);
+    h->lr = hp->lr;
+    h->lrwd = hp->lr * hp->weight_decay;
     if (!(h->bc1 > 0.0f) || !(h->bc2 > 0.0f)) return ZERO_EINVAL;
     return ZERO_OK;
 }

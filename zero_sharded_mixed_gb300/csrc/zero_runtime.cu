@@ -108,5 +108,7 @@ extern "C" int zero_status_check(void* stream) {
     zgb::note_cuda_error(e);
     zgb::note_cuda_error(last);
     if (e != cudaSuccess || last != cudaSuccess) return ZERO_ECUDA;
-    return zgb::take_device_status();   // ZERO_ETIMEOUT if a bounded device wait gave up
+    const int rc = zgb::take_device_status();   // ZERO_ETIMEOUT if a bounded device wait gave up
+    const int rs = zgb::take_schedule_status();  // ZERO_ERANGE if a schedule index left its table
+    return rc != ZERO_OK ? rc : rs;
 }

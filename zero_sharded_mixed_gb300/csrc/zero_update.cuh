@@ -23,9 +23,23 @@ struct AdamwScalars {
     float b1, b2, omb1, omb2;       // beta1, beta2, 1-beta1, 1-beta2 (fp32)
     float bc1, bc2;                 // 1 - beta^t in fp64, rounded to fp32
     float lr, lrwd, eps;            // lr, lr*wd (fp32), eps
+    float wd;                       // weight decay (lr*wd is formed from it when sched is set)
     float max_norm;                 // clipping threshold (used when norm_sq is set)
     const double* norm_sq;          // device: squared global gradient norm, or nullptr
+    const float* sched;             // device: {lr, bc1, bc2} of this step, or nullptr
 };
+
+// The scalars that change from step to step: from the parameters, or from
+// device memory (zero_schedule_advance) when h.sched is set.
+struct StepScalars {
+    float lr, lrwd, bc1, bc2;
+};
+
+__device__ __forceinline__ StepScalars step_scalars(const AdamwScalars& h) {
+    if (h.sched == nullptr) return StepScalars{h.lr, h.lrwd, h.bc1, h.bc2};
+    const float lr = __ldg(h.sched);
+    return StepScalars{lr, __fmul_rn(lr, h.wd), __ldg(h.sched + 1), __ldg(h.sched + 2)};
+}
 
 // The clipping coefficient, or 1 when no norm is given.
 __device__ __forceinline__ float clip_coef(const AdamwScalars& h) {
@@ -35,16 +49,16 @@ __device__ __forceinline__ float clip_coef(const AdamwScalars& h) {
     return c < 1.0f ? c : 1.0f;
 }
 
-// g is the mean gradient (already divided and clipped).
+// g is the mean gradient (already divided and clipped); st the step's scalars.
 __device__ __forceinline__ void adamw_update(float g, float& w, float& m, float& v,
-                                             const AdamwScalars& h) {
+                                             const AdamwScalars& h, const StepScalars& st) {
     const float mi = __fadd_rn(__fmul_rn(h.b1, m), __fmul_rn(h.omb1, g));
     const float vi = __fadd_rn(__fmul_rn(h.b2, v), __fmul_rn(h.omb2, __fmul_rn(g, g)));
-    const float m_hat = __fdiv_rn(mi, h.bc1);
-    const float v_hat = __fdiv_rn(vi, h.bc2);
-    float wi = __fsub_rn(w, __fmul_rn(h.lrwd, w));                        // decoupled decay
+    const float m_hat = __fdiv_rn(mi, st.bc1);
+    const float v_hat = __fdiv_rn(vi, st.bc2);
+    float wi = __fsub_rn(w, __fmul_rn(st.lrwd, w));                       // decoupled decay
     const float denom = __fadd_rn(__fsqrt_rn(v_hat), h.eps);
-    wi = __fsub_rn(wi, __fmul_rn(h.lr, __fdiv_rn(m_hat, denom)));          // Adam step
+    wi = __fsub_rn(wi, __fmul_rn(st.lr, __fdiv_rn(m_hat, denom)));         // Adam step
     w = wi;
     m = mi;
     v = vi;
@@ -65,8 +79,9 @@ __device__ __forceinline__ uint4 update_vec(const P& p, int64_t e, const float (
     float w[8] = {st[0].x, st[0].y, st[0].z, st[0].w, st[1].x, st[1].y, st[1].z, st[1].w};
     float m[8] = {st[2].x, st[2].y, st[2].z, st[2].w, st[3].x, st[3].y, st[3].z, st[3].w};
     float v[8] = {st[4].x, st[4].y, st[4].z, st[4].w, st[5].x, st[5].y, st[5].z, st[5].w};
+    const StepScalars sc = step_scalars(p.h);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_update(mean_grad(s[j], p.h, coef), w[j], m[j], v[j], p.h);
+    for (int j = 0; j < 8; ++j) adamw_update(mean_grad(s[j], p.h, coef), w[j], m[j], v[j], p.h, sc);
     st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
     st_stream_f4(p.w + e + 4, make_float4(w[4], w[5], w[6], w[7]));
     st_stream_f4(p.m + e, make_float4(m[0], m[1], m[2], m[3]));
@@ -164,5 +179,10 @@ int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end,
 int check_target_ptrs(const UpdateTarget& t);
 // Hyper-parameter checks and the fp32 scalars of the update.
 int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h);
+// 1 - b1^t and 1 - b2^t in fp64 from the fp32 betas, rounded once to fp32.
+void bias_corrections(float b1, float b2, int64_t t, float* bc1, float* bc2);
+// Reads and clears the status word of zero_schedule_advance (ZERO_OK or
+// ZERO_ERANGE); synchronizes the device.
+int take_schedule_status();
 
 }  // namespace zgb

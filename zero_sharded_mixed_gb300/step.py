@@ -57,6 +57,54 @@ def split_ranges(ranges, chunk_elems: int | None):
 
 
 # --------------------------------------------------------------------------
+# per-step scalars in device memory, and steps captured in CUDA graphs
+# --------------------------------------------------------------------------
+
+class StepSchedule:
+    """lr and the bias corrections of steps first_step .. first_step+n_steps-1
+    in device memory: advance() (a one-thread kernel on the stream) moves the
+    current-step scalars to the next step, and hp() is the AdamW block whose
+    kernels read them.  A step captured in a CUDA graph after advance() is
+    then a new step at every replay; lrs gives a learning rate per step."""
+
+    def __init__(self, lr, beta1, beta2, eps, weight_decay, n_steps: int, first_step: int = 1,
+                 lrs=None, device="cuda"):
+        base = zb.ZeroAdamW.make(lr, beta1, beta2, eps, weight_decay, first_step)
+        self.table = zb.zero_schedule_fill(base, first_step, n_steps, lrs).to(device)
+        self.index = torch.zeros(1, dtype=torch.int64, device=device)
+        self.sched = torch.zeros(3, dtype=torch.float32, device=device)
+        self._hp = zb.ZeroAdamW.make(lr, beta1, beta2, eps, weight_decay, first_step, sched=self.sched)
+
+    def hp(self) -> zb.ZeroAdamW:
+        return self._hp
+
+    def advance(self, stream=None):
+        zb.zero_schedule_advance(self.table, self.index, self.sched, stream)
+
+
+class GraphStep:
+    """A step captured once in a CUDA graph and replayed.  fn() must launch the
+    whole step on the current stream with fixed buffers (the gradients of each
+    step written into the same tensors) and read its per-step scalars from a
+    StepSchedule that fn() advances first.  Capture runs one warm-up call on a
+    side stream (which performs a step) before recording."""
+
+    def __init__(self, fn, warmup: int = 1):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+
+    def replay(self):
+        self.graph.replay()
+
+
+# --------------------------------------------------------------------------
 # gradient accumulation ("ZeRO and FSDP", paragraph on accumulation)
 # --------------------------------------------------------------------------
 
