@@ -473,6 +473,21 @@ int zero_memory_bytes(double n, int32_t n_dp, int32_t stage, double k_bytes, dou
 int zero_comm_bytes(double n, int32_t n_dp, int32_t stage, double param_bytes,
                     double grad_bytes, double* out);
 
+/* The learning rate of optimizer step t (t >= 1) under the "WarmupDecayLR"
+ * schedule of the example configuration in "DeepSpeed ZeRO", "The
+ * configuration file" (warmup_min_lr, warmup_max_lr, warmup_num_steps,
+ * total_num_steps).  The page names the schedule and its four parameters but
+ * not its shape; the reading taken: with k = t - 1 schedule steps taken,
+ *   k <  warmup:          lr = min + (max - min) * k / warmup   (linear warmup)
+ *   warmup <= k < total:  lr = max * (total - k) / (total - warmup)
+ *                                                     (linear decay to 0)
+ *   k >= total:           lr = 0
+ * evaluated in double precision and rounded once to float.  Host only.
+ * ZERO_EINVAL for t < 1, warmup < 0, total <= warmup, non-finite or negative
+ * rates, or a null out. */
+int zero_lr_warmup_decay(int64_t t, double min_lr, double max_lr, int64_t warmup_steps,
+                         int64_t total_steps, float* lr_out);
+
 #ifdef __cplusplus
 }
 #endif

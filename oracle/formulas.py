@@ -14,8 +14,17 @@ Both follow "ZeRO and FSDP" (zerotofrontier.app):
   GPU and an all-reduce twice that; stage 0 all-reduces gradients, stages 1
   and 2 reduce-scatter gradients and all-gather weights, stage 3 all-gathers
   weights twice and reduce-scatters gradients.
+
+``warmup_decay_lr`` follows "DeepSpeed ZeRO", "The configuration file": the
+example configuration's "WarmupDecayLR" scheduler with warmup_min_lr,
+warmup_max_lr, warmup_num_steps and total_num_steps.  The page gives no
+shape; the reading is linear warmup from the minimum to the maximum over the
+warmup steps, then linear decay to 0 at total_num_steps, the first optimizer
+step taking the value at 0 schedule steps.
 """
 from __future__ import annotations
+
+import numpy as np
 
 
 def zero_memory(N, n_dp, stage, K=12):
@@ -44,3 +53,21 @@ def zero_comm_bytes(N, n_dp, stage, param_bytes=2, grad_bytes=2):
     if stage in (1, 2):
         return one_pass * grad_bytes + one_pass * param_bytes  # RS(grads) + AG(weights)
     return one_pass * grad_bytes + 2 * one_pass * param_bytes  # RS(grads) + 2 x AG(weights)
+
+
+def warmup_decay_lr(t, min_lr, max_lr, warmup_steps, total_steps):
+    """Learning rate of optimizer step t (t >= 1): the piecewise-linear curve
+    through (0, min_lr), (warmup_steps, max_lr), (total_steps, 0), flat at 0
+    beyond, read at k = t - 1 schedule steps; rounded once to float32."""
+    if t < 1 or warmup_steps < 0 or total_steps <= warmup_steps:
+        raise ValueError("need t >= 1 and 0 <= warmup_steps < total_steps")
+    k = t - 1
+    if k < warmup_steps:
+        frac = k / warmup_steps
+        lr = min_lr + frac * (max_lr - min_lr)
+    elif k < total_steps:
+        frac = (k - warmup_steps) / (total_steps - warmup_steps)
+        lr = max_lr - frac * max_lr
+    else:
+        lr = 0.0
+    return float(np.float32(lr))

@@ -137,3 +137,48 @@ def test_zero3_engine(zlib, cuda_device, K, clip, qw, qg):
         else:
             assert np.array_equal(parity.bits(u.shards).reshape(-1), out_ref)
     assert eng.ring.resident == 0 and eng.ring.peak <= 2
+
+
+def test_engines_follow_the_scheduler(zlib, cuda_device):
+    """WarmupDecayLR ("DeepSpeed ZeRO", "The configuration file"): every step's
+    lr from the schedule, the update bit-exact against the oracle at that lr."""
+    from oracle import formulas
+    sched = {"type": "WarmupDecayLR", "params": {"warmup_min_lr": 1e-5, "warmup_max_lr": 1e-3,
+                                                 "warmup_num_steps": 2, "total_num_steps": 4}}
+    n_dp, N = 4, 50_001
+    cfg = ZeroConfig.from_dict({"zero_optimization": {"stage": 2},
+                                "optimizer": {"type": "AdamW", "params": {
+                                    "lr": HP.lr, "betas": [HP.beta1, HP.beta2], "eps": HP.eps,
+                                    "weight_decay": HP.weight_decay}},
+                                "scheduler": sched})
+    eng = ZeroEngine([N], n_dp, cfg, master=inputs.master_weights(N, 50_016, seed=5).cuda())
+    P = eng.L.padded_n
+    units = [[7_001], [30_000, 13]]
+    eng3 = Zero3Engine(units, n_dp, ZeroConfig.from_dict({**{"zero_optimization": {"stage": 3}},
+                                                         "optimizer": cfg_opt(), "scheduler": sched}))
+    state = [parity.f32(eng.master), np.zeros(P, np.float32), np.zeros(P, np.float32)]
+    states3 = [[parity.f32(u.master), np.zeros(u.layout.padded_n, np.float32),
+                np.zeros(u.layout.padded_n, np.float32)] for u in eng3.units]
+    for t in range(1, 6):                      # past total_num_steps: lr 0, decay still 0
+        hp = oracle.AdamW(lr=formulas.warmup_decay_lr(t, 1e-5, 1e-3, 2, 4), beta1=HP.beta1, beta2=HP.beta2,
+                          eps=HP.eps, weight_decay=HP.weight_decay)
+        g = inputs.grads_bf16(n_dp, N, P, seed=6, step=t)
+        eng.backward(g.cuda())
+        eng.step()
+        for i, u in enumerate(eng3.units):
+            g3 = inputs.grads_bf16(n_dp, u.layout.n, u.layout.padded_n, seed=7 + i, step=t)
+            eng3.backward(i, g3.cuda())
+            out3, *states3[i] = oracle.rs_adamw_reference(parity.bits(g3), n_dp, *states3[i], hp, t)
+            torch.cuda.synchronize()
+            parity.assert_state([u.master, u.m, u.v], states3[i], what=f"unit {i} t={t} ")
+            assert np.array_equal(parity.bits(u.shards).reshape(-1), out3)
+        eng3.step()
+        torch.cuda.synchronize()
+        out_ref, *state = oracle.rs_adamw_reference(parity.bits(g), n_dp, *state, hp, t)
+        parity.assert_state([eng.master, eng.m, eng.v], state, what=f"t={t} ")
+        assert np.array_equal(parity.bits(eng.weights), out_ref)
+
+
+def cfg_opt():
+    return {"type": "AdamW", "params": {"lr": HP.lr, "betas": [HP.beta1, HP.beta2], "eps": HP.eps,
+                                        "weight_decay": HP.weight_decay}}

@@ -3,6 +3,7 @@ import json
 import math
 import os
 
+import numpy as np
 import pytest
 
 from oracle import formulas
@@ -118,3 +119,48 @@ def test_comm_llama3_70b_printed():
             continue
         got = formulas.zero_comm_bytes(case["N"], case["n_dp"], case["stage"]) / 1e9
         assert got == pytest.approx(case["gb"], rel=case["rel_tol"]), (case["source"], got)
+
+
+# The learning-rate schedule of the example configuration ("DeepSpeed ZeRO",
+# "The configuration file": WarmupDecayLR with warmup_min_lr 0, warmup_max_lr
+# 1e-4, warmup_num_steps 100, total_num_steps 10000), read as linear warmup
+# then linear decay to 0, the first step at 0 schedule steps.
+SCHED = dict(min_lr=0.0, max_lr=1e-4, warmup_steps=100, total_steps=10000)
+
+
+def _lr(t, **kw):
+    return formulas.warmup_decay_lr(t, **{**SCHED, **kw})
+
+
+def test_schedule_points_of_the_example_configuration():
+    f32 = lambda x: float(np.float32(x))
+    assert _lr(1) == 0.0                   # the first step: warmup_min_lr
+    assert _lr(51) == f32(5e-5)            # half way up
+    assert _lr(101) == f32(1e-4)           # the end of warmup: warmup_max_lr
+    assert _lr(5051) == f32(5e-5)          # half way down
+    assert _lr(10001) == 0.0 and _lr(10_000_000) == 0.0   # 0 from total_num_steps on
+
+
+def test_schedule_is_linear_in_each_phase():
+    up = np.diff([_lr(t) for t in range(1, 102)])
+    down = np.diff([_lr(t) for t in range(101, 10002)])
+    assert np.allclose(up, 1e-6, rtol=1e-4)            # (1e-4 - 0) / 100 per step
+    assert np.allclose(down, -1e-4 / 9900, rtol=2e-3)  # 1e-4 / (10000 - 100) per step
+    assert (up > 0).all() and (down < 0).all()
+
+
+def test_schedule_with_a_minimum_and_without_warmup():
+    f32 = lambda x: float(np.float32(x))
+    kw = dict(min_lr=1e-5, max_lr=1e-4, warmup_steps=10, total_steps=20)
+    assert _lr(1, **kw) == f32(1e-5)
+    assert _lr(6, **kw) == f32(1e-5 + 0.5 * 9e-5)    # half way up from the minimum
+    assert _lr(16, **kw) == f32(5e-5)                 # half way down to 0, not to the minimum
+    assert _lr(1, min_lr=1e-5, warmup_steps=0) == f32(1e-4)   # no warmup: the maximum at once
+
+
+@pytest.mark.parametrize("bad", [dict(t=0), dict(warmup_steps=-1), dict(total_steps=100),
+                                 dict(total_steps=50)])
+def test_schedule_rejects_bad_parameters(bad):
+    t = bad.pop("t", 1)
+    with pytest.raises(ValueError):
+        _lr(t, **bad)

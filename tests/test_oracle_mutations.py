@@ -191,7 +191,7 @@ def test_a_planted_composition_mistake_fails_a_pin(what, name, fn, monkeypatch):
     assert caught, f"no pin noticed: {what}"
 
 
-# Mistakes in the memory and communication formulas (oracle/formulas.py):
+# Mistakes in the memory, communication and schedule formulas (oracle/formulas.py):
 # each mutant is loaded as a module in place of the real one, and the pins of
 # tests/test_oracle_formulas.py (the pages' printed numbers, the ring factor,
 # the invalid-stage rule) run against it.
@@ -208,6 +208,11 @@ FORMULA_MUTATIONS = [
     ("stage 0 reduce-scatters only", "return 2 * one_pass * grad_bytes", "return one_pass * grad_bytes"),
     ("stage 4 accepted", "if stage not in (0, 1, 2, 3):\n        raise ValueError(f\"ZeRO stage must be 0, 1, 2 or 3, got {stage!r}\")\n    weights",
      "if stage not in (0, 1, 2, 3, 4):\n        raise ValueError(f\"ZeRO stage must be 0, 1, 2 or 3, got {stage!r}\")\n    weights"),
+    ("schedule read at step t instead of t - 1", "    k = t - 1\n", "    k = t\n"),
+    ("decay ends at the minimum", "lr = max_lr - frac * max_lr", "lr = max_lr - frac * (max_lr - min_lr)"),
+    ("warmup runs down from the maximum", "lr = min_lr + frac * (max_lr - min_lr)",
+     "lr = max_lr - frac * (max_lr - min_lr)"),
+    ("the maximum kept after total_num_steps", "        lr = 0.0", "        lr = max_lr"),
 ]
 
 
@@ -228,6 +233,8 @@ def test_a_planted_formula_mistake_fails_a_pin(what, old, new, monkeypatch):
              pf.test_comm_stage12_equals_dp_and_stage3_is_one_and_a_half, pf.test_comm_exact_ring_factor,
              pf.test_comm_fp32_gradients_double_the_gradient_term, pf.test_comm_llama3_70b_printed]
     pins += [lambda s=s: pf.test_invalid_stage_raises(s) for s in (-1, 4, 5, "1", None, 1.5)]
+    pins += [pf.test_schedule_points_of_the_example_configuration, pf.test_schedule_is_linear_in_each_phase,
+             pf.test_schedule_with_a_minimum_and_without_warmup]
     caught = 0
     for pin in pins:
         try:

@@ -137,6 +137,7 @@ def load():
                                           P(ctypes.c_double)]
         lib.zero_comm_bytes.argtypes = [ctypes.c_double, i32, i32, ctypes.c_double,
                                         ctypes.c_double, P(ctypes.c_double)]
+        lib.zero_lr_warmup_decay.argtypes = [i64, ctypes.c_double, ctypes.c_double, i64, i64, P(f32)]
         for name in ("zero_layout", "zero_bucket_range", "zero_shard_range",
                      "zero_reduce_scatter_adamw", "zero_reduce_scatter_adamw_clip",
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
@@ -146,7 +147,8 @@ def load():
                      "zero_reduce_scatter_adamw_q8", "zero_reduce_scatter_adamw_int8_q8",
                      "zero_schedule_fill", "zero_schedule_advance",
                      "zero_accumulate_int8", "zero_gather_layer", "zero_accumulate",
-                     "zero_status_check", "zero_memory_bytes", "zero_comm_bytes"):
+                     "zero_status_check", "zero_memory_bytes", "zero_comm_bytes",
+                     "zero_lr_warmup_decay"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -189,6 +191,15 @@ def zero_shard_range(L: ZeroLayout, rank: int):
     _check(load().zero_shard_range(ctypes.byref(L), int(rank), ctypes.byref(lo), ctypes.byref(hi),
                                    ctypes.byref(valid)), "zero_shard_range")
     return lo.value, hi.value, valid.value
+
+
+def zero_lr_warmup_decay(t: int, min_lr: float, max_lr: float, warmup_steps: int,
+                         total_steps: int) -> float:
+    """The learning rate of optimizer step t (>= 1) under WarmupDecayLR."""
+    out = ctypes.c_float()
+    _check(load().zero_lr_warmup_decay(int(t), float(min_lr), float(max_lr), int(warmup_steps),
+                                       int(total_steps), ctypes.byref(out)), "zero_lr_warmup_decay")
+    return out.value
 
 
 def zero_memory_bytes(n, n_dp, stage, k_bytes=12.0) -> float:

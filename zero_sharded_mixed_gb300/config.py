@@ -4,8 +4,8 @@
 "Running it with DeepSpeed": a JSON configuration names the ZeRO stage, the
 reduce bucket size, the number of gradient-accumulation steps, the clipping
 threshold, the optimizer (AdamW with lr, betas, eps, weight_decay) and the
-precision (bf16); "Offload and ZeRO++" adds zero_quantized_weights and
-zero_quantized_gradients.  ``ZeroConfig.from_dict`` reads those keys, refuses
+precision (bf16), and a "WarmupDecayLR" learning-rate scheduler; "Offload and
+ZeRO++" adds zero_quantized_weights and zero_quantized_gradients.  ``ZeroConfig.from_dict`` reads those keys, refuses
 what this build does not do (fp16 loss scaling, offload, another optimizer),
 and lists the keys it did not use instead of failing on them.
 """
@@ -14,7 +14,7 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 
 _USED_TOP = {"zero_optimization", "optimizer", "gradient_accumulation_steps", "gradient_clipping",
-             "bf16", "fp16"}
+             "bf16", "fp16", "scheduler"}
 _USED_ZERO = {"stage", "reduce_bucket_size", "zero_quantized_weights", "zero_quantized_gradients",
               "offload_optimizer", "offload_param"}
 
@@ -32,6 +32,8 @@ class ZeroConfig:
     zero_quantized_weights: bool = False      # stage 3: 8-bit weight gathers
     zero_quantized_gradients: bool = False    # 8-bit gradient reduce-scatter
     quant_block: int = 256
+    # WarmupDecayLR: {"min_lr", "max_lr", "warmup_steps", "total_steps"}, or None for a constant lr
+    scheduler: dict | None = None
     ignored: list = field(default_factory=list)
 
     def __post_init__(self):
@@ -47,6 +49,22 @@ class ZeroConfig:
             raise ValueError("zero_quantized_weights applies to stage 3 (the weight all-gather)")
         if not (0.0 <= self.betas[0] < 1.0 and 0.0 <= self.betas[1] < 1.0):
             raise ValueError(f"betas must lie in [0, 1), got {self.betas!r}")
+        if self.scheduler is not None:
+            sc = self.scheduler
+            if not (0 <= sc["warmup_steps"] < sc["total_steps"]):
+                raise ValueError("the scheduler needs 0 <= warmup_num_steps < total_num_steps")
+            if not (sc["min_lr"] >= 0.0 and sc["max_lr"] >= 0.0):
+                raise ValueError("the scheduler's learning rates must be non-negative")
+
+    def lr_at(self, t: int) -> float:
+        """The learning rate of optimizer step t (t >= 1): the optimizer's lr, or
+        the scheduler's value at that step (computed by the library)."""
+        if self.scheduler is None:
+            return self.lr
+        from . import binding
+        sc = self.scheduler
+        return binding.zero_lr_warmup_decay(t, sc["min_lr"], sc["max_lr"], sc["warmup_steps"],
+                                            sc["total_steps"])
 
     @classmethod
     def from_dict(cls, cfg: dict) -> "ZeroConfig":
@@ -63,6 +81,21 @@ class ZeroConfig:
         if str(opt.get("type", "AdamW")).lower() != "adamw":
             raise ValueError(f"optimizer {opt.get('type')!r}: this build implements AdamW")
         p = opt.get("params", {})
+        scheduler = None
+        if cfg.get("scheduler") is not None:
+            sch = cfg["scheduler"]
+            if sch.get("type") != "WarmupDecayLR":
+                raise ValueError(f"scheduler {sch.get('type')!r}: this build implements WarmupDecayLR")
+            sp = sch.get("params", {})
+            if sp.get("warmup_type", "linear") != "linear":
+                raise ValueError("WarmupDecayLR is implemented with a linear warmup")
+            missing = [k for k in ("warmup_num_steps", "total_num_steps") if k not in sp]
+            if missing:
+                raise ValueError(f"WarmupDecayLR needs {', '.join(missing)}")
+            scheduler = {"min_lr": float(sp.get("warmup_min_lr", 0.0)),
+                         "max_lr": float(sp.get("warmup_max_lr", p.get("lr", 1e-4))),
+                         "warmup_steps": int(sp["warmup_num_steps"]),
+                         "total_steps": int(sp["total_num_steps"])}
         ignored = sorted([k for k in cfg if k not in _USED_TOP] +
                          [f"zero_optimization.{k}" for k in zo if k not in _USED_ZERO])
         return cls(
@@ -76,5 +109,6 @@ class ZeroConfig:
             weight_decay=float(p.get("weight_decay", 0.0)),
             zero_quantized_weights=bool(zo.get("zero_quantized_weights", False)),
             zero_quantized_gradients=bool(zo.get("zero_quantized_gradients", False)),
+            scheduler=scheduler,
             ignored=ignored,
         )

@@ -112,3 +112,17 @@ extern "C" int zero_comm_bytes(double n, int32_t n_dp, int32_t stage, double par
     *out = ring * (grad_passes * grad_bytes + gather_passes * param_bytes);
     return ZERO_OK;
 }
+
+extern "C" int zero_lr_warmup_decay(int64_t t, double min_lr, double max_lr, int64_t warmup_steps,
+                                    int64_t total_steps, float* lr_out) {
+    if (!lr_out || t < 1 || warmup_steps < 0 || total_steps <= warmup_steps) return ZERO_EINVAL;
+    if (!std::isfinite(min_lr) || !std::isfinite(max_lr) || min_lr < 0 || max_lr < 0) return ZERO_EINVAL;
+    const int64_t k = t - 1;                         // schedule steps taken before step t
+    double lr = 0.0;
+    if (k < warmup_steps)
+        lr = min_lr + (max_lr - min_lr) * ((double)k / (double)warmup_steps);
+    else if (k < total_steps)
+        lr = max_lr * ((double)(total_steps - k) / (double)(total_steps - warmup_steps));
+    *lr_out = (float)lr;
+    return ZERO_OK;
+}

@@ -29,7 +29,7 @@ from .config import ZeroConfig
 
 
 def _hp(cfg: ZeroConfig, t: int) -> zb.ZeroAdamW:
-    return zb.ZeroAdamW.make(cfg.lr, cfg.betas[0], cfg.betas[1], cfg.eps, cfg.weight_decay, t)
+    return zb.ZeroAdamW.make(cfg.lr_at(t), cfg.betas[0], cfg.betas[1], cfg.eps, cfg.weight_decay, t)
 
 
 class ZeroEngine:
