@@ -107,10 +107,11 @@ int launch_status();
 void note_cuda_error(cudaError_t e);
 const char* last_cuda_error_name();
 // Grid for a grid-stride loop over `work` items with `per_cta` items per CTA
-// pass, capped at `resident` CTAs (so every CTA is resident at once).
-inline unsigned grid_for(int64_t work, int64_t per_cta, int64_t resident) {
+// pass, capped at `cap` CTAs (callers pass the CTAs resident at once times a
+// measured number of waves).
+inline unsigned grid_for(int64_t work, int64_t per_cta, int64_t cap) {
     int64_t g = (work + per_cta - 1) / per_cta;
-    if (g > resident) g = resident;
+    if (g > cap) g = cap;
     if (g < 1) g = 1;
     return (unsigned)g;
 }

@@ -595,6 +595,8 @@ extern "C" int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,
     p.m = t.m;
     p.v = t.v;
     p.out = t.out;
+    p.q = nullptr;
+    p.qscale = nullptr;
     p.n = t.n;
     p.n_src = n_grads;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

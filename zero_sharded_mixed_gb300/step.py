@@ -1,8 +1,11 @@
 """Host-side orchestration of the C-ABI calls: the bucket loop of a ZeRO-1/2
-step, the two gradient-accumulation orders, and the ZeRO-3 per-unit
-gather / release / reduce-scatter / update sequence with a two-slot ring of
-gathered buffers.  No arithmetic happens here; every element is touched only
-by the library's kernels.
+step, the two gradient-accumulation orders, clipping by the global norm, the
+ZeRO-3 per-unit gather / release / reduce-scatter / update sequence with a
+two-slot ring of gathered buffers (and its prefetching variant), the ZeRO++
+8-bit weight and gradient paths, steps fed from pinned host memory, and
+per-step scalars in device memory for steps replayed from a CUDA graph.  No
+arithmetic happens here; every element is touched only by the library's
+kernels.
 
 Buffer conventions (simulated ranks in one GPU):
 * ``grads``: n_dp bf16 tensors, rank r's full local gradient of P elements.
