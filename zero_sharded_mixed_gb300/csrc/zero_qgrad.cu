@@ -151,9 +151,9 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
 #pragma unroll
         for (int r = 0; r < R; ++r) add_codes8(s, x[u].c[r], x[u].s[r]);
         if constexpr (kQ8) {
-            finish_vec_q8(p, e, s, x[u].st, 1.0f, p.qout, p.qoscale);
+            finish_vec_q8<true>(p, e, s, x[u].st, 1.0f, p.qout, p.qoscale);
         } else if constexpr (kUpdate) {
-            finish_vec(p, e, s, x[u].st, 1.0f);
+            finish_vec<true>(p, e, s, x[u].st, 1.0f);
         } else {
             const float4 d[2] = {x[u].st[0], x[u].st[1]};
             store_acc(p, e, s, d);
@@ -174,9 +174,9 @@ __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) 
         float4 st[6];
         load_state(p, e, st);
         if constexpr (kQ8)
-            finish_vec_q8(p, e, s, st, 1.0f, p.qout, p.qoscale);
+            finish_vec_q8<true>(p, e, s, st, 1.0f, p.qout, p.qoscale);
         else
-            finish_vec(p, e, s, st, 1.0f);
+            finish_vec<true>(p, e, s, st, 1.0f);
     } else {
         float4 d[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
         if (!p.first) {

@@ -58,6 +58,12 @@ namespace zgb {
 
 enum SrcKind { kPlainBf16 = 0, kPlainF32 = 1, kAccLocal = 2, kAccReduce = 3 };
 
+// Whether a kind's kernels apply a power-of-two divisor as a multiply (mean_grad).
+template <int KIND>
+__host__ __device__ constexpr bool kPow2Kind() {
+    return KIND != kPlainF32;
+}
+
 __device__ __forceinline__ void add_bf16x8(float (&s)[8], const uint4 x) {
     s[0] = __fadd_rn(s[0], bf16_lo(x.x));
     s[1] = __fadd_rn(s[1], bf16_hi(x.x));
@@ -198,9 +204,9 @@ __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, in
         float s[8];
         sum_src<KIND, R>(src[u], s);
         if constexpr (kQ8)
-            finish_vec_q8(p, (vi0 + u * stride) * 8, s, st[u], coef, p.q, p.qscale);
+            finish_vec_q8<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef, p.q, p.qscale);
         else
-            finish_vec(p, (vi0 + u * stride) * 8, s, st[u], coef);
+            finish_vec<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef);
     }
 }
 
@@ -213,9 +219,9 @@ __device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, 
     float4 st[6];
     load_state(p, e, st);
     if constexpr (kQ8)
-        finish_vec_q8(p, e, s, st, coef, p.q, p.qscale);
+        finish_vec_q8<kPow2Kind<KIND>()>(p, e, s, st, coef, p.q, p.qscale);
     else
-        finish_vec(p, e, s, st, coef);
+        finish_vec<kPow2Kind<KIND>()>(p, e, s, st, coef);
 }
 
 // One element (ragged tails and ranges not on 16-byte boundaries).
@@ -409,6 +415,9 @@ int make_scalars(const zero_adamw_t* hp, float divisor, AdamwScalars* h) {
         !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
         return ZERO_EINVAL;
     h->divisor = divisor;
+    int e2 = 0;
+    const float mant = std::frexp(divisor, &e2);          // divisor = mant * 2^e2, mant in [0.5, 1)
+    h->inv_divisor = (mant == 0.5f && e2 >= -125 && e2 <= 127) ? std::ldexp(1.0f, 1 - e2) : 0.0f;
     h->b1 = hp->beta1;
     h->b2 = hp->beta2;
     h->omb1 = 1.0f - hp->beta1;
