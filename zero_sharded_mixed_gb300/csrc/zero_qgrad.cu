@@ -132,7 +132,8 @@ __device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float
 
 // U vectors (vi0, vi0 + kThreads, ...) with a compile-time source count.
 template <int R, bool kUpdate, int U, bool kQ8>
-__device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, int64_t nv) {
+__device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, int64_t nv,
+                                           const StepScalars& sc) {
     QVec<R, kUpdate> x[U];
     bool ok[U];
 #pragma unroll
@@ -151,9 +152,9 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
 #pragma unroll
         for (int r = 0; r < R; ++r) add_codes8(s, x[u].c[r], x[u].s[r]);
         if constexpr (kQ8) {
-            finish_vec_q8<true>(p, e, s, x[u].st, 1.0f, p.qout, p.qoscale);
+            finish_vec_q8<true>(p, e, s, x[u].st, 1.0f, sc, p.qout, p.qoscale);
         } else if constexpr (kUpdate) {
-            finish_vec<true>(p, e, s, x[u].st, 1.0f);
+            finish_vec<true>(p, e, s, x[u].st, 1.0f, sc);
         } else {
             const float4 d[2] = {x[u].st[0], x[u].st[1]};
             store_acc(p, e, s, d);
@@ -163,7 +164,7 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
 
 // One vector with a runtime source count, one source at a time.
 template <bool kUpdate, bool kQ8>
-__device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) {
+__device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi, const StepScalars& sc) {
     const int64_t e = vi * 8;
     const int64_t b = (p.k0 + e) >> p.block_shift;
     float s[8];
@@ -174,9 +175,9 @@ __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) 
         float4 st[6];
         load_state(p, e, st);
         if constexpr (kQ8)
-            finish_vec_q8<true>(p, e, s, st, 1.0f, p.qout, p.qoscale);
+            finish_vec_q8<true>(p, e, s, st, 1.0f, sc, p.qout, p.qoscale);
         else
-            finish_vec<true>(p, e, s, st, 1.0f);
+            finish_vec<true>(p, e, s, st, 1.0f, sc);
     } else {
         float4 d[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
         if (!p.first) {
@@ -189,13 +190,13 @@ __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi) 
 
 // One element (ragged tails, ranges off the 8-element grid).
 template <bool kUpdate>
-__device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i) {
+__device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i, const StepScalars& sc) {
     const int64_t b = (p.k0 + i) >> p.block_shift;
     float s = 0.0f;
     for (int r = 0; r < p.n_src; ++r) s = __fadd_rn(s, __fmul_rn((float)p.q[r][i], __ldg(p.scale[r] + b)));
     if constexpr (kUpdate) {
         float w = p.w[i], m = p.m[i], v = p.v[i];
-        adamw_update(mean_grad(s, p.h, 1.0f), w, m, v, p.h, step_scalars(p.h));
+        adamw_update(mean_grad(s, p.h, 1.0f), w, m, v, p.h, sc);
         p.w[i] = w;
         p.m[i] = m;
         p.v[i] = v;
@@ -253,6 +254,7 @@ template <int R, bool kUpdate, bool kQ8 = false>
 __global__ void __launch_bounds__(kThreads, !kUpdate ? ZGB_QACC_MINBLOCKS
                                            : qgrad_vectors_per_iter<R, kUpdate>() == 1 ? ZGB_QGRAD_MINBLOCKS : 2)
 qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
+    const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if constexpr (R > 0) {
@@ -262,23 +264,24 @@ qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
             if constexpr (ZGB_QGRAD_PREFETCH > 0)
                 prefetch_chunk<R, kUpdate>(p, v0 - threadIdx.x + ZGB_QGRAD_PREFETCH * (int64_t)gridDim.x * chunk,
                                            chunk, nv);
-            qgrad_vecs<R, kUpdate, U, kQ8>(p, v0, nv);
+            qgrad_vecs<R, kUpdate, U, kQ8>(p, v0, nv, sc);
         }
     } else {
         const int64_t stride = (int64_t)gridDim.x * kThreads;
-        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, vi);
+        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, vi, sc);
     }
     if constexpr (!kQ8) {
         const int64_t tail = p.n - (nv << 3);
-        if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid);
+        if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid, sc);
     }
 }
 
 template <bool kUpdate>
 __global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_constant__ QGradParams p) {
+    const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n; i += stride)
-        qgrad_one<kUpdate>(p, i);
+        qgrad_one<kUpdate>(p, i, sc);
 }
 
 template <int R, bool kUpdate, bool kQ8 = false>

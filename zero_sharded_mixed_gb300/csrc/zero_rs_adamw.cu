@@ -185,7 +185,7 @@ __device__ __forceinline__ void sum_src_dyn(const UpdateParams& p, int64_t e, fl
 // load of all U vectors is issued before the first add.
 template <int KIND, int R, int U, bool kQ8>
 __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, int64_t stride,
-                                          int64_t nv, float coef) {
+                                          int64_t nv, float coef, const StepScalars& sc) {
     SrcRegs<KIND, R> src[U];
     float4 st[U][6];
     bool ok[U];
@@ -204,29 +204,31 @@ __device__ __forceinline__ void step_vecs(const UpdateParams& p, int64_t vi0, in
         float s[8];
         sum_src<KIND, R>(src[u], s);
         if constexpr (kQ8)
-            finish_vec_q8<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef, p.q, p.qscale);
+            finish_vec_q8<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef, sc, p.q, p.qscale);
         else
-            finish_vec<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef);
+            finish_vec<kPow2Kind<KIND>()>(p, (vi0 + u * stride) * 8, s, st[u], coef, sc);
     }
 }
 
 // One vector with a runtime source count.
 template <int KIND, bool kQ8>
-__device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, float coef) {
+__device__ __forceinline__ void step_vec_dyn(const UpdateParams& p, int64_t vi, float coef,
+                                             const StepScalars& sc) {
     const int64_t e = vi * 8;
     float s[8];
     sum_src_dyn<KIND>(p, e, s);
     float4 st[6];
     load_state(p, e, st);
     if constexpr (kQ8)
-        finish_vec_q8<kPow2Kind<KIND>()>(p, e, s, st, coef, p.q, p.qscale);
+        finish_vec_q8<kPow2Kind<KIND>()>(p, e, s, st, coef, sc, p.q, p.qscale);
     else
-        finish_vec<kPow2Kind<KIND>()>(p, e, s, st, coef);
+        finish_vec<kPow2Kind<KIND>()>(p, e, s, st, coef, sc);
 }
 
 // One element (ragged tails and ranges not on 16-byte boundaries).
 template <int KIND>
-__device__ __forceinline__ void step_one(const UpdateParams& p, int64_t i, float coef) {
+__device__ __forceinline__ void step_one(const UpdateParams& p, int64_t i, float coef,
+                                         const StepScalars& sc) {
     float s = 0.0f;
     for (int r = 0; r < p.n_src; ++r) {
         float x;
@@ -240,7 +242,7 @@ __device__ __forceinline__ void step_one(const UpdateParams& p, int64_t i, float
     }
     if constexpr (KIND == kAccReduce) s = __fadd_rn(p.acc[0][i], s);
     float w = p.w[i], m = p.m[i], v = p.v[i];
-    adamw_update(mean_grad(s, p.h, coef), w, m, v, p.h, step_scalars(p.h));
+    adamw_update(mean_grad(s, p.h, coef), w, m, v, p.h, sc);
     p.w[i] = w;
     p.m[i] = m;
     p.v[i] = v;
@@ -278,6 +280,7 @@ template <int KIND, int R, bool kQ8 = false>
 __global__ void __launch_bounds__(kThreads, ZGB_RS_MINBLOCKS)
 rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
     const float coef = clip_coef(p.h);
+    const StepScalars sc = step_scalars(p.h);
     const int64_t nv = p.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -288,22 +291,23 @@ rs_adamw_vec_kernel(const __grid_constant__ UpdateParams p) {
         constexpr int U = vectors_per_iter<KIND, R>();
         const int64_t chunk = (int64_t)U * kThreads;
         for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk)
-            step_vecs<KIND, R, U, kQ8>(p, v0, kThreads, nv, coef);
+            step_vecs<KIND, R, U, kQ8>(p, v0, kThreads, nv, coef, sc);
     } else {
-        for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND, kQ8>(p, vi, coef);
+        for (int64_t vi = tid; vi < nv; vi += stride) step_vec_dyn<KIND, kQ8>(p, vi, coef, sc);
     }
     if constexpr (!kQ8) {
         const int64_t tail = p.n - (nv << 3);
-        if (tid < tail) step_one<KIND>(p, (nv << 3) + tid, coef);
+        if (tid < tail) step_one<KIND>(p, (nv << 3) + tid, coef, sc);
     }
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads) rs_adamw_scalar_kernel(const __grid_constant__ UpdateParams p) {
     const float coef = clip_coef(p.h);
+    const StepScalars sc = step_scalars(p.h);
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n; i += stride)
-        step_one<KIND>(p, i, coef);
+        step_one<KIND>(p, i, coef, sc);
 }
 
 template <int KIND, int R, bool kQ8 = false>

@@ -126,6 +126,7 @@ rs_adamw_tma_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
     __shared__ __align__(8) uint64_t full[kStages];
     const int tid = threadIdx.x;
     const float coef = clip_coef(p.h);
+    const StepScalars sc = step_scalars(p.h);
     const int64_t n8 = (p.n >> 3) << 3;                   // the tiles cover [0, n8)
     // the k-th tile of this CTA
 #if ZGB_TMA_INTERLEAVE
@@ -191,7 +192,7 @@ rs_adamw_tma_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
             float m[4] = {m4.x, m4.y, m4.z, m4.w};
             float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) adamw_update(mean_grad(sum[q], p.h, coef), w[q], m[q], v[q], p.h, step_scalars(p.h));
+            for (int q = 0; q < 4; ++q) adamw_update(mean_grad(sum[q], p.h, coef), w[q], m[q], v[q], p.h, sc);
             st_stream_f4(p.w + e0 + j, make_float4(w[0], w[1], w[2], w[3]));
             st_stream_f4(p.m + e0 + j, make_float4(m[0], m[1], m[2], m[3]));
             st_stream_f4(p.v + e0 + j, make_float4(v[0], v[1], v[2], v[3]));
@@ -219,7 +220,7 @@ rs_adamw_tma_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
         float sum = 0.0f;
         for (int r = 0; r < NDP; ++r) sum = __fadd_rn(sum, bf16_one(static_cast<const uint16_t*>(p.src[r])[i]));
         float w = p.w[i], m = p.m[i], v = p.v[i];
-        adamw_update(mean_grad(sum, p.h, coef), w, m, v, p.h, step_scalars(p.h));
+        adamw_update(mean_grad(sum, p.h, coef), w, m, v, p.h, sc);
         p.w[i] = w;
         p.m[i] = m;
         p.v[i] = v;
@@ -334,6 +335,7 @@ rs_adamw_ws_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
         }
     } else {
         const float coef = clip_coef(p.h);
+        const StepScalars sc = step_scalars(p.h);
         const int j = (warp - 1) * 128 + lane * 4;
         for (int64_t k = 0; k < count; ++k) {
             const int s = (int)(k % kWsStages);
@@ -363,7 +365,7 @@ rs_adamw_ws_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
                 float m[4] = {m4.x, m4.y, m4.z, m4.w};
                 float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) adamw_update(mean_grad(sum[q], p.h, coef), w[q], m[q], v[q], p.h, step_scalars(p.h));
+                for (int q = 0; q < 4; ++q) adamw_update(mean_grad(sum[q], p.h, coef), w[q], m[q], v[q], p.h, sc);
                 st_stream_f4(p.w + e0 + j, make_float4(w[0], w[1], w[2], w[3]));
                 st_stream_f4(p.m + e0 + j, make_float4(m[0], m[1], m[2], m[3]));
                 st_stream_f4(p.v + e0 + j, make_float4(v[0], v[1], v[2], v[3]));
@@ -380,7 +382,7 @@ rs_adamw_ws_kernel(const __grid_constant__ UpdateParams p, int64_t n_tiles) {
             for (int r = 0; r < NDP; ++r)
                 sum = __fadd_rn(sum, bf16_one(static_cast<const uint16_t*>(p.src[r])[i]));
             float w = p.w[i], m = p.m[i], v = p.v[i];
-            adamw_update(mean_grad(sum, p.h, coef), w, m, v, p.h, step_scalars(p.h));
+            adamw_update(mean_grad(sum, p.h, coef), w, m, v, p.h, sc);
             p.w[i] = w;
             p.m[i] = m;
             p.v[i] = v;

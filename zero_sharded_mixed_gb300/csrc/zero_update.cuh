@@ -89,14 +89,14 @@ __device__ __forceinline__ float mean_grad(float sum, const AdamwScalars& h, flo
 
 // Update 8 elements at e from their source sums and loaded state; store the
 // state and return the 8 bf16 results packed in a 16-byte vector.  P is a
-// parameter block with the update target w, m, v and scalars h.
+// parameter block with the update target w, m, v and scalars h; sc is the
+// step's scalars, resolved once per thread (step_scalars).
 template <bool kPow2, class P>
 __device__ __forceinline__ uint4 update_vec(const P& p, int64_t e, const float (&s)[8],
-                                            const float4 (&st)[6], float coef) {
+                                            const float4 (&st)[6], float coef, const StepScalars& sc) {
     float w[8] = {st[0].x, st[0].y, st[0].z, st[0].w, st[1].x, st[1].y, st[1].z, st[1].w};
     float m[8] = {st[2].x, st[2].y, st[2].z, st[2].w, st[3].x, st[3].y, st[3].z, st[3].w};
     float v[8] = {st[4].x, st[4].y, st[4].z, st[4].w, st[5].x, st[5].y, st[5].z, st[5].w};
-    const StepScalars sc = step_scalars(p.h);
 #pragma unroll
     for (int j = 0; j < 8; ++j) adamw_update(mean_grad<kPow2>(s[j], p.h, coef), w[j], m[j], v[j], p.h, sc);
     st_stream_f4(p.w + e, make_float4(w[0], w[1], w[2], w[3]));
@@ -116,8 +116,8 @@ __device__ __forceinline__ uint4 update_vec(const P& p, int64_t e, const float (
 // The same, storing the bf16 results at out + e.
 template <bool kPow2, class P>
 __device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&s)[8],
-                                           const float4 (&st)[6], float coef) {
-    st_stream_u4(p.out + e, update_vec<kPow2>(p, e, s, st, coef));
+                                           const float4 (&st)[6], float coef, const StepScalars& sc) {
+    st_stream_u4(p.out + e, update_vec<kPow2>(p, e, s, st, coef, sc));
 }
 
 // The same with the 8-bit output: the bf16 results in the 8-bit block format
@@ -127,9 +127,9 @@ __device__ __forceinline__ void finish_vec(const P& p, int64_t e, const float (&
 // scale are computed exactly as by the quantizer (zero_quantize_int8).
 template <bool kPow2, class P>
 __device__ __forceinline__ void finish_vec_q8(const P& p, int64_t e, const float (&s)[8],
-                                              const float4 (&st)[6], float coef, int8_t* qout,
-                                              float* qscale) {
-    const uint4 o = update_vec<kPow2>(p, e, s, st, coef);
+                                              const float4 (&st)[6], float coef, const StepScalars& sc,
+                                              int8_t* qout, float* qscale) {
+    const uint4 o = update_vec<kPow2>(p, e, s, st, coef, sc);
     const float a = warp_block_absmax(absmax8_bits(o, 0u));
     const float inv = a == 0.0f ? 0.0f : __fdiv_rn(127.0f, a);          // a zero block: codes 0
     *reinterpret_cast<uint2*>(qout + e) = quant8(o, inv);
