@@ -38,9 +38,9 @@
 #ifndef ZGB_QACC_WAVES
 #define ZGB_QACC_WAVES 1     // accumulation: the same (measured: 5.7 TB/s at x1, 5.2 at x64)
 #endif
-#ifndef ZGB_QGRAD_PREFETCH
-#define ZGB_QGRAD_PREFETCH 0 // grid-stride passes ahead whose chunk a CTA prefetches into L2
-                             // (0: off; measured: 1 or 2 ahead cost the update 2-3 %)
+#ifndef ZGB_QGRAD_MULTI
+#define ZGB_QGRAD_MULTI 1    // 1: a call over several whole shards is one launch (blockIdx.y =
+                             // owner) when every slice takes the vector kernel; 0: one per owner
 #endif
 #ifndef ZGB_QGRAD_MINBLOCKS
 #define ZGB_QGRAD_MINBLOCKS 3 // update with one vector per thread: CTAs per SM the register
@@ -59,9 +59,14 @@
 
 namespace zgb {
 
+// One launch covers one owner's slice (owners == 0: n, k0 describe it, every
+// pointer is offset to its first element) or, with owners > 0, the slices of
+// owners o_first .. o_first + owners - 1 that meet [begin, end), one per
+// blockIdx.y (every pointer offset to `begin`, the scale pointers to the
+// start of the sources' scale arrays).
 struct QGradParams {
-    const int8_t* q[ZERO_MAX_SRC];     // rank r's codes, offset to the launch's first element
-    const float* scale[ZERO_MAX_SRC];  // rank r's block scales of this owner's slice
+    const int8_t* q[ZERO_MAX_SRC];     // rank r's codes
+    const float* scale[ZERO_MAX_SRC];  // rank r's block scales (of this owner's slice if owners == 0)
     float* w;                          // update: state, offset like q
     float* m;
     float* v;
@@ -69,13 +74,33 @@ struct QGradParams {
     float* dst;                        // accumulation: fp32 destination, offset like q
     int8_t* qout;                      // update with 8-bit output: codes, offset like w
     float* qoscale;                    // and their block scales (one per 256 elements)
-    int64_t n;                         // elements of the launch, all in one owner's slice
-    int64_t k0;                        // slice-local index of the launch's first element
+    int64_t n;                         // owners == 0: elements of the launch, in one owner's slice
+    int64_t k0;                        // owners == 0: slice-local index of its first element
+    int64_t begin, end;                // owners > 0: the flat range of the call
+    int64_t S;                         // owners > 0: shard length
+    int64_t nb;                        // owners > 0: scale blocks per shard
+    int32_t o_first;                   // owners > 0: the first owner
+    int32_t owners;
     int32_t n_src;
     int32_t block_shift;               // log2(block)
     int32_t first;                     // accumulation: 1 overwrites dst, 0 adds to it
     AdamwScalars h;
 };
+
+// The slice a CTA works on.  eoff: its first element's offset from the code
+// and target pointers; k0: that element's slice-local index (the block grid);
+// n: its length; soff: the offset of its scales from the scale pointers.
+struct QSlice {
+    int64_t eoff, k0, n, soff;
+};
+
+__device__ __forceinline__ QSlice qslice(const QGradParams& p) {
+    if (p.owners == 0) return QSlice{0, p.k0, p.n, 0};
+    const int64_t o = (int64_t)p.o_first + blockIdx.y;
+    const int64_t lo = p.begin > o * p.S ? p.begin : o * p.S;
+    const int64_t hi = p.end < (o + 1) * p.S ? p.end : (o + 1) * p.S;
+    return QSlice{lo - p.begin, lo - o * p.S, hi - lo, o * p.nb};
+}
 
 // Code j (0..3) of a 32-bit word as an fp32 value (exact: |code| <= 127).
 __device__ __forceinline__ float code_f32(uint32_t word, int j) {
@@ -100,23 +125,27 @@ struct QVec {
     float4 st[kUpdate ? 6 : 2];
 };
 
+// e: the element's index in the slice.
 template <int R, bool kUpdate>
-__device__ __forceinline__ void load_qvec(const QGradParams& p, int64_t e, QVec<R, kUpdate>& x) {
-    const int64_t b = (p.k0 + e) >> p.block_shift;
+__device__ __forceinline__ void load_qvec(const QGradParams& p, const QSlice& sl, int64_t e,
+                                          QVec<R, kUpdate>& x) {
+    const int64_t b = sl.soff + ((sl.k0 + e) >> p.block_shift);
+    const int64_t g = sl.eoff + e;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        x.c[r] = ld_stream_u2(p.q[r] + e);
+        x.c[r] = ld_stream_u2(p.q[r] + g);
         x.s[r] = __ldg(p.scale[r] + b);
     }
     if constexpr (kUpdate) {
-        load_state(p, e, x.st);
+        load_state(p, g, x.st);
     } else if (!p.first) {
-        x.st[0] = ld_stream_f4(p.dst + e);
-        x.st[1] = ld_stream_f4(p.dst + e + 4);
+        x.st[0] = ld_stream_f4(p.dst + g);
+        x.st[1] = ld_stream_f4(p.dst + g + 4);
     }
 }
 
-// The accumulation's result of one vector: (dst +) the source sum.
+// The accumulation's result of one vector: (dst +) the source sum; e indexes
+// from the target pointers.
 __device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float (&x)[8],
                                           const float4 (&d)[2]) {
     if (!p.first) {
@@ -132,20 +161,20 @@ __device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float
 
 // U vectors (vi0, vi0 + kThreads, ...) with a compile-time source count.
 template <int R, bool kUpdate, int U, bool kQ8>
-__device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, int64_t nv,
-                                           const StepScalars& sc) {
+__device__ __forceinline__ void qgrad_vecs(const QGradParams& p, const QSlice& sl, int64_t vi0,
+                                           int64_t nv, const StepScalars& sc) {
     QVec<R, kUpdate> x[U];
     bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t vi = vi0 + u * kThreads;
         ok[u] = vi < nv;
-        if (ok[u]) load_qvec<R, kUpdate>(p, vi * 8, x[u]);
+        if (ok[u]) load_qvec<R, kUpdate>(p, sl, vi * 8, x[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         if (!ok[u]) continue;
-        const int64_t e = (vi0 + u * kThreads) * 8;
+        const int64_t e = sl.eoff + (vi0 + u * kThreads) * 8;
         float s[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) s[j] = 0.0f;
@@ -164,9 +193,10 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, int64_t vi0, in
 
 // One vector with a runtime source count, one source at a time.
 template <bool kUpdate, bool kQ8>
-__device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi, const StepScalars& sc) {
-    const int64_t e = vi * 8;
-    const int64_t b = (p.k0 + e) >> p.block_shift;
+__device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, const QSlice& sl, int64_t vi,
+                                              const StepScalars& sc) {
+    const int64_t b = sl.soff + ((sl.k0 + vi * 8) >> p.block_shift);
+    const int64_t e = sl.eoff + vi * 8;
     float s[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) s[j] = 0.0f;
@@ -189,9 +219,12 @@ __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, int64_t vi, 
 }
 
 // One element (ragged tails, ranges off the 8-element grid).
+// i: the element's index in the slice.
 template <bool kUpdate>
-__device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i, const StepScalars& sc) {
-    const int64_t b = (p.k0 + i) >> p.block_shift;
+__device__ __forceinline__ void qgrad_one(const QGradParams& p, const QSlice& sl, int64_t il,
+                                          const StepScalars& sc) {
+    const int64_t b = sl.soff + ((sl.k0 + il) >> p.block_shift);
+    const int64_t i = sl.eoff + il;
     float s = 0.0f;
     for (int r = 0; r < p.n_src; ++r) s = __fadd_rn(s, __fmul_rn((float)p.q[r][i], __ldg(p.scale[r] + b)));
     if constexpr (kUpdate) {
@@ -203,38 +236,6 @@ __device__ __forceinline__ void qgrad_one(const QGradParams& p, int64_t i, const
         p.out[i] = to_bf16(w);
     } else {
         p.dst[i] = p.first ? s : __fadd_rn(p.dst[i], s);
-    }
-}
-
-// Asks the TMA engine to bring [p, p + bytes) into L2: no registers, nothing to
-// wait for.  The range is shrunk to the whole 16-byte units inside it, so the
-// prefetch never leaves the bytes the launch itself reads.
-__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
-    const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15);
-    if (hi > lo)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo))
-                     : "memory");
-}
-
-// Threads 0 .. R+2 of a CTA prefetch one array each of the CTA's chunk
-// [c0, c0 + chunk) (in vectors): the R code arrays, then w, m, v (update) or
-// dst (accumulation that adds).
-template <int R, bool kUpdate>
-__device__ __forceinline__ void prefetch_chunk(const QGradParams& p, int64_t c0, int64_t chunk,
-                                               int64_t nv) {
-    const int t = threadIdx.x;
-    if (t >= R + 3 || c0 >= nv) return;
-    const int64_t e0 = c0 * 8;
-    const int64_t n = ((c0 + chunk < nv ? c0 + chunk : nv) - c0) * 8;
-    if (t < R) {
-        prefetch_l2(p.q[t] + e0, n);
-    } else if constexpr (kUpdate) {
-        const float* a = t == R ? p.w : t == R + 1 ? p.m : p.v;
-        prefetch_l2(a + e0, n * 4);
-    } else if (t == R && !p.first) {
-        prefetch_l2(p.dst + e0, n * 4);
     }
 }
 
@@ -255,70 +256,75 @@ __global__ void __launch_bounds__(kThreads, !kUpdate ? ZGB_QACC_MINBLOCKS
                                            : qgrad_vectors_per_iter<R, kUpdate>() == 1 ? ZGB_QGRAD_MINBLOCKS : 2)
 qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
     const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
-    const int64_t nv = p.n >> 3;
+    const QSlice sl = qslice(p);
+    const int64_t nv = sl.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if constexpr (R > 0) {
         constexpr int U = qgrad_vectors_per_iter<R, kUpdate>();
         const int64_t chunk = (int64_t)U * kThreads;
-        for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk) {
-            if constexpr (ZGB_QGRAD_PREFETCH > 0)
-                prefetch_chunk<R, kUpdate>(p, v0 - threadIdx.x + ZGB_QGRAD_PREFETCH * (int64_t)gridDim.x * chunk,
-                                           chunk, nv);
-            qgrad_vecs<R, kUpdate, U, kQ8>(p, v0, nv, sc);
-        }
+        for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk)
+            qgrad_vecs<R, kUpdate, U, kQ8>(p, sl, v0, nv, sc);
     } else {
         const int64_t stride = (int64_t)gridDim.x * kThreads;
-        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, vi, sc);
+        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, sl, vi, sc);
     }
     if constexpr (!kQ8) {
-        const int64_t tail = p.n - (nv << 3);
-        if (tid < tail) qgrad_one<kUpdate>(p, (nv << 3) + tid, sc);
+        const int64_t tail = sl.n - (nv << 3);
+        if (tid < tail) qgrad_one<kUpdate>(p, sl, (nv << 3) + tid, sc);
     }
 }
 
 template <bool kUpdate>
 __global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_constant__ QGradParams p) {
     const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
+    const QSlice sl = qslice(p);
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < p.n; i += stride)
-        qgrad_one<kUpdate>(p, i, sc);
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < sl.n; i += stride)
+        qgrad_one<kUpdate>(p, sl, i, sc);
 }
 
+// p.owners == 0: one owner's slice of p.n elements; else `owners` slices of
+// at most `slice_max` elements, one per blockIdx.y, sharing the grid's CTAs.
 template <int R, bool kUpdate, bool kQ8 = false>
-int launch_qgrad_vec(const QGradParams& p, cudaStream_t s) {
+int launch_qgrad_vec(const QGradParams& p, int64_t slice_max, cudaStream_t s) {
     const int occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate, kQ8>, kThreads, 0);
     const int64_t per_cta = (int64_t)qgrad_vectors_per_iter<R, kUpdate>() * kThreads;
     const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
-    const unsigned grid = grid_for(p.n >> 3, per_cta, (int64_t)sm_count() * occupancy * waves);
+    const int64_t slices = p.owners > 0 ? p.owners : 1;
+    const int64_t cap = (int64_t)sm_count() * occupancy * waves / slices;
+    const dim3 grid(grid_for(slice_max >> 3, per_cta, cap > 0 ? cap : 1), (unsigned)slices);
     qgrad_vec_kernel<R, kUpdate, kQ8><<<grid, kThreads, 0, s>>>(p);
     return launch_status();
 }
 
+// vec: every slice of the launch takes the vector kernel (8-aligned slice
+// starts, aligned pointers); the scalar kernel serves single-owner launches.
 template <bool kUpdate, bool kQ8 = false>
-int launch_qgrad(const QGradParams& p, bool vec, cudaStream_t s) {
+int launch_qgrad(const QGradParams& p, bool vec, int64_t slice_max, cudaStream_t s) {
     if constexpr (kQ8) {                 // vector kernels only: whole 256-element blocks per warp
         if (!vec) return ZERO_EALIGN;
         switch (p.n_src) {
-            case 1: return launch_qgrad_vec<1, kUpdate, true>(p, s);
-            case 2: return launch_qgrad_vec<2, kUpdate, true>(p, s);
-            case 4: return launch_qgrad_vec<4, kUpdate, true>(p, s);
-            case 8: return launch_qgrad_vec<8, kUpdate, true>(p, s);
-            default: return launch_qgrad_vec<0, kUpdate, true>(p, s);
+            case 1: return launch_qgrad_vec<1, kUpdate, true>(p, slice_max, s);
+            case 2: return launch_qgrad_vec<2, kUpdate, true>(p, slice_max, s);
+            case 4: return launch_qgrad_vec<4, kUpdate, true>(p, slice_max, s);
+            case 8: return launch_qgrad_vec<8, kUpdate, true>(p, slice_max, s);
+            default: return launch_qgrad_vec<0, kUpdate, true>(p, slice_max, s);
         }
     }
     if (!vec) {
+        if (p.owners != 0) return ZERO_EINVAL;   // not reached: multi-owner launches are vector only
         const int occupancy = ctas_per_sm((const void*)qgrad_scalar_kernel<kUpdate>, kThreads, 0);
         const unsigned grid = grid_for(p.n, kThreads, (int64_t)sm_count() * occupancy);
         qgrad_scalar_kernel<kUpdate><<<grid, kThreads, 0, s>>>(p);
         return launch_status();
     }
     switch (p.n_src) {
-        case 1: return launch_qgrad_vec<1, kUpdate>(p, s);
-        case 2: return launch_qgrad_vec<2, kUpdate>(p, s);
-        case 4: return launch_qgrad_vec<4, kUpdate>(p, s);
-        case 8: return launch_qgrad_vec<8, kUpdate>(p, s);
-        case 16: return launch_qgrad_vec<16, kUpdate>(p, s);
-        default: return launch_qgrad_vec<0, kUpdate>(p, s);
+        case 1: return launch_qgrad_vec<1, kUpdate>(p, slice_max, s);
+        case 2: return launch_qgrad_vec<2, kUpdate>(p, slice_max, s);
+        case 4: return launch_qgrad_vec<4, kUpdate>(p, slice_max, s);
+        case 8: return launch_qgrad_vec<8, kUpdate>(p, slice_max, s);
+        case 16: return launch_qgrad_vec<16, kUpdate>(p, slice_max, s);
+        default: return launch_qgrad_vec<0, kUpdate>(p, slice_max, s);
     }
 }
 
@@ -360,15 +366,18 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
     const int64_t nb = (S + block - 1) / block;
     base.n_src = n_src;
     base.block_shift = qgrad_block_shift(block);
+    base.owners = 0;
+    base.o_first = 0;
+    base.begin = base.end = base.S = base.nb = 0;
     for (int r = n_src; r < ZERO_MAX_SRC; ++r) {
         base.q[r] = nullptr;
         base.scale[r] = nullptr;
     }
-    for (int64_t o = begin / S; o < L->n_dp; ++o) {
+    // owner o's launch parameters and whether its slice takes the vector kernel
+    auto owner_params = [&](int64_t o, QGradParams& p) {
         const int64_t lo = begin > o * S ? begin : o * S;
         const int64_t hi = end < (o + 1) * S ? end : (o + 1) * S;
-        if (lo >= hi) break;
-        QGradParams p = base;
+        p = base;
         p.n = hi - lo;
         p.k0 = lo - o * S;
         bool vec = (p.k0 & 7) == 0;
@@ -377,8 +386,42 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
             p.scale[r] = scale_src[r] + o * nb;
             vec = vec && (reinterpret_cast<uintptr_t>(p.q[r]) & 7u) == 0;
         }
-        vec = place(p, lo) && vec;
-        const int rc = launch_qgrad<kUpdate, kQ8>(p, vec, s);
+        return place(p, lo) && vec;
+    };
+    const int64_t o_first = begin / S;
+    const int64_t o_end = (end + S - 1) / S;               // owners o_first .. o_end - 1 meet the range
+    bool all_vec = true;
+    int64_t slice_max = 0;
+    QGradParams p;
+    for (int64_t o = o_first; o < o_end; ++o) {
+        all_vec = owner_params(o, p) && all_vec;
+        slice_max = p.n > slice_max ? p.n : slice_max;
+    }
+    // Whole shards only: the owners share the grid's CTAs evenly, so slices of
+    // unequal length would leave the CTAs of the short ones idle (measured:
+    // -10 % on 5e8-element buckets over three owners, +4 to +11 % on the
+    // per-unit calls over whole shards).
+    const bool whole = begin % S == 0 && end % S == 0;
+    if (ZGB_QGRAD_MULTI && whole && all_vec && o_end - o_first > 1 && o_end - o_first <= 65535) {
+        // one launch, blockIdx.y = owner: every pointer at `begin`, the scales at their start
+        p = base;
+        p.owners = (int32_t)(o_end - o_first);
+        p.o_first = (int32_t)o_first;
+        p.begin = begin;
+        p.end = end;
+        p.S = S;
+        p.nb = nb;
+        p.n = p.k0 = 0;
+        for (int r = 0; r < n_src; ++r) {
+            p.q[r] = q_src[r] + begin;
+            p.scale[r] = scale_src[r];
+        }
+        (void)place(p, begin);
+        return launch_qgrad<kUpdate, kQ8>(p, true, slice_max, s);
+    }
+    for (int64_t o = o_first; o < o_end; ++o) {
+        const bool vec = owner_params(o, p);
+        const int rc = launch_qgrad<kUpdate, kQ8>(p, vec, p.n, s);
         if (rc) return rc;
     }
     return ZERO_OK;

@@ -44,6 +44,9 @@
 #ifndef ZGB_RS_WAVES
 #define ZGB_RS_WAVES 0       // grid = resident CTAs x this; 0 = the measured choice per kind
 #endif
+#ifndef ZGB_RS_WAVES_F32
+#define ZGB_RS_WAVES_F32 32  // the same for fp32 sources alone, when ZGB_RS_WAVES is 0
+#endif
 #ifndef ZGB_RS_MULTI
 #define ZGB_RS_MULTI 1       // 0: one vector per thread and iteration everywhere
 #endif
@@ -266,12 +269,12 @@ __host__ __device__ constexpr int vectors_per_iter() {
 // stretch of each stream, which DRAM serves better than a persistent grid
 // whose every pass spans the whole range.  Measured on GB300 (GPT-2-XL and
 // Llama-7B shapes): x64 for bf16 sources and the stage-1 fused finish, x8 for
-// the stage-2 fused finish, x1 for fp32 sources (the ZeRO-3 unit update lost
-// 3 % at x64).
+// the stage-2 fused finish, x32 for fp32 sources (the ZeRO-3 unit update:
+// +3.5 % over x1, x64 and x128 0.8 % and 3 % below x32).
 template <int KIND, int R>
 __host__ __device__ constexpr int rs_waves() {
     return ZGB_RS_WAVES > 0 ? ZGB_RS_WAVES
-         : KIND == kPlainF32 ? 1 : KIND == kAccReduce ? 8 : 64;
+         : KIND == kPlainF32 ? ZGB_RS_WAVES_F32 : KIND == kAccReduce ? 8 : 64;
 }
 
 // kQ8: the output is 8-bit codes and block scales (p.q, p.qscale) instead of
