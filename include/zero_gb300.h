@@ -331,7 +331,9 @@ int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* const* q_sha
  *   (first = 1, divisor applied by the update) or stage-2 accumulation.
  * q_src and scale_src are host arrays of n_src device pointers; the codes are
  * read at flat offsets [begin, end), the scales of the owners met.  A call runs
- * one launch per owner met, in order, on `stream`.  Vector kernels need the
+ * on `stream`: one launch when [begin, end) is whole shards and every slice
+ * qualifies for the vector kernels, else one launch per owner met, in order.
+ * Vector kernels need the
  * slice-local start k a multiple of 8, 8-byte aligned codes at `begin` and
  * 16-byte aligned state, output and dst; anything else runs element by element
  * on the GPU.  Gradients must be finite.

@@ -25,9 +25,10 @@
 // reads 256 consecutive bytes of each source), the source's block scale
 // through the read-only path (blocks are >= 256 elements, so the 32 lanes of a
 // warp share one scale), the fp32 state as 128-bit loads; every load of a
-// vector is issued before the first add.  The host splits a call at owner
-// boundaries into one launch per owner, so that all elements of a launch lie
-// in one slice and the scale index is (k0 + i) >> log2(block).
+// vector is issued before the first add.  Every CTA works inside one owner's
+// slice, where the scale index is (k0 + i) >> log2(block): a call over whole
+// shards is one launch with blockIdx.y = owner, any other call one launch per
+// owner it meets.
 #include <cmath>
 
 #include "zero_update.cuh"
@@ -355,9 +356,10 @@ int check_qsource_ptrs(const int8_t* const* q_src, const float* const* scale_src
     return ZERO_OK;
 }
 
-// One launch per owner o whose slice meets [begin, end).  `place` sets the
-// target pointers of a launch covering flat [lo, hi) and returns whether they
-// allow the vector kernel.
+// The launches of a call over [begin, end): one over all owners' slices when
+// the range is whole shards and every slice takes the vector kernel, else one
+// per owner whose slice meets the range.  `place` sets the target pointers of a
+// launch starting at flat `lo` and returns whether they allow the vector kernel.
 template <bool kUpdate, bool kQ8, class Place>
 int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* const* scale_src,
               int32_t n_src, int32_t block, int64_t begin, int64_t end, QGradParams base,
