@@ -820,6 +820,7 @@ def cpu_sample(wl, n):
 
 def time_oracle(sample, seconds, n_dp):
     import oracle
+    oracle.build()                       # compiled before the timed region, if stale
     g, w, m, v = sample
     hp = oracle.AdamW(**HP)
     t = 1
@@ -833,6 +834,91 @@ def time_oracle(sample, seconds, n_dp):
         if el >= seconds:
             break
     return done / el, el, done
+
+
+WORKLOAD_SAMPLE = 1 << 19     # elements of each extra workload's oracle sample
+WORKLOAD_ORACLE_SECONDS = 1.0
+
+
+def oracle_workload_step(name, n):
+    """The oracle's statement of one step of workload `name` over a seeded host
+    sample of n owned elements with the workload's rank count and structure
+    (gathers, quantization, accumulation, clipping, update): returns (step(t),
+    elements updated per step, a description).  Runs on the host only."""
+    import numpy as np
+    import oracle
+    from zero_sharded_mixed_gb300 import inputs
+    hp = oracle.AdamW(**HP)
+    n_dp = 4 if name.startswith("accum") else 8
+    n -= n % (n_dp * 256)
+    K = 4 if name.startswith("accum") else 1
+    st = {"w": inputs.master_weights(n, n, seed=SEED).numpy(), "m": np.zeros(n, np.float32),
+          "v": np.zeros(n, np.float32)}
+    outlier = 0.01 if name == "llama7b-shard" else 0.0
+    grads = [inputs.bf16_bits(inputs.grads_bf16(n_dp, n, n, seed=SEED, step=1, micro=k, outlier_p=outlier))
+             for k in range(K)]
+    g = grads[0]
+    st["shards"] = oracle.cast_bf16(st["w"]).reshape(n_dp, -1)
+    int8w = name in ("zero3-int8", "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused")
+    int8g = name in ("gpt2xl-qgrad", "zero3-zeropp", "zero3-zeropp-fused")
+    zero3 = name.startswith("zero3")
+    if int8w:
+        st["q"] = [oracle.quantize_int8(st["shards"][o], 256) for o in range(n_dp)]
+
+    def step(t):
+        if zero3:                            # gather before forward and before backward
+            for _ in range(2):
+                if int8w:
+                    oracle.all_gather(np.stack([oracle.dequantize_int8(q, sc, 256) for q, sc in st["q"]]))
+                else:
+                    oracle.all_gather(st["shards"])
+        clip = None
+        if int8g:
+            q, sc = oracle.quantize_grad_int8(g, n_dp, 256)
+            src = oracle.accumulate_reduce_int8(None, q, sc, n_dp, 256, True)[None, :]
+        elif name == "accum-zero1":
+            acc = [None] * n_dp
+            for k in range(K):
+                acc = [oracle.accumulate_local(acc[r], grads[k][r], k == 0) for r in range(n_dp)]
+            src = np.stack(acc)
+        elif name == "accum-zero2" or (zero3 and "fused" not in name):
+            A = None
+            for k in range(K):
+                A = oracle.accumulate_reduce(A, grads[k], k == 0)
+            src = A[None, :]
+        else:
+            src = g
+        if name == "gpt2xl-clip":
+            clip = (oracle.grad_norm_sq(src, n_dp * K), 1.0)
+        out, st["w"], st["m"], st["v"] = oracle.rs_adamw_reference(src, n_dp * K, st["w"], st["m"],
+                                                                   st["v"], hp, t, clip=clip)
+        st["shards"] = out.reshape(n_dp, -1)
+        if int8w:
+            st["q"] = [oracle.quantize_int8(st["shards"][o], 256) for o in range(n_dp)]
+
+    what = ("%d owned elements, %d gradient slices%s%s%s%s" %
+            (n, n_dp, ", %d micro-batches" % K if K > 1 else "", ", two gathers" if zero3 else "",
+             ", 8-bit weights" if int8w else "", ", 8-bit gradients" if int8g else ""))
+    return step, n, what
+
+
+def time_oracle_workload(name, seconds):
+    import oracle
+    oracle.build()                       # compiled before the timed region, if stale
+    step, n, what = oracle_workload_step(name, WORKLOAD_SAMPLE)
+    step(1)                              # one untimed step (first-touch allocations)
+    t, done = 2, 0
+    t0 = time.perf_counter()
+    while True:
+        step(t)
+        t += 1
+        done += n
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%s; %d timed oracle steps after one untimed, %.1f s single-threaded"
+                      % (what, t - 2, el)}
 
 
 # --------------------------------------------------------------------------
@@ -936,6 +1022,8 @@ def run_ours(args):
                     "sample": "first %d owned elements of the workload (all %d gradient slices), "
                               "%d oracle steps, %.1f s single-threaded" % (sample[1].size, wl.n_src,
                                                                           done // sample[1].size, secs)}
+        if not is_primary and not args.no_cpu_baseline and world == 1 and rank == 0:
+            res["cpu_baseline"] = time_oracle_workload(name, WORKLOAD_ORACLE_SECONDS)
         results[name] = res
         wl.free()
         del wl

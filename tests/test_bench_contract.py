@@ -3,6 +3,8 @@ import io
 import json
 from contextlib import redirect_stdout
 
+import pytest
+
 import bench
 
 
@@ -46,3 +48,21 @@ def test_owner_count_of_a_range():
     assert bench._owners(L, 0, 101) == 2
     assert bench._owners(L, 99, 201) == 3
     assert bench._owners(L, 150, 150) == 0
+
+
+@pytest.mark.parametrize("name", ["gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
+                                  "accum-zero2", "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch",
+                                  "zero3-int8", "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused"])
+def test_every_workload_has_an_oracle_step(name):
+    """The bench times the oracle beside every workload: its statement of the
+    step runs on a small sample and moves the weights."""
+    import numpy as np
+
+    import bench
+    step, n, what = bench.oracle_workload_step(name, 4096)
+    assert n == 4096 and "owned elements" in what
+    cells = step.__closure__
+    step(1)
+    step(2)
+    st = next(c.cell_contents for c in cells if isinstance(c.cell_contents, dict) and "w" in c.cell_contents)
+    assert np.isfinite(st["w"]).all() and (st["m"] != 0).any()
