@@ -190,3 +190,60 @@ def _raw_sources(qs, ss):
     n = len(qs)
     return ((ctypes.c_void_p * n)(*[x.data_ptr() for x in qs]),
             (ctypes.c_void_p * n)(*[x.data_ptr() for x in ss]))
+
+
+def test_whole_shards_of_later_owners(zlib, cuda_device):
+    """Owners 1 and 2 of 4 over exactly their shards [S, 3S) -- one launch over
+    both slices starting at owner 1: the update into the owners' own shards,
+    the update with 8-bit output, and the accumulation into a buffer based at S,
+    each bit-exact against the oracle and writing nothing outside its range."""
+    zb = zlib
+    N, n_dp, block = 60_000, 4, 256
+    L = zb.zero_layout([N], n_dp, align=256)
+    S, P = L.shard, L.padded_n
+    g = inputs.grads_bf16(n_dp, N, P, seed=13, step=1)
+    qg, q_ref, s_ref = _quantized(zb, L, g, block)
+    qs, ss = qg.sources()
+    w0 = inputs.master_weights(N, P, seed=13)
+    z = np.zeros(P, np.float32)
+    out_ref, w_ref, m_ref, v_ref = oracle.qgrad_rs_adamw_reference(q_ref, s_ref, n_dp, block, n_dp,
+                                                                    parity.f32(w0), z, z, HP, 1)
+    sel = slice(S, 3 * S)
+    # bf16 into the owners' shards; 16-byte guard bands keep every buffer aligned
+    # for the vector kernel, so the call takes the one-launch path
+    bufs = [torch.full((2 * S + 8,), 7.0, device="cuda") for _ in range(3)]
+    bufs[0][4:-4] = w0[sel].cuda()
+    bufs[1][4:-4] = 0.0
+    bufs[2][4:-4] = 0.0
+    out = torch.full((2 * S + 16,), 5.0, dtype=torch.bfloat16, device="cuda")
+    zb.zero_reduce_scatter_adamw_int8(L, qs, ss, block, float(n_dp), 1, 3, S, 3 * S, bufs[0][4:-4],
+                                      bufs[1][4:-4], bufs[2][4:-4], out[8:-8], zb.ZERO_OUT_SHARD, _hp(zb, 1))
+    # the 8-bit output
+    w8 = w0[sel].clone().cuda()
+    m8, v8 = torch.zeros(2 * S, device="cuda"), torch.zeros(2 * S, device="cuda")
+    q8 = torch.zeros(2 * S + 32, dtype=torch.int8, device="cuda")
+    s8 = torch.full((2 * S // 256 + 2,), 9.0, device="cuda")
+    zb.zero_reduce_scatter_adamw_int8_q8(L, qs, ss, block, float(n_dp), 1, 3, S, 3 * S, w8, m8, v8,
+                                         q8[16:-16], s8[1:-1], 256, _hp(zb, 1))
+    # the accumulation into a buffer of 2S elements based at flat S
+    A = torch.full((2 * S + 8,), 11.0, device="cuda")
+    zb.zero_accumulate_int8(L, qs, ss, block, A[4:-4], S, S, 3 * S, True)
+    torch.cuda.synchronize()
+    for got, ref in zip(bufs, (w_ref, m_ref, v_ref)):
+        x = parity.f32(got)
+        parity.assert_bit_exact_f32(x[4:-4], ref[sel])
+        assert (x[:4] == 7.0).all() and (x[-4:] == 7.0).all()
+    ob = parity.bits(out)
+    assert np.array_equal(ob[8:-8], out_ref[sel])
+    five = oracle.cast_bf16(np.array([5.0], np.float32))[0]
+    assert (ob[:8] == five).all() and (ob[-8:] == five).all()
+    parity.assert_bit_exact_f32(w8, w_ref[sel])
+    for o in range(2):
+        qo, so = oracle.quantize_int8(out_ref[(1 + o) * S:(2 + o) * S], 256)
+        assert np.array_equal(q8[16 + o * S:16 + (o + 1) * S].cpu().numpy(), qo)
+        assert np.array_equal(s8[1 + o * (S // 256):1 + (o + 1) * (S // 256)].cpu().numpy(), so)
+    assert (q8[:16] == 0).all() and (q8[-16:] == 0).all() and s8[0] == 9.0 and s8[-1] == 9.0
+    A_ref = oracle.accumulate_reduce_int8(None, q_ref, s_ref, n_dp, block, True)
+    a = parity.f32(A)
+    parity.assert_bit_exact_f32(a[4:-4], A_ref[sel])
+    assert (a[:4] == 11.0).all() and (a[-4:] == 11.0).all()
