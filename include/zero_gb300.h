@@ -437,6 +437,10 @@ typedef struct {
 int zero_ckpt_write_shard(const char* path, const zero_ckpt_header_t* h, const float* master,
                           const float* m, const float* v, const uint16_t* w_bf16);
 int zero_ckpt_read_header(const char* path, zero_ckpt_header_t* h, int32_t* has_bf16);
+/* The payload CRC-32 recorded in a shard file's header (the header alone is
+ * read; zero_ckpt_read_shard verifies the payload against it).  ZERO_EINVAL
+ * (null), ZERO_EIO (cannot open), ZERO_ECORRUPT (bad magic or version). */
+int zero_ckpt_payload_crc(const char* path, uint32_t* crc);
 int zero_ckpt_read_shard(const char* path, zero_ckpt_header_t* h, float* master, float* m,
                          float* v, uint16_t* w_bf16, int64_t capacity);
 uint32_t zero_crc32(const void* data, int64_t n);

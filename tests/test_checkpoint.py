@@ -18,9 +18,29 @@ def _state(P, seed):
 
 
 def test_crc32_matches_zlib(zlib):
-    for n in (0, 1, 7, 4096, 100_003):
-        data = np.random.default_rng(n).integers(0, 256, n, dtype=np.uint8)
-        assert ck.crc32(data) == (zlib_ref.crc32(data.tobytes()) & 0xFFFFFFFF)
+    """Every length 0..40 (the 8-byte loop and the byte tail), start offsets off
+    the 8-byte grid, and long buffers."""
+    buf = np.random.default_rng(0).integers(0, 256, 1 << 20, dtype=np.uint8)
+    for n in list(range(41)) + [4096, 100_003, 1 << 20]:
+        for off in (0, 1, 3, 7):
+            data = buf[off:off + n]
+            assert ck.crc32(data) == (zlib_ref.crc32(data.tobytes()) & 0xFFFFFFFF), (n, off)
+    assert ck.crc32(np.zeros(8, np.uint8)) == (zlib_ref.crc32(bytes(8)) & 0xFFFFFFFF)
+    assert ck.crc32(np.full(9, 255, np.uint8)) == (zlib_ref.crc32(b"\xff" * 9) & 0xFFFFFFFF)
+
+
+def test_the_header_records_the_payload_crc(zlib, tmp_path):
+    S = 777
+    h = zb.ZeroCkptHeader(3100, 3108, S, 1, 2, 4, 1, 1e-4, 0.9, 0.999, 1e-8, 0.1, 0)
+    rng = np.random.default_rng(1)
+    a = [rng.standard_normal(S).astype(np.float32) for _ in range(3)]
+    w = rng.integers(0, 1 << 16, S).astype(np.uint16)
+    p = str(tmp_path / "r.bin")
+    ck.write_shard(p, h, *a, w)
+    payload = b"".join(x.tobytes() for x in a + [w])
+    assert ck.payload_crc(p) == (zlib_ref.crc32(payload) & 0xFFFFFFFF)
+    with pytest.raises(zb.ZeroError):
+        ck.payload_crc(str(tmp_path / "missing.bin"))
 
 
 def test_shard_round_trip_and_corruption(zlib, tmp_path):

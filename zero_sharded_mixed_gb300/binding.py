@@ -113,6 +113,7 @@ def load():
         lib.zero_schedule_fill.argtypes = [P(ZeroAdamW), i64, i64, p, p]
         lib.zero_schedule_advance.argtypes = [p, i64, p, p, p]
         lib.zero_crc32.argtypes = [p, i64]
+        lib.zero_ckpt_payload_crc.argtypes = [ctypes.c_char_p, P(ctypes.c_uint32)]
         lib.zero_crc32.restype = ctypes.c_uint32
         lib.zero_gather_layer_int8.argtypes = [P(ZeroLayout), P(p), P(p), i32, p, p]
         lib.zero_reduce_scatter_adamw_q8.argtypes = [
@@ -143,6 +144,7 @@ def load():
                      "zero_accumulate_adamw", "zero_grad_norm_workspace", "zero_grad_norm_sq",
                      "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
                      "zero_ckpt_write_shard", "zero_ckpt_read_header", "zero_ckpt_read_shard",
+                     "zero_ckpt_payload_crc",
                      "zero_selftest_bounded_wait", "zero_reduce_scatter_adamw_int8",
                      "zero_reduce_scatter_adamw_q8", "zero_reduce_scatter_adamw_int8_q8",
                      "zero_schedule_fill", "zero_schedule_advance",

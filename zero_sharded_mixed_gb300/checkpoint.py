@@ -16,13 +16,18 @@ Layout of a checkpoint directory:
   optionally, its bf16 weights, with a CRC-32 over the payload.
 
 The file IO and the CRC run in the native library; this module only copies
-shards between device and (pinned) host memory and lays out the files.
+shards between device and (pinned) host memory and lays out the files.  The
+rank files of one call are written or read by up to ``MAX_WORKERS`` threads at
+once (the library releases the interpreter lock while it hashes and moves
+bytes), each with its own host staging buffers.
 """
 from __future__ import annotations
 
 import ctypes
 import json
 import os
+import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -31,6 +36,11 @@ from . import binding as zb
 
 META = "meta.json"
 FORMAT = "zero_gb300 sharded checkpoint"
+MAX_WORKERS = 8        # threads writing or reading rank files at once (each stages one shard)
+
+
+def _workers(n_ranks: int) -> int:
+    return max(1, min(n_ranks, MAX_WORKERS, os.cpu_count() or 1))
 
 
 def _rank_file(rank: int) -> str:
@@ -75,6 +85,13 @@ def crc32(data) -> int:
     return int(zb.load().zero_crc32(_ptr(a) if a.size else None, a.nbytes))
 
 
+def payload_crc(path) -> int:
+    """The payload CRC-32 a shard file's header records (computed when written)."""
+    c = ctypes.c_uint32()
+    zb._check(zb.load().zero_ckpt_payload_crc(os.fsencode(path), ctypes.byref(c)), "zero_ckpt_payload_crc")
+    return int(c.value)
+
+
 def save(dirpath, L: zb.ZeroLayout, numels, master, m, v, step: int, hp: zb.ZeroAdamW,
          out_bf16=None, rank_begin: int = 0):
     """Save the owners rank_begin.. of layout L: ``master``/``m``/``v`` hold their
@@ -85,23 +102,28 @@ def save(dirpath, L: zb.ZeroLayout, numels, master, m, v, step: int, hp: zb.Zero
     n_ranks = master.numel() // S if S else 0
     if master.numel() != n_ranks * S:
         raise ValueError("master must hold whole shards")
-    crcs = {}
-    host = [torch.empty(S, dtype=torch.float32, pin_memory=torch.cuda.is_available()) for _ in range(3)]
-    hw = torch.empty(S, dtype=torch.bfloat16, pin_memory=torch.cuda.is_available()) \
-        if out_bf16 is not None else None
-    for k in range(n_ranks):
+    pin = torch.cuda.is_available()
+    local = threading.local()
+
+    def write_rank(k):
+        if not hasattr(local, "host"):        # this worker's staging buffers
+            local.host = [torch.empty(S, dtype=torch.float32, pin_memory=pin) for _ in range(3)]
+            local.hw = torch.empty(S, dtype=torch.bfloat16, pin_memory=pin) if out_bf16 is not None else None
         r = rank_begin + k
-        for dst, src in zip(host, (master, m, v)):
+        for dst, src in zip(local.host, (master, m, v)):
             dst.copy_(src[k * S:(k + 1) * S])
-        if hw is not None:
-            hw.copy_(out_bf16[r * S:(r + 1) * S])
+        if local.hw is not None:
+            local.hw.copy_(out_bf16[r * S:(r + 1) * S])
         h = zb.ZeroCkptHeader(L.n, L.padded_n, S, L.align, int(step), L.n_dp, r, hp.lr, hp.beta1,
                               hp.beta2, hp.eps, hp.weight_decay, 0)
-        arrs = [x.numpy() for x in host]
-        wb = hw.view(torch.int16).numpy().view(np.uint16) if hw is not None else None
-        write_shard(os.path.join(dirpath, _rank_file(r)), h, *arrs, wb)
-        payload = [a.view(np.uint8) for a in arrs] + ([wb.view(np.uint8)] if wb is not None else [])
-        crcs[_rank_file(r)] = crc32(np.concatenate(payload)) if payload else 0
+        arrs = [x.numpy() for x in local.host]
+        wb = local.hw.view(torch.int16).numpy().view(np.uint16) if local.hw is not None else None
+        path = os.path.join(dirpath, _rank_file(r))
+        write_shard(path, h, *arrs, wb)
+        return _rank_file(r), payload_crc(path)
+
+    with ThreadPoolExecutor(_workers(n_ranks)) as ex:
+        crcs = dict(ex.map(write_rank, range(n_ranks)))
     offsets = np.concatenate([[0], np.cumsum(numels)[:-1]]).astype(int).tolist() if len(numels) else []
     meta_path = os.path.join(dirpath, META)
     meta = {}
@@ -138,7 +160,8 @@ def restore(dirpath, L: zb.ZeroLayout, master, m, v, rank_begin: int = 0, out_bf
         raise ValueError("the checkpoint was saved for another layout: reshard it first")
     S = L.shard
     n_ranks = master.numel() // S if S else 0
-    for k in range(n_ranks):
+
+    def read_rank(k):
         r = rank_begin + k
         h, ms, mm, mv, w = read_shard(os.path.join(dirpath, _rank_file(r)),
                                       with_bf16=out_bf16 is not None)
@@ -148,6 +171,9 @@ def restore(dirpath, L: zb.ZeroLayout, master, m, v, rank_begin: int = 0, out_bf
             dst[k * S:(k + 1) * S].copy_(torch.from_numpy(src))
         if out_bf16 is not None and w is not None:
             out_bf16[r * S:(r + 1) * S].copy_(torch.from_numpy(w.view(np.int16)).view(torch.bfloat16))
+
+    with ThreadPoolExecutor(_workers(n_ranks)) as ex:
+        list(ex.map(read_rank, range(n_ranks)))
     return int(meta["step"])
 
 
