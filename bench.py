@@ -661,8 +661,8 @@ class Zero3Workload(Workload):
                         q.scales.view(-1), 256, hp)
                     self.ring.release(("bwd", i))
                 out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads, kernels=n))
-                out.append(Op("rs_adamw_int8_q8", P * (n + 25) + n * sbytes + (P // 256) * 4, rs_upd_int8_q8,
-                              kernels=n))
+                # a call over the unit's whole shards is one launch (blockIdx.y = owner)
+                out.append(Op("rs_adamw_int8_q8", P * (n + 25) + n * sbytes + (P // 256) * 4, rs_upd_int8_q8))
                 continue
             if self.fused and q is not None:
                 def rs_upd_q8(u=u, i=i, grads=grads, q=q):
@@ -680,7 +680,7 @@ class Zero3Workload(Workload):
                 n = u.layout.n_dp
                 sbytes = n * (-(-u.layout.shard // QGRAD_BLOCK)) * 4
                 out.append(Op("quantize_grad", n * (P * 3 + sbytes), quant_grads, kernels=n))
-                out.append(Op("accumulate_int8", P * (n + 4) + n * sbytes, rs_int8, kernels=n))
+                out.append(Op("accumulate_int8", P * (n + 4) + n * sbytes, rs_int8))   # one launch per unit
             else:
                 out.append(Op("accumulate_reduce", P * (2 * u.layout.n_dp + 4), rs))
             out.append(Op("rs_adamw", P * 30, upd))
