@@ -374,7 +374,7 @@ class Zero2Workload(Workload):
                     zb.zero_grad_norm_sq(self.L, self.grad_list, zb.ZERO_BF16, self.src_base,
                                          float(n_dp), s, e, self.norm.workspace, self.norm.norm_sq,
                                          j > 0)
-                out.append(Op("grad_norm", (e - s) * 2 * n_dp, fn))
+                out.append(Op("grad_norm", (e - s) * 2 * n_dp, fn, kernels=2))   # partial sums + finalize
             for s, e in self.ranges:
                 def fn(s=s, e=e):
                     zb.zero_reduce_scatter_adamw_clip(
