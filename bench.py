@@ -68,7 +68,7 @@ def parse_args(argv=None):
                                            "probe", "accum-zero1", "accum-zero2", "zero3",
                                            "zero3-int8", "zero3-prefetch", "zero3-zeropp",
                                            "zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused",
-                                           "zero3-fused-graph"],
+                                           "zero3-fused-graph", "zero3-compute", "zero3-prefetch-compute"],
                     default="gpt2xl",
                     help="probe: N = 2^26 at n_dp = 8 in one launch (about 2 GB on the device, "
                          "larger than L2), the case used for ncu section captures")
@@ -499,7 +499,9 @@ class Zero3Workload(Workload):
         self.graph = name == "zero3-fused-graph"
         self.fused = name in ("zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph")
         self.int8 = name in ("zero3-int8", "zero3-zeropp", "zero3-int8-fused", "zero3-zeropp-fused")
-        self.prefetch = name == "zero3-prefetch"
+        self.prefetch = name in ("zero3-prefetch", "zero3-prefetch-compute")
+        # a stand-in for each layer's own work, to show what the prefetch hides
+        self.with_compute = name in ("zero3-compute", "zero3-prefetch-compute")
         n_dp = 8
         self.units = []
         total = 0
@@ -574,21 +576,46 @@ class Zero3Workload(Workload):
             self.dominant = "zero3_graph_step"
             self.kernel_label = ("one CUDA graph: zgb::schedule_advance_kernel, gather_vec_kernel, "
                                  "rs_adamw_vec_kernel<0,8> (own-shard output)")
+        if self.with_compute:
+            # forward: X[T, 4096] @ W once; backward: twice (data and weight gradients),
+            # with W the gathered unit's first 4096 x cols elements (cols = P / 4096
+            # rounded down to a multiple of 64, so the rows stay 128-byte aligned)
+            self.X = torch.randn(COMPUTE_TOKENS, 4096, device=device).to(torch.bfloat16)
+            self.Y = torch.empty(COMPUTE_TOKENS * (cap // 4096), device=device, dtype=torch.bfloat16)
+
+            def compute(i, buf, phase):
+                cols = self.units[i].layout.padded_n // 4096 // 64 * 64
+                W = buf[:4096 * cols].view(4096, cols)
+                Y = self.Y[:COMPUTE_TOKENS * cols].view(COMPUTE_TOKENS, cols)
+                for _ in range(1 if phase == "fwd" else 2):
+                    torch.mm(self.X, W, out=Y)
+            self.compute_fn = compute
+            self.compute_flops = sum(3 * 2 * COMPUTE_TOKENS * 4096 * (u.layout.padded_n // 4096 // 64 * 64)
+                                     for u in self.units)
         if self.prefetch:
             self.dominant = "zero3_step_prefetched"
             self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
             self.pf = zstep.Zero3Prefetcher(self.units, self.ring, device=device)
+        if self.with_compute:
+            self.dominant = "zero3_step"
+            self.kernel_label = ("gather, stand-in layer matmuls (cuBLAS), layer RS, update"
+                                 + (", gathers one unit ahead on a side stream" if self.prefetch else ""))
         self.desc = {"workload": "llama7b_zero3_units" + ("_int8_gather" if self.int8 else "")
                      + ("_int8_grads" if self.zeropp else "")
                      + ("_fused_rs_update" if self.fused else "")
                      + ("_align256" if align == 256 else "")
                      + ("_prefetch" if self.prefetch else "")
+                     + ("_with_layer_compute" if self.with_compute else "")
                      + ("_cuda_graph" if self.graph else ""),
                      "model": "Llama-7B shapes",
                      "units": len(self.units), "N": sum(u.layout.n for u in self.units), "n_dp": n_dp,
                      "ring_slots": 2}
         if self.int8:
             self.desc["quant_block"] = 256
+        if self.with_compute:
+            self.desc["layer_compute"] = ("stand-in: bf16 X[%d, 4096] @ unit[4096, cols], once forward, "
+                                          "twice backward (cuBLAS), %.3g FLOP per step"
+                                          % (COMPUTE_TOKENS, self.compute_flops))
         self.device_bytes = total * (12 + 2) + 2 * cap * 2 + g.numel() * 2 + cap * 4
         if self.zeropp:
             self.device_bytes += self.qg.q.numel() + self.qg.scales.numel() * 4
@@ -602,13 +629,27 @@ class Zero3Workload(Workload):
     def _step_ops(self, hp):
         zb, zs = self.zb, self.zstep
         out = []
+        grads_of = lambda i: [self._g[r, :self.units[i].layout.padded_n] for r in range(self.units[i].layout.n_dp)]
         if self.prefetch:
             def step_all():
-                zs.zero3_step_prefetched(
-                    self.pf, lambda i: [self._g[r, :self.units[i].layout.padded_n]
-                                        for r in range(self.units[i].layout.n_dp)], self.A, hp)
-            out.append(Op("zero3_step_prefetched", self.elems * self.bytes_per_elem, step_all,
-                          kernels=4 * len(self.units)))
+                zs.zero3_step_prefetched(self.pf, grads_of, self.A, hp,
+                                         compute=self.compute_fn if self.with_compute else None)
+            out.append(Op("zero3_step" if self.with_compute else "zero3_step_prefetched",
+                          self.elems * self.bytes_per_elem, step_all, kernels=4 * len(self.units)))
+            return out
+        if self.with_compute:
+            def step_seq():
+                for i, u in enumerate(self.units):
+                    self.compute_fn(i, zs.zero3_gather(u, self.ring, ("fwd", i)), "fwd")
+                    self.ring.release(("fwd", i))
+                for i in reversed(range(len(self.units))):
+                    u = self.units[i]
+                    P = u.layout.padded_n
+                    self.compute_fn(i, zs.zero3_gather(u, self.ring, ("bwd", i)), "bwd")
+                    zs.zero3_layer_reduce_scatter(u, grads_of(i), self.A[:P])
+                    self.ring.release(("bwd", i))
+                    zs.zero3_update(u, self.A[:P], hp)
+            out.append(Op("zero3_step", self.elems * self.bytes_per_elem, step_seq, kernels=4 * len(self.units)))
             return out
         for i, u in enumerate(self.units):
             P = u.layout.padded_n
@@ -699,7 +740,8 @@ def make_workload(name, device, elems=0):
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
     if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused",
-                "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph"):
+                "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph", "zero3-compute",
+                "zero3-prefetch-compute"):
         return Zero3Workload(name, device, elems)
     raise ValueError(name)
 
@@ -836,6 +878,7 @@ def time_oracle(sample, seconds, n_dp):
     return done / el, el, done
 
 
+COMPUTE_TOKENS = 1024         # tokens of the stand-in layer compute of the ZeRO-3 overlap workloads
 WORKLOAD_SAMPLE = 1 << 19     # elements of each extra workload's oracle sample
 WORKLOAD_ORACLE_SECONDS = 1.0
 
@@ -1009,6 +1052,7 @@ def run_ours(args):
     primary = args.workload
     extras = [w for w in ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
                           "accum-zero2", "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch",
+                          "zero3-compute", "zero3-prefetch-compute",
                           "zero3-int8",
                           "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused")
               if w != primary]
@@ -1079,6 +1123,15 @@ def run_ours(args):
         wl.free()
         del wl
         torch.cuda.empty_cache()
+
+    if "zero3-compute" in results and "zero3-prefetch-compute" in results:
+        seq, pf = results["zero3-compute"]["ms_per_step"], results["zero3-prefetch-compute"]["ms_per_step"]
+        gathers = results["zero3"]["kernels"]["gather"]["ms_per_step"] if "zero3" in results else None
+        results["zero3-prefetch-compute"]["overlap"] = {
+            "sequential_ms": seq, "prefetched_ms": pf, "hidden_ms": seq - pf,
+            "gather_ms_alone": gathers,
+            "note": "the same step with the stand-in layer compute, gathers in line vs one unit ahead "
+                    "on a side stream; gather_ms_alone is the gathers' own time in the zero3 workload"}
 
     checkpoint = None
     if rank == 0 and not args.no_extra and not args.elems and primary != "probe":

@@ -52,7 +52,8 @@ def test_owner_count_of_a_range():
 
 @pytest.mark.parametrize("name", ["gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
                                   "accum-zero2", "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch",
-                                  "zero3-int8", "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused"])
+                                  "zero3-int8", "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused",
+                                  "zero3-compute", "zero3-prefetch-compute"])
 def test_every_workload_has_an_oracle_step(name):
     """The bench times the oracle beside every workload: its statement of the
     step runs on a small sample and moves the weights."""
