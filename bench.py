@@ -597,6 +597,8 @@ class Zero3Workload(Workload):
             self.kernel_label = "gathers on a side stream one unit ahead of RS + update"
             self.pf = zstep.Zero3Prefetcher(self.units, self.ring, device=device)
         if self.with_compute:
+            # the step's HBM bytes over the whole step, matmuls included: not a kernel roofline
+            self.bound = "mixed"
             self.dominant = "zero3_step"
             self.kernel_label = ("gather, stand-in layer matmuls (cuBLAS), layer RS, update"
                                  + (", gathers one unit ahead on a side stream" if self.prefetch else ""))
@@ -1084,7 +1086,7 @@ def run_ours(args):
             "hbm_gbs_step": bytes_step / (ms_step / 1e3) / 1e9,
             "bytes_per_param_step": wl.bytes_per_elem,
             "config": dict(wl.desc, l2="inputs %.1f GB > 129 MB L2, no flush" % (wl.device_bytes / 1e9)),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "roofline": {"bound": getattr(wl, "bound", "hbm"), "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": (tpe * dom_bytes / wl.bytes_per_elem) if tpe is not None else None,
                          "algorithmic_bytes_per_launch": dom_bytes,
