@@ -10,18 +10,24 @@ One step is one pass of the path over the workload.  The headline workload
 blocks, d 1600, ffn 6400, vocab 50257) flattened for n_dp = 8 simulated ranks
 with 5e8-element buckets, every owned shard updated each step.  Measured in the
 same run and reported under "workloads", with fewer steps:
-  llama7b-shard  one owned shard of Llama-7B shapes (S = 842,301,952), 8 slices
-                 with 1 % outliers x100;
-  gpt2xl-clip    the GPT-2-XL step with clipping by the global gradient norm
-                 (a norm pass, then the clipped fused update);
-  accum-zero1/2  gradient accumulation, GPT-2-XL shapes, n_dp = 4, 4 micro-batches,
-                 in the stage-1 and stage-2 orders;
-  zero3          the per-unit gather / reduce-scatter / update path over the 34
-                 Llama-7B units at n_dp = 8;
-  zero3-prefetch the same with each unit's gather issued one unit ahead on a
-                 side stream (at most two units resident);
-  zero3-int8     the same with 8-bit weight gathers (ZeRO++): each owner
-                 re-quantizes its shard after the update.
+  llama7b-shard       one owned shard of Llama-7B shapes (S = 842,301,952), 8 slices
+                      with 1 % outliers x100;
+  gpt2xl-clip         the GPT-2-XL step with clipping by the global gradient norm
+                      (a norm pass, then the clipped fused update);
+  gpt2xl-qgrad        the GPT-2-XL step with ZeRO++ 8-bit gradients;
+  accum-zero1/2       gradient accumulation, GPT-2-XL shapes, n_dp = 4, 4
+                      micro-batches, in the stage-1 and stage-2 orders;
+  zero3               the per-unit gather / reduce-scatter / update path over the
+                      34 Llama-7B units at n_dp = 8;
+  zero3-fused         the same with each unit's reduce-scatter and update in one
+                      pass; zero3-fused-graph: that step captured in a CUDA graph;
+  zero3-prefetch      each unit's gather issued one unit ahead on a side stream;
+  zero3-compute,      the unfused step with a stand-in layer matmul per unit,
+  zero3-prefetch-compute   gathers in line, and one unit ahead;
+  zero3-int8[-fused]  8-bit weight gathers (ZeRO++);
+  zero3-zeropp[-fused] both ZeRO++ 8-bit paths.
+Each carries the oracle timed on the same kind of step beside it
+(cpu_baseline), and the line ends with a checkpoint save / restore timing.
 Every launch is timed with CUDA events on its stream; `roofline` uses the
 dominant kernel's algorithmic bytes per launch over its average launch time.
 
