@@ -140,3 +140,18 @@ def test_schedule_past_its_table_is_reported(zlib, cuda_device):
     assert e.value.code == zb.ZERO_ERANGE
     assert int(sch.index.item()) == 2
     zb.zero_status_check()                                      # reported once
+
+
+def test_the_adamw_block_keeps_its_schedule_memory(zlib, cuda_device):
+    """A block made with sched=<a temporary tensor> holds that tensor, so the
+    pointer it carries stays valid after the caller drops its own reference."""
+    import gc
+    import weakref
+    zb = zlib
+    hp = zb.ZeroAdamW.make(LR, B1, B2, EPS, WD, 1, sched=torch.tensor([LR, 0.1, 0.001], device="cuda"))
+    ref = weakref.ref(hp._sched_tensor)
+    gc.collect()
+    assert ref() is not None and hp.sched == ref().data_ptr()
+    del hp
+    gc.collect()
+    assert ref() is None

@@ -63,11 +63,14 @@ class ZeroAdamW(ctypes.Structure):
     @classmethod
     def make(cls, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1, sched=None):
         """sched: None, or a CUDA float32 tensor of 3 elements {lr, bc1, bc2}
-        that the kernels read in place of lr and step."""
+        that the kernels read in place of lr and step.  The block keeps a
+        reference to it, so the memory outlives every call made with the block."""
         ptr = None
         if sched is not None:
             ptr = _tensor(sched, "sched", torch.float32, 3)
-        return cls(lr, beta1, beta2, eps, weight_decay, 0, step, ptr)
+        hp = cls(lr, beta1, beta2, eps, weight_decay, 0, step, ptr)
+        hp._sched_tensor = sched
+        return hp
 
 
 _lock = threading.Lock()
