@@ -17,7 +17,9 @@ _BINDING_NAMES = {
     "zero_reduce_scatter_adamw_int8", "zero_accumulate_int8", "zero_reduce_scatter_adamw_q8",
     "zero_reduce_scatter_adamw_int8_q8", "zero_schedule_fill", "zero_schedule_advance",
     "zero_status_check", "zero_strerror", "zero_memory_bytes", "zero_comm_bytes",
-    "zero_bucket_range", "zero_shard_range", "zero_selftest_bounded_wait", "ZERO_ETIMEOUT",
+    "zero_bucket_range", "zero_shard_range", "zero_selftest_bounded_wait", "zero_lr_warmup_decay",
+    "ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ERANGE", "ZERO_ECUDA", "ZERO_ETIMEOUT",
+    "ZERO_EIO", "ZERO_ECORRUPT",
     "ZERO_BF16", "ZERO_F32", "ZERO_OUT_FULL", "ZERO_OUT_SHARD",
     "ZERO_ACC_LOCAL", "ZERO_ACC_REDUCE", "ZERO_MAX_SRC",
 }
