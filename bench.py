@@ -853,7 +853,15 @@ def time_e2e(wl, steps, warmup, t0, dist):
     torch.cuda.synchronize()
     barrier(dist)
     ms = start.elapsed_time(end) / steps
-    return ms, host_g.numel() * 2, host_out.numel() * 2
+    # the host link on this machine: one plain copy of the step's gradients, pinned host to device
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    wl.grads.copy_(host_g, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    link_gbs = host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9
+    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs
 
 
 def cpu_sample(wl, n):
@@ -1107,11 +1115,16 @@ def run_ours(args):
                 fits = host_fits(need * int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
                 if all_ranks_agree(dist, fits, device):
                     e2e_steps = max(1, min(args.steps, 10))
-                    e_ms, h2d, d2h = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
+                    e_ms, h2d, d2h, link_gbs = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
                     e_ms = max_over_ranks(dist, e_ms, device)
+                    link_ms = h2d / (link_gbs * 1e9) * 1e3
                     res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
                                   "ms_per_step": e_ms, "steps": e2e_steps,
-                                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                  "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
+                                           "frac": link_ms / e_ms,
+                                           "note": "one plain pinned host-to-device copy of the step's "
+                                                   "gradients on this box, after the e2e steps"}}
                 else:
                     res["e2e"] = {"value": None, "unit": UNIT,
                                   "unavailable": "host memory: %s local ranks x %.1f GB of pinned "
