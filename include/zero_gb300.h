@@ -13,7 +13,9 @@
  *  - Memory: the caller owns every buffer.  The library never allocates or
  *    frees device memory and never synchronizes, except zero_status_check().
  *    Every buffer argument must be device memory of the current device
- *    (checked: host or other-device pointers give ZERO_EINVAL) and at least
+ *    (checked: host or other-device pointers give ZERO_EINVAL; the gradient
+ *    sources of zero_reduce_scatter_adamw may also be pinned host memory, and
+ *    the layout, schedule-table and checkpoint calls work on host memory) and at least
  *    element-aligned (2 bytes for bf16, 4 for fp32; else ZERO_EALIGN).  When all
  *    the pointers of a call, after offsetting to the start of the range, are
  *    16-byte aligned the kernels move 128-bit vectors; otherwise the same
@@ -45,9 +47,10 @@ enum {
     ZERO_OK = 0,
     ZERO_EINVAL = -1,   /* an argument is out of its domain (null, range, mode, pointer kind) */
     ZERO_EALIGN = -2,   /* a pointer is not aligned to its element size */
-    ZERO_ERANGE = -3,   /* a size does not fit (int64 overflow, too many sources) */
+    ZERO_ERANGE = -3,   /* a size does not fit (int64 overflow, too many sources), or a
+                           step schedule was advanced past its table */
     ZERO_ECUDA = -4,    /* the CUDA runtime reported an error (launch or earlier async fault) */
-    ZERO_ETIMEOUT = -5, /* reserved: a bounded device-side wait gave up */
+    ZERO_ETIMEOUT = -5, /* a bounded device-side wait gave up (zero_status_check) */
     ZERO_EIO = -6,      /* a checkpoint file could not be opened, written or read */
     ZERO_ECORRUPT = -7  /* a checkpoint file has a wrong magic, version or CRC */
 };
@@ -191,12 +194,14 @@ int zero_reduce_scatter_adamw_q8(const zero_layout_t* L, const void* const* src,
  *
  * zero_grad_norm_sq: for every flat i in [begin, end) forms the mean gradient
  *   g_i exactly as zero_reduce_scatter_adamw does (same sources, base, divisor)
- *   and adds g_i^2 (exact in fp64) into an fp64 sum; *norm_sq (DEVICE pointer,
- *   8-byte aligned) receives the sum (accumulate = 0) or has it added
- *   (accumulate = 1, for the second and later buckets of one step).  Nothing
- *   is returned to the host.  The summation order is fixed for a given GPU and
- *   range, so results repeat run to run; against a sequential fp64 sum they
- *   differ only by fp64 rounding.
+ *   and sums g_i^2: each thread in a compensated pair of fp32 values (about 48
+ *   significant bits; squares outside that pair's exact range in fp64), then
+ *   fp64 across threads and CTAs.  *norm_sq (DEVICE pointer, 8-byte aligned)
+ *   receives the sum (accumulate = 0) or has it added (accumulate = 1, for the
+ *   second and later buckets of one step).  Nothing is returned to the host.
+ *   The summation order is fixed for a given GPU and range, so results repeat
+ *   run to run; against a sequential fp64 sum they differ by about 1e-12
+ *   relative.
  *   workspace: DEVICE scratch of at least zero_grad_norm_workspace() bytes,
  *   8-byte aligned, owned by the caller; its contents on entry do not matter and
  *   are overwritten (per-CTA partial sums).  Calls that share a workspace must
@@ -333,10 +338,9 @@ int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* const* q_sha
  * read at flat offsets [begin, end), the scales of the owners met.  A call runs
  * on `stream`: one launch when [begin, end) is whole shards and every slice
  * qualifies for the vector kernels, else one launch per owner met, in order.
- * Vector kernels need the
- * slice-local start k a multiple of 8, 8-byte aligned codes at `begin` and
- * 16-byte aligned state, output and dst; anything else runs element by element
- * on the GPU.  Gradients must be finite.
+ * Vector kernels need the slice-local start k a multiple of 8, 8-byte aligned
+ * codes at `begin` and 16-byte aligned state, output and dst; anything else
+ * runs element by element on the GPU.  Gradients must be finite.
  * Errors: ZERO_EINVAL (null, block not 256/512/1024/2048, range, pointer kind,
  * hyper-parameters), ZERO_ERANGE (n_src > ZERO_MAX_SRC), ZERO_EALIGN (scales
  * not 4-byte aligned, state or dst not element-aligned), ZERO_ECUDA. */
@@ -450,8 +454,9 @@ uint32_t zero_crc32(const void* data, int64_t n);
  * this thread) failed; ZERO_ETIMEOUT if a bounded device-side wait (the
  * mbarrier waits of the TMA-staged update) gave up since the last check -- the
  * kernel that gave up recorded it, drained its own copies and returned, so
- * the context stays usable; the record is cleared by this call.  Else ZERO_OK.
- * The only call that blocks. */
+ * the context stays usable; the record is cleared by this call.  ZERO_ERANGE
+ * if a zero_schedule_advance found its index past the table since the last
+ * check (also cleared).  Else ZERO_OK.  The only call that waits on the GPU. */
 int zero_status_check(void* stream);
 
 /* Launches one CTA that waits on an mbarrier nothing ever completes, bounded
