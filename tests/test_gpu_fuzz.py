@@ -4,13 +4,15 @@ Each case draws a layout (tensor split, rank count, alignment, bucket), a
 source count and dtype, an owner range and a flat sub-range inside it (starts
 off the 8-element grid included), a source base, an output mode, non-zero
 optimizer state and hyper-parameters, then checks every element in the range
-bit for bit against the oracle and every element outside it unchanged."""
+bit for bit against the oracle and every element outside it unchanged.  The
+8-bit-output updates and the clipped update are drawn the same way."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from tests import parity
+from zero_sharded_mixed_gb300 import step as zstep
 
 pytestmark = pytest.mark.gpu
 
@@ -193,3 +195,107 @@ def test_int8_gradient_paths(zlib, cuda_device, case):
     assert (ob[rest] == SENTINEL_BF16).all(), what + "output outside the range"
     A_ref = oracle.reduce_mean(deq[:, a:b].copy(), 1.0)
     parity.assert_bit_exact_f32(parity.f32(A)[:b - a], A_ref, what=f"case {case}: accumulation [{a}, {b}) ")
+
+
+def _range256(rng, L):
+    """Owners and a non-empty range on the 256-element grid (L laid out with align 256)."""
+    rb = int(rng.integers(0, L.n_dp))
+    re = int(rng.integers(rb + 1, L.n_dp + 1))
+    blocks = (re - rb) * L.shard // 256
+    a, b = _span(rng, 0, blocks)
+    return rb, re, rb * L.shard + 256 * a, rb * L.shard + 256 * b
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_updates_with_8bit_output(zlib, cuda_device, case):
+    """The update writing the 8-bit block format, from bf16 gradients and from
+    8-bit gradients: codes and scales equal the oracle's quantization of the
+    oracle's bf16 result; the state as for the bf16 output."""
+    zb = zlib
+    rng = np.random.default_rng(5000 + case)
+    n_dp = int(rng.integers(1, 13))
+    L = zb.zero_layout([int(rng.integers(1, 120_000))], n_dp, align=256)
+    S, P = L.shard, L.padded_n
+    rb, re, begin, end = _range256(rng, L)
+    own = (re - rb) * S
+    sel = slice(begin - rb * S, end - rb * S)
+    hp, t = _hp(rng), int(rng.integers(1, 1000))
+    mk = lambda: zb.ZeroAdamW.make(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, t)
+    w0 = (rng.standard_normal(own) * 0.02).astype(np.float32)
+    m0 = (rng.standard_normal(own) * 1e-3).astype(np.float32)
+    v0 = (rng.random(own) * 1e-6).astype(np.float32)
+    g = _bf16_rows(rng, n_dp, P, 1e-2)
+    block = int(rng.choice([256, 512, 1024, 2048]))
+    nb = -(-S // block)
+    q = torch.empty((n_dp, P), dtype=torch.int8, device="cuda")
+    sc = torch.empty((n_dp, n_dp * nb), device="cuda")
+    for r in range(n_dp):
+        zb.zero_quantize_int8(L, g[r].cuda(), q[r], sc[r], block)
+    q_ref, s_ref = oracle.quantize_grad_int8(parity.bits(g), n_dp, block)
+    deq = oracle.dequantize_grad_int8(q_ref, s_ref, n_dp, block)
+    for kind in ("bf16", "int8"):
+        st = [torch.from_numpy(x.copy()).cuda() for x in (w0, m0, v0)]
+        codes = torch.zeros(own, dtype=torch.int8, device="cuda")
+        scales = torch.full((own // 256,), 9.0, device="cuda")
+        if kind == "bf16":
+            zb.zero_reduce_scatter_adamw_q8(L, [g[r].cuda() for r in range(n_dp)], zb.ZERO_BF16, 0, float(n_dp),
+                                            rb, re, begin, end, *st, codes, scales, 256, mk())
+            rows = parity.bits(g[:, begin:end].contiguous())
+        else:
+            zb.zero_reduce_scatter_adamw_int8_q8(L, [q[r] for r in range(n_dp)], [sc[r] for r in range(n_dp)],
+                                                 block, float(n_dp), rb, re, begin, end, *st, codes, scales,
+                                                 256, mk())
+            rows = deq[:, begin:end].copy()
+        torch.cuda.synchronize()
+        out_ref, *ref = oracle.rs_adamw_reference(rows, float(n_dp), w0[sel], m0[sel], v0[sel], hp, t)
+        what = f"case {case} {kind}: n_dp={n_dp} S={S} ranks {rb}..{re} [{begin}, {end}) "
+        for got, r in zip(st, ref):
+            parity.assert_bit_exact_f32(parity.f32(got)[sel], r, what=what)
+        qo, so = oracle.quantize_int8(out_ref, 256)
+        c = codes.cpu().numpy()
+        assert np.array_equal(c[sel], qo), what + "codes"
+        s8 = scales.cpu().numpy()
+        k0 = (begin - rb * S) // 256
+        assert np.array_equal(s8[k0:k0 + len(so)].view(np.uint32), so.view(np.uint32)), what + "scales"
+        untouched = np.ones(own // 256, bool)
+        untouched[k0:k0 + len(so)] = False
+        assert (s8[untouched] == 9.0).all(), what + "scales outside the range"
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_clipped_update(zlib, cuda_device, case):
+    """The squared global norm over random buckets, then the clipped update:
+    the norm within 1e-12 of the oracle's fp64 sum, the clip coefficient and so
+    the state within the contract's tolerance (bit-exact whenever the fp32
+    coefficient agrees)."""
+    zb = zlib
+    rng = np.random.default_rng(6000 + case)
+    L = _layout(zb, rng)
+    P, n_dp = L.padded_n, L.n_dp
+    n_src = int(rng.integers(1, 13))
+    g = _bf16_rows(rng, n_src, P, float(rng.choice([1e-3, 1.0, 30.0])))
+    srcs = [g[r].cuda() for r in range(n_src)]
+    divisor = float(n_src)
+    max_norm = float(rng.choice([0.1, 1.0, 1e6]))
+    bufs = zstep.NormBuffers("cuda")
+    cuts = sorted({0, P, *(int(x) for x in rng.integers(0, P + 1, size=int(rng.integers(0, 4))))})
+    for j, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        zb.zero_grad_norm_sq(L, srcs, zb.ZERO_BF16, 0, divisor, a, b, bufs.workspace, bufs.norm_sq, j > 0)
+    torch.cuda.synchronize()
+    rows = parity.bits(g)
+    ref_norm = oracle.grad_norm_sq(rows, divisor)
+    got_norm = float(bufs.norm_sq.item())
+    assert abs(got_norm - ref_norm) <= 1e-12 * ref_norm + 1e-300, (case, got_norm, ref_norm)
+    hp, t = _hp(rng), int(rng.integers(1, 1000))
+    w0 = (rng.standard_normal(P) * 0.02).astype(np.float32)
+    z = np.zeros(P, np.float32)
+    st = [torch.from_numpy(x.copy()).cuda() for x in (w0, z, z)]
+    out = torch.empty(P, dtype=torch.bfloat16, device="cuda")
+    zb.zero_reduce_scatter_adamw_clip(L, srcs, zb.ZERO_BF16, 0, divisor, 0, n_dp, 0, P, *st, out,
+                                      zb.ZERO_OUT_FULL,
+                                      zb.ZeroAdamW.make(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, t),
+                                      bufs.norm_sq, max_norm)
+    torch.cuda.synchronize()
+    out_ref, *ref = oracle.rs_adamw_reference(rows, divisor, w0, z, z, hp, t, clip=(ref_norm, max_norm))
+    parity.assert_state(st, ref, exact=False, what=f"case {case}: ")
+    parity.assert_bf16_close(out, out_ref)
