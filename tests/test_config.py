@@ -19,8 +19,8 @@ def test_reads_the_keys_of_a_deepspeed_configuration():
     assert (cfg.gradient_clipping, cfg.lr, cfg.betas, cfg.eps, cfg.weight_decay) == (1.0, 3e-4, (0.9, 0.95),
                                                                                     1e-8, 0.1)
     assert not cfg.zero_quantized_weights and not cfg.zero_quantized_gradients
-    assert cfg.ignored == ["train_micro_batch_size_per_gpu", "zero_optimization.contiguous_gradients",
-                           "zero_optimization.overlap_comm"]
+    assert cfg.ignored == ["train_micro_batch_size_per_gpu", "zero_optimization.contiguous_gradients"]
+    assert cfg.overlap_comm
 
 
 def test_defaults_and_zeropp_switches():

@@ -7,6 +7,7 @@ import torch
 import oracle
 from tests import parity
 from zero_sharded_mixed_gb300 import inputs
+from zero_sharded_mixed_gb300 import step as zstep
 from zero_sharded_mixed_gb300.config import ZeroConfig
 from zero_sharded_mixed_gb300.engine import Zero3Engine, ZeroEngine
 
@@ -182,3 +183,51 @@ def test_engines_follow_the_scheduler(zlib, cuda_device):
 def cfg_opt():
     return {"type": "AdamW", "params": {"lr": HP.lr, "betas": [HP.beta1, HP.beta2], "eps": HP.eps,
                                         "weight_decay": HP.weight_decay}}
+
+
+@pytest.mark.parametrize("qw", [False, True])
+def test_zero3_engine_overlap_comm(zlib, cuda_device, qw):
+    """overlap_comm: every gather after the first is served from a prefetch one
+    unit ahead on a side stream; the gathered weights and the step's state are
+    bit-identical to the engine without it, with at most two units resident."""
+    n_dp = 4
+    units = [[4097], [33_031], [1000, 24, 3, 5000], [77]]
+
+    def run(overlap):
+        cfg = ZeroConfig.from_dict({"zero_optimization": {"stage": 3, "overlap_comm": overlap,
+                                                          "zero_quantized_weights": qw},
+                                    "optimizer": cfg_opt()})
+        eng = Zero3Engine(units, n_dp, cfg)
+        for i, u in enumerate(eng.units):
+            u.master.copy_(inputs.master_weights(u.layout.n, u.layout.padded_n, seed=40 + i).cuda())
+            u.shards.copy_(u.master.view(n_dp, -1).to(torch.bfloat16))
+            if eng.q8 is not None:
+                zstep.zero3_quantize(u, eng.q8[i])
+        seen, served = [], 0
+        for t in (1, 2):
+            for i in range(len(units)):
+                served += int(eng.pf is not None and ("fwd", i) in eng.pf.pending)
+                seen.append(eng.gather(i, "fwd").clone())
+                eng.release(i, "fwd")
+            for i in reversed(range(len(units))):
+                served += int(eng.pf is not None and ("bwd", i) in eng.pf.pending)
+                seen.append(eng.gather(i, "bwd").clone())
+                eng.release(i, "bwd")
+                u = eng.units[i]
+                eng.backward(i, inputs.grads_bf16(n_dp, u.layout.n, u.layout.padded_n, seed=50 + i,
+                                                  step=t).cuda())
+            eng.step()
+        torch.cuda.synchronize()
+        assert eng.ring.peak <= 2 and eng.ring.resident == 0
+        return eng, seen, served
+
+    a, seen_a, served_a = run(False)
+    b, seen_b, served_b = run(True)
+    assert served_a == 0 and served_b == 2 * (2 * len(units) - 1)     # all but each step's first gather
+    assert not b.pf.pending
+    for x, y in zip(seen_a, seen_b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    for ua, ub in zip(a.units, b.units):
+        for x, y in ((ua.master, ub.master), (ua.m, ub.m), (ua.v, ub.v), (ua.shards, ub.shards)):
+            assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
+                               y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16))

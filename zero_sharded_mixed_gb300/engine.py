@@ -10,11 +10,15 @@ sequence of library calls (step.py) that one training step needs:
   once; stage 2 reduce-scatters every micro-batch ("ZeRO and FSDP", the
   paragraph on gradient accumulation).  The last micro-batch is fused into the
   update unless clipping needs the whole gradient's norm first.
-* ``Zero3Engine`` (stage 3, per unit): ``gather(i)`` before a unit's forward
-  or backward, ``release(i)`` after, ``backward(i, grads, micro)`` with the
-  unit's gradient, ``step()`` at the end.  With one micro-batch and no
-  clipping a unit is updated as soon as its gradient is reduced (one pass);
-  otherwise the reduced gradients wait in fp32 until ``step()``.
+* ``Zero3Engine`` (stage 3, per unit): ``gather(i, phase)`` before a unit's
+  forward (phase "fwd") or backward ("bwd"), ``release(i, phase)`` after,
+  ``backward(i, grads, micro)`` with the unit's gradient, ``step()`` at the
+  end.  With one micro-batch and no clipping a unit is updated as soon as its
+  gradient is reduced (one pass); otherwise the reduced gradients wait in fp32
+  until ``step()``.  With ``overlap_comm`` each gather also starts the next
+  unit's gather on a side stream (forward in order, then backward in reverse:
+  "DeepSpeed ZeRO", "Stage 3 step by step", prefetching), when a ring slot is
+  free.
 
 Every element is computed by the library's kernels; the engines only hold
 buffers and order the calls.
@@ -168,17 +172,46 @@ class Zero3Engine:
         self.A = None if self.fused else [torch.empty(u.layout.padded_n, device=device)
                                           for u in self.units]
         self.norm = zs.NormBuffers(device) if config.gradient_clipping > 0 else None
+        self.pf = zs.Zero3Prefetcher(self.units, self.ring, int8=self.q8, device=device) \
+            if config.overlap_comm else None
         self.t = 0
 
-    def gather(self, i: int, tag="use") -> torch.Tensor:
-        """Unit i's full bf16 weights in a ring slot, until release(i)."""
-        u = self.units[i]
-        if self.q8 is not None:
-            return zs.zero3_gather_int8(u, self.q8[i], self.ring, (tag, i))
-        return zs.zero3_gather(u, self.ring, (tag, i))
+    def _next(self, i: int, phase: str):
+        """The gather that follows unit i's in the step's traversal, or None."""
+        n = len(self.units)
+        if phase == "fwd":
+            return (i + 1, "fwd") if i + 1 < n else (n - 1, "bwd")
+        if phase == "bwd" and i > 0:
+            return (i - 1, "bwd")
+        return None
 
-    def release(self, i: int, tag="use"):
-        self.ring.release((tag, i))
+    def _cancel_prefetches(self):
+        """Drop pending prefetches: the caller's stream waits for them, then
+        their ring slots are free for reuse."""
+        for (tag, i) in list(self.pf.pending):
+            self.pf.get(i, tag)
+            self.ring.release((tag, i))
+
+    def gather(self, i: int, phase="fwd") -> torch.Tensor:
+        """Unit i's full bf16 weights in a ring slot, until release(i, phase)."""
+        u = self.units[i]
+        if self.pf is not None and (phase, i) in self.pf.pending:
+            buf = self.pf.get(i, phase)
+        else:
+            if self.pf is not None:
+                self._cancel_prefetches()
+            if self.q8 is not None:
+                buf = zs.zero3_gather_int8(u, self.q8[i], self.ring, (phase, i))
+            else:
+                buf = zs.zero3_gather(u, self.ring, (phase, i))
+        if self.pf is not None:
+            nxt = self._next(i, phase)
+            if nxt is not None and self.ring.resident < self.ring.slots:
+                self.pf.prefetch(nxt[0], nxt[1])
+        return buf
+
+    def release(self, i: int, phase="fwd"):
+        self.ring.release((phase, i))
 
     def backward(self, i: int, grads: torch.Tensor, micro: int = 0):
         """Unit i's gradient of one micro-batch: grads[r] is rank r's bf16 gradient."""
@@ -205,6 +238,8 @@ class Zero3Engine:
             zs.zero3_layer_reduce_scatter(u, rows, self.A[i], first=(micro == 0))
 
     def step(self):
+        if self.pf is not None:
+            self._cancel_prefetches()
         hp = _hp(self.cfg, self.t + 1)
         if not self.fused:
             if self.norm is not None:
