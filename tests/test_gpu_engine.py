@@ -231,3 +231,91 @@ def test_zero3_engine_overlap_comm(zlib, cuda_device, qw):
         for x, y in ((ua.master, ub.master), (ua.m, ub.m), (ua.v, ub.v), (ua.shards, ub.shards)):
             assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
                                y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16))
+
+
+def _cfg_dict(stage, **zo):
+    return {"zero_optimization": {"stage": stage, **zo}, "optimizer": cfg_opt()}
+
+
+def test_zero12_engine_checkpoint_resume_and_16bit_model(zlib, cuda_device, tmp_path):
+    """Two steps, save, a fresh engine loads and both take a third step: the
+    same state bit for bit.  The 16-bit model file holds the engine's bf16
+    weights without padding, split at the tensors' boundaries."""
+    from zero_sharded_mixed_gb300 import checkpoint as ck
+    n_dp, numels = 4, [30_001, 7, 20_000]
+    cfg = ZeroConfig.from_dict(_cfg_dict(2))
+    N = sum(numels)
+    a = ZeroEngine(numels, n_dp, cfg, master=inputs.master_weights(N, 50_016, seed=3).cuda())
+    P = a.L.padded_n
+    grads = lambda t: inputs.grads_bf16(n_dp, N, P, seed=8, step=t).cuda()
+    for t in (1, 2):
+        a.backward(grads(t))
+        a.step()
+    a.save_checkpoint(str(tmp_path / "ck"))
+    a.save_16bit_model(str(tmp_path / "w16"))
+    b = ZeroEngine(numels, n_dp, cfg)
+    assert b.load_checkpoint(str(tmp_path / "ck")) == 2
+    for e in (a, b):
+        e.backward(grads(3))
+        e.step()
+    torch.cuda.synchronize()
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert torch.equal(a.weights.view(torch.int16), b.weights.view(torch.int16))
+    w16 = ck.load_16bit_model(str(tmp_path / "w16"), split=True)
+    assert [len(x) for x in w16] == numels
+    # the file holds the weights after step 2: recompute them from the oracle's step
+    state = [parity.f32(inputs.master_weights(N, 50_016, seed=3)), np.zeros(P, np.float32),
+             np.zeros(P, np.float32)]
+    for t in (1, 2):
+        out_ref, *state = oracle.rs_adamw_reference(parity.bits(grads(t)), n_dp, *state, HP, t)
+    assert np.array_equal(np.concatenate(w16), out_ref[:N])
+
+
+@pytest.mark.parametrize("qw", [False, True])
+def test_zero3_engine_checkpoint_resume_and_16bit_model(zlib, cuda_device, tmp_path, qw):
+    from zero_sharded_mixed_gb300 import checkpoint as ck
+    n_dp = 4
+    units = [[4097], [33_031], [1000, 24, 3, 5000]]
+    zo = {"zero_quantized_weights": qw, "stage3_gather_16bit_weights_on_model_save": True}
+    cfg = ZeroConfig.from_dict(_cfg_dict(3, **zo))
+
+    def engine():
+        e = Zero3Engine(units, n_dp, cfg)
+        for i, u in enumerate(e.units):
+            u.master.copy_(inputs.master_weights(u.layout.n, u.layout.padded_n, seed=60 + i).cuda())
+            u.shards.view(-1).copy_(u.master.to(torch.bfloat16))
+            if e.q8 is not None:
+                zstep.zero3_quantize(u, e.q8[i])
+        return e
+
+    def step(e, t):
+        for i in reversed(range(len(units))):
+            u = e.units[i]
+            e.gather(i, "bwd")
+            e.release(i, "bwd")
+            e.backward(i, inputs.grads_bf16(n_dp, u.layout.n, u.layout.padded_n, seed=70 + i, step=t).cuda())
+        e.step()
+
+    a = engine()
+    step(a, 1)
+    a.save_checkpoint(str(tmp_path / "ck"))
+    a.save_16bit_model(str(tmp_path / "w16"))
+    b = Zero3Engine(units, n_dp, cfg)
+    assert b.load_checkpoint(str(tmp_path / "ck")) == 1
+    step(a, 2)
+    step(b, 2)
+    torch.cuda.synchronize()
+    for ua, ub in zip(a.units, b.units):
+        for x, y in ((ua.master, ub.master), (ua.m, ub.m), (ua.v, ub.v)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    if qw:
+        for qa, qb in zip(a.q8, b.q8):
+            assert torch.equal(qa.q, qb.q) and torch.equal(qa.scales, qb.scales)
+    w16 = ck.load_16bit_model(str(tmp_path / "w16"))
+    masters = np.concatenate([ck.consolidate(str(tmp_path / "ck" / f"unit_{i:05d}"))["master"]
+                              for i in range(len(units))])
+    assert np.array_equal(w16, oracle.cast_bf16(masters))
+    plain = Zero3Engine(units, n_dp, ZeroConfig.from_dict(_cfg_dict(3)))
+    with pytest.raises(RuntimeError):
+        plain.save_16bit_model(str(tmp_path / "refused"))

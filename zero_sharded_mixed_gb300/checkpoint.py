@@ -279,3 +279,46 @@ def reshard_units(dir_in, dir_out, n_dp: int, align: int | None = None):
         meta = json.load(f)
     with open(os.path.join(dir_out, UNITS), "w") as f:
         json.dump(meta, f, indent=1)
+
+
+# --------------------------------------------------------------------------
+# one full 16-bit weight file ("ZeRO Optimizer, in depth": with
+# stage3_gather_16bit_weights_on_model_save, save_16bit_model gathers the
+# 16-bit weights at save time, for inference or sharing)
+# --------------------------------------------------------------------------
+
+MODEL16 = "model_16bit.bin"
+MODEL16_META = "model_16bit.json"
+
+
+def save_16bit_model(dirpath, weights_bf16, numels):
+    """Write the model's bf16 weights as one file: ``weights_bf16`` is the flat
+    vector of the N real elements in flattening order (device or host); the
+    metadata lists the tensors' element counts and the CRC-32 of the file."""
+    os.makedirs(dirpath, exist_ok=True)
+    n = int(sum(numels))
+    w = weights_bf16.reshape(-1)[:n]
+    host = w.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+    if host.size != n:
+        raise ValueError(f"the weights hold {host.size} elements, the tensors {n}")
+    path = os.path.join(dirpath, MODEL16)
+    host.tofile(path)
+    meta = {"format": FORMAT + " (16-bit weights)", "version": 1, "dtype": "bf16", "n": n,
+            "numels": [int(x) for x in numels], "crc32": crc32(host.view(np.uint8))}
+    with open(os.path.join(dirpath, MODEL16_META), "w") as f:
+        json.dump(meta, f, indent=1)
+    return meta
+
+
+def load_16bit_model(dirpath, split: bool = False):
+    """The saved bf16 weights as uint16 bit patterns (the flat vector, or a list
+    per tensor with split); the CRC-32 is checked."""
+    with open(os.path.join(dirpath, MODEL16_META)) as f:
+        meta = json.load(f)
+    w = np.fromfile(os.path.join(dirpath, MODEL16), dtype=np.uint16)
+    if w.size != meta["n"] or crc32(w.view(np.uint8)) != meta["crc32"]:
+        raise ValueError(f"{dirpath}: the 16-bit weight file does not match its metadata")
+    if not split:
+        return w
+    offs = np.concatenate([[0], np.cumsum(meta["numels"])]).astype(int)
+    return [w[a:b] for a, b in zip(offs[:-1], offs[1:])]

@@ -16,7 +16,8 @@ from dataclasses import dataclass, field
 _USED_TOP = {"zero_optimization", "optimizer", "gradient_accumulation_steps", "gradient_clipping",
              "bf16", "fp16", "scheduler"}
 _USED_ZERO = {"stage", "reduce_bucket_size", "zero_quantized_weights", "zero_quantized_gradients",
-              "offload_optimizer", "offload_param", "overlap_comm"}
+              "offload_optimizer", "offload_param", "overlap_comm",
+              "stage3_gather_16bit_weights_on_model_save"}
 
 
 @dataclass
@@ -32,6 +33,7 @@ class ZeroConfig:
     zero_quantized_weights: bool = False      # stage 3: 8-bit weight gathers
     zero_quantized_gradients: bool = False    # 8-bit gradient reduce-scatter
     overlap_comm: bool = False                # stage 3: gathers one unit ahead on a side stream
+    stage3_gather_16bit_weights_on_model_save: bool = False   # stage 3: save_16bit_model allowed
     quant_block: int = 256
     # WarmupDecayLR: {"min_lr", "max_lr", "warmup_steps", "total_steps"}, or None for a constant lr
     scheduler: dict | None = None
@@ -111,6 +113,8 @@ class ZeroConfig:
             zero_quantized_weights=bool(zo.get("zero_quantized_weights", False)),
             zero_quantized_gradients=bool(zo.get("zero_quantized_gradients", False)),
             overlap_comm=bool(zo.get("overlap_comm", False)),
+            stage3_gather_16bit_weights_on_model_save=bool(
+                zo.get("stage3_gather_16bit_weights_on_model_save", False)),
             scheduler=scheduler,
             ignored=ignored,
         )

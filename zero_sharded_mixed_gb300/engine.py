@@ -28,6 +28,7 @@ from __future__ import annotations
 import torch
 
 from . import binding as zb
+from . import checkpoint as ck
 from . import step as zs
 from .config import ZeroConfig
 
@@ -44,6 +45,7 @@ class ZeroEngine:
         if config.stage not in (1, 2):
             raise ValueError("ZeroEngine runs stages 1 and 2; use Zero3Engine for stage 3")
         self.cfg = config
+        self.numels = [int(x) for x in numels]
         self.K = config.gradient_accumulation_steps
         if config.zero_quantized_gradients and config.stage == 1 and self.K > 1:
             raise ValueError("stage 1 accumulates locally before it communicates: quantized "
@@ -141,6 +143,28 @@ class ZeroEngine:
         self.micro = 0
         self._last = None
 
+    # -- checkpoints ("ZeRO Optimizer, in depth", "Checkpoints: sharded on the
+    # way in, consolidated on the way out")
+
+    def save_checkpoint(self, dirpath):
+        """Every rank's shard of master / m / v and its bf16 weights, one file
+        per rank, with the step count."""
+        if self.micro:
+            raise RuntimeError("save_checkpoint() between micro-batches: finish the step first")
+        return ck.save(dirpath, self.L, self.numels, self.master, self.m, self.v, self.t,
+                       _hp(self.cfg, max(1, self.t)), out_bf16=self.out)
+
+    def load_checkpoint(self, dirpath) -> int:
+        """Restore the state saved by save_checkpoint; returns the step count."""
+        self.t = ck.restore(dirpath, self.L, self.master, self.m, self.v, out_bf16=self.out)
+        self.micro = 0
+        self._last = None
+        return self.t
+
+    def save_16bit_model(self, dirpath):
+        """The full bf16 weights (every rank holds them after a step) as one file."""
+        return ck.save_16bit_model(dirpath, self.out, self.numels)
+
 
 class Zero3Engine:
     """Stage 3 over a list of units, each flattened, padded and sharded alone."""
@@ -149,6 +173,7 @@ class Zero3Engine:
         if config.stage != 3:
             raise ValueError("Zero3Engine runs stage 3")
         self.cfg = config
+        self.numels = [[int(x) for x in u] for u in units_numels]
         self.K = config.gradient_accumulation_steps
         # the update that writes 8-bit shards itself needs 256-element slices
         self.fused = self.K == 1 and config.gradient_clipping == 0
@@ -255,3 +280,50 @@ class Zero3Engine:
                     else:
                         zs.zero3_update(u, self.A[i], hp, n_micro=self.K)
         self.t += 1
+
+    # -- checkpoints: one sharded checkpoint per unit
+
+    def _bf16_shards_current(self):
+        """With 8-bit weights the update writes only the 8-bit shards; the bf16
+        shards are brought back to bf16(master) -- the update's own cast, round
+        to nearest even, which torch's conversion of finite values matches."""
+        if self.q8 is not None:
+            for u in self.units:
+                u.shards.view(-1).copy_(u.master.to(torch.bfloat16))
+
+    def save_checkpoint(self, dirpath):
+        """Every unit's shards of master / m / v and its owners' bf16 shards."""
+        if self.pf is not None:
+            self._cancel_prefetches()
+        self._bf16_shards_current()
+        ck.save_units(dirpath, self.units, self.numels, self.t, _hp(self.cfg, max(1, self.t)),
+                      with_bf16=True)
+
+    def load_checkpoint(self, dirpath) -> int:
+        """Restore the state saved by save_checkpoint (the 8-bit shards are
+        re-derived from the bf16 ones); returns the step count."""
+        if self.pf is not None:
+            self._cancel_prefetches()
+        self.t = ck.restore_units(dirpath, self.units, with_bf16=True)
+        if self.q8 is not None:
+            for u, q in zip(self.units, self.q8):
+                zs.zero3_quantize(u, q)
+        return self.t
+
+    def save_16bit_model(self, dirpath):
+        """With stage3_gather_16bit_weights_on_model_save: every unit's bf16
+        shards gathered (by the library's gather, unit by unit through the ring)
+        into one file of the model's weights, padding dropped."""
+        if not self.cfg.stage3_gather_16bit_weights_on_model_save:
+            raise RuntimeError("save_16bit_model at stage 3 needs "
+                               "zero_optimization.stage3_gather_16bit_weights_on_model_save")
+        if self.pf is not None:
+            self._cancel_prefetches()
+        self._bf16_shards_current()
+        parts = []
+        for i, u in enumerate(self.units):
+            buf = zs.zero3_gather(u, self.ring, ("save", i))     # the bf16 shards, not the 8-bit copies
+            parts.append(buf[:u.layout.n].to("cpu"))
+            self.ring.release(("save", i))
+        flat = torch.cat(parts) if parts else torch.empty(0, dtype=torch.bfloat16)
+        return ck.save_16bit_model(dirpath, flat, [x for u in self.numels for x in u])
