@@ -319,3 +319,26 @@ def test_zero3_engine_checkpoint_resume_and_16bit_model(zlib, cuda_device, tmp_p
     plain = Zero3Engine(units, n_dp, ZeroConfig.from_dict(_cfg_dict(3)))
     with pytest.raises(RuntimeError):
         plain.save_16bit_model(str(tmp_path / "refused"))
+
+
+def test_engine_tracing(zlib, cuda_device):
+    """Step time, the gradient norm (with clipping) against the oracle, and the
+    memory estimate by the pages' formula."""
+    n_dp, N = 4, 100_003
+    cfg = ZeroConfig.from_dict({**_cfg_dict(2), "gradient_clipping": 1.0})
+    eng = ZeroEngine([N], n_dp, cfg, master=inputs.master_weights(N, 100_032, seed=1).cuda())
+    assert eng.last_step_ms() is None and eng.grad_norm() is None
+    P = eng.L.padded_n
+    g = inputs.grads_bf16(n_dp, N, P, seed=2, step=1, std=1.0)
+    eng.backward(g.cuda())
+    eng.step()
+    assert eng.last_step_ms() > 0
+    ref = oracle.grad_norm_sq(parity.bits(g), n_dp) ** 0.5
+    assert abs(eng.grad_norm() - ref) <= 1e-9 * ref
+    est = eng.memory_estimate()
+    assert est["params"] == N
+    assert est["stage0"] == 16 * N and abs(est["stage2"] - (2 * N + 14 * N / n_dp)) < 1e-6 * N
+    assert abs(est["stage3"] - 16 * N / n_dp) < 1e-6 * N
+    assert est["this_process_bytes"] >= P * 12 + P * 2
+    z3 = Zero3Engine([[4097], [33_031]], n_dp, ZeroConfig.from_dict(_cfg_dict(3)))
+    assert z3.memory_estimate()["params"] == 4097 + 33_031 and z3.grad_norm() is None

@@ -37,7 +37,49 @@ def _hp(cfg: ZeroConfig, t: int) -> zb.ZeroAdamW:
     return zb.ZeroAdamW.make(cfg.lr_at(t), cfg.betas[0], cfg.betas[1], cfg.eps, cfg.weight_decay, t)
 
 
-class ZeroEngine:
+class _Tracing:
+    """Step time, gradient norm and the memory estimate ("DeepSpeed ZeRO",
+    "Monitoring": track step time and memory use, log gradient norms; "Reading
+    the memory report": the engine can report an estimate of memory per GPU at
+    startup, to compare with what a run reaches)."""
+
+    def _trace_init(self):
+        self._ev = None
+
+    def _step_begin(self):
+        self._ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        self._ev[0].record()
+
+    def _step_end(self):
+        self._ev[1].record()
+
+    def last_step_ms(self) -> float | None:
+        """Device time of the last step() (CUDA events on the caller's stream;
+        waits for it to finish)."""
+        if self._ev is None:
+            return None
+        self._ev[1].synchronize()
+        return self._ev[0].elapsed_time(self._ev[1])
+
+    def grad_norm(self) -> float | None:
+        """The global L2 norm of the last step's mean gradient, before clipping
+        (only kept when gradient_clipping is configured; reads the device)."""
+        if self.norm is None or self.t == 0:
+            return None
+        return float(self.norm.norm_sq.item()) ** 0.5
+
+    def memory_estimate(self) -> dict:
+        """Model-state bytes per GPU of a real n_dp-GPU job at every stage by the
+        pages' formula (2 + 2 + 12 bytes per parameter, sharded by stage), and
+        the bytes this process holds for all simulated ranks."""
+        n = self._n_params()
+        est = {f"stage{s}": zb.zero_memory_bytes(n, self._n_dp(), s) for s in range(4)}
+        est["params"] = n
+        est["this_process_bytes"] = sum(t.numel() * t.element_size() for t in self._held())
+        return est
+
+
+class ZeroEngine(_Tracing):
     """Stages 1 and 2 over n_dp simulated ranks of one flat parameter vector."""
 
     def __init__(self, numels, n_dp: int, config: ZeroConfig, master: torch.Tensor | None = None,
@@ -65,6 +107,19 @@ class ZeroEngine:
         self.t = 0
         self.micro = 0
         self._last = None
+        self._trace_init()
+
+    def _n_params(self):
+        return self.L.n
+
+    def _n_dp(self):
+        return self.L.n_dp
+
+    def _held(self):
+        held = [self.master, self.m, self.v, self.out] + (self.acc or []) + ([self.A] if self.A is not None else [])
+        if self.qg is not None:
+            held += [self.qg.q, self.qg.scales]
+        return held
 
     @property
     def weights(self) -> torch.Tensor:
@@ -99,6 +154,7 @@ class ZeroEngine:
     def step(self):
         if self.micro != self.K:
             raise RuntimeError(f"step() after {self.micro} of {self.K} micro-batches")
+        self._step_begin()
         L, cfg, K = self.L, self.cfg, self.K
         hp = _hp(cfg, self.t + 1)
         n = L.n_dp
@@ -139,6 +195,7 @@ class ZeroEngine:
             zs.zero1_finish_fused(L, self.acc, self._last, K, self.master, self.m, self.v, self.out, hp)
         else:
             zs.zero2_finish_fused(L, self.A, self._last, K, self.master, self.m, self.v, self.out, hp)
+        self._step_end()
         self.t += 1
         self.micro = 0
         self._last = None
@@ -166,8 +223,10 @@ class ZeroEngine:
         return ck.save_16bit_model(dirpath, self.out, self.numels)
 
 
-class Zero3Engine:
-    """Stage 3 over a list of units, each flattened, padded and sharded alone."""
+class Zero3Engine(_Tracing):
+    """Stage 3 over a list of units, each flattened, padded and sharded alone.
+    last_step_ms() times step() itself: the updates that wait for it (with
+    accumulation or clipping), not the per-unit fused updates of backward()."""
 
     def __init__(self, units_numels, n_dp: int, config: ZeroConfig, masters=None, device="cuda"):
         if config.stage != 3:
@@ -200,6 +259,22 @@ class Zero3Engine:
         self.pf = zs.Zero3Prefetcher(self.units, self.ring, int8=self.q8, device=device) \
             if config.overlap_comm else None
         self.t = 0
+        self._trace_init()
+
+    def _n_params(self):
+        return sum(u.layout.n for u in self.units)
+
+    def _n_dp(self):
+        return self.units[0].layout.n_dp if self.units else 1
+
+    def _held(self):
+        held = [x for u in self.units for x in (u.master, u.m, u.v, u.shards)] + self.ring.buffers
+        held += self.A or []
+        if self.q8 is not None:
+            held += [x for q in self.q8 for x in (q.q, q.scales)]
+        if self.qg is not None:
+            held += [x for q in self.qg for x in (q.q, q.scales)]
+        return held
 
     def _next(self, i: int, phase: str):
         """The gather that follows unit i's in the step's traversal, or None."""
@@ -265,6 +340,7 @@ class Zero3Engine:
     def step(self):
         if self.pf is not None:
             self._cancel_prefetches()
+        self._step_begin()
         hp = _hp(self.cfg, self.t + 1)
         if not self.fused:
             if self.norm is not None:
@@ -279,6 +355,7 @@ class Zero3Engine:
                         zs.zero3_update_q8(u, self.A[i], self.q8[i], hp, n_micro=self.K)
                     else:
                         zs.zero3_update(u, self.A[i], hp, n_micro=self.K)
+        self._step_end()
         self.t += 1
 
     # -- checkpoints: one sharded checkpoint per unit
