@@ -6,7 +6,7 @@ reduce bucket size, the number of gradient-accumulation steps, the clipping
 threshold, the optimizer (AdamW with lr, betas, eps, weight_decay) and the
 precision (bf16), and a "WarmupDecayLR" learning-rate scheduler; "Offload and
 ZeRO++" adds zero_quantized_weights and zero_quantized_gradients.  ``ZeroConfig.from_dict`` reads those keys, refuses
-what this build does not do (fp16 loss scaling, offload, another optimizer),
+what the library does not do (fp16 loss scaling, offload, another optimizer),
 and lists the keys it did not use instead of failing on them.
 """
 from __future__ import annotations
@@ -75,20 +75,20 @@ class ZeroConfig:
         for key in ("offload_optimizer", "offload_param"):
             dev = (zo.get(key) or {}).get("device", "none")
             if dev not in ("none", None):
-                raise ValueError(f"zero_optimization.{key} to {dev!r}: offload is not part of this build")
+                raise ValueError(f"zero_optimization.{key} to {dev!r}: offload is not supported by this library")
         if (cfg.get("fp16") or {}).get("enabled", False):
-            raise ValueError("fp16 with loss scaling is not part of this build: use bf16")
+            raise ValueError("fp16 with loss scaling is not supported by this library: use bf16")
         if not (cfg.get("bf16") or {"enabled": True}).get("enabled", True):
-            raise ValueError("this build keeps weights and gradients in bf16: bf16.enabled must be true")
+            raise ValueError("this library keeps weights and gradients in bf16: bf16.enabled must be true")
         opt = cfg.get("optimizer") or {"type": "AdamW", "params": {}}
         if str(opt.get("type", "AdamW")).lower() != "adamw":
-            raise ValueError(f"optimizer {opt.get('type')!r}: this build implements AdamW")
+            raise ValueError(f"optimizer {opt.get('type')!r}: this library implements AdamW")
         p = opt.get("params", {})
         scheduler = None
         if cfg.get("scheduler") is not None:
             sch = cfg["scheduler"]
             if sch.get("type") != "WarmupDecayLR":
-                raise ValueError(f"scheduler {sch.get('type')!r}: this build implements WarmupDecayLR")
+                raise ValueError(f"scheduler {sch.get('type')!r}: this library implements WarmupDecayLR")
             sp = sch.get("params", {})
             if sp.get("warmup_type", "linear") != "linear":
                 raise ValueError("WarmupDecayLR is implemented with a linear warmup")

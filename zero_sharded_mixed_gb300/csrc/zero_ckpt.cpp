@@ -12,7 +12,7 @@
 // value and final xor 0xFFFFFFFF), computed eight bytes at a time with eight
 // 256-entry tables built on first use ("slicing by 8": table k maps a byte to
 // its CRC contribution k bytes further on; the bytes are read little-endian,
-// the order of both host architectures this builds for).
+// the byte order of x86-64 and AArch64 hosts alike).
 #include <cstdio>
 #include <cstring>
 #include <mutex>
