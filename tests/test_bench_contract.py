@@ -25,7 +25,7 @@ def test_reference_arm_line(monkeypatch):
                 "cpu_baseline", "e2e", "impl"):
         assert key in line, key
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
 
 
@@ -67,3 +67,15 @@ def test_every_workload_has_an_oracle_step(name):
     step(2)
     st = next(c.cell_contents for c in cells if isinstance(c.cell_contents, dict) and "w" in c.cell_contents)
     assert np.isfinite(st["w"]).all() and (st["m"] != 0).any()
+
+
+def test_threaded_oracle_timing_covers_the_sample():
+    """The all-cores CPU baseline steps every chunk of the sample."""
+    import numpy as np
+
+    from zero_sharded_mixed_gb300 import inputs
+    n, n_dp = 10_000, 4
+    g = inputs.bf16_bits(inputs.grads_bf16(n_dp, n, n, seed=1, step=1))
+    sample = (g, inputs.master_weights(n, n, seed=1).numpy(), np.zeros(n, np.float32), np.zeros(n, np.float32))
+    rate, secs, done = bench.time_oracle(sample, 0.2, n_dp, threads=3)
+    assert rate > 0 and secs >= 0.2 and done >= n
