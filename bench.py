@@ -989,74 +989,36 @@ def oracle_workload_step(name, n):
     return step, n, what
 
 
-def time_oracle_workload(name, seconds):
+def time_oracle_workload(name, seconds, threads=1):
+    """The oracle's statement of workload `name` on every host core: each
+    thread steps its own copy of the step over 1/threads of the sample, after
+    one untimed step."""
     import oracle
     oracle.build()                       # compiled before the timed region, if stale
-    step, n, what = oracle_workload_step(name, WORKLOAD_SAMPLE)
-    step(1)                              # one untimed step (first-touch allocations)
-    t, done = 2, 0
+    per = max(WORKLOAD_SAMPLE // threads, 8 * 256)
+    steps = [oracle_workload_step(name, per) for _ in range(threads)]
+    for step, _, _ in steps:
+        step(1)                          # one untimed step each (first-touch allocations)
+    done = [0] * threads
     t0 = time.perf_counter()
-    while True:
-        step(t)
-        t += 1
-        done += n
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": done / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%s; %d timed oracle steps after one untimed, %.1f s single-threaded"
-                      % (what, t - 2, el)}
 
+    def run(k):
+        step, n, _ = steps[k]
+        t = 2
+        while time.perf_counter() - t0 < seconds:
+            step(t)
+            t += 1
+            done[k] += n
 
-def time_checkpoint(device):
-    """Save and restore one Llama-7B block unit's sharded state (n_dp = 8: fp32
-    master, m, v and the bf16 shards, one file per rank with its CRC-32) in a
-    temporary directory, through checkpoint.save / restore; the restored state
-    must equal the saved one bit for bit.  Host-bound: device-to-host copies,
-    the CRC and the file system."""
-    import shutil
-    import tempfile
-
-    import torch
-    from zero_sharded_mixed_gb300 import binding as zb
-    from zero_sharded_mixed_gb300 import checkpoint as ck
-    from zero_sharded_mixed_gb300 import inputs
-    numels = inputs.llama7b_block_numels()
-    L = zb.zero_layout(numels, 8)
-    P = L.padded_n
-    st = [_master(L.n, P, device), torch.randn(P, device=device) * 1e-4, torch.rand(P, device=device) * 1e-8]
-    shards = st[0].to(torch.bfloat16)
-    hp = zb.ZeroAdamW.make(step=7, **HP)
-    nbytes = P * 14
-    d = tempfile.mkdtemp(prefix="zgb_ckpt_")
-    try:
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        ck.save(d, L, numels, *st, 7, hp, out_bf16=shards)
-        t_save = time.perf_counter() - t0
-        back = [torch.empty_like(x) for x in st]
-        back_w = torch.empty_like(shards)
-        t0 = time.perf_counter()
-        step = ck.restore(d, L, *back, out_bf16=back_w)
-        torch.cuda.synchronize()
-        t_restore = time.perf_counter() - t0
-        same = step == 7 and all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(st, back)) \
-            and torch.equal(shards.view(torch.int16), back_w.view(torch.int16))
-        host = torch.zeros(L.shard * 12, dtype=torch.uint8)          # one rank's fp32 payload
-        t0 = time.perf_counter()
-        ck.crc32(host.numpy())
-        crc_gbs = host.numel() / (time.perf_counter() - t0) / 1e9
-    except OSError as e:
-        return {"unavailable": "checkpoint directory: %s" % e}
-    finally:
-        shutil.rmtree(d, ignore_errors=True)
-    return {"workload": "llama7b_block_unit_checkpoint", "params": L.n, "n_dp": 8, "files": 8,
-            "bytes": nbytes, "save_s": t_save, "restore_s": t_restore,
-            "save_gbs": nbytes / t_save / 1e9, "restore_gbs": nbytes / t_restore / 1e9,
-            "crc_gbs_one_core": crc_gbs, "round_trip_bit_exact": bool(same),
-            "threads": ck._workers(8),
-            "bound": "host: the CRC-32 (crc_gbs_one_core per thread), page-cache copies, "
-                     "device-host copies"}
+    ts = [threading.Thread(target=run, args=(k,)) for k in range(threads)]
+    for th in ts:
+        th.start()
+    for th in ts:
+        th.join()
+    el = time.perf_counter() - t0
+    what = steps[0][2]
+    return {"value": sum(done) / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d threads, each its own copy of the step over %s; %.1f s" % (threads, what, el)}
 
 
 # --------------------------------------------------------------------------
@@ -1170,7 +1132,7 @@ def run_ours(args):
                               "contiguous chunks, one thread each; %.1f passes in %.1f s"
                               % (sample[1].size, wl.n_src, cores, done / sample[1].size, secs)}
         if not is_primary and not args.no_cpu_baseline and world == 1 and rank == 0:
-            res["cpu_baseline"] = time_oracle_workload(name, WORKLOAD_ORACLE_SECONDS)
+            res["cpu_baseline"] = time_oracle_workload(name, WORKLOAD_ORACLE_SECONDS, threads=host_cores())
         results[name] = res
         wl.free()
         del wl
