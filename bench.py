@@ -1021,6 +1021,57 @@ def time_oracle_workload(name, seconds, threads=1):
             "sample": "%d threads, each its own copy of the step over %s; %.1f s" % (threads, what, el)}
 
 
+def time_checkpoint(device):
+    """Save and restore one Llama-7B block unit's sharded state (n_dp = 8: fp32
+    master, m, v and the bf16 shards, one file per rank with its CRC-32) in a
+    temporary directory, through checkpoint.save / restore; the restored state
+    must equal the saved one bit for bit.  Host-bound: device-to-host copies,
+    the CRC and the file system."""
+    import shutil
+    import tempfile
+
+    import torch
+    from zero_sharded_mixed_gb300 import binding as zb
+    from zero_sharded_mixed_gb300 import checkpoint as ck
+    from zero_sharded_mixed_gb300 import inputs
+    numels = inputs.llama7b_block_numels()
+    L = zb.zero_layout(numels, 8)
+    P = L.padded_n
+    st = [_master(L.n, P, device), torch.randn(P, device=device) * 1e-4, torch.rand(P, device=device) * 1e-8]
+    shards = st[0].to(torch.bfloat16)
+    hp = zb.ZeroAdamW.make(step=7, **HP)
+    nbytes = P * 14
+    d = tempfile.mkdtemp(prefix="zgb_ckpt_")
+    try:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ck.save(d, L, numels, *st, 7, hp, out_bf16=shards)
+        t_save = time.perf_counter() - t0
+        back = [torch.empty_like(x) for x in st]
+        back_w = torch.empty_like(shards)
+        t0 = time.perf_counter()
+        step = ck.restore(d, L, *back, out_bf16=back_w)
+        torch.cuda.synchronize()
+        t_restore = time.perf_counter() - t0
+        same = step == 7 and all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(st, back)) \
+            and torch.equal(shards.view(torch.int16), back_w.view(torch.int16))
+        host = torch.zeros(L.shard * 12, dtype=torch.uint8)          # one rank's fp32 payload
+        t0 = time.perf_counter()
+        ck.crc32(host.numpy())
+        crc_gbs = host.numel() / (time.perf_counter() - t0) / 1e9
+    except OSError as e:
+        return {"unavailable": "checkpoint directory: %s" % e}
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+    return {"workload": "llama7b_block_unit_checkpoint", "params": L.n, "n_dp": 8, "files": 8,
+            "bytes": nbytes, "save_s": t_save, "restore_s": t_restore,
+            "save_gbs": nbytes / t_save / 1e9, "restore_gbs": nbytes / t_restore / 1e9,
+            "crc_gbs_one_core": crc_gbs, "round_trip_bit_exact": bool(same),
+            "threads": ck._workers(8),
+            "bound": "host: the CRC-32 (crc_gbs_one_core per thread), page-cache copies, "
+                     "device-host copies"}
+
+
 # --------------------------------------------------------------------------
 # arms
 # --------------------------------------------------------------------------
