@@ -853,14 +853,17 @@ def time_e2e(wl, steps, warmup, t0, dist):
     torch.cuda.synchronize()
     barrier(dist)
     ms = start.elapsed_time(end) / steps
-    # the host link on this machine: one plain copy of the step's gradients, pinned host to device
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record()
-    wl.grads.copy_(host_g, non_blocking=True)
-    b.record()
-    torch.cuda.synchronize()
-    link_gbs = host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9
+    # the host link on this machine: plain copies of the step's gradients, pinned host to device;
+    # the fastest of three (the link's rate varies from moment to moment on a shared host)
+    link_gbs = 0.0
+    for _ in range(3):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        wl.grads.copy_(host_g, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        link_gbs = max(link_gbs, host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
     return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs
 
 
@@ -1164,8 +1167,8 @@ def run_ours(args):
                                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                   "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
                                            "frac": link_ms / e_ms,
-                                           "note": "one plain pinned host-to-device copy of the step's "
-                                                   "gradients on this box, after the e2e steps"}}
+                                           "note": "the fastest of three plain pinned host-to-device copies "
+                                                   "of the step's gradients on this box, after the e2e steps"}}
                 else:
                     res["e2e"] = {"value": None, "unit": UNIT,
                                   "unavailable": "host memory: %s local ranks x %.1f GB of pinned "
