@@ -267,9 +267,15 @@ class Workload:
 
 
 def _owners(L, begin, end):
-    """Owners whose shards [begin, end) overlaps: the 8-bit gradient kernels
-    launch once per owner."""
-    return (end - 1) // L.shard - begin // L.shard + 1 if end > begin else 0
+    """Launches of one 8-bit gradient call over [begin, end): one for a range
+    of several whole shards (the owners share one grid), else one per owner
+    whose shard the range meets."""
+    if end <= begin:
+        return 0
+    owners = (end - 1) // L.shard - begin // L.shard + 1
+    if owners > 1 and begin % L.shard == 0 and end % L.shard == 0:
+        return 1
+    return owners
 
 
 def _master(n_real, n, device):

@@ -39,7 +39,8 @@ def test_reference_arm_other_ranks_are_silent(monkeypatch):
 
 
 def test_owner_count_of_a_range():
-    """The 8-bit gradient kernels launch once per owner a range overlaps."""
+    """The 8-bit gradient kernels launch once per owner a range meets, or once
+    for a range of several whole shards."""
     import bench
 
     class L:
@@ -48,6 +49,9 @@ def test_owner_count_of_a_range():
     assert bench._owners(L, 0, 101) == 2
     assert bench._owners(L, 99, 201) == 3
     assert bench._owners(L, 150, 150) == 0
+    assert bench._owners(L, 0, 800) == 1
+    assert bench._owners(L, 200, 500) == 1
+    assert bench._owners(L, 200, 550) == 4
 
 
 @pytest.mark.parametrize("name", ["gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
