@@ -511,3 +511,88 @@ def test_llama7b_zero3_fused_int8_gradients_q8(zlib, cuda_device):
             assert torch.equal(a.view(torch.int32), b.view(torch.int32))
         assert torch.equal(qs[0].q, qs[1].q)
         assert torch.equal(qs[0].scales.view(torch.int32), qs[1].scales.view(torch.int32))
+
+
+def test_llama7b_zero3_fused_graph_replay(zlib, cuda_device):
+    """The fused ZeRO-3 step captured once in a CUDA graph, as the benchmark's
+    graph workload captures it (the schedule's advance, then per unit the
+    forward gather, and in reverse the backward gather with the fused
+    reduce-scatter + update), on the Llama-7B embedding and two block units at
+    n_dp = 8.  The capture's warm-up call is step 1; three replays with new
+    gradients in the same buffer and a new lr each step equal four eager steps
+    with the scalars by value on every element, and the oracle on sampled
+    elements."""
+    zb = zlib
+    dev = cuda_device
+    n_dp = 8
+    units_numels = inputs.llama7b_units()[:3]
+    layouts = [zb.zero_layout(u, n_dp) for u in units_numels]
+    cap = max(L.padded_n for L in layouts)
+    lrs = [1e-4, 8e-5, 6e-5, 4e-5]
+
+    def make_units(seed):
+        out = []
+        for i, L in enumerate(layouts):
+            w = inputs.master_weights(L.n, L.padded_n, seed=seed + i, device=dev)
+            out.append(zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w,
+                                       torch.zeros(L.padded_n, device=dev), torch.zeros(L.padded_n, device=dev)))
+        return out
+
+    def step_ops(units, ring, gbuf, hp_of):
+        for i, u in enumerate(units):
+            zstep.zero3_gather(u, ring, ("fwd", i))
+            ring.release(("fwd", i))
+        for i in reversed(range(len(units))):
+            u = units[i]
+            P = u.layout.padded_n
+            zstep.zero3_gather(u, ring, ("bwd", i))
+            zstep.zero3_reduce_scatter_update(u, [gbuf[r, :P] for r in range(n_dp)], hp_of())
+            ring.release(("bwd", i))
+
+    def fill(gbuf, t):
+        for r in range(n_dp):
+            inputs.grad_bf16_into(gbuf[r], cap, SEED + 90, step=t, rank=r)
+
+    graph_units, eager_units = make_units(SEED + 80), make_units(SEED + 80)
+    u0 = graph_units[0]
+    rng = np.random.default_rng(9)
+    idx = np.unique(np.concatenate([rng.integers(0, u0.layout.padded_n, 1 << 16),
+                                    [o * u0.layout.shard for o in range(n_dp)]]))
+    idx_dev = torch.from_numpy(idx).to(dev)
+    ref = [parity.f32(_take(u0.master, idx_dev)), np.zeros(idx.size, np.float32),
+           np.zeros(idx.size, np.float32)]
+
+    gbuf = torch.empty((n_dp, cap), dtype=torch.bfloat16, device=dev)      # the graph's fixed input
+    ring = zstep.GatherRing(cap, device=str(dev))
+    sch = zstep.StepSchedule(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay, n_steps=len(lrs), lrs=lrs)
+
+    def graph_step():
+        sch.advance()
+        step_ops(graph_units, ring, gbuf, sch.hp)
+
+    fill(gbuf, 1)
+    gs = zstep.GraphStep(graph_step)                                       # warm-up = step 1
+    for t in range(2, len(lrs) + 1):
+        fill(gbuf, t)
+        gs.replay()
+    torch.cuda.synchronize()
+    assert int(sch.index.item()) == len(lrs)
+
+    ebuf = torch.empty_like(gbuf)
+    ering = zstep.GatherRing(cap, device=str(dev))
+    o = oracle.AdamW(lr=HP.lr, beta1=HP.beta1, beta2=HP.beta2, eps=HP.eps, weight_decay=HP.weight_decay)
+    for t in range(1, len(lrs) + 1):
+        fill(ebuf, t)
+        hp = zb.ZeroAdamW.make(lrs[t - 1], HP.beta1, HP.beta2, HP.eps, HP.weight_decay, t)
+        step_ops(eager_units, ering, ebuf, lambda: hp)
+        gs_bits = np.stack([_bits_at(ebuf[r, :u0.layout.padded_n], idx_dev) for r in range(n_dp)])
+        o.lr = float(np.float32(lrs[t - 1]))
+        out_ref, *ref = oracle.rs_adamw_reference(gs_bits, n_dp, *ref, o, t)
+    zb.zero_status_check()
+    for g_u, e_u in zip(graph_units, eager_units):
+        for a, b in ((g_u.master, e_u.master), (g_u.m, e_u.m), (g_u.v, e_u.v)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.equal(g_u.shards.view(torch.int16), e_u.shards.view(torch.int16))
+    parity.assert_state([_take(x, idx_dev) for x in (u0.master, u0.m, u0.v)], ref, what="graph unit 0 ")
+    assert np.array_equal(_bits_at(u0.shards.view(-1), idx_dev), out_ref)
+    assert ring.resident == 0 and ering.resident == 0
