@@ -157,3 +157,34 @@ def test_stage3_units_save_consolidate_reshard_restore(zlib, tmp_path):
         assert torch.equal(a.shards.view(torch.int16), b.shards.view(torch.int16))
     with pytest.raises(ValueError):
         ck.restore_units(str(tmp_path / "u"), fresh[:2])
+
+
+def test_16bit_model_round_trip_and_corruption(zlib, tmp_path):
+    """The 16-bit weight file: the real elements only, split back per tensor;
+    a flipped byte or a truncated file is refused."""
+    numels = [5, 1, 4097, 33]
+    n = sum(numels)
+    bits = np.random.default_rng(3).integers(0, 1 << 16, size=n + 11, dtype=np.uint16)  # + padding
+    w = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    d = str(tmp_path / "w16")
+    meta = ck.save_16bit_model(d, w, numels)
+    assert meta["n"] == n and meta["numels"] == numels
+    flat = ck.load_16bit_model(d)
+    assert np.array_equal(flat, bits[:n])
+    parts = ck.load_16bit_model(d, split=True)
+    assert [p.size for p in parts] == numels
+    assert np.array_equal(np.concatenate(parts), bits[:n])
+    with pytest.raises(ValueError):
+        ck.save_16bit_model(str(tmp_path / "short"), w[:n - 1], numels)
+    path = tmp_path / "w16" / ck.MODEL16
+    raw = bytearray(path.read_bytes())
+    raw[1234] ^= 0x10
+    path.write_bytes(bytes(raw))
+    with pytest.raises(ValueError):
+        ck.load_16bit_model(d)
+    raw[1234] ^= 0x10
+    path.write_bytes(bytes(raw[:-2]))
+    with pytest.raises(ValueError):
+        ck.load_16bit_model(d)
+    path.write_bytes(bytes(raw))
+    assert np.array_equal(ck.load_16bit_model(d), bits[:n])
