@@ -74,3 +74,32 @@ def test_pageable_host_sources_are_refused(zlib, cuda_device):
         zb.zero_reduce_scatter_adamw(L, gd, zb.ZERO_BF16, 0, 2.0, 0, 2, 0, P, w_pinned, st[1], st[2],
                                      out, zb.ZERO_OUT_FULL, _hp(zb, 1))
     zb.zero_status_check()
+
+
+@pytest.mark.parametrize("defer_out", [False, True])
+@pytest.mark.parametrize("N,n_dp,bucket,chunk", [(300_007, 4, 100_000, None), (65_541, 8, 20_000, 7_000)])
+def test_copy_pipeline_matches_the_oracle(zlib, cuda_device, N, n_dp, bucket, chunk, defer_out):
+    """The e2e pipeline (gradients copied from pinned host memory bucket by
+    bucket, each bucket updated once its copies land, the bf16 result copied
+    back to pinned host memory, overlapped or after the last gradient copy):
+    the state and the host result equal the oracle's, three steps."""
+    zb = zlib
+    L = zb.zero_layout([N], n_dp, bucket_elems=bucket)
+    P = L.padded_n
+    w0 = inputs.master_weights(N, P, seed=n_dp + 1)
+    st = [w0.cuda(), torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")]
+    out = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    dev_g = torch.empty((n_dp, P), dtype=torch.bfloat16, device="cuda")
+    host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    pipe = zstep.HostPipeline(L, chunk_elems=chunk, defer_out=defer_out)
+    ref = [parity.f32(w0), np.zeros(P, np.float32), np.zeros(P, np.float32)]
+    for t in (1, 2, 3):
+        g = inputs.grads_bf16(n_dp, N, P, seed=n_dp + 1, step=t)
+        g_host = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        g_host.copy_(g)
+        pipe.step(g_host, dev_g, *st, out, host_out, _hp(zb, t))
+        torch.cuda.synchronize()
+        out_ref, *ref = oracle.rs_adamw_reference(parity.bits(g), n_dp, *ref, HP, t)
+        parity.assert_state(st, ref, what=f"t={t} ")
+        assert np.array_equal(parity.bits(host_out), out_ref)
+        assert torch.equal(dev_g.cpu().view(torch.int16), g.view(torch.int16))

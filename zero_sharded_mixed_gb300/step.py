@@ -315,10 +315,14 @@ class HostPipeline:
     copies run on one stream, its fused update on the caller's stream once they
     have landed, and its device-to-host copy on a third stream, so the copies of
     one bucket overlap the update of the previous one ("ZeRO and FSDP", stage
-    2: each bucket is reduce-scattered as soon as it is ready)."""
+    2: each bucket is reduce-scattered as soon as it is ready).  With
+    defer_out the result copies start only once every gradient copy has
+    landed: on hosts where the two directions of the link slow each other
+    down, the gradients then have the link to themselves."""
 
-    def __init__(self, L, device=None, chunk_elems: int | None = None):
+    def __init__(self, L, device=None, chunk_elems: int | None = None, defer_out: bool = False):
         self.L = L
+        self.defer_out = defer_out
         self.ranges = split_ranges(bucket_ranges(L), chunk_elems)
         self.h2d = torch.cuda.Stream(device=device)
         self.d2h = torch.cuda.Stream(device=device)
@@ -342,6 +346,8 @@ class HostPipeline:
                                          master, m, v, out, zb.ZERO_OUT_FULL, hp, comp)
             self.ev_done[j].record(comp)
         with torch.cuda.stream(self.d2h):
+            if self.defer_out and self.ranges:
+                self.d2h.wait_event(self.ev_in[-1])
             for j, (s, e) in enumerate(self.ranges):
                 self.d2h.wait_event(self.ev_done[j])
                 host_out[s:e].copy_(out[s:e], non_blocking=True)
