@@ -836,35 +836,18 @@ def time_e2e(wl, steps, warmup, t0, dist):
     """The same step through the public API with host buffers: every step copies
     the n_dp gradient buffers from pinned host memory to the device and reads the
     updated bf16 weights back into pinned host memory (step.HostPipeline, which
-    overlaps bucket b's copies with bucket b-1's update).  The result copies
-    either overlap the gradient copies or wait for the last of them
-    (defer_out); after the warm-up, one step of each is timed and the faster
-    runs the timed steps, since on some hosts the link's two directions slow
-    each other down."""
+    overlaps bucket b's copies with bucket b-1's update, and the result copies
+    with the gradient copies)."""
     import torch
     from zero_sharded_mixed_gb300.step import HostPipeline
     host_g = torch.empty(wl.grads.shape, dtype=wl.grads.dtype, pin_memory=True)
     host_g.copy_(wl.grads)
     host_out = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
-    pipes = {"overlapped": HostPipeline(wl.L, device=wl.device),
-             "deferred": HostPipeline(wl.L, device=wl.device, defer_out=True)}
+    pipe = HostPipeline(wl.L, device=wl.device)
     t = t0
     for _ in range(warmup):
-        pipes["overlapped"].step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
+        pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
         t += 1
-    trial = {}
-    for name, p in pipes.items():
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        a.record()
-        p.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
-        b.record()
-        torch.cuda.synchronize()
-        trial[name] = a.elapsed_time(b)
-        t += 1
-    mode = min(trial, key=trial.get)
-    pipe = pipes[mode]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -888,7 +871,7 @@ def time_e2e(wl, steps, warmup, t0, dist):
         b.record()
         torch.cuda.synchronize()
         link_gbs = max(link_gbs, host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
-    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs, {"mode": mode, "trial_ms": trial}
+    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs
 
 
 def cpu_sample(wl, n):
@@ -1183,7 +1166,7 @@ def run_ours(args):
                 fits = host_fits(need * int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
                 if all_ranks_agree(dist, fits, device):
                     e2e_steps = max(1, min(args.steps, 10))
-                    e_ms, h2d, d2h, link_gbs, mode = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
+                    e_ms, h2d, d2h, link_gbs = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
                     e_ms = max_over_ranks(dist, e_ms, device)
                     link_ms = h2d / (link_gbs * 1e9) * 1e3
                     res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
@@ -1192,10 +1175,7 @@ def run_ours(args):
                                   "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
                                            "frac": link_ms / e_ms,
                                            "note": "the fastest of three plain pinned host-to-device copies "
-                                                   "of the step's gradients on this box, after the e2e steps"},
-                                  "pipeline": dict(mode, note="result copies overlapped with the gradient "
-                                                   "copies or deferred until they have landed: one warm-up "
-                                                   "step of each, the faster timed")}
+                                                   "of the step's gradients on this box, after the e2e steps"}}
                 else:
                     res["e2e"] = {"value": None, "unit": UNIT,
                                   "unavailable": "host memory: %s local ranks x %.1f GB of pinned "
