@@ -83,3 +83,79 @@ def test_threaded_oracle_timing_covers_the_sample():
     sample = (g, inputs.master_weights(n, n, seed=1).numpy(), np.zeros(n, np.float32), np.zeros(n, np.float32))
     rate, secs, done = bench.time_oracle(sample, 0.2, n_dp, threads=3)
     assert rate > 0 and secs >= 0.2 and done >= n
+
+
+def _fake_result(workload, value, ms, frac):
+    roof = {"bound": "hbm", "achieved": frac * 6675.2, "peak": 6675.2, "unit": "GB/s", "frac": frac,
+            "peak_kind": "measured", "traffic": 42.02 * 194701400, "algorithmic_bytes_per_launch": 21e9,
+            "kernel": "rs_adamw", "kernel_symbols": "zgb::rs_adamw_vec_kernel<0,8> (bf16 sources x 8)"}
+    return {
+        "value": value, "ms_per_step": ms, "steps": 20, "step_ms_median": ms, "step_ms_min": ms * 0.99,
+        "hbm_gbs_step": 7000.0, "bytes_per_param_step": 42,
+        "config": {"workload": workload, "model": "GPT-2-XL shapes", "N": 1557611200, "n_dp": 8,
+                   "shard": 194701400, "padded_n": 1557611200, "bucket": 500000000, "buckets": 4,
+                   "l2": "inputs 50.0 GB > 129 MB L2, no flush"},
+        "roofline": roof,
+        "kernels": {"rs_adamw": {"launches_per_step": 4, "ms_per_step": ms, "bytes_per_step": 65419670400,
+                                 "achieved_gbs": 7000.0}},
+        "gpu_launches": 80,
+        "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_w_max": 1086.5, "samples": 40,
+                   "reasons": []},
+        "e2e": {"value": 1.2e10, "unit": bench.UNIT, "ms_per_step": 130.0, "steps": 10,
+                "h2d_bytes_per_step": 24921779200, "d2h_bytes_per_step": 3115222400,
+                "link": {"h2d_gbs": 190.0, "h2d_ms_per_step": 124.0, "frac": 0.95}},
+        "cpu_baseline": {"value": 1.4e9, "unit": bench.UNIT, "cores": 16, "kind": "oracle",
+                         "single_core_value": 9e7,
+                         "sample": "first 33554432 owned elements (all 8 gradient slices), 16 chunks, one "
+                                   "thread each; 12.3 passes in 6.0 s"},
+    }
+
+
+def test_headline_line_is_compact_and_parses():
+    """The headline line carries every key of the contract, parses as JSON on
+    its own and stays under 2 KB, so that a short tail of the log holds it."""
+    args = bench.parse_args(["--steps", "20", "--warmup", "5"])
+    p = _fake_result("gpt2xl_zero2_all_shards", 1.68e11, 9.26, 1.06)
+    seven = bench.target_7b(dict(_fake_result("llama7b_zero2_one_shard", 2.0e11, 4.2, 1.04)))
+    line = bench.headline_line(p, args, 1, seven)
+    text = json.dumps(line)
+    assert len(text) < 2048
+    back = json.loads(text)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
+                "clocks", "gpu_launches", "impl", "target_7b"):
+        assert key in back, key
+    assert back["config"]["workload"] == "gpt2xl_zero2_all_shards" and back["value"] > 0
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in back["roofline"], key
+    assert back["e2e"]["h2d_bytes_per_step"] > 0 and back["e2e"]["d2h_bytes_per_step"] > 0
+    assert back["target_7b"]["frac"] == 1.04 and back["target_7b"]["met"] is True
+    assert back["cpu_baseline"]["cores"] == 16 and back["impl"] == "ours"
+
+
+def test_headline_line_stays_short_with_long_fields():
+    """Long optional fields are dropped before the line passes the limit."""
+    args = bench.parse_args([])
+    p = _fake_result("gpt2xl_zero2_all_shards", 1.68e11, 9.26, 1.06)
+    p["cpu_baseline"]["sample"] = "x" * 3000
+    line = bench.headline_line(p, args, 1, None)
+    assert len(json.dumps(line)) <= bench.HEADLINE_MAX_CHARS
+    assert line["value"] == p["value"] and line["cpu_baseline"]["value"] == p["cpu_baseline"]["value"]
+
+
+def test_workload_lines_carry_no_headline_keys():
+    """The lines of the other workloads cannot be taken for the headline."""
+    line = bench.workload_line("llama7b-shard", _fake_result("llama7b_zero2_one_shard", 2e11, 4.2, 1.04))
+    assert "metric" not in line and "value" not in line
+    assert line["workload_result"] == "llama7b-shard" and line["params_per_s"] == 2e11
+    json.loads(json.dumps(line))
+
+
+def test_default_run_has_no_stand_in_matmuls():
+    """The workloads with cuBLAS stand-in layer compute run only on request."""
+    order = bench.workload_order(bench.parse_args([]))
+    assert order[0] == "gpt2xl" and "llama7b-shard" in order
+    assert not set(bench.COMPUTE_WORKLOADS) & set(order)
+    assert set(bench.COMPUTE_WORKLOADS) <= set(bench.workload_order(bench.parse_args(["--with-compute"])))
+    assert bench.workload_order(bench.parse_args(["--no-extra"])) == ["gpt2xl"]
+    assert bench.workload_order(bench.parse_args(["--workload", "probe"])) == ["probe"]
