@@ -159,6 +159,33 @@ def test_rs_adamw_argument_checks(zlib, over, code):
     assert _rs_call(zlib, **over) == code
 
 
+def test_internal_output_mode_is_refused(zlib):
+    """out_mode -1 (the library's internal 8-bit-output marker) with a null
+    output is refused by every public entry point with a bf16 output, even on
+    an empty range, which returns before any launch; a mode outside {0, 1} or
+    a null output with a valid mode is refused the same way."""
+    lib = zlib.load()
+    L = zlib.zero_layout([4096], 4)
+    Lp = ctypes.byref(L)
+    hp = zlib.ZeroAdamW.make(step=1)
+    src = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    norm = ctypes.c_void_p(FAKE)
+    for mode, out in ((-1, None), (-1, FAKE), (2, FAKE), (0, None), (1, None)):
+        assert _rs_call(zlib, mode=mode, out=out, begin=64, end=64) == -1, (mode, out)
+        assert lib.zero_reduce_scatter_adamw_clip(Lp, src, 4, 0, 0, 4.0, 0, 4, 64, 64, FAKE, FAKE, FAKE,
+                                                  out, mode, ctypes.byref(hp), norm, ctypes.c_float(1.0),
+                                                  None) == -1, (mode, out)
+        assert lib.zero_accumulate_adamw(Lp, 1, src, 1, 0, src, 4, 0, 4.0, 0, 4, 64, 64, FAKE, FAKE, FAKE,
+                                         out, mode, ctypes.byref(hp), None) == -1, (mode, out)
+        assert lib.zero_reduce_scatter_adamw_int8(Lp, src, src, 4, 256, 4.0, 0, 4, 64, 64, FAKE, FAKE, FAKE,
+                                                  out, mode, ctypes.byref(hp), None) == -1, (mode, out)
+    # the valid modes with an output still pass the empty-range call
+    for mode in (0, 1):
+        assert _rs_call(zlib, mode=mode, begin=64, end=64) == 0
+        assert lib.zero_accumulate_adamw(Lp, 1, src, 1, 0, src, 4, 0, 4.0, 0, 4, 64, 64, FAKE, FAKE, FAKE,
+                                         FAKE, mode, ctypes.byref(hp), None) == 0
+
+
 def test_accumulate_and_gather_argument_checks(zlib):
     lib = zlib.load()
     L = zlib.zero_layout([4096], 4)

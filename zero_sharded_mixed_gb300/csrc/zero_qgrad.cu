@@ -456,7 +456,8 @@ int qgrad_update(const zero_layout_t* L, const int8_t* const* q_src, const float
         if (check_aligned(scales_out, 4)) return ZERO_EALIGN;
     }
     UpdateTarget t;
-    if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode, &t)))
+    if ((rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode,
+                             q_out != nullptr, &t)))
         return rc;
     QGradParams base;
     if ((rc = make_scalars(hp, divisor, &base.h))) return rc;

@@ -380,11 +380,13 @@ int dispatch(const UpdateParams& p, bool vec, cudaStream_t s) {
 
 int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
                    int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
-                   UpdateTarget* t) {
+                   bool q8_out, UpdateTarget* t) {
     if (!L || !master || !m || !v) return ZERO_EINVAL;
-    if (out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD && out_mode != ZERO_OUT_NONE)
+    if (q8_out) {
+        if (out_mode != ZERO_OUT_NONE || out != nullptr) return ZERO_EINVAL;
+    } else if ((out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD) || out == nullptr) {
         return ZERO_EINVAL;
-    if ((out_mode == ZERO_OUT_NONE) != (out == nullptr)) return ZERO_EINVAL;
+    }
     if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
     if (rank_begin < 0 || rank_end > L->n_dp || rank_begin >= rank_end) return ZERO_EINVAL;
     const int64_t own_lo = (int64_t)rank_begin * L->shard;
@@ -467,7 +469,8 @@ int rs_adamw_plain(const zero_layout_t* L, const void* const* src, int32_t n_src
     if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
     if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
     UpdateTarget t;
-    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out, out_mode, &t);
+    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out, out_mode,
+                            q8 != nullptr, &t);
     if (rc) return rc;
     if (src_base > begin) return ZERO_EINVAL;
     UpdateParams p;
@@ -574,7 +577,8 @@ extern "C" int zero_accumulate_adamw(const zero_layout_t* L, int32_t mode,
     if (n_grads > ZERO_MAX_SRC) return ZERO_ERANGE;
     if (mode == ZERO_ACC_LOCAL ? n_acc != n_grads : n_acc != 1) return ZERO_EINVAL;
     UpdateTarget t;
-    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode, &t);
+    int rc = prepare_target(L, rank_begin, rank_end, begin, end, master, m, v, out_bf16, out_mode,
+                            false, &t);
     if (rc) return rc;
     if (acc_base > begin || grad_base > begin) return ZERO_EINVAL;
     UpdateParams p;

@@ -188,10 +188,13 @@ constexpr int32_t ZERO_OUT_NONE = -1;
 
 // Argument checks that need no CUDA call, then the offsets (zero_gb300.h,
 // zero_reduce_scatter_adamw: state of i at [i - rank_begin*S]; out at [i] for
-// ZERO_OUT_FULL, like the state for ZERO_OUT_SHARD; no out for ZERO_OUT_NONE).
+// ZERO_OUT_FULL, like the state for ZERO_OUT_SHARD).  A bf16 output
+// (q8_out false) needs out_mode ZERO_OUT_FULL or ZERO_OUT_SHARD and a non-null
+// out; only the library's 8-bit-output updates (q8_out true) pass
+// ZERO_OUT_NONE with a null out, so no public argument reaches a null store.
 int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end, int64_t begin,
                    int64_t end, float* master, float* m, float* v, uint16_t* out, int32_t out_mode,
-                   UpdateTarget* t);
+                   bool q8_out, UpdateTarget* t);
 // The pointer-kind checks (CUDA calls) of a prepared target.
 int check_target_ptrs(const UpdateTarget& t);
 // Hyper-parameter checks and the fp32 scalars of the update.
