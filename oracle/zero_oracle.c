@@ -320,34 +320,59 @@ void oracle_all_gather_bf16(const uint16_t* shards, int32_t n_dp, int64_t shard,
  * 1.0: the gradient is scaled so that its global L2 norm does not exceed it.
  * Reading taken (the pages give no formula): the global norm is the L2 norm of
  * the mean gradient over all elements, ||g|| = sqrt(sum g_i^2); the scale is
- * min(1, max_norm / (||g|| + 1e-6)), applied as one fp32 multiply.  Squares
- * and their sum are taken in fp64 (each square of an fp32 value is exact);
- * the quotient is taken in fp64 and rounded once to fp32. */
+ * min(1, max_norm / (||g|| + 1e-6)), applied as one fp32 multiply.  Each
+ * square of an fp32 value is exact in fp64; the squares are summed in fp64
+ * with Neumaier's compensation (A. Neumaier, "Rundungsfehleranalyse einiger
+ * Verfahren zur Summation endlicher Summen", ZAMM 54, 1974): the running sum
+ * plus a running correction that collects every addition's rounding error, so
+ * that for these non-negative terms the result is within a few units in the
+ * last place of the exact sum whatever the number of terms (a plain running
+ * fp64 sum drifts by up to about n units).  The quotient is taken in fp64 and
+ * rounded once to fp32. */
+
+typedef struct {
+    double sum, comp;
+} oracle_csum;
+
+static void oracle_csum_add(oracle_csum* k, double x)
+{
+    double t = k->sum + x;
+    if (fabs(k->sum) >= fabs(x))
+        k->comp = k->comp + ((k->sum - t) + x);
+    else
+        k->comp = k->comp + ((x - t) + k->sum);
+    k->sum = t;
+}
+
+static double oracle_csum_value(const oracle_csum* k)
+{
+    return k->sum + k->comp;
+}
 
 double oracle_grad_norm_sq_bf16(const uint16_t* src, int32_t n_src, int64_t ld, int64_t n,
                                 float divisor)
 {
-    double sum = 0.0;
+    oracle_csum acc = {0.0, 0.0};
     for (int64_t i = 0; i < n; ++i) {
         float s = 0.0f;
         for (int32_t r = 0; r < n_src; ++r) s = s + oracle_bf16_to_f32(src[(int64_t)r * ld + i]);
         double g = (double)(s / divisor);
-        sum = sum + g * g;
+        oracle_csum_add(&acc, g * g);
     }
-    return sum;
+    return oracle_csum_value(&acc);
 }
 
 double oracle_grad_norm_sq_f32(const float* src, int32_t n_src, int64_t ld, int64_t n,
                                float divisor)
 {
-    double sum = 0.0;
+    oracle_csum acc = {0.0, 0.0};
     for (int64_t i = 0; i < n; ++i) {
         float s = 0.0f;
         for (int32_t r = 0; r < n_src; ++r) s = s + src[(int64_t)r * ld + i];
         double g = (double)(s / divisor);
-        sum = sum + g * g;
+        oracle_csum_add(&acc, g * g);
     }
-    return sum;
+    return oracle_csum_value(&acc);
 }
 
 float oracle_clip_coef(double norm_sq, float max_norm)

@@ -1,7 +1,10 @@
 """Pins for the oracle's clipping by the global gradient norm
 ("DeepSpeed ZeRO", "The configuration file": gradient_clipping 1.0):
 torch.nn.utils.clip_grad_norm_ (a library routine with an fp32 norm),
-numpy's fp64 sum of squares, and closed forms."""
+numpy's fp64 sum of squares, the exactly rounded sum of the squares
+(math.fsum), and closed forms."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +20,19 @@ def test_norm_matches_numpy_fp64():
         src = oracle.cast_bf16(x) if dtype == "bf16" else x
         g = oracle.reduce_mean(src, n_src).astype(np.float64)
         assert oracle.grad_norm_sq(src, n_src) == pytest.approx(float(np.sum(g * g)), rel=1e-12)
+
+
+def test_norm_is_the_exact_sum_of_squares():
+    """The squares of the fp32 mean are exact in fp64, so the norm's only
+    rounding is the sum's: against the exactly rounded sum (math.fsum) it is
+    within a few units in the last place, also for millions of terms, where a
+    plain running fp64 sum drifts by about 1e-11."""
+    for n_src, n, dtype, seed in [(3, 2_000_003, "bf16", 5), (8, 3_000_017, "bf16", 1), (2, 77_777, "f32", 4)]:
+        x = (np.random.default_rng(seed).standard_normal((n_src, n)) * 1e-2).astype(np.float32)
+        src = oracle.cast_bf16(x) if dtype == "bf16" else x
+        g = oracle.reduce_mean(src, n_src).astype(np.float64)
+        exact = math.fsum((g * g).tolist())
+        assert oracle.grad_norm_sq(src, n_src) == pytest.approx(exact, rel=1e-15, abs=0)
 
 
 @pytest.mark.parametrize("max_norm,scale", [(1.0, 1e-2), (1.0, 1.0), (0.5, 3e-3), (1.0, 1e-5)])

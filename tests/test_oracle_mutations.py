@@ -51,6 +51,9 @@ MUTATIONS = [
      "full[(int64_t)o * shard + i] = shards[(int64_t)(n_dp - 1 - o) * shard + i];"),
     ("clip divides by the squared norm", "(sqrt(norm_sq) + 1e-6)", "(norm_sq + 1e-6)"),
     ("clip coefficient not capped at 1", "return c < 1.0f ? c : 1.0f;", "return c;"),
+    ("norm sum drops its compensation", "return k->sum + k->comp;", "return k->sum;"),
+    ("norm sum adds each square twice", "oracle_csum_add(&acc, g * g);\n    }\n    return oracle_csum_value(&acc);\n}\n\nfloat",
+     "oracle_csum_add(&acc, g * g);\n        oracle_csum_add(&acc, g * g);\n    }\n    return oracle_csum_value(&acc);\n}\n\nfloat"),
     ("8-bit scale uses 126", "float inv = 127.0f / amax;", "float inv = 126.0f / amax;"),
     ("8-bit codes truncated", "nearbyintf(oracle_bf16_to_f32(w[i]) * inv)",
      "truncf(oracle_bf16_to_f32(w[i]) * inv)"),
@@ -90,6 +93,7 @@ def _pins():
         ("clip vs torch", lambda: pk.test_clip_matches_torch(1.0, 1.0)),
         ("clip closed forms", pk.test_closed_forms),
         ("norm vs numpy", pk.test_norm_matches_numpy_fp64),
+        ("norm vs exact sum", pk.test_norm_is_the_exact_sum_of_squares),
         ("quant error bound", lambda: pq.test_roundtrip_error_bound(256, 4097)),
         ("quant max and symmetry", pq.test_block_max_maps_to_127_and_symmetry),
         ("quant ties and zeros", pq.test_ties_to_even_and_zero_blocks),
