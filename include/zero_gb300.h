@@ -221,14 +221,18 @@ int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_
  * every allocation on the device, or code that must not call cudaMalloc
  * because of the device-wide synchronization it can imply.  The pages have no
  * counterpart: this is an interface convenience of this library.
- * The per-CTA partial sums live in a library-owned device array of 4096
- * doubles (32 KiB, allocated when the library is loaded and held by every GPU
- * that loads it until the process exits), so the call allocates nothing and
- * calls no allocating routine.  Limits: a device needing more than 4096
- * partials (more than 512 SMs) gets ZERO_ERANGE.  The first call on each device
- * looks up that array's device address (cudaGetSymbolAddress, with that device
+ * The per-CTA partial sums live in a library-owned device array sized for
+ * GPUs of up to 512 SMs: 512 x (2048 / CTA threads) doubles, that is 4096
+ * doubles (32 KiB) in the default build of 256 threads per CTA (16384, 128
+ * KiB, in a 64-thread build).  It is allocated when the library is loaded and
+ * held by every GPU that loads it until the process exits, so the call
+ * allocates nothing and calls no allocating routine.  Limits: a device with
+ * more than 512 SMs gets ZERO_ERANGE.  The first call on each device looks up
+ * that array's device address (cudaGetSymbolAddress, with that device
  * current) and caches it; make the first call on a device before any stream
- * capture begins.  Every call shares the one array and overwrites the partials
+ * capture begins.  If the cached address is no longer device memory of the
+ * current device (its context was destroyed by cudaDeviceReset and created
+ * again), the call looks it up again.  Every call shares the one array and overwrites the partials
  * it reads, so no clearing is needed between calls, but calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race on
  * the array: order them, or use zero_grad_norm_sq with one workspace each.

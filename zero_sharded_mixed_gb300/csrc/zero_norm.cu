@@ -290,10 +290,12 @@ extern "C" int zero_grad_norm_sq(const zero_layout_t* L, const void* const* src,
 namespace zgb {
 
 // Capacity of the library-owned partials: one fp64 per CTA of the partial
-// pass, which launches at most (SMs x resident CTAs per SM) CTAs -- 4096
-// covers GPUs of up to 512 SMs.  32 KiB, held by every GPU that loads the
-// library until the process exits.
-constexpr int64_t kStaticPartials = 4096;
+// pass, which launches at most (SMs x kMaxCtasPerSm) CTAs.  Sized for GPUs of
+// up to 512 SMs whatever the build's CTA size: 4096 doubles (32 KiB) at the
+// default 256 threads, 16384 (128 KiB) at 64.  Held by every GPU that loads
+// the library until the process exits.
+constexpr int64_t kStaticMaxSms = 512;
+constexpr int64_t kStaticPartials = kStaticMaxSms * kMaxCtasPerSm;
 static __device__ __align__(256) double g_static_partials[kStaticPartials];
 
 namespace {
@@ -302,15 +304,16 @@ std::atomic<double*> g_static_partials_addr[kMaxStaticDevices];
 }  // namespace
 
 // The device address of g_static_partials on the current device, looked up
-// once per device (cudaGetSymbolAddress with that device current) and cached.
-int static_partials(double** out) {
+// once per device (cudaGetSymbolAddress with that device current) and cached;
+// refresh = true looks it up again (after the device's context was replaced).
+int static_partials(double** out, bool refresh) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         (void)cudaGetLastError();
         return ZERO_ECUDA;
     }
     if (dev >= kMaxStaticDevices) return ZERO_ERANGE;
-    double* p = g_static_partials_addr[dev].load(std::memory_order_acquire);
+    double* p = refresh ? nullptr : g_static_partials_addr[dev].load(std::memory_order_acquire);
     if (p == nullptr) {
         void* addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_static_partials) != cudaSuccess || addr == nullptr) {
@@ -334,8 +337,11 @@ extern "C" int zero_grad_norm_sq_static(const zero_layout_t* L, const void* cons
     if (!L || !src || !norm_sq) return ZERO_EINVAL;
     if (norm_partials_capacity() > kStaticPartials) return ZERO_ERANGE;   // more SMs than it holds
     double* partials = nullptr;
-    const int rc = static_partials(&partials);
+    int rc = static_partials(&partials, false);
     if (rc) return rc;
+    // A cached address that is no longer device memory of this device means the
+    // context it came from was destroyed (cudaDeviceReset): look it up again.
+    if (check_device_ptr(partials) && (rc = static_partials(&partials, true))) return rc;
     // Every partial the finalize pass reads is written by the partial pass of
     // the same call, so nothing in the array needs clearing between calls.
     return grad_norm_sq(L, src, n_src, src_dtype, src_base, divisor, begin, end, partials,
