@@ -293,6 +293,24 @@ int zero_schedule_advance(const float* table, int64_t n_steps, int64_t* step_ind
 int zero_gather_layer(const zero_layout_t* unit, const uint16_t* const* shards,
                       uint16_t* full_out, void* stream);
 
+/* ---- fp32 -> bf16 cast of weights ------------------------------------------
+ * "ZeRO and FSDP", "The idea, one stage at a time": the owners cast their
+ * updated fp32 master shards to bf16 before the all-gather.  The fused update
+ * casts every step; this call casts on its own, for the first bf16 weights of
+ * freshly initialised master weights and for bf16 weights rebuilt from
+ * restored master weights.
+ *
+ * dst[i] = bf16 of src[i] for i in [0, n), rounded to nearest, ties to even;
+ * values at or beyond the largest finite bf16 plus half an ulp become +-inf,
+ * subnormals are kept, and a NaN keeps its sign and top payload bits with the
+ * quiet bit set (the upper half of its bits OR 0x0040).  src (n fp32) and dst
+ * (n bf16 bit patterns) are DEVICE buffers of the caller, 4- and 2-byte
+ * aligned (16-byte alignment of both takes the vector path); they must not
+ * overlap.  n = 0 does nothing.
+ * Errors: ZERO_EINVAL (n < 0, a null or non-device pointer), ZERO_EALIGN,
+ * ZERO_ECUDA. */
+int zero_cast_bf16(const float* src, uint16_t* dst, int64_t n, void* stream);
+
 /* ---- stage-3 gather with 8-bit weights (ZeRO++) ---------------------------
  * "ZeRO Optimizer, in depth", "Offload and ZeRO++" (zero_quantized_weights
  * quantises the weight all-gather) and "ZeRO and FSDP", "Fewer bytes on the

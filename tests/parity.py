@@ -74,3 +74,47 @@ def assert_state(got_wmv, ref_wmv, exact=True, what=""):
         assert_f32_close(g, r, what=f"{what}{name}")
         if exact:
             assert_bit_exact_f32(g, r, what=f"{what}{name}")
+
+
+def zero3_oracle_run(states, shards, grads, hp, steps, n_dp, block=None):
+    """The oracle's statement of the stage-3 step sequence over a list of
+    units, on the host: per step t, every unit gathered for forward in order,
+    then in reverse every unit gathered for backward, its gradient
+    reduce-scattered (fp32 sum over ranks) and its owned shards updated, bf16
+    into the owners' shards ("ZeRO and FSDP", "FSDP, ZeRO-3 inside PyTorch";
+    "DeepSpeed ZeRO", "Stage 3 step by step").  With block set, the weights
+    travel as 8-bit shards: each owner's bf16 shard is quantized after every
+    update and the gathers dequantize ("ZeRO and FSDP", "Fewer bytes on the
+    wire").
+
+    states[i] = [w, m, v] fp32 arrays (padded length), shards[i] the bf16 bit
+    patterns (padded length), grads[i](t) the (n_dp, P) bf16 bit patterns of
+    unit i's gradient at step t.  Returns (gathered, states, shards):
+    gathered = [(phase, i, bits)] in gather order; states and shards are new
+    arrays (the inputs are not modified)."""
+    import oracle
+    states = [[np.asarray(x, np.float32).copy() for x in st] for st in states]
+    shards = [np.asarray(s, np.uint16).copy() for s in shards]
+
+    def quant(s):
+        return [oracle.quantize_int8(o, block) for o in s.reshape(n_dp, -1)]
+
+    q = [quant(s) for s in shards] if block else None
+
+    def gather(i):
+        if block:
+            return oracle.all_gather(np.stack([oracle.dequantize_int8(qq, sc, block) for qq, sc in q[i]]))
+        return oracle.all_gather(shards[i].reshape(n_dp, -1))
+
+    gathered = []
+    for t in steps:
+        for i in range(len(states)):
+            gathered.append(("fwd", i, gather(i)))
+        for i in reversed(range(len(states))):
+            gathered.append(("bwd", i, gather(i)))
+            A = oracle.accumulate_reduce(None, grads[i](t), first=True)
+            out, *states[i] = oracle.rs_adamw_reference(A[None, :], n_dp, *states[i], hp, t)
+            shards[i] = out
+            if block:
+                q[i] = quant(out)
+    return gathered, states, shards

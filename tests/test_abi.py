@@ -186,6 +186,18 @@ def test_internal_output_mode_is_refused(zlib):
                                          FAKE, mode, ctypes.byref(hp), None) == 0
 
 
+def test_cast_argument_checks(zlib):
+    """zero_cast_bf16 refuses a negative length, null pointers and misaligned
+    pointers, and does nothing for n = 0, before any CUDA call."""
+    lib = zlib.load()
+    assert lib.zero_cast_bf16(FAKE, FAKE, -1, None) == -1
+    assert lib.zero_cast_bf16(None, FAKE, 8, None) == -1
+    assert lib.zero_cast_bf16(FAKE, None, 8, None) == -1
+    assert lib.zero_cast_bf16(FAKE + 2, FAKE, 8, None) == -2
+    assert lib.zero_cast_bf16(FAKE, FAKE + 1, 8, None) == -2
+    assert lib.zero_cast_bf16(FAKE, FAKE, 0, None) == 0
+
+
 def test_accumulate_and_gather_argument_checks(zlib):
     lib = zlib.load()
     L = zlib.zero_layout([4096], 4)

@@ -200,7 +200,7 @@ def test_zero3_engine_overlap_comm(zlib, cuda_device, qw):
         eng = Zero3Engine(units, n_dp, cfg)
         for i, u in enumerate(eng.units):
             u.master.copy_(inputs.master_weights(u.layout.n, u.layout.padded_n, seed=40 + i).cuda())
-            u.shards.copy_(u.master.view(n_dp, -1).to(torch.bfloat16))
+            zlib.zero_cast_bf16(u.master, u.shards.view(-1))
             if eng.q8 is not None:
                 zstep.zero3_quantize(u, eng.q8[i])
         seen, served = [], 0
@@ -231,6 +231,21 @@ def test_zero3_engine_overlap_comm(zlib, cuda_device, qw):
         for x, y in ((ua.master, ub.master), (ua.m, ub.m), (ua.v, ub.v), (ua.shards, ub.shards)):
             assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16),
                                y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16))
+    # both against the oracle's stage-3 sequence from the same initial state
+    layouts = [u.layout for u in b.units]
+    init_w = [inputs.master_weights(L.n, L.padded_n, seed=40 + i).numpy() for i, L in enumerate(layouts)]
+    gathered, st, sh = parity.zero3_oracle_run(
+        [[w, np.zeros_like(w), np.zeros_like(w)] for w in init_w], [oracle.cast_bf16(w) for w in init_w],
+        [lambda t, i=i, L=L: parity.bits(inputs.grads_bf16(n_dp, L.n, L.padded_n, seed=50 + i, step=t))
+         for i, L in enumerate(layouts)], HP, (1, 2), n_dp, 256 if qw else None)
+    assert len(gathered) == len(seen_b)
+    for x, (p, i, ref) in zip(seen_b, gathered):
+        assert np.array_equal(parity.bits(x), ref), (p, i)
+    if qw:          # the 8-bit update writes only the 8-bit shards: bring the bf16 ones up to date
+        b._bf16_shards_current()
+    for i, ub in enumerate(b.units):
+        parity.assert_state([ub.master, ub.m, ub.v], st[i], what=f"unit {i} ")
+        assert np.array_equal(parity.bits(ub.shards).reshape(-1), sh[i])
 
 
 def _cfg_dict(stage, **zo):

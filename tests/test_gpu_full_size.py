@@ -56,7 +56,8 @@ def _full_properties(master, out_slice, n_real_in_slice):
 
 def test_gpt2xl_zero2_all_shards(zlib, cuda_device):
     """GPT-2-XL shapes (N = 1,557,611,200), n_dp = 8, 5e8-element buckets,
-    all eight owned shards updated per step, 2 steps."""
+    all eight owned shards updated per step, 5 steps (the later ones with
+    non-zero moments)."""
     zb = zlib
     dev = cuda_device
     L = zb.zero_layout(inputs.gpt2xl_numels(), 8, 8, 500_000_000)
@@ -71,7 +72,7 @@ def test_gpt2xl_zero2_all_shards(zlib, cuda_device):
     idx = _sample_indices(0, P, bounds)
     idx_dev = torch.from_numpy(idx).to(dev)
     ref = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
-    for t in (1, 2):
+    for t in range(1, 6):
         for r in range(8):
             inputs.grad_bf16_into(g[r], L.n, SEED, step=t, rank=r)
         gs = np.stack([_bits_at(g[r], idx_dev) for r in range(8)])
@@ -86,7 +87,7 @@ def test_gpt2xl_zero2_all_shards(zlib, cuda_device):
 def test_llama7b_one_shard(zlib, cuda_device):
     """Llama-7B shapes (N = 6,738,415,616) at n_dp = 8: one owned shard of
     842,301,952 elements, 8 bf16 gradient slices with 1 % outliers x100, the
-    fused update writing into the full bf16 buffer, 2 steps."""
+    fused update writing into the full bf16 buffer, 5 steps."""
     zb = zlib
     dev = cuda_device
     L = zb.zero_layout(inputs.llama7b_numels(), 8, 8, 500_000_000)
@@ -103,7 +104,7 @@ def test_llama7b_one_shard(zlib, cuda_device):
     idx = _sample_indices(0, S, bounds, seed=1)
     idx_dev = torch.from_numpy(idx).to(dev)
     ref = [parity.f32(_take(x, idx_dev)) for x in (master, m, v)]
-    for t in (1, 2):
+    for t in range(1, 6):
         for r in range(8):
             inputs.grad_bf16_into(g[r], S, SEED, step=t, rank=r, outlier_p=0.01)
         gs = np.stack([_bits_at(g[r], idx_dev) for r in range(8)])

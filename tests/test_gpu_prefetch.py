@@ -1,7 +1,12 @@
-"""ZeRO-3 with gathers one unit ahead on a side stream: the same results as the
-sequential path, bit for bit, with at most two gathered units resident."""
+"""ZeRO-3 with gathers one unit ahead on a side stream ("ZeRO and FSDP",
+"FSDP, ZeRO-3 inside PyTorch": the next unit is gathered while the current one
+computes, at most two resident): every gathered unit and the final state equal
+the oracle's stage-3 sequence, and the sequential path, bit for bit."""
+import numpy as np
 import pytest
 import torch
+
+import oracle
 
 from tests import parity
 from zero_sharded_mixed_gb300 import inputs
@@ -16,7 +21,9 @@ def _units(zb, numels_list, n_dp, seed):
         L = zb.zero_layout(numels, n_dp)
         P = L.padded_n
         w = inputs.master_weights(L.n, P, seed=seed + i).cuda()
-        units.append(zstep.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w,
+        shards = torch.empty(P, dtype=torch.bfloat16, device="cuda")
+        zb.zero_cast_bf16(w, shards)
+        units.append(zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w,
                                      torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")))
     return units
 
@@ -80,3 +87,18 @@ def test_prefetched_equals_sequential(zlib, cuda_device, int8):
         for x, y in ((ua.master, ub.master), (ua.m, ub.m), (ua.v, ub.v)):
             parity.assert_bit_exact_f32(x, y)
         assert torch.equal(ua.shards.view(torch.int16), ub.shards.view(torch.int16))
+    # the oracle's sequence from the same initial state: every gathered unit at
+    # the moment it was gathered, and the final master / m / v / shards
+    init = _units(zb, numels_list, n_dp, 60)
+    host_grads = [parity.bits(g) for g in grads]
+    gathered, st, sh = parity.zero3_oracle_run(
+        [[parity.f32(u.master), np.zeros(u.layout.padded_n, np.float32), np.zeros(u.layout.padded_n, np.float32)]
+         for u in init],
+        [parity.bits(u.shards).reshape(-1) for u in init],
+        [lambda t, g=g: g for g in host_grads], oracle.AdamW(), (1, 2), n_dp, 256 if int8 else None)
+    assert [(p, i) for p, i, _ in seen["a"]] == [(p, i) for p, i, _ in gathered]
+    for (p, i, x), (_, _, ref) in zip(seen["a"], gathered):
+        assert np.array_equal(parity.bits(x), ref), (p, i)
+    for i, ua in enumerate(a):
+        parity.assert_state([ua.master, ua.m, ua.v], st[i], what=f"unit {i} ")
+        assert np.array_equal(parity.bits(ua.shards).reshape(-1), sh[i])

@@ -11,7 +11,7 @@ from __future__ import annotations
 
 _BINDING_NAMES = {
     "ZeroError", "ZeroLayout", "ZeroAdamW", "lib_path", "load",
-    "zero_layout", "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate",
+    "zero_layout", "zero_reduce_scatter_adamw", "zero_gather_layer", "zero_accumulate", "zero_cast_bf16",
     "zero_reduce_scatter_adamw_clip", "zero_accumulate_adamw", "zero_grad_norm_workspace",
     "zero_grad_norm_sq", "zero_grad_norm_sq_static", "zero_quantize_int8", "zero_gather_layer_int8",
     "zero_reduce_scatter_adamw_int8", "zero_accumulate_int8", "zero_reduce_scatter_adamw_q8",

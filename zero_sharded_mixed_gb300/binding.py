@@ -108,6 +108,7 @@ def load():
         lib.zero_grad_norm_sq_static.argtypes = [P(ZeroLayout), P(p), i32, i32, i64, f32, i64,
                                                  i64, p, i32, p]
         lib.zero_gather_layer.argtypes = [P(ZeroLayout), P(p), p, p]
+        lib.zero_cast_bf16.argtypes = [p, p, i64, p]
         lib.zero_quantize_int8.argtypes = [P(ZeroLayout), p, p, p, i32, p]
         lib.zero_ckpt_write_shard.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), p, p, p, p]
         lib.zero_ckpt_read_header.argtypes = [ctypes.c_char_p, P(ZeroCkptHeader), P(i32)]
@@ -414,6 +415,14 @@ def zero_gather_layer(unit: ZeroLayout, shards, full_out: torch.Tensor, stream=N
                                   _tensor(full_out, "full_out", torch.bfloat16, unit.padded_n),
                                   _stream_ptr(stream))
     _check(rc, "zero_gather_layer")
+
+
+def zero_cast_bf16(src: torch.Tensor, dst: torch.Tensor, n: int = None, stream=None):
+    """dst[:n] = bf16 of src[:n] (nearest, ties to even); n defaults to src.numel()."""
+    n = src.numel() if n is None else int(n)
+    rc = load().zero_cast_bf16(_tensor(src, "src", torch.float32, n), _tensor(dst, "dst", torch.bfloat16, n),
+                               n, _stream_ptr(stream))
+    _check(rc, "zero_cast_bf16")
 
 
 def zero_accumulate(L: ZeroLayout, mode: int, srcs, src_dtype: int, src_base: int,

@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libzero_gb300.so")
 
 CUDA_SOURCES = ["zero_runtime.cu", "zero_rs_adamw.cu", "zero_accumulate.cu", "zero_gather.cu",
                 "zero_norm.cu", "zero_quant.cu", "zero_rs_adamw_tma.cu", "zero_qgrad.cu",
-                "zero_schedule.cu"]
+                "zero_schedule.cu", "zero_cast.cu"]
 HOST_SOURCES = ["zero_host.cpp", "zero_ckpt.cpp"]
 HEADERS = ["zero_common.cuh", "zero_update.cuh", "zero_quant.cuh"]
 

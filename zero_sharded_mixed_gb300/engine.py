@@ -97,7 +97,8 @@ class ZeroEngine(_Tracing):
         self.master = torch.zeros(P, device=device) if master is None else master
         self.m = torch.zeros(P, device=device)
         self.v = torch.zeros(P, device=device)
-        self.out = self.master.to(torch.bfloat16)          # the initial bf16 weights
+        self.out = torch.empty(P, dtype=torch.bfloat16, device=device)
+        zb.zero_cast_bf16(self.master, self.out, P)         # the initial bf16 weights
         self.acc = [torch.empty(P, device=device) for _ in range(n_dp)] \
             if (config.stage == 1 and self.K > 1) else None
         self.A = torch.empty(P, device=device) if (config.stage == 2 and self.K > 1) else None
@@ -242,7 +243,9 @@ class Zero3Engine(_Tracing):
             L = zb.zero_layout(numels, n_dp, align)
             P = L.padded_n
             w = torch.zeros(P, device=device) if masters is None else masters[i]
-            self.units.append(zs.Zero3Unit(L, w.to(torch.bfloat16).view(n_dp, L.shard), w,
+            shards = torch.empty(P, dtype=torch.bfloat16, device=device)
+            zb.zero_cast_bf16(w, shards, P)                 # the initial bf16 shards
+            self.units.append(zs.Zero3Unit(L, shards.view(n_dp, L.shard), w,
                                            torch.zeros(P, device=device), torch.zeros(P, device=device)))
         cap = max(u.layout.padded_n for u in self.units)
         self.ring = zs.GatherRing(cap, device=str(device))
@@ -362,11 +365,11 @@ class Zero3Engine(_Tracing):
 
     def _bf16_shards_current(self):
         """With 8-bit weights the update writes only the 8-bit shards; the bf16
-        shards are brought back to bf16(master) -- the update's own cast, round
-        to nearest even, which torch's conversion of finite values matches."""
+        shards are brought back to bf16(master) by the library's cast, round to
+        nearest even like the update's own."""
         if self.q8 is not None:
             for u in self.units:
-                u.shards.view(-1).copy_(u.master.to(torch.bfloat16))
+                zb.zero_cast_bf16(u.master, u.shards.view(-1), u.layout.padded_n)
 
     def save_checkpoint(self, dirpath):
         """Every unit's shards of master / m / v and its owners' bf16 shards."""
