@@ -125,6 +125,7 @@ struct DequantParams {
     uint16_t* out;       // the first of these shards' places in the full buffer
     int64_t shard;
     int32_t block;
+    int32_t block_shift; // log2(block): the block of element k is k >> block_shift
 };
 
 __device__ __forceinline__ uint4 dequant8(const uint2 raw, const float s) {
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) dequant_gather_vec_kernel(const __gr
             const int64_t k = (vi + u * kThreads) * 8;
             if (vi + u * kThreads < nv) {
                 raw[u] = __ldcs(reinterpret_cast<const uint2*>(q + k));
-                s[u] = __ldg(sc + k / p.block);                      // one block: block % 8 == 0
+                s[u] = __ldg(sc + (k >> p.block_shift));             // one block: block % 8 == 0
             }
         }
 #pragma unroll
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) dequant_gather_scalar_kernel(const _
     uint16_t* dst = p.out + (int64_t)blockIdx.y * p.shard;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < p.shard; k += stride)
-        dst[k] = to_bf16(__fmul_rn((float)q[k], sc[k / p.block]));
+        dst[k] = to_bf16(__fmul_rn((float)q[k], sc[k >> p.block_shift]));
 }
 
 bool valid_block(int32_t block) {
@@ -270,6 +271,8 @@ extern "C" int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* c
         p.out = full_out + (int64_t)o0 * unit->shard;
         p.shard = unit->shard;
         p.block = block;
+        p.block_shift = 0;
+        while ((1 << p.block_shift) < block) ++p.block_shift;   // block is a power of two
         vec = vec && aligned16(p.out);
         const int64_t resident = (int64_t)sm_count() * (vec ? occ_vec * ZGB_DEQUANT_WAVES : occ_scalar);
         const int64_t per_shard = resident / cnt > 0 ? resident / cnt : 1;
