@@ -30,9 +30,16 @@ def pytest_collection_modifyitems(config, items):
 
 @pytest.fixture(scope="session")
 def zlib():
-    """The built C-ABI library (compiled in-tree for sm_103a if stale)."""
+    """The built C-ABI library (compiled in-tree for sm_103a if stale), or the
+    prebuilt variant library named by ZGB_TEST_LIB: a test that checks an
+    opt-in build runs this suite's cases against it in a child process."""
     from zero_sharded_mixed_gb300 import binding, build
-    build.build()
+    variant = os.environ.get("ZGB_TEST_LIB")
+    if variant:
+        binding.lib_path = variant
+        binding._lib = None
+    else:
+        build.build()
     binding.load()
     return binding
 

@@ -26,7 +26,7 @@ CUDA_SOURCES = ["zero_runtime.cu", "zero_rs_adamw.cu", "zero_accumulate.cu", "ze
                 "zero_norm.cu", "zero_quant.cu", "zero_rs_adamw_tma.cu", "zero_qgrad.cu",
                 "zero_schedule.cu", "zero_cast.cu"]
 HOST_SOURCES = ["zero_host.cpp", "zero_ckpt.cpp"]
-HEADERS = ["zero_common.cuh", "zero_update.cuh", "zero_quant.cuh"]
+HEADERS = ["zero_common.cuh", "zero_update.cuh", "zero_quant.cuh", "zero_tma.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Host code: no FMA contraction either (the bias corrections are formed on the host).

@@ -31,6 +31,7 @@
 // owner it meets.
 #include <cmath>
 
+#include "zero_tma.cuh"
 #include "zero_update.cuh"
 
 #ifndef ZGB_QGRAD_WAVES
@@ -57,6 +58,22 @@
 #endif
 #ifndef ZGB_QACC_U
 #define ZGB_QACC_U 0         // the same for the accumulation
+#endif
+#ifndef ZGB_QWS
+#define ZGB_QWS 0            // opt-in: the code streams staged by bulk copies (qgrad_ws_kernel)
+                             // for 1, 2, 4 or 8 sources with 16-byte aligned slices: bit 0 the
+                             // accumulation, bit 1 the updates.  Bit-exact, but measured slower
+                             // than the register-staged kernels (update 6093 against 6350 GB/s,
+                             // accumulation 6133 against 6292, 8-bit output 6115 against 6432)
+#endif
+#ifndef ZGB_QWS_STAGES
+#define ZGB_QWS_STAGES 4     // stages of its ring per CTA
+#endif
+#ifndef ZGB_QWS_MINBLOCKS
+#define ZGB_QWS_MINBLOCKS 2  // CTAs per SM its register allocation must allow
+#endif
+#ifndef ZGB_QWS_TIMEOUT_CYCLES
+#define ZGB_QWS_TIMEOUT_CYCLES (1ll << 31)   // SM cycles before a wait gives up (~1 s)
 #endif
 
 namespace zgb {
@@ -292,6 +309,201 @@ __global__ void __launch_bounds__(kThreads) qgrad_scalar_kernel(const __grid_con
         qgrad_one<kUpdate>(p, sl, i, sc);
 }
 
+// ----------------------------------------------------------------------------
+// Warp-specialized variant: the code streams staged by bulk copies.
+//
+// The register-staged kernel above holds 8 bytes of codes per source in flight
+// per thread and waits for them before it computes, so the SM's bytes in
+// flight fall with every pass's compute.  Here warp 0's lane 0 (the producer)
+// copies tile k's R code streams -- kQWsTile bytes each, 1-D bulk copies
+// (cp.async.bulk) -- into stage k % S of a shared-memory ring, arming the
+// stage's "full" mbarrier with the byte count, once every consumer warp has
+// released the stage's previous tile (its "empty" mbarrier, one arrival per
+// consumer warp).  Consumer warps 1..C each own 256 consecutive elements of a
+// tile, 8 per lane: they load their block scales and (for the update) their
+// fp32 state or (for an accumulation that adds) their fp32 destination
+// before waiting on the stage, read their codes from it, release it, and then
+// compute and store exactly as the register-staged kernel does -- the same
+// functions, so the results are bit-identical.  No CTA-wide barrier sits in
+// the loop.  Tile u of a stage completes phase u of both barriers; waits pass
+// the parity u & 1 (the producer cannot refill a stage before every consumer
+// released it, and a consumer cannot release a tile that was not issued, so no
+// wait trails by two phases).
+//
+// Bulk copies start on 16-byte boundaries and move multiples of 16 bytes: the
+// host takes this kernel only when every source's slice starts 16-byte
+// aligned; the tiles cover the first n16 = n & ~15 elements of the slice, and
+// the last n - n16 (< 16) go element by element to CTA 0's first consumer warp.
+//
+// Every wait is bounded: a wait that gives up records ZERO_ETIMEOUT in
+// g_qgrad_status (read by zero_status_check) and ends that warp's loop; the
+// producer then waits, bounded again, for the copies of the last S tiles it
+// issued, so that no copy lands in the shared memory of a finished CTA.
+// ----------------------------------------------------------------------------
+
+__device__ int g_qgrad_status;   // ZERO_OK, or ZERO_ETIMEOUT once a bounded wait gave up
+
+constexpr int kQWsConsumers = 8;
+constexpr int kQWsThreads = 32 * (kQWsConsumers + 1);
+constexpr int kQWsTile = 256 * kQWsConsumers;        // elements (= bytes per source) per tile
+constexpr int kQWsStages = ZGB_QWS_STAGES;
+static_assert(kQWsStages >= 2 && kQWsStages <= 8, "the code ring runs with 2 to 8 stages");
+static_assert(kQWsTile % 256 == 0, "a consumer warp's 256 elements must be whole 8-bit blocks");
+
+template <int R>
+constexpr uint32_t qws_smem_bytes() {
+    return (uint32_t)(R * kQWsTile * kQWsStages);
+}
+static_assert(qws_smem_bytes<8>() <= 227 * 1024, "the ring must fit the shared memory of one CTA");
+
+template <int R, bool kUpdate, bool kQ8>
+__global__ void __launch_bounds__(kQWsThreads, ZGB_QWS_MINBLOCKS)
+qgrad_ws_kernel(const __grid_constant__ QGradParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kQWsStages];
+    __shared__ __align__(8) uint64_t empty[kQWsStages];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const QSlice sl = qslice(p);
+    const int64_t n16 = sl.n & ~(int64_t)15;
+    const int64_t n_tiles = (n16 + kQWsTile - 1) / kQWsTile;
+    const int64_t count = blockIdx.x < n_tiles ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto tile_e0 = [&](int64_t k) { return ((int64_t)blockIdx.x + k * gridDim.x) * kQWsTile; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQWsStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kQWsConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int64_t k = 0;
+            for (; k < count; ++k) {
+                const int s = (int)(k % kQWsStages);
+                if (k >= kQWsStages &&
+                    !mbar_wait_bounded(&empty[s], (uint32_t)((k / kQWsStages - 1) & 1), ZGB_QWS_TIMEOUT_CYCLES)) {
+                    atomicExch(&g_qgrad_status, ZERO_ETIMEOUT);
+                    break;
+                }
+                const int64_t e0 = tile_e0(k);
+                const uint32_t bytes = (uint32_t)min((int64_t)kQWsTile, n16 - e0);   // a multiple of 16
+                unsigned char* st = smem + (size_t)s * R * kQWsTile;
+                mbar_arrive_expect_tx(&full[s], bytes * (uint32_t)R);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    bulk_g2s(st + r * kQWsTile, p.q[r] + sl.eoff + e0, bytes, &full[s]);
+            }
+            // the copies of the last stages issued must land before the CTA ends
+            for (int64_t j = k > kQWsStages ? k - kQWsStages : 0; j < k; ++j)
+                (void)mbar_wait_bounded(&full[j % kQWsStages], (uint32_t)((j / kQWsStages) & 1),
+                                        ZGB_QWS_TIMEOUT_CYCLES);
+        }
+        return;
+    }
+    const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
+    const int off = (warp - 1) * 256 + lane * 8;          // this lane's first element in a tile
+    for (int64_t k = 0; k < count; ++k) {
+        const int s = (int)(k % kQWsStages);
+        const int64_t e0 = tile_e0(k);
+        const bool act = off < min((int64_t)kQWsTile, n16 - e0);
+        const int64_t e = e0 + off;                         // slice-local index
+        const int64_t g = sl.eoff + e;                      // index from the code and target pointers
+        float scale[R];
+        float4 st[kUpdate ? 6 : 2];
+        if (act) {
+            const int64_t b = sl.soff + ((sl.k0 + e) >> p.block_shift);
+#pragma unroll
+            for (int r = 0; r < R; ++r) scale[r] = __ldg(p.scale[r] + b);
+            if constexpr (kUpdate) {
+                load_state(p, g, st);
+            } else if (!p.first) {
+                st[0] = ld_stream_f4(p.dst + g);
+                st[1] = ld_stream_f4(p.dst + g + 4);
+            }
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)((k / kQWsStages) & 1),
+                                                                  ZGB_QWS_TIMEOUT_CYCLES));
+        if (!ok) {
+            if (lane == 0) atomicExch(&g_qgrad_status, ZERO_ETIMEOUT);
+            break;
+        }
+        uint2 c[R];
+        if (act) {
+            const unsigned char* stage = smem + (size_t)s * R * kQWsTile + off;
+#pragma unroll
+            for (int r = 0; r < R; ++r) c[r] = *reinterpret_cast<const uint2*>(stage + r * kQWsTile);
+        }
+        __syncwarp();                                        // the warp is done with stage s
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (act) {
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) add_codes8(x, c[r], scale[r]);
+            if constexpr (kQ8) {
+                finish_vec_q8<true>(p, g, x, st, 1.0f, sc, p.qout, p.qoscale);
+            } else if constexpr (kUpdate) {
+                finish_vec<true>(p, g, x, st, 1.0f, sc);
+            } else {
+                const float4 d[2] = {st[0], st[1]};
+                store_acc(p, g, x, d);
+            }
+        }
+    }
+    // the last n - n16 elements of the slice, element by element
+    if constexpr (!kQ8) {
+        if (blockIdx.x == 0 && warp == 1 && lane < sl.n - n16) qgrad_one<kUpdate>(p, sl, n16 + lane, sc);
+    }
+}
+
+// Reads and clears the status word of the bounded waits above (ZERO_OK or
+// ZERO_ETIMEOUT); synchronizes the device.
+int take_qgrad_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qgrad_status, sizeof v) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ZERO_ECUDA;
+    }
+    if (v != ZERO_OK) {
+        const int zero = ZERO_OK;
+        if (cudaMemcpyToSymbol(g_qgrad_status, &zero, sizeof zero) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return ZERO_ECUDA;
+        }
+    }
+    return v == ZERO_OK ? ZERO_OK : ZERO_ETIMEOUT;
+}
+
+template <int R, bool kUpdate, bool kQ8>
+int launch_qgrad_ws(const QGradParams& p, int64_t slice_max, cudaStream_t s) {
+    const uint32_t smem = qws_smem_bytes<R>();
+    const void* fn = (const void*)qgrad_ws_kernel<R, kUpdate, kQ8>;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        note_cuda_error(e);
+        return ZERO_ECUDA;
+    }
+    const int occupancy = ctas_per_sm(fn, kQWsThreads, smem);
+    const int64_t slices = p.owners > 0 ? p.owners : 1;
+    const int64_t cap = (int64_t)sm_count() * (occupancy > 0 ? occupancy : 1) / slices;
+    const int64_t tiles = ((slice_max & ~(int64_t)15) + kQWsTile - 1) / kQWsTile;
+    const dim3 grid((unsigned)(tiles < 1 ? 1 : (tiles < cap ? tiles : (cap > 0 ? cap : 1))), (unsigned)slices);
+    qgrad_ws_kernel<R, kUpdate, kQ8><<<grid, kQWsThreads, smem, s>>>(p);
+    return launch_status();
+}
+
+// Whether a launch of this kind takes the warp-specialized kernel.
+template <bool kUpdate>
+bool qgrad_ws_enabled() {
+    return (ZGB_QWS & (kUpdate ? 2 : 1)) != 0;
+}
+
 // p.owners == 0: one owner's slice of p.n elements; else `owners` slices of
 // at most `slice_max` elements, one per blockIdx.y, sharing the grid's CTAs.
 template <int R, bool kUpdate, bool kQ8 = false>
@@ -309,7 +521,16 @@ int launch_qgrad_vec(const QGradParams& p, int64_t slice_max, cudaStream_t s) {
 // vec: every slice of the launch takes the vector kernel (8-aligned slice
 // starts, aligned pointers); the scalar kernel serves single-owner launches.
 template <bool kUpdate, bool kQ8 = false>
-int launch_qgrad(const QGradParams& p, bool vec, int64_t slice_max, cudaStream_t s) {
+int launch_qgrad(const QGradParams& p, bool vec, bool ws, int64_t slice_max, cudaStream_t s) {
+    if (vec && ws && qgrad_ws_enabled<kUpdate>()) {
+        switch (p.n_src) {
+            case 1: return launch_qgrad_ws<1, kUpdate, kQ8>(p, slice_max, s);
+            case 2: return launch_qgrad_ws<2, kUpdate, kQ8>(p, slice_max, s);
+            case 4: return launch_qgrad_ws<4, kUpdate, kQ8>(p, slice_max, s);
+            case 8: return launch_qgrad_ws<8, kUpdate, kQ8>(p, slice_max, s);
+            default: break;                 // the register-staged kernels below
+        }
+    }
     if constexpr (kQ8) {                 // vector kernels only: whole 256-element blocks per warp
         if (!vec) return ZERO_EALIGN;
         switch (p.n_src) {
@@ -383,6 +604,14 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
         base.q[r] = nullptr;
         base.scale[r] = nullptr;
     }
+    // whether every source's slice of owner o starts on a 16-byte boundary (the
+    // bulk copies of the warp-specialized kernel)
+    auto slice_aligned16 = [&](int64_t o) {
+        const int64_t lo = begin > o * S ? begin : o * S;
+        for (int r = 0; r < n_src; ++r)
+            if (!aligned16(q_src[r] + lo)) return false;
+        return true;
+    };
     // owner o's launch parameters and whether its slice takes the vector kernel
     auto owner_params = [&](int64_t o, QGradParams& p) {
         const int64_t lo = begin > o * S ? begin : o * S;
@@ -400,11 +629,12 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
     };
     const int64_t o_first = begin / S;
     const int64_t o_end = (end + S - 1) / S;               // owners o_first .. o_end - 1 meet the range
-    bool all_vec = true;
+    bool all_vec = true, all_ws = true;
     int64_t slice_max = 0;
     QGradParams p;
     for (int64_t o = o_first; o < o_end; ++o) {
         all_vec = owner_params(o, p) && all_vec;
+        all_ws = all_ws && slice_aligned16(o);
         slice_max = p.n > slice_max ? p.n : slice_max;
     }
     // Whole shards only: the owners share the grid's CTAs evenly, so slices of
@@ -427,11 +657,11 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
             p.scale[r] = scale_src[r];
         }
         (void)place(p, begin);
-        return launch_qgrad<kUpdate, kQ8>(p, true, slice_max, s);
+        return launch_qgrad<kUpdate, kQ8>(p, true, all_ws, slice_max, s);
     }
     for (int64_t o = o_first; o < o_end; ++o) {
         const bool vec = owner_params(o, p);
-        const int rc = launch_qgrad<kUpdate, kQ8>(p, vec, p.n, s);
+        const int rc = launch_qgrad<kUpdate, kQ8>(p, vec, slice_aligned16(o), p.n, s);
         if (rc) return rc;
     }
     return ZERO_OK;

@@ -109,6 +109,7 @@ extern "C" int zero_status_check(void* stream) {
     zgb::note_cuda_error(last);
     if (e != cudaSuccess || last != cudaSuccess) return ZERO_ECUDA;
     const int rc = zgb::take_device_status();   // ZERO_ETIMEOUT if a bounded device wait gave up
+    const int rq = zgb::take_qgrad_status();    // the same for the 8-bit gradient kernels' waits
     const int rs = zgb::take_schedule_status();  // ZERO_ERANGE if a schedule index left its table
-    return rc != ZERO_OK ? rc : rs;
+    return rc != ZERO_OK ? rc : rq != ZERO_OK ? rq : rs;
 }
