@@ -8,6 +8,12 @@
 #include "zero_update.cuh"
 
 namespace zgb {
+// Reads and clears the status word of the opt-in staged 8-bit gradient
+// kernel's bounded waits (zero_qgrad.cu): ZERO_OK or ZERO_ETIMEOUT.
+int take_qgrad_status();
+}  // namespace zgb
+
+namespace zgb {
 
 int check_device_ptr(const void* p) {
     cudaPointerAttributes a;

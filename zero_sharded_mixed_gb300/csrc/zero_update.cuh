@@ -171,8 +171,6 @@ int launch_rs_adamw_tma(const UpdateParams& p, cudaStream_t stream);
 // Reads and clears the device status word of the bounded waits (ZERO_OK or
 // ZERO_ETIMEOUT); synchronizes the device.
 int take_device_status();
-// The same for the 8-bit gradient kernels' bounded waits (zero_qgrad.cu).
-int take_qgrad_status();
 
 // Where an update over flat [begin, end) of the owners rank_begin..rank_end-1
 // reads and writes: state and output pointers already offset to `begin`.
