@@ -66,6 +66,7 @@ CPU_SAMPLE = 1 << 25          # elements of the cpu_baseline sample
 CPU_BASELINE_SECONDS = 6.0    # wall seconds of the all-cores cpu_baseline leg (plus a quarter on one core)
 HEADLINE_MAX_CHARS = 2000     # the headline JSON line stays short enough to survive a tail of the log
 TARGET_FRAC_7B = 0.8          # the bandwidth fraction asked of the fused update on the Llama-7B shard
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e nominal bandwidth, beside the measured copy peak
 REF_SAMPLE = 1 << 25          # elements per step of the reference arm (bounded CPU sample)
 
 
@@ -1138,15 +1139,16 @@ def _compact_roofline(r):
 
 def target_7b(res):
     """The fused update on one owned shard of the Llama-7B shapes: its step
-    time, rate and fraction of the measured copy peak, against the 80 % asked
-    of it."""
+    time, rate and fraction of the measured copy peak (and of the nominal HBM
+    bandwidth), against the 80 % asked of it."""
     if res is None:
         return None
     r = res["roofline"]
     return {"workload": res["config"]["workload"], "ms_per_step": res["ms_per_step"],
             "params_per_s": res["value"], "hbm_gbs_step": res["hbm_gbs_step"],
-            "frac": r["frac"], "frac_step": res["hbm_gbs_step"] / r["peak"], "target_frac": TARGET_FRAC_7B,
-            "met": r["frac"] >= TARGET_FRAC_7B}
+            "frac": r["frac"], "frac_step": res["hbm_gbs_step"] / r["peak"],
+            "frac_nominal": r["achieved"] / NOMINAL_HBM_GBS, "target_frac": TARGET_FRAC_7B,
+            "met": min(r["frac"], r["achieved"] / NOMINAL_HBM_GBS) >= TARGET_FRAC_7B}
 
 
 def headline_line(p, args, world, seven_b=None):

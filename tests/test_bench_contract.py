@@ -130,6 +130,7 @@ def test_headline_line_is_compact_and_parses():
         assert key in back["roofline"], key
     assert back["e2e"]["h2d_bytes_per_step"] > 0 and back["e2e"]["d2h_bytes_per_step"] > 0
     assert back["target_7b"]["frac"] == 1.04 and back["target_7b"]["met"] is True
+    assert back["target_7b"]["frac_nominal"] == pytest.approx(1.04 * 6675.2 / bench.NOMINAL_HBM_GBS)
     assert back["cpu_baseline"]["cores"] == 16 and back["impl"] == "ours"
 
 
