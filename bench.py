@@ -87,6 +87,9 @@ def parse_args(argv=None):
     ap.add_argument("--elems", type=int, default=0,
                     help="replace the model shape by a flat vector of this many elements "
                          "(small cases for profiling; not a headline workload)")
+    ap.add_argument("--bucket", type=int, default=500_000_000,
+                    help="reduce bucket in elements of the ZeRO-1/2 workloads run with --elems "
+                         "(small cases for profiling; the model workloads keep 5e8)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
@@ -275,13 +278,16 @@ class Workload:
 
 
 def _owners(L, begin, end):
-    """Launches of one 8-bit gradient call over [begin, end): one for a range
-    of several whole shards (the owners share one grid), else one per owner
-    whose shard the range meets."""
+    """Launches of one 8-bit gradient call over [begin, end) (aligned buffers):
+    one for a range of several whole shards (the owners share one grid) or of
+    several owners whose boundaries lie on the range's 8-element grid (one
+    stream over the range), else one per owner whose shard the range meets."""
     if end <= begin:
         return 0
     owners = (end - 1) // L.shard - begin // L.shard + 1
     if owners > 1 and begin % L.shard == 0 and end % L.shard == 0:
+        return 1
+    if owners > 1 and L.shard % 8 == 0 and begin % 8 == 0:
         return 1
     return owners
 
@@ -300,7 +306,7 @@ class Zero2Workload(Workload):
     """ZeRO-2 step: the bucketed fused update of every owned element in
     [lo, hi) from n_dp bf16 gradient buffers."""
 
-    def __init__(self, name, device, elems=0):
+    def __init__(self, name, device, elems=0, bucket=500_000_000):
         import torch
         from zero_sharded_mixed_gb300 import inputs
         from zero_sharded_mixed_gb300.step import bucket_ranges
@@ -312,7 +318,7 @@ class Zero2Workload(Workload):
         self.qgrad = name == "gpt2xl-qgrad"
         if name in ("gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad"):
             numels = [elems] if elems else inputs.gpt2xl_numels()
-            L = zb.zero_layout(numels, n_dp, 8, 500_000_000)
+            L = zb.zero_layout(numels, n_dp, 8, bucket if elems else 500_000_000)
             lo, hi, self.rank_begin, self.rank_end = 0, L.padded_n, 0, n_dp
             src_len, outlier = L.padded_n, 0.0
             self.desc = {"workload": ("flat%d_zero2" % elems if elems else "gpt2xl_zero2_all_shards")
@@ -531,7 +537,8 @@ class Zero3Workload(Workload):
             L = zb.zero_layout(numels, n_dp, align=align)
             P = L.padded_n
             w = _master(L.n, P, device)
-            shards = w.to(torch.bfloat16)
+            shards = torch.empty(P, dtype=torch.bfloat16, device=device)
+            zb.zero_cast_bf16(w, shards)
             self.units.append(zstep.Zero3Unit(L, shards.view(n_dp, L.shard), w,
                                               torch.zeros(P, device=device), torch.zeros(P, device=device)))
             total += P
@@ -754,9 +761,9 @@ class Zero3Workload(Workload):
         return out
 
 
-def make_workload(name, device, elems=0):
+def make_workload(name, device, elems=0, bucket=500_000_000):
     if name in ("gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad"):
-        return Zero2Workload(name, device, elems)
+        return Zero2Workload(name, device, elems, bucket)
     if name in ("llama7b-shard", "probe"):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
@@ -856,18 +863,18 @@ def time_e2e(wl, steps, warmup, t0, dist):
     for _ in range(warmup):
         pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
         t += 1
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     torch.cuda.synchronize()
     barrier(dist)
-    start.record()
-    for _ in range(steps):
+    marks[0].record()
+    for k in range(steps):
         pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
+        marks[k + 1].record()
         t += 1
-    end.record()
     torch.cuda.synchronize()
     barrier(dist)
-    ms = start.elapsed_time(end) / steps
+    ms = marks[0].elapsed_time(marks[-1]) / steps
+    per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(steps))
     # the host link on this machine: plain copies of the step's gradients, pinned host to device;
     # the fastest of three (the link's rate varies from moment to moment on a shared host)
     link_gbs = 0.0
@@ -879,7 +886,7 @@ def time_e2e(wl, steps, warmup, t0, dist):
         b.record()
         torch.cuda.synchronize()
         link_gbs = max(link_gbs, host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
-    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs
+    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs, per_step
 
 
 def cpu_sample(wl, n):
@@ -1056,7 +1063,8 @@ def time_checkpoint(device):
     L = zb.zero_layout(numels, 8)
     P = L.padded_n
     st = [_master(L.n, P, device), torch.randn(P, device=device) * 1e-4, torch.rand(P, device=device) * 1e-8]
-    shards = st[0].to(torch.bfloat16)
+    shards = torch.empty(P, dtype=torch.bfloat16, device=device)
+    zb.zero_cast_bf16(st[0], shards)
     hp = zb.ZeroAdamW.make(step=7, **HP)
     nbytes = P * 14
     d = tempfile.mkdtemp(prefix="zgb_ckpt_")
@@ -1158,8 +1166,8 @@ def headline_line(p, args, world, seven_b=None):
                % (world, p["config"].get("n_dp", 8)))
     e2e = p.get("e2e")
     if e2e is not None:
-        e2e = {k: e2e[k] for k in ("value", "unit", "ms_per_step", "steps", "h2d_bytes_per_step",
-                                   "d2h_bytes_per_step", "unavailable") if k in e2e}
+        e2e = {k: e2e[k] for k in ("value", "unit", "ms_per_step", "steps", "step_ms_min", "step_ms_median",
+                                   "h2d_bytes_per_step", "d2h_bytes_per_step", "unavailable") if k in e2e}
         if "link" in p["e2e"]:
             e2e["link_h2d_gbs"] = p["e2e"]["link"]["h2d_gbs"]
             e2e["link_frac"] = p["e2e"]["link"]["frac"]
@@ -1214,7 +1222,7 @@ def run_ours(args):
     primary = args.workload
     results = {}
     for name in workload_order(args):
-        wl = make_workload(name, device, args.elems if name == primary else 0)
+        wl = make_workload(name, device, args.elems if name == primary else 0, args.bucket)
         torch.cuda.synchronize()
         is_primary = name == primary
         steps = args.steps if is_primary else max(1, min(args.steps, 10))
@@ -1252,11 +1260,12 @@ def run_ours(args):
                 fits = host_fits(need * int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
                 if all_ranks_agree(dist, fits, device):
                     e2e_steps = max(1, min(args.steps, 10))
-                    e_ms, h2d, d2h, link_gbs = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
+                    e_ms, h2d, d2h, link_gbs, per_step = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
                     e_ms = max_over_ranks(dist, e_ms, device)
                     link_ms = h2d / (link_gbs * 1e9) * 1e3
                     res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
                                   "ms_per_step": e_ms, "steps": e2e_steps,
+                                  "step_ms_min": per_step[0], "step_ms_median": per_step[len(per_step) // 2],
                                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                   "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
                                            "frac": link_ms / e_ms}}

@@ -53,6 +53,13 @@ def test_owner_count_of_a_range():
     assert bench._owners(L, 200, 500) == 1
     assert bench._owners(L, 200, 550) == 4
 
+    class L8:
+        shard = 96
+    assert bench._owners(L8, 0, 150) == 1          # one stream over owners 0 and 1
+    assert bench._owners(L8, 8, 500) == 1
+    assert bench._owners(L8, 4, 150) == 2          # off the 8-element grid: one launch per owner
+    assert bench._owners(L8, 100, 150) == 1
+
 
 @pytest.mark.parametrize("name", ["gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1",
                                   "accum-zero2", "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch",
@@ -101,7 +108,8 @@ def _fake_result(workload, value, ms, frac):
         "gpu_launches": 80,
         "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_w_max": 1086.5, "samples": 40,
                    "reasons": []},
-        "e2e": {"value": 1.2e10, "unit": bench.UNIT, "ms_per_step": 130.0, "steps": 10,
+        "e2e": {"value": 1.2e10, "unit": bench.UNIT, "ms_per_step": 130.0, "steps": 10, "step_ms_min": 124.8,
+                "step_ms_median": 126.0,
                 "h2d_bytes_per_step": 24921779200, "d2h_bytes_per_step": 3115222400,
                 "link": {"h2d_gbs": 190.0, "h2d_ms_per_step": 124.0, "frac": 0.95}},
         "cpu_baseline": {"value": 1.4e9, "unit": bench.UNIT, "cores": 16, "kind": "oracle",

@@ -25,10 +25,14 @@
 // reads 256 consecutive bytes of each source), the source's block scale
 // through the read-only path (blocks are >= 256 elements, so the 32 lanes of a
 // warp share one scale), the fp32 state as 128-bit loads; every load of a
-// vector is issued before the first add.  Every CTA works inside one owner's
-// slice, where the scale index is (k0 + i) >> log2(block): a call over whole
-// shards is one launch with blockIdx.y = owner, any other call one launch per
-// owner it meets.
+// vector is issued before the first add.  The scale index of an element is
+// its owner's scale offset plus (slice-local index) >> log2(block).  A call
+// over several whole shards is one launch with blockIdx.y = owner (every CTA
+// inside one owner's slice); a call over several owners whose range cuts a
+// shard is one launch over the whole range (kFlat), each vector finding its
+// owner by comparing its index with a cached owner boundary; a call inside one
+// owner's slice, or whose owner boundaries fall off the 8-element vector grid,
+// is one launch per owner it meets.
 #include <cmath>
 
 #include "zero_tma.cuh"
@@ -59,6 +63,11 @@
 #ifndef ZGB_QACC_U
 #define ZGB_QACC_U 0         // the same for the accumulation
 #endif
+#ifndef ZGB_QGRAD_FLAT
+#define ZGB_QGRAD_FLAT 1     // a call over several owners' slices as one launch over its whole
+                             // range, each vector finding its owner (kFlat): 0 never, 1 for
+                             // ranges that cut shards only, 2 for every multi-owner call
+#endif
 #ifndef ZGB_QWS
 #define ZGB_QWS 0            // opt-in: the code streams staged by bulk copies (qgrad_ws_kernel)
                              // for 1, 2, 4 or 8 sources with 16-byte aligned slices: bit 0 the
@@ -82,7 +91,9 @@ namespace zgb {
 // pointer is offset to its first element) or, with owners > 0, the slices of
 // owners o_first .. o_first + owners - 1 that meet [begin, end), one per
 // blockIdx.y (every pointer offset to `begin`, the scale pointers to the
-// start of the sources' scale arrays).
+// start of the sources' scale arrays), or, with owners < 0 (the kFlat
+// kernels), the whole range [begin, end) as one stream of vectors, pointers
+// as for owners > 0, each vector's owner found from its flat index.
 struct QGradParams {
     const int8_t* q[ZERO_MAX_SRC];     // rank r's codes
     const float* scale[ZERO_MAX_SRC];  // rank r's block scales (of this owner's slice if owners == 0)
@@ -115,10 +126,36 @@ struct QSlice {
 
 __device__ __forceinline__ QSlice qslice(const QGradParams& p) {
     if (p.owners == 0) return QSlice{0, p.k0, p.n, 0};
+    if (p.owners < 0) return QSlice{0, 0, p.n, 0};     // kFlat: the whole range, owners per vector
     const int64_t o = (int64_t)p.o_first + blockIdx.y;
     const int64_t lo = p.begin > o * p.S ? p.begin : o * p.S;
     const int64_t hi = p.end < (o + 1) * p.S ? p.end : (o + 1) * p.S;
     return QSlice{lo - p.begin, lo - o * p.S, hi - lo, o * p.nb};
+}
+
+// kFlat: the owner slice that holds the last vector a thread looked up:
+// flat element i lies in [lo, hi) = [o*S, (o+1)*S), and owner o's scales start
+// at soff = o*nb.  A thread's vectors advance by the grid's stride, far less
+// than a shard, so the 64-bit division that finds an owner runs about once
+// per owner a thread meets.
+struct OwnerCache {
+    int64_t lo = 0, hi = 0, soff = 0;
+};
+
+// The slice of vector (or element) e: the launch's own, or with kFlat the
+// owner's that holds flat element begin + sl.eoff + e, as a QSlice with the
+// same eoff whose k0 + e is that element's slice-local index.
+template <bool kFlat>
+__device__ __forceinline__ QSlice slice_of(const QGradParams& p, const QSlice& sl, int64_t e, OwnerCache& c) {
+    if constexpr (!kFlat) return sl;
+    const int64_t i = p.begin + sl.eoff + e;
+    if (i < c.lo || i >= c.hi) {
+        const int64_t o = i / p.S;
+        c.lo = o * p.S;
+        c.hi = c.lo + p.S;
+        c.soff = o * p.nb;
+    }
+    return QSlice{sl.eoff, p.begin + sl.eoff - c.lo, sl.n, c.soff};
 }
 
 // Code j (0..3) of a 32-bit word as an fp32 value (exact: |code| <= 127).
@@ -179,16 +216,16 @@ __device__ __forceinline__ void store_acc(const QGradParams& p, int64_t e, float
 }
 
 // U vectors (vi0, vi0 + kThreads, ...) with a compile-time source count.
-template <int R, bool kUpdate, int U, bool kQ8>
+template <int R, bool kUpdate, int U, bool kQ8, bool kFlat>
 __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, const QSlice& sl, int64_t vi0,
-                                           int64_t nv, const StepScalars& sc) {
+                                           int64_t nv, const StepScalars& sc, OwnerCache& oc) {
     QVec<R, kUpdate> x[U];
     bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t vi = vi0 + u * kThreads;
         ok[u] = vi < nv;
-        if (ok[u]) load_qvec<R, kUpdate>(p, sl, vi * 8, x[u]);
+        if (ok[u]) load_qvec<R, kUpdate>(p, slice_of<kFlat>(p, sl, vi * 8, oc), vi * 8, x[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -214,7 +251,7 @@ __device__ __forceinline__ void qgrad_vecs(const QGradParams& p, const QSlice& s
 template <bool kUpdate, bool kQ8>
 __device__ __forceinline__ void qgrad_vec_dyn(const QGradParams& p, const QSlice& sl, int64_t vi,
                                               const StepScalars& sc) {
-    const int64_t b = sl.soff + ((sl.k0 + vi * 8) >> p.block_shift);
+    const int64_t b = sl.soff + ((sl.k0 + vi * 8) >> p.block_shift);   // sl: the vector's slice
     const int64_t e = sl.eoff + vi * 8;
     float s[8];
 #pragma unroll
@@ -278,25 +315,30 @@ __host__ __device__ constexpr int qgrad_min_blocks() {
 
 // kQ8 (with kUpdate): the output is 8-bit codes and block scales (p.qout,
 // p.qoscale) instead of bf16; the host guarantees whole 256-element blocks.
-template <int R, bool kUpdate, bool kQ8 = false>
+// kFlat: the launch covers [begin, end) as one stream (p.owners < 0), each
+// vector's owner looked up; the host takes it only when every owner boundary
+// lies on the launch's 8-element vector grid.
+template <int R, bool kUpdate, bool kQ8 = false, bool kFlat = false>
 __global__ void __launch_bounds__(kThreads, (qgrad_min_blocks<R, kUpdate>()))
 qgrad_vec_kernel(const __grid_constant__ QGradParams p) {
     const StepScalars sc = kUpdate ? step_scalars(p.h) : StepScalars{};
     const QSlice sl = qslice(p);
     const int64_t nv = sl.n >> 3;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    OwnerCache oc;
     if constexpr (R > 0) {
         constexpr int U = qgrad_vectors_per_iter<R, kUpdate>();
         const int64_t chunk = (int64_t)U * kThreads;
         for (int64_t v0 = (int64_t)blockIdx.x * chunk + threadIdx.x; v0 < nv; v0 += (int64_t)gridDim.x * chunk)
-            qgrad_vecs<R, kUpdate, U, kQ8>(p, sl, v0, nv, sc);
+            qgrad_vecs<R, kUpdate, U, kQ8, kFlat>(p, sl, v0, nv, sc, oc);
     } else {
         const int64_t stride = (int64_t)gridDim.x * kThreads;
-        for (int64_t vi = tid; vi < nv; vi += stride) qgrad_vec_dyn<kUpdate, kQ8>(p, sl, vi, sc);
+        for (int64_t vi = tid; vi < nv; vi += stride)
+            qgrad_vec_dyn<kUpdate, kQ8>(p, slice_of<kFlat>(p, sl, vi * 8, oc), vi, sc);
     }
     if constexpr (!kQ8) {
         const int64_t tail = sl.n - (nv << 3);
-        if (tid < tail) qgrad_one<kUpdate>(p, sl, (nv << 3) + tid, sc);
+        if (tid < tail) qgrad_one<kUpdate>(p, slice_of<kFlat>(p, sl, (nv << 3) + tid, oc), (nv << 3) + tid, sc);
     }
 }
 
@@ -508,6 +550,14 @@ bool qgrad_ws_enabled() {
 // at most `slice_max` elements, one per blockIdx.y, sharing the grid's CTAs.
 template <int R, bool kUpdate, bool kQ8 = false>
 int launch_qgrad_vec(const QGradParams& p, int64_t slice_max, cudaStream_t s) {
+    if (p.owners < 0) {                       // one stream over the whole range
+        const int occ = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate, kQ8, true>, kThreads, 0);
+        const int64_t per = (int64_t)(R > 0 ? qgrad_vectors_per_iter<R, kUpdate>() : 1) * kThreads;
+        const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
+        const unsigned grid = grid_for(p.n >> 3, per, (int64_t)sm_count() * occ * waves);
+        qgrad_vec_kernel<R, kUpdate, kQ8, true><<<grid, kThreads, 0, s>>>(p);
+        return launch_status();
+    }
     const int occupancy = ctas_per_sm((const void*)qgrad_vec_kernel<R, kUpdate, kQ8>, kThreads, 0);
     const int64_t per_cta = (int64_t)qgrad_vectors_per_iter<R, kUpdate>() * kThreads;
     const int64_t waves = kUpdate ? ZGB_QGRAD_WAVES : ZGB_QACC_WAVES;
@@ -522,7 +572,7 @@ int launch_qgrad_vec(const QGradParams& p, int64_t slice_max, cudaStream_t s) {
 // starts, aligned pointers); the scalar kernel serves single-owner launches.
 template <bool kUpdate, bool kQ8 = false>
 int launch_qgrad(const QGradParams& p, bool vec, bool ws, int64_t slice_max, cudaStream_t s) {
-    if (vec && ws && qgrad_ws_enabled<kUpdate>()) {
+    if (vec && ws && p.owners >= 0 && qgrad_ws_enabled<kUpdate>()) {
         switch (p.n_src) {
             case 1: return launch_qgrad_ws<1, kUpdate, kQ8>(p, slice_max, s);
             case 2: return launch_qgrad_ws<2, kUpdate, kQ8>(p, slice_max, s);
@@ -642,6 +692,31 @@ int qgrad_run(const zero_layout_t* L, const int8_t* const* q_src, const float* c
     // -10 % on 5e8-element buckets over three owners, +4 to +11 % on the
     // per-unit calls over whole shards).
     const bool whole = begin % S == 0 && end % S == 0;
+    // One stream over the whole range when every owner boundary lies on the
+    // range's 8-element vector grid: a bucket that cuts shards is one launch
+    // instead of one per owner (measured on GPT-2-XL shapes: 6466 against 6347
+    // GB/s for the update).  Calls over whole shards keep the blockIdx.y grid
+    // below, which measured faster than one stream for them (accumulation 6279
+    // against 6075 GB/s; splitting the stream into equal blockIdx.y pieces did
+    // not help either).
+    const bool flat_grid = S % 8 == 0 && begin % 8 == 0;
+    if (all_vec && flat_grid && o_end - o_first > 1 && (ZGB_QGRAD_FLAT == 2 || (ZGB_QGRAD_FLAT == 1 && !whole))) {
+        p = base;
+        p.owners = -1;
+        p.o_first = (int32_t)o_first;
+        p.begin = begin;
+        p.end = end;
+        p.S = S;
+        p.nb = nb;
+        p.n = end - begin;
+        p.k0 = 0;
+        for (int r = 0; r < n_src; ++r) {
+            p.q[r] = q_src[r] + begin;
+            p.scale[r] = scale_src[r];
+        }
+        (void)place(p, begin);
+        return launch_qgrad<kUpdate, kQ8>(p, true, false, p.n, s);
+    }
     if (ZGB_QGRAD_MULTI && whole && all_vec && o_end - o_first > 1 && o_end - o_first <= 65535) {
         // one launch, blockIdx.y = owner: every pointer at `begin`, the scales at their start
         p = base;
