@@ -1177,7 +1177,7 @@ def headline_line(p, args, world, seven_b=None):
         "step_ms_median": p["step_ms_median"], "step_ms_min": p["step_ms_min"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "storage": "bf16 grads/weights, fp32 master/m/v",
-        "data": "synthetic (seeded normal gradients and weights, model shapes only)",
+        "data": "synthetic (seeded normal draws, model shapes)",
         "config": cfg,
         "hbm_gbs_step": p["hbm_gbs_step"],
         "bytes_per_param_step": p["bytes_per_param_step"],
@@ -1244,7 +1244,7 @@ def run_ours(args):
             "step_ms_median": step_list[len(step_list) // 2], "step_ms_min": step_list[0],
             "hbm_gbs_step": bytes_step / (ms_step / 1e3) / 1e9,
             "bytes_per_param_step": wl.bytes_per_elem,
-            "config": dict(wl.desc, l2="inputs %.1f GB > 129 MB L2, no flush" % (wl.device_bytes / 1e9)),
+            "config": dict(wl.desc, l2="%.1f GB > L2, no flush" % (wl.device_bytes / 1e9)),
             "roofline": {"bound": getattr(wl, "bound", "hbm"), "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": (tpe * dom_bytes / wl.bytes_per_elem) if tpe is not None else None,
