@@ -26,6 +26,8 @@ headline (key "workload_result"):
   zero3-prefetch      each unit's gather issued one unit ahead on a side stream;
   zero3-int8[-fused]  8-bit weight gathers (ZeRO++);
   zero3-zeropp[-fused] both ZeRO++ 8-bit paths;
+  cast                the bf16 cast of GPT-2-XL-sized master weights on its own
+                      (zero_cast_bf16, the engines' set-up and restore step);
   checkpoint          a save / restore of one Llama-7B block unit's shards.
 Only with --with-compute: zero3-compute and zero3-prefetch-compute, the
 unfused step with a stand-in layer matmul (cuBLAS) per unit, gathers in line
@@ -77,7 +79,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["gpt2xl", "gpt2xl-clip", "gpt2xl-qgrad", "llama7b-shard",
-                                           "probe", "accum-zero1", "accum-zero2", "zero3",
+                                           "probe", "accum-zero1", "accum-zero2", "cast", "zero3",
                                            "zero3-int8", "zero3-prefetch", "zero3-zeropp",
                                            "zero3-fused", "zero3-int8-fused", "zero3-zeropp-fused",
                                            "zero3-fused-graph", "zero3-compute", "zero3-prefetch-compute"],
@@ -505,6 +507,37 @@ class AccumWorkload(Workload):
         return out
 
 
+class CastWorkload(Workload):
+    """The cast of freshly initialised master weights to bf16 on its own
+    (zero_cast_bf16), GPT-2-XL shapes: 4 bytes read and 2 written per element.
+    The engines run it once at set-up and after a restore; it is timed here so
+    that it, too, stands against the copy peak."""
+
+    n_src = 0
+    kernel_label = "zgb::cast_bf16_vec_kernel"
+
+    def __init__(self, name, device, elems=0):
+        import torch
+        from zero_sharded_mixed_gb300 import inputs
+        super().__init__(device)
+        numels = [elems] if elems else inputs.gpt2xl_numels()
+        n = sum(numels)
+        self.name = name
+        self.master = _master(n, n, device)
+        self.out = torch.empty(n, dtype=torch.bfloat16, device=device)
+        self.elems = n
+        self.bytes_per_elem = 6
+        self.dominant = "cast_bf16"
+        self.desc = {"workload": ("flat%d" % elems if elems else "gpt2xl") + "_cast_master_bf16",
+                     "model": "flat vector" if elems else "GPT-2-XL shapes", "N": n}
+        self.device_bytes = n * 6
+
+    def ops(self, t):
+        def fn():
+            self.zb.zero_cast_bf16(self.master, self.out)
+        return [Op("cast_bf16", self.elems * 6, fn)]
+
+
 class Zero3Workload(Workload):
     """ZeRO-3 per-unit path, Llama-7B units at n_dp = 8 (embedding, 32 blocks,
     head).  Per unit and step: gather the bf16 shards into a ring buffer for
@@ -768,6 +801,8 @@ def make_workload(name, device, elems=0, bucket=500_000_000):
         return Zero2Workload(name, device)
     if name in ("accum-zero1", "accum-zero2"):
         return AccumWorkload(name, device, elems)
+    if name == "cast":
+        return CastWorkload(name, device, elems)
     if name in ("zero3", "zero3-int8", "zero3-prefetch", "zero3-zeropp", "zero3-fused",
                 "zero3-int8-fused", "zero3-zeropp-fused", "zero3-fused-graph", "zero3-compute",
                 "zero3-prefetch-compute"):
@@ -960,6 +995,12 @@ def oracle_workload_step(name, n):
     import numpy as np
     import oracle
     from zero_sharded_mixed_gb300 import inputs
+    if name == "cast":
+        w = inputs.master_weights(n, n, seed=SEED).numpy()
+
+        def cast_step(t):
+            oracle.cast_bf16(w)
+        return cast_step, n, "%d owned elements, the bf16 cast of master weights" % n
     hp = oracle.AdamW(**HP)
     n_dp = 4 if name.startswith("accum") else 8
     n -= n % (n_dp * 256)
@@ -1114,7 +1155,7 @@ def _kernels_summary(per_kind, steps):
 
 EXTRA_WORKLOADS = ("gpt2xl", "llama7b-shard", "gpt2xl-clip", "gpt2xl-qgrad", "accum-zero1", "accum-zero2",
                    "zero3", "zero3-fused", "zero3-fused-graph", "zero3-prefetch", "zero3-int8",
-                   "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused")
+                   "zero3-int8-fused", "zero3-zeropp", "zero3-zeropp-fused", "cast")
 COMPUTE_WORKLOADS = ("zero3-compute", "zero3-prefetch-compute")
 
 

@@ -168,3 +168,12 @@ def test_default_run_has_no_stand_in_matmuls():
     assert set(bench.COMPUTE_WORKLOADS) <= set(bench.workload_order(bench.parse_args(["--with-compute"])))
     assert bench.workload_order(bench.parse_args(["--no-extra"])) == ["gpt2xl"]
     assert bench.workload_order(bench.parse_args(["--workload", "probe"])) == ["probe"]
+
+
+def test_cast_workload_oracle_step_and_order():
+    """The cast workload is a default extra workload, and the oracle's
+    statement of it casts the sample's master weights."""
+    assert "cast" in bench.workload_order(bench.parse_args([]))
+    step, n, what = bench.oracle_workload_step("cast", 4096)
+    assert n == 4096 and "owned elements" in what and "cast" in what
+    step(1)
