@@ -909,7 +909,9 @@ def time_e2e(wl, steps, warmup, t0, dist):
     torch.cuda.synchronize()
     barrier(dist)
     ms = marks[0].elapsed_time(marks[-1]) / steps
-    per_step = sorted(marks[k].elapsed_time(marks[k + 1]) for k in range(steps))
+    steps_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
+    print("e2e steps (ms): " + " ".join("%.1f" % x for x in steps_ms), file=sys.stderr, flush=True)
+    per_step = sorted(steps_ms)
     # the host link on this machine: plain copies of the step's gradients, pinned host to device;
     # the fastest of three (the link's rate varies from moment to moment on a shared host)
     link_gbs = 0.0
@@ -1203,7 +1205,7 @@ def target_7b(res):
 def headline_line(p, args, world, seven_b=None):
     """The headline JSON line: the contract's keys for the primary workload,
     compact (the other workloads have lines of their own)."""
-    cfg = dict(p["config"], parallelism="replicas x%d (simulated n_dp=%d per GPU)"
+    cfg = dict(p["config"], parallelism="replicas x%d, n_dp=%d simulated per GPU"
                % (world, p["config"].get("n_dp", 8)))
     e2e = p.get("e2e")
     if e2e is not None:
@@ -1217,7 +1219,7 @@ def headline_line(p, args, world, seven_b=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": p["ms_per_step"],
         "step_ms_median": p["step_ms_median"], "step_ms_min": p["step_ms_min"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "storage": "bf16 grads/weights, fp32 master/m/v",
+        "dtype": "f32",
         "data": "synthetic (seeded normal draws, model shapes)",
         "config": cfg,
         "hbm_gbs_step": p["hbm_gbs_step"],
@@ -1231,7 +1233,7 @@ def headline_line(p, args, world, seven_b=None):
         "impl": "ours",
     }
     # never let an optional field push the line past the limit
-    for k in ("bytes_per_param_step", "step_ms_median", "storage"):
+    for k in ("bytes_per_param_step", "step_ms_median"):
         if len(json.dumps(line)) <= HEADLINE_MAX_CHARS:
             break
         line.pop(k, None)
