@@ -855,9 +855,11 @@ def time_workload(wl, steps, warmup, dist, device, sampler=None):
     return start.elapsed_time(end), per_kind, clocks, t + steps
 
 
-def e2e_host_bytes(wl):
-    """Pinned host bytes the e2e leg holds: every rank's gradients and the result."""
-    return wl.grads.numel() * wl.grads.element_size() + wl.out.numel() * wl.out.element_size()
+def e2e_host_bytes(wl, shared_rows=False):
+    """Pinned host bytes the e2e leg holds: every rank's gradients (or one row
+    that every simulated rank's copy reads) and the result."""
+    rows = 1 if shared_rows else wl.grads.shape[0]
+    return rows * wl.grads.shape[1] * wl.grads.element_size() + wl.out.numel() * wl.out.element_size()
 
 
 def host_fits(nbytes) -> bool:
@@ -882,16 +884,23 @@ def all_ranks_agree(dist, flag: bool, device) -> bool:
     return bool(t.item())
 
 
-def time_e2e(wl, steps, warmup, t0, dist):
+def time_e2e(wl, steps, warmup, t0, dist, shared_rows=False):
     """The same step through the public API with host buffers: every step copies
     the n_dp gradient buffers from pinned host memory to the device and reads the
     updated bf16 weights back into pinned host memory (step.HostPipeline, which
     overlaps bucket b's copies with bucket b-1's update, and the result copies
-    with the gradient copies)."""
+    with the gradient copies).  shared_rows: when the host cannot pin every
+    rank's gradients (several GPUs per host), each simulated rank's copy reads
+    one shared pinned row (rank 0's gradient) -- the same bytes move each step."""
     import torch
     from zero_sharded_mixed_gb300.step import HostPipeline
-    host_g = torch.empty(wl.grads.shape, dtype=wl.grads.dtype, pin_memory=True)
-    host_g.copy_(wl.grads)
+    if shared_rows:
+        row = torch.empty(wl.grads.shape[1], dtype=wl.grads.dtype, pin_memory=True)
+        row.copy_(wl.grads[0])
+        host_g = row.expand(wl.grads.shape)         # every rank's row is the same host memory
+    else:
+        host_g = torch.empty(wl.grads.shape, dtype=wl.grads.dtype, pin_memory=True)
+        host_g.copy_(wl.grads)
     host_out = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
     pipe = HostPipeline(wl.L, device=wl.device)
     t = t0
@@ -919,7 +928,8 @@ def time_e2e(wl, steps, warmup, t0, dist):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        wl.grads.copy_(host_g, non_blocking=True)
+        for r in range(host_g.shape[0]):
+            wl.grads[r].copy_(host_g[r], non_blocking=True)
         b.record()
         torch.cuda.synchronize()
         link_gbs = max(link_gbs, host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
@@ -1210,7 +1220,8 @@ def headline_line(p, args, world, seven_b=None):
     e2e = p.get("e2e")
     if e2e is not None:
         e2e = {k: e2e[k] for k in ("value", "unit", "ms_per_step", "steps", "step_ms_min", "step_ms_median",
-                                   "h2d_bytes_per_step", "d2h_bytes_per_step", "unavailable") if k in e2e}
+                                   "h2d_bytes_per_step", "d2h_bytes_per_step", "host_rows", "unavailable")
+               if k in e2e}
         if "link" in p["e2e"]:
             e2e["link_h2d_gbs"] = p["e2e"]["link"]["h2d_gbs"]
             e2e["link_frac"] = p["e2e"]["link"]["frac"]
@@ -1299,24 +1310,27 @@ def run_ours(args):
         if is_primary:
             res["clocks"] = clocks
             if not args.no_e2e and isinstance(wl, Zero2Workload):
+                local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
                 need = e2e_host_bytes(wl)
-                fits = host_fits(need * int(os.environ.get("LOCAL_WORLD_SIZE", "1")))
-                if all_ranks_agree(dist, fits, device):
+                shared = not all_ranks_agree(dist, host_fits(need * local), device)
+                fits = not shared or all_ranks_agree(dist, host_fits(e2e_host_bytes(wl, True) * local), device)
+                if fits:
                     e2e_steps = max(1, min(args.steps, 10))
-                    e_ms, h2d, d2h, link_gbs, per_step = time_e2e(wl, e2e_steps, 1, t_next + 1, dist)
+                    e_ms, h2d, d2h, link_gbs, per_step = time_e2e(wl, e2e_steps, 1, t_next + 1, dist, shared)
                     e_ms = max_over_ranks(dist, e_ms, device)
                     link_ms = h2d / (link_gbs * 1e9) * 1e3
                     res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
                                   "ms_per_step": e_ms, "steps": e2e_steps,
                                   "step_ms_min": per_step[0], "step_ms_median": per_step[len(per_step) // 2],
+                                  "host_rows": "shared" if shared else "per rank",
                                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                   "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
                                            "frac": link_ms / e_ms}}
                 else:
                     res["e2e"] = {"value": None, "unit": UNIT,
-                                  "unavailable": "host memory: %s local ranks x %.1f GB of pinned "
+                                  "unavailable": "host memory: %d local ranks x %.1f GB of pinned "
                                   "step inputs and results exceed 85%% of the available host memory"
-                                  % (os.environ.get("LOCAL_WORLD_SIZE", "1"), need / 1e9)}
+                                  % (local, e2e_host_bytes(wl, True) / 1e9)}
             if not args.no_cpu_baseline and world == 1 and rank == 0 and isinstance(wl, Zero2Workload):
                 sample = cpu_sample(wl, CPU_SAMPLE)
                 cores = host_cores()

@@ -177,3 +177,14 @@ def test_cast_workload_oracle_step_and_order():
     step, n, what = bench.oracle_workload_step("cast", 4096)
     assert n == 4096 and "owned elements" in what and "cast" in what
     step(1)
+
+
+def test_e2e_host_bytes_with_a_shared_row():
+    """The e2e fallback pins one gradient row instead of one per rank."""
+    import torch
+
+    class W:
+        grads = torch.empty((8, 1000), dtype=torch.bfloat16)
+        out = torch.empty(1000, dtype=torch.bfloat16)
+    assert bench.e2e_host_bytes(W) == 8 * 1000 * 2 + 1000 * 2
+    assert bench.e2e_host_bytes(W, shared_rows=True) == 1000 * 2 + 1000 * 2

@@ -103,3 +103,32 @@ def test_copy_pipeline_matches_the_oracle(zlib, cuda_device, N, n_dp, bucket, ch
         parity.assert_state(st, ref, what=f"t={t} ")
         assert np.array_equal(parity.bits(host_out), out_ref)
         assert torch.equal(dev_g.cpu().view(torch.int16), g.view(torch.int16))
+
+
+def test_copy_pipeline_from_one_shared_host_row(zlib, cuda_device):
+    """The e2e pipeline fed by one pinned host row that every simulated rank's
+    copy reads (a stride-0 view; the benchmark's fallback when the host cannot
+    pin every rank's gradients): every device row receives that row, and the
+    step equals the oracle's with all ranks holding it."""
+    zb = zlib
+    N, n_dp, bucket = 200_003, 8, 60_000
+    L = zb.zero_layout([N], n_dp, bucket_elems=bucket)
+    P = L.padded_n
+    w0 = inputs.master_weights(N, P, seed=11)
+    st = [w0.cuda(), torch.zeros(P, device="cuda"), torch.zeros(P, device="cuda")]
+    out = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    dev_g = torch.empty((n_dp, P), dtype=torch.bfloat16, device="cuda")
+    host_out = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    g = inputs.grads_bf16(1, N, P, seed=12, step=1)
+    row = torch.empty(P, dtype=torch.bfloat16, pin_memory=True)
+    row.copy_(g[0])
+    shared = row.expand(n_dp, P)
+    assert shared.is_pinned() and shared.stride(0) == 0
+    zstep.HostPipeline(L).step(shared, dev_g, *st, out, host_out, _hp(zb, 1))
+    torch.cuda.synchronize()
+    rows = np.repeat(parity.bits(g), n_dp, axis=0)
+    assert np.array_equal(dev_g.cpu().view(torch.int16).numpy().view(np.uint16), rows)
+    out_ref, *ref = oracle.rs_adamw_reference(rows, n_dp, parity.f32(w0), np.zeros(P, np.float32),
+                                              np.zeros(P, np.float32), HP, 1)
+    parity.assert_state(st, ref)
+    assert np.array_equal(parity.bits(host_out), out_ref)
