@@ -91,3 +91,13 @@ def test_widen_is_exact():
 ])
 def test_worked_values(value, expected):
     assert int(oracle.cast_bf16(np.array([value], np.float32))[0]) == expected
+
+
+def test_quiet_nan_payload_survives_a_widening_round_trip():
+    """IEEE 754-2019, 6.2.3: a quiet NaN converted to a wider format and back
+    keeps its payload.  Every quiet bf16 NaN pattern of both signs, widened
+    exactly to fp32 (its bits in the upper half), must come back unchanged."""
+    quiet = np.array([h for h in range(1 << 16) if (h & 0x7FC0) == 0x7FC0], dtype=np.uint32)
+    assert quiet.size == 2 * 64
+    widened = (quiet << 16).astype(np.uint32).view(np.float32)
+    np.testing.assert_array_equal(oracle.cast_bf16(widened), quiet.astype(np.uint16))

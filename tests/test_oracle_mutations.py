@@ -43,6 +43,8 @@ MUTATIONS = [
      "s = s + src[(int64_t)(n_src - 1 - r) * ld + i];\n        g[i] = s / divisor;"),
     ("bf16 ties rounded away from zero", "if (kept & 1u) kept += 1u;", "kept += 1u;"),
     ("bf16 cast truncates", "if (dropped > 0x8000u) {", "if (dropped > 0xffffu) {"),
+    ("bf16 cast makes every NaN the canonical one", "return (uint16_t)((u >> 16) | 0x0040u);",
+     "return (uint16_t)((u >> 16 & 0x8000u) | 0x7fc0u);"),
     ("shard length not rounded up to the alignment", "if (shard * align < per_rank) shard += 1;", ";"),
     ("shard length floors N / n_dp", "if (per_rank * n_dp < total) per_rank += 1;", ";"),
     ("accumulation ignores the first flag", "acc[i] = first ? x : acc[i] + x;", "acc[i] = acc[i] + x;"),
@@ -88,6 +90,7 @@ def _pins():
         ("gather", ps.test_all_gather_is_concatenation),
         ("cast specials", pc.test_special_values),
         ("cast low halves", pc.test_every_low_half_for_some_upper_halves),
+        ("cast NaN round trip", pc.test_quiet_nan_payload_survives_a_widening_round_trip),
         ("layout brute force", lambda: pl.test_brute_force_small(8)),
         ("workload layouts", pl.test_workload_layouts),
         ("clip vs torch", lambda: pk.test_clip_matches_torch(1.0, 1.0)),
