@@ -101,3 +101,16 @@ def test_quiet_nan_payload_survives_a_widening_round_trip():
     assert quiet.size == 2 * 64
     widened = (quiet << 16).astype(np.uint32).view(np.float32)
     np.testing.assert_array_equal(oracle.cast_bf16(widened), quiet.astype(np.uint16))
+
+
+def test_signalling_nans_come_out_quiet():
+    """IEEE 754-2019, 6.2: an operation on a signalling NaN delivers a quiet
+    NaN.  Signalling fp32 NaNs of both signs (quiet bit clear, payload anywhere
+    in the 22 bits below it) cast to quiet bf16 NaNs with the same sign."""
+    rng = np.random.default_rng(3)
+    payload = rng.integers(1, 1 << 22, size=20_000, dtype=np.uint32)
+    sign = rng.integers(0, 2, size=payload.size, dtype=np.uint32) << 31
+    snan = (sign | 0x7F800000 | payload).astype(np.uint32)
+    out = oracle.cast_bf16(snan.view(np.float32))
+    assert np.all((out & 0x7FC0) == 0x7FC0)                     # a quiet NaN
+    np.testing.assert_array_equal(out >> 15, (snan >> 31).astype(np.uint16))
