@@ -131,3 +131,58 @@ def test_int8_gradient_update(zlib, big):
         parity.assert_state([w[a:b], m[a:b], v[a:b]], st, what=what)
         assert np.array_equal(parity.bits(out[a:b]), out_ref), what + "bf16 output"
     zb.zero_status_check()
+
+
+def test_int8_gradient_update_over_a_range_cutting_a_shard(zlib, big):
+    """The 8-bit update over [lo, P) with lo inside owner 0's slice: one stream
+    over a range longer than 2^32 that crosses the owner boundary at S > 2^31,
+    each vector finding its owner.  Elements before lo stay untouched."""
+    zb = zlib
+    L, g = big["L"], big["g"]
+    S, P = L.shard, L.padded_n
+    nb = -(-S // BLOCK)
+    q = torch.empty((N_DP, P), dtype=torch.int8, device="cuda")
+    sc = torch.empty((N_DP, N_DP * nb), dtype=torch.float32, device="cuda")
+    for r in range(N_DP):
+        zb.zero_quantize_int8(L, g[r], q[r], sc[r], BLOCK)
+    lo = (2 ** 30 // BLOCK) * BLOCK + 8 * 37           # on the vector grid, off the block grid
+    w, m, v = _fresh_state(P)
+    slices = [(a, b) for a, b in big["slices"] if a >= lo] + [(lo, lo + 4096)]
+    w0 = {ab: parity.f32(w[ab[0]:ab[1]]) for ab in slices + [(lo - 64, lo)]}
+    out = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    hp = zb.ZeroAdamW.make(HP.lr, HP.beta1, HP.beta2, HP.eps, HP.weight_decay, 1)
+    zb.zero_reduce_scatter_adamw_int8(L, [q[r] for r in range(N_DP)], [sc[r] for r in range(N_DP)],
+                                      BLOCK, float(N_DP), 0, N_DP, lo, P, w, m, v, out,
+                                      zb.ZERO_OUT_FULL, hp)
+    torch.cuda.synchronize()
+    for a, b in slices:
+        o = a // S
+        k0 = (a - o * S) // BLOCK
+        k1 = -(-(b - o * S) // BLOCK)
+        off = (a - o * S) - k0 * BLOCK                   # the slice's offset inside its first block
+        qs = q[:, a - off:b].cpu().numpy()
+        ss = sc[:, o * nb + k0:o * nb + k1].cpu().numpy()
+        n = b - a
+        out_ref, *st = oracle.qgrad_rs_adamw_reference(qs, ss, 1, BLOCK, N_DP, np.concatenate(
+            [np.zeros(off, np.float32), w0[(a, b)]]), np.zeros(n + off, np.float32),
+            np.zeros(n + off, np.float32), HP, 1)
+        what = f"[{a}, {b}) "
+        parity.assert_state([w[a:b], m[a:b], v[a:b]], [x[off:] for x in st], what=what)
+        assert np.array_equal(parity.bits(out[a:b]), out_ref[off:]), what + "bf16 output"
+    parity.assert_bit_exact_f32(w[lo - 64:lo], w0[(lo - 64, lo)], what="before the range")
+    assert not m[lo - 64:lo].any() and not out[lo - 64:lo].view(torch.int16).any()
+    zb.zero_status_check()
+
+
+def test_cast_of_the_whole_vector(zlib, big):
+    """The library's bf16 cast over P > 2^32 elements, sampled slices bit for
+    bit against the oracle's cast."""
+    zb = zlib
+    P = big["L"].padded_n
+    w, _, _ = _fresh_state(P)
+    out = torch.empty(P, dtype=torch.bfloat16, device="cuda")
+    zb.zero_cast_bf16(w, out)
+    torch.cuda.synchronize()
+    for a, b in big["slices"]:
+        assert np.array_equal(parity.bits(out[a:b]), oracle.cast_bf16(parity.f32(w[a:b]))), f"[{a}, {b})"
+    zb.zero_status_check()
