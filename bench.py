@@ -382,11 +382,10 @@ class Zero2Workload(Workload):
         if self.qgrad:
             P = self.L.padded_n
             sb = n_dp * 4 / QGRAD_BLOCK
-            for r in range(n_dp):
-                def quant(r=r):
-                    zb.zero_quantize_int8(self.L, self.grad_list[r], self.qg.q[r], self.qg.scales[r],
-                                          QGRAD_BLOCK)
-                out.append(Op("quantize_grad", int(P * (3 + 4 / QGRAD_BLOCK)), quant))
+
+            def quant():
+                self.qg.quantize(self.grad_list)          # every simulated rank at once
+            out.append(Op("quantize_grad", int(n_dp * P * (3 + 4 / QGRAD_BLOCK)), quant, kernels=n_dp))
             qs, ss = self.qg.sources()
             for s, e in self.ranges:
                 def fn(s=s, e=e):
@@ -607,6 +606,7 @@ class Zero3Workload(Workload):
             self.kernel_label = "zgb::dequant_gather_vec_kernel, rs_adamw_vec_kernel<0,8,q8>"
         if self.zeropp:
             self.qg = zstep.Int8Grads(zb.zero_layout([cap], n_dp, align=align), n_dp, QGRAD_BLOCK, device)
+            self.side = zstep.side_streams(n_dp, device)
             sb = n_dp * 4 / QGRAD_BLOCK
             # + every rank quantizes its unit gradient; the RS reads 1 B per source (+ scales)
             self.bytes_per_elem = 3 + 3 + (n_dp * 3 + sb) + (n_dp + sb + 4) + 30 + 3
@@ -736,9 +736,9 @@ class Zero3Workload(Workload):
                 self.ring.release(("bwd", i))
 
             def quant_grads(u=u, P=P, grads=grads):
-                for r in range(u.layout.n_dp):
-                    zb.zero_quantize_int8(u.layout, grads[r], self.qg.q[r, :P],
-                                          self.qg.scales[r], QGRAD_BLOCK)
+                # every simulated rank at once, on side streams joined back (step.quantize_ranks)
+                zs.quantize_ranks(u.layout, grads, [self.qg.q[r, :P] for r in range(u.layout.n_dp)],
+                                  [self.qg.scales[r] for r in range(u.layout.n_dp)], QGRAD_BLOCK, self.side)
 
             def rs_int8(u=u, i=i, P=P):
                 zb.zero_accumulate_int8(u.layout, [self.qg.q[r, :P] for r in range(u.layout.n_dp)],
@@ -902,11 +902,33 @@ def time_e2e(wl, steps, warmup, t0, dist, shared_rows=False):
         host_g = torch.empty(wl.grads.shape, dtype=wl.grads.dtype, pin_memory=True)
         host_g.copy_(wl.grads)
     host_out = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
-    pipe = HostPipeline(wl.L, device=wl.device)
+    # the pipeline's two modes: result copies overlapped with the gradient copies,
+    # or deferred until every gradient copy has landed.  `warmup` timed steps of
+    # each; the timed steps run the one whose warm-up steps took less (the max
+    # over ranks, so that every rank picks the same).  On most boxes overlapping
+    # is faster (125 against 134 ms); on some, steps of the overlapped pipeline
+    # alternated between 128 and 370 ms.
+    pipes = {"overlap": HostPipeline(wl.L, device=wl.device),
+             "deferred": HostPipeline(wl.L, device=wl.device, defer_out=True)}
     t = t0
-    for _ in range(warmup):
-        pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
-        t += 1
+    warm = {}
+    for name, pipe in pipes.items():
+        warm[name] = []
+        for _ in range(max(1, warmup)):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            pipe.step(host_g, wl.grads, wl.master, wl.m, wl.v, wl.out, host_out, wl.hp(t))
+            b.record()
+            torch.cuda.synchronize()
+            warm[name].append(a.elapsed_time(b))
+            t += 1
+    cost = {name: max_over_ranks(dist, sum(v), wl.device) for name, v in warm.items()}
+    mode = min(cost, key=cost.get)
+    pipe = pipes[mode]
+    print("e2e warm-up (ms): " + "; ".join("%s %s" % (k, " ".join("%.1f" % x for x in v))
+                                          for k, v in warm.items()) + "; timed: " + mode,
+          file=sys.stderr, flush=True)
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     torch.cuda.synchronize()
     barrier(dist)
@@ -933,7 +955,7 @@ def time_e2e(wl, steps, warmup, t0, dist, shared_rows=False):
         b.record()
         torch.cuda.synchronize()
         link_gbs = max(link_gbs, host_g.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9)
-    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs, per_step
+    return ms, host_g.numel() * 2, host_out.numel() * 2, link_gbs, per_step, mode
 
 
 def cpu_sample(wl, n):
@@ -1190,7 +1212,19 @@ def workload_line(name, res):
               "roofline", "kernels", "gpu_launches", "cpu_baseline", "overlap"):
         if k in res:
             line[k] = res[k]
-    return line
+    return _rounded(line)
+
+
+def _rounded(x, digits=6):
+    """Floats to `digits` significant digits, recursively (the printed lines
+    stay short; no figure here is known to more digits than that)."""
+    if isinstance(x, float):
+        return float("%.*g" % (digits, x))
+    if isinstance(x, dict):
+        return {k: _rounded(v, digits) for k, v in x.items()}
+    if isinstance(x, list):
+        return [_rounded(v, digits) for v in x]
+    return x
 
 
 def _compact_roofline(r):
@@ -1220,7 +1254,7 @@ def headline_line(p, args, world, seven_b=None):
     e2e = p.get("e2e")
     if e2e is not None:
         e2e = {k: e2e[k] for k in ("value", "unit", "ms_per_step", "steps", "step_ms_min", "step_ms_median",
-                                   "h2d_bytes_per_step", "d2h_bytes_per_step", "host_rows", "unavailable")
+                                   "h2d_bytes_per_step", "d2h_bytes_per_step", "host_rows", "mode", "unavailable")
                if k in e2e}
         if "link" in p["e2e"]:
             e2e["link_h2d_gbs"] = p["e2e"]["link"]["h2d_gbs"]
@@ -1243,6 +1277,7 @@ def headline_line(p, args, world, seven_b=None):
         "target_7b": seven_b,
         "impl": "ours",
     }
+    line = _rounded(line)
     # never let an optional field push the line past the limit
     for k in ("bytes_per_param_step", "step_ms_median"):
         if len(json.dumps(line)) <= HEADLINE_MAX_CHARS:
@@ -1316,13 +1351,14 @@ def run_ours(args):
                 fits = not shared or all_ranks_agree(dist, host_fits(e2e_host_bytes(wl, True) * local), device)
                 if fits:
                     e2e_steps = max(1, min(args.steps, 10))
-                    e_ms, h2d, d2h, link_gbs, per_step = time_e2e(wl, e2e_steps, 1, t_next + 1, dist, shared)
+                    e_ms, h2d, d2h, link_gbs, per_step, mode = time_e2e(wl, e2e_steps, 2, t_next + 1, dist,
+                                                                        shared)
                     e_ms = max_over_ranks(dist, e_ms, device)
                     link_ms = h2d / (link_gbs * 1e9) * 1e3
                     res["e2e"] = {"value": replica_value(wl.elems, world, e_ms), "unit": UNIT,
                                   "ms_per_step": e_ms, "steps": e2e_steps,
                                   "step_ms_min": per_step[0], "step_ms_median": per_step[len(per_step) // 2],
-                                  "host_rows": "shared" if shared else "per rank",
+                                  "host_rows": "shared" if shared else "per rank", "mode": mode,
                                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                   "link": {"h2d_gbs": link_gbs, "h2d_ms_per_step": link_ms,
                                            "frac": link_ms / e_ms}}

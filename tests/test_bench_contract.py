@@ -188,3 +188,8 @@ def test_e2e_host_bytes_with_a_shared_row():
         out = torch.empty(1000, dtype=torch.bfloat16)
     assert bench.e2e_host_bytes(W) == 8 * 1000 * 2 + 1000 * 2
     assert bench.e2e_host_bytes(W, shared_rows=True) == 1000 * 2 + 1000 * 2
+
+
+def test_printed_floats_keep_six_significant_digits():
+    r = bench._rounded({"a": 168211715564.56232, "b": [1.0595268135262763, 3], "c": {"d": 0.000123456789}})
+    assert r == {"a": 168212000000.0, "b": [1.05953, 3], "c": {"d": 0.000123457}}
