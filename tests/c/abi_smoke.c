@@ -2,9 +2,10 @@
  *
  *   abi_smoke          host-only calls (layout, ranges, formulas, strerror,
  *                      argument checks that return before any CUDA call)
- *   abi_smoke --gpu    also one fused ZeRO step on the GPU (cudaMalloc'd
- *                      buffers, the default stream), checked against the
- *                      oracle linked into this test program.
+ *   abi_smoke --gpu    also the cast of the master weights and two fused
+ *                      ZeRO steps on the GPU (cudaMalloc'd buffers, the
+ *                      default stream), checked against the oracle linked
+ *                      into this test program.
  *
  * Test infrastructure: it links both the library and the oracle; neither of
  * them links the other.  Exit status 0 = pass. */
@@ -65,6 +66,8 @@ static int host_part(void) {
     CHECK(zero_layout(numel, 3, 4, 8, 1000, offs, &L) == ZERO_OK, "layout");
     CHECK(zero_reduce_scatter_adamw(&L, src, 1, ZERO_BF16, 0, 4.0f, 0, 4, 0, 64, f, f, f, o,
                                     ZERO_OUT_FULL, &hp, NULL) == ZERO_EINVAL, "step 0 accepted");
+    CHECK(zero_cast_bf16(NULL, NULL, 16, NULL) == ZERO_EINVAL, "null cast buffers accepted");
+    CHECK(zero_cast_bf16(NULL, NULL, -1, NULL) == ZERO_EINVAL, "negative cast length accepted");
     return 0;
 }
 
@@ -90,6 +93,13 @@ static int gpu_part(void) {
     const void* src[4];
     for (int r = 0; r < n_dp; ++r) src[r] = (const char*)dg + (size_t)(r * P * 2);
     memcpy(w2, w, (size_t)P * 4);
+    /* the first bf16 weights: the library's cast of the master weights, every
+       element equal to the oracle's round-to-nearest-even conversion */
+    CHECK(zero_cast_bf16((const float*)dw, (uint16_t*)dout, P, NULL) == ZERO_OK, "zero_cast_bf16");
+    CHECK(cudaDeviceSynchronize() == 0, "sync");
+    cudaMemcpy(out, dout, (size_t)P * 2, 2);
+    for (int64_t i = 0; i < P; ++i)
+        CHECK(out[i] == oracle_f32_to_bf16(w[i]), "cast differs from the oracle at %lld", (long long)i);
     for (int64_t t = 1; t <= 2; ++t) {
         zero_adamw_t hp = {1e-4f, 0.9f, 0.999f, 1e-8f, 0.1f, 0, t};
         for (int64_t b = 0; b < L.n_buckets; ++b) {
