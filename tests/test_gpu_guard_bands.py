@@ -228,3 +228,15 @@ def test_int8_gradient_update_with_8bit_output(zlib, cuda_device):
                                          zb.ZeroAdamW.make(step=1))
     _check({"w": w, "m": m, "v": v, "q": q, "scales": sc},
            {**{f"qg[{r}]": x for r, x in enumerate(qg_in)}, **{f"sg[{r}]": x for r, x in enumerate(sg_in)}})
+
+
+@pytest.mark.parametrize("shift", [0, 1])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 100_003])
+def test_cast(zlib, cuda_device, n, shift):
+    """The bf16 cast of master weights: the output's guard bands and the fp32
+    source stay untouched, on the vector kernel and off the 16-byte grid."""
+    w = Guarded(n, torch.float32, shift, inputs.master_weights(n, n, seed=5).cuda())
+    out = Guarded(n, torch.bfloat16, shift)
+    zlib.zero_cast_bf16(w.t, out.t)
+    _check({"out": out}, {"master": w})
+    assert torch.equal(out.t.view(torch.int16), w.t.to(torch.bfloat16).view(torch.int16))
