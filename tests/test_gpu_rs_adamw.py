@@ -57,6 +57,33 @@ def test_tiny_zero1_three_steps(zlib, cuda_device):
         assert np.array_equal(parity.bits(out), ref_out)
 
 
+@pytest.mark.parametrize("N,n_dp,bucket", [(100_003, 3, 30_000), (65_541, 8, 500_000_000)])
+def test_sharded_step_equals_data_parallel(zlib, cuda_device, N, n_dp, bucket):
+    """"ZeRO and FSDP", "The idea, one stage at a time": ZeRO-1/2 computes the
+    same step as plain data parallelism.  The library's sharded step (each
+    owner updates its shard, the bf16 result gathered into the full buffer)
+    against the oracle's data-parallel step (an all-reduce mean, then AdamW on
+    the full vector by every rank): the concatenated fp32 state equals every
+    rank's full copy, and the gathered bf16 weights every rank's, bit for bit,
+    over three steps."""
+    zb = zlib
+    L, state, out = _setup(zb, N, n_dp, bucket=bucket, seed=7)
+    P = L.padded_n
+    w0 = parity.f32(state[0])
+    full_w = np.tile(w0, (n_dp, 1))
+    full_m = np.zeros((n_dp, P), np.float32)
+    full_v = np.zeros((n_dp, P), np.float32)
+    for t in (1, 2, 3):
+        g = _grads_cpu(L, 7, t)
+        zstep.zero12_step(L, [g[r].to("cuda") for r in range(n_dp)], *state, out, _hp(zb, t))
+        torch.cuda.synchronize()
+        dp_out, full_w, full_m, full_v = oracle.dp_step(parity.bits(g), full_w, full_m, full_v, HP_ORACLE, t)
+        for r in range(n_dp):
+            for got, ref in zip(state, (full_w[r], full_m[r], full_v[r])):
+                parity.assert_bit_exact_f32(got, ref, what=f"t={t} rank {r} ")
+            assert np.array_equal(parity.bits(out), dp_out[r]), f"t={t} rank {r} bf16"
+
+
 @pytest.mark.parametrize("n_dp", [1, 2, 3, 4, 5, 7, 8, 16])
 @pytest.mark.parametrize("align", [8, 1])
 def test_ragged_sizes_and_rank_counts(zlib, cuda_device, n_dp, align):
