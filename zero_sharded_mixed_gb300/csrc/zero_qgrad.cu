@@ -34,7 +34,8 @@
 // owner's slice, or whose owner boundaries fall off the 8-element vector grid,
 // is one launch per owner it meets.  The update with 8-bit output moves its
 // fp32 state with 256-bit loads and stores where every slice's state starts on
-// a 32-byte boundary (the other kinds measured slower with them).
+// a 32-byte boundary (the other kinds measured slower with them); the update
+// with bf16 output asks L2 for 256-byte blocks of the code streams.
 #include <cmath>
 
 #include "zero_tma.cuh"
@@ -80,6 +81,12 @@
                              // the accumulation, bit 1 the update, bit 2 the update with 8-bit
                              // output (measured on the Llama-7B units: 8-bit output +2.4 %,
                              // 6588 against 6434 GB/s; the update -2.3 %, the accumulation -0.4 %)
+#endif
+#ifndef ZGB_QCODE_PF256
+#define ZGB_QCODE_PF256 2    // code loads that ask L2 for the enclosing 256 bytes: bit 0 the
+                             // accumulation, bit 1 the update, bit 2 the update with 8-bit output
+                             // (measured: the update +0.8 %, 6589 against 6537 GB/s on GPT-2-XL
+                             // buckets; the others within 0.2 %, and 128 bytes changed nothing)
 #endif
 #ifndef ZGB_QWS
 #define ZGB_QWS 0            // opt-in: the code streams staged by bulk copies (qgrad_ws_kernel)
@@ -197,6 +204,20 @@ __device__ __forceinline__ void st_v8(float* p, const float (&x)[8]) {
 }
 #endif
 
+// One lane's 8 codes of a source, evict-first; for the kinds in
+// ZGB_QCODE_PF256 the miss fetches the enclosing 256-byte block into L2 (the
+// warp reads 256 consecutive bytes of each source).
+template <bool kUpdate, bool kQ8>
+__device__ __forceinline__ uint2 ld_codes(const int8_t* p) {
+    if constexpr ((ZGB_QCODE_PF256 & (kQ8 ? 4 : kUpdate ? 2 : 1)) != 0) {
+        uint2 c;
+        asm volatile("ld.global.cs.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(c.x), "=r"(c.y) : "l"(p));
+        return c;
+    } else {
+        return ld_stream_u2(p);
+    }
+}
+
 // x[j] = x[j] + code_j * scale for the 8 codes of c; each product and each
 // sum one IEEE rounding.
 __device__ __forceinline__ void add_codes8(float (&x)[8], const uint2 c, const float s) {
@@ -223,7 +244,7 @@ __device__ __forceinline__ void load_qvec(const QGradParams& p, const QSlice& sl
     const int64_t g = sl.eoff + e;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        x.c[r] = ld_stream_u2(p.q[r] + g);
+        x.c[r] = ld_codes<kUpdate, kQ8>(p.q[r] + g);
         x.s[r] = __ldg(p.scale[r] + b);
     }
 #if ZGB_QV8
