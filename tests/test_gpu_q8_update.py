@@ -148,3 +148,42 @@ def test_int8_gradient_update_with_8bit_output(zlib, cuda_device, numels, n_dp):
         cq, cs = _oracle_codes(out_ref, n_dp, S)
         np.testing.assert_array_equal(qb.q.cpu().numpy().reshape(-1), cq)
         np.testing.assert_array_equal(qb.scales[:, :qb.nb].cpu().numpy().reshape(-1), cs)
+
+
+@pytest.mark.parametrize("n_dp", [1, 8])
+def test_int8_gradient_update_with_8bit_output_state_off_the_32_byte_grid(zlib, cuda_device, n_dp):
+    """The update from 8-bit gradients to 8-bit shards moves its fp32 state with
+    256-bit accesses where every slice's state starts on a 32-byte boundary,
+    and with 128-bit ones otherwise: state 32-byte aligned and state 16 bytes
+    off that grid give the same bits, and both equal the oracle."""
+    zb = zlib
+    L = zb.zero_layout([33_031], n_dp, align=BLOCK)
+    P, S = L.padded_n, L.shard
+    w0 = inputs.master_weights(L.n, P, seed=91)
+    g = inputs.grads_bf16(n_dp, L.n, P, seed=92, step=1, outlier_p=0.01)
+    qg = zstep.Int8Grads(L, n_dp, BLOCK)
+    qg.quantize([g[r].cuda() for r in range(n_dp)])
+    qs, ss = qg.sources()
+    q_ref, s_ref = oracle.quantize_grad_int8(parity.bits(g), n_dp, BLOCK)
+    out_ref, *ref = oracle.qgrad_rs_adamw_reference(q_ref, s_ref, n_dp, BLOCK, n_dp, parity.f32(w0),
+                                                    np.zeros(P, np.float32), np.zeros(P, np.float32), HP, 1)
+    cq, cs = _oracle_codes(out_ref, n_dp, S)
+    results = []
+    for off in (0, 4):                       # floats: 0 keeps the 32-byte grid, 4 is 16 bytes off it
+        bufs = [torch.zeros(P + 8, device="cuda") for _ in range(3)]
+        st = [b[off:off + P] for b in bufs]
+        st[0].copy_(w0.cuda())
+        assert st[0].data_ptr() % 32 == (0 if off == 0 else 16)
+        q_out = torch.zeros(P, dtype=torch.int8, device="cuda")
+        s_out = torch.zeros(P // BLOCK, device="cuda")
+        zb.zero_reduce_scatter_adamw_int8_q8(L, qs, ss, BLOCK, float(n_dp), 0, n_dp, 0, P, *st, q_out, s_out,
+                                             BLOCK, _hp(zb, 1))
+        torch.cuda.synchronize()
+        parity.assert_state(st, ref, what=f"offset {off} floats ")
+        np.testing.assert_array_equal(q_out.cpu().numpy(), cq)
+        np.testing.assert_array_equal(s_out.cpu().numpy(), cs)
+        for b in bufs:                           # nothing written outside the state
+            assert torch.count_nonzero(b[:off]) == 0 and torch.count_nonzero(b[off + P:]) == 0
+        results.append([x.clone() for x in st] + [q_out, s_out])
+    for x, y in zip(*results):
+        assert torch.equal(x, y)
