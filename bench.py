@@ -1018,7 +1018,7 @@ def time_oracle(sample, seconds, n_dp, threads=1):
 
 COMPUTE_TOKENS = 1024         # tokens of the stand-in layer compute of the ZeRO-3 overlap workloads
 WORKLOAD_SAMPLE = 1 << 19     # elements of each extra workload's oracle sample
-WORKLOAD_ORACLE_SECONDS = 0.3
+WORKLOAD_ORACLE_SECONDS = 0.2  # each extra workload's oracle timing on every core (half that on one)
 
 
 def oracle_workload_step(name, n):
@@ -1314,8 +1314,9 @@ def run_ours(args):
         wl = make_workload(name, device, args.elems if name == primary else 0, args.bucket)
         torch.cuda.synchronize()
         is_primary = name == primary
-        steps = args.steps if is_primary else max(1, min(args.steps, 10))
-        warm = args.warmup if is_primary else max(1, min(args.warmup, 2))
+        # the other workloads: up to 20 timed steps after up to 3 warm-up steps
+        steps = args.steps if is_primary else max(1, min(args.steps, 20))
+        warm = args.warmup if is_primary else max(1, min(args.warmup, 3))
         sampler = ClockSampler(local) if is_primary else None
         total_ms, per_kind, clocks, t_next = time_workload(wl, steps, warm, dist, device, sampler)
         step_list = sorted(per_kind.pop("_steps"))
