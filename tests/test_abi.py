@@ -326,3 +326,32 @@ def test_schedule_fill_matches_the_oracle_bias_corrections(zlib):
     assert lib.zero_schedule_advance(None, 4, FAKE, FAKE, None) == -1
     assert lib.zero_schedule_advance(FAKE, 0, FAKE, FAKE, None) == -1
     assert lib.zero_schedule_advance(FAKE, 4, FAKE + 4, FAKE, None) == -2      # index 8-byte aligned
+
+
+def test_layout_whose_size_overflows_is_refused(zlib):
+    """A hand-made layout whose shard * n_dp overflows int64 (2^62 * 4 wraps to
+    0, the padded_n given) is refused by every entry point that takes a
+    layout, even on an empty range, which returns before any launch; the
+    same calls with zero_layout's own layout pass."""
+    lib = zlib.load()
+    good = zlib.zero_layout([4096], 4)
+    bad = zlib.zero_layout([4096], 4)
+    bad.shard, bad.padded_n, bad.n = 1 << 62, 0, 0
+    src = (ctypes.c_void_p * 4)(*[FAKE] * 4)
+    hp = zlib.ZeroAdamW.make(step=1)
+    hpp = ctypes.byref(hp)
+    for L, want in ((good, 0), (bad, -1)):
+        Lp = ctypes.byref(L)
+        assert lib.zero_reduce_scatter_adamw(Lp, src, 4, 0, 0, 4.0, 0, 4, 0, 0, FAKE, FAKE, FAKE, FAKE, 0,
+                                             hpp, None) == want
+        assert lib.zero_reduce_scatter_adamw_int8(Lp, src, src, 4, 256, 4.0, 0, 4, 0, 0, FAKE, FAKE, FAKE,
+                                                  FAKE, 0, hpp, None) == want
+        assert lib.zero_accumulate(Lp, 1, src, 4, 0, 0, FAKE, 0, 0, 0, 1, None) == want
+        assert lib.zero_accumulate_int8(Lp, src, src, 4, 256, FAKE, 0, 0, 0, 1, None) == want
+        assert lib.zero_accumulate_adamw(Lp, 1, src, 1, 0, src, 4, 0, 4.0, 0, 4, 0, 0, FAKE, FAKE, FAKE,
+                                         FAKE, 0, hpp, None) == want
+    Lp = ctypes.byref(bad)
+    assert lib.zero_gather_layer(Lp, src, FAKE, None) == -1
+    assert lib.zero_quantize_int8(Lp, FAKE, FAKE, FAKE, 256, None) == -1
+    assert lib.zero_gather_layer_int8(Lp, src, src, 256, FAKE, None) == -1
+    assert lib.zero_grad_norm_sq(Lp, src, 4, 0, 0, 4.0, 0, 0, FAKE, 1 << 20, FAKE, 0, None) == -1

@@ -270,7 +270,7 @@ extern "C" int zero_accumulate(const zero_layout_t* L, int32_t mode, const void*
     if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
     if (mode == ZERO_ACC_LOCAL && n_src != 1) return ZERO_EINVAL;
     if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
-    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp)
+    if (!layout_shape_ok(L))
         return ZERO_EINVAL;
     if (begin < 0 || end > L->padded_n || begin > end) return ZERO_EINVAL;
     if (src_base > begin || dst_base > begin) return ZERO_EINVAL;

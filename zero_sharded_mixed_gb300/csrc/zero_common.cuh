@@ -91,6 +91,15 @@ int check_device_ptr(const void* p);
 // Also 0 for pinned host memory that the device addresses at the same pointer
 // (read by the kernels over the host link).
 int check_source_ptr(const void* p);
+// Whether a caller's layout has the shape zero_layout gives: n_dp >= 1,
+// shard >= 0 and padded_n = shard * n_dp, with the product at most
+// INT64_MAX / 8 (zero_layout's own limit, which keeps every byte offset in
+// range) and computed only once it cannot overflow.
+inline bool layout_shape_ok(const zero_layout_t* L) {
+    constexpr int64_t kMaxElems = INT64_MAX / 8;
+    return L->n_dp >= 1 && L->shard >= 0 && L->shard <= kMaxElems / L->n_dp &&
+           L->padded_n == L->shard * (int64_t)L->n_dp;
+}
 // ZERO_EALIGN unless p is a multiple of `bytes`.
 inline int check_aligned(const void* p, int bytes) {
     return (reinterpret_cast<uintptr_t>(p) % (uintptr_t)bytes) ? ZERO_EALIGN : ZERO_OK;

@@ -61,7 +61,7 @@ extern "C" int zero_gather_layer(const zero_layout_t* unit, const uint16_t* cons
                                  uint16_t* full_out, void* stream) {
     using namespace zgb;
     if (!unit || !shards || !full_out) return ZERO_EINVAL;
-    if (unit->n_dp < 1 || unit->shard < 0 || unit->padded_n != unit->shard * (int64_t)unit->n_dp)
+    if (!layout_shape_ok(unit))
         return ZERO_EINVAL;
     const int n_dp = unit->n_dp;
     for (int o = 0; o < n_dp; ++o)

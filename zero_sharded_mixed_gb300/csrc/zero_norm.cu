@@ -230,7 +230,7 @@ int grad_norm_sq(const zero_layout_t* L, const void* const* src, int32_t n_src, 
     if (n_src < 1) return ZERO_EINVAL;
     if (n_src > ZERO_MAX_SRC) return ZERO_ERANGE;
     if (src_dtype != ZERO_BF16 && src_dtype != ZERO_F32) return ZERO_EINVAL;
-    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
+    if (!layout_shape_ok(L)) return ZERO_EINVAL;
     if (begin < 0 || end > L->padded_n || begin > end || src_base > begin) return ZERO_EINVAL;
     if (!(divisor > 0.0f) || !(divisor < 3.4e38f)) return ZERO_EINVAL;
     for (int r = 0; r < n_src; ++r)

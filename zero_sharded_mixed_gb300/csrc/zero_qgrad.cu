@@ -987,7 +987,7 @@ extern "C" int zero_accumulate_int8(const zero_layout_t* L, const int8_t* const*
     if (!L || !dst) return ZERO_EINVAL;
     int rc = check_qsources(q_src, scale_src, n_src, block);
     if (rc) return rc;
-    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp)
+    if (!layout_shape_ok(L))
         return ZERO_EINVAL;
     if (begin < 0 || end > L->padded_n || begin > end) return ZERO_EINVAL;
     if (dst_base > begin) return ZERO_EINVAL;

@@ -188,7 +188,7 @@ extern "C" int zero_quantize_int8(const zero_layout_t* unit, const uint16_t* sha
     using namespace zgb;
     if (!unit || !shards_bf16 || !q || !scales) return ZERO_EINVAL;
     if (!valid_block(block)) return ZERO_EINVAL;
-    if (unit->n_dp < 1 || unit->shard < 0 || unit->padded_n != unit->shard * (int64_t)unit->n_dp)
+    if (!layout_shape_ok(unit))
         return ZERO_EINVAL;
     if (check_aligned(shards_bf16, 2) || check_aligned(scales, 4)) return ZERO_EALIGN;
     if (unit->shard == 0) return ZERO_OK;
@@ -240,7 +240,7 @@ extern "C" int zero_gather_layer_int8(const zero_layout_t* unit, const int8_t* c
     using namespace zgb;
     if (!unit || !q_shards || !scale_shards || !full_out) return ZERO_EINVAL;
     if (!valid_block(block)) return ZERO_EINVAL;
-    if (unit->n_dp < 1 || unit->shard < 0 || unit->padded_n != unit->shard * (int64_t)unit->n_dp)
+    if (!layout_shape_ok(unit))
         return ZERO_EINVAL;
     const int n_dp = unit->n_dp;
     for (int o = 0; o < n_dp; ++o)

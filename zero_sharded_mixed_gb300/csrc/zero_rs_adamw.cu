@@ -387,7 +387,7 @@ int prepare_target(const zero_layout_t* L, int32_t rank_begin, int32_t rank_end,
     } else if ((out_mode != ZERO_OUT_FULL && out_mode != ZERO_OUT_SHARD) || out == nullptr) {
         return ZERO_EINVAL;
     }
-    if (L->n_dp < 1 || L->shard < 0 || L->padded_n != L->shard * (int64_t)L->n_dp) return ZERO_EINVAL;
+    if (!layout_shape_ok(L)) return ZERO_EINVAL;
     if (rank_begin < 0 || rank_end > L->n_dp || rank_begin >= rank_end) return ZERO_EINVAL;
     const int64_t own_lo = (int64_t)rank_begin * L->shard;
     const int64_t own_hi = (int64_t)rank_end * L->shard;
