@@ -89,6 +89,16 @@ def test_bucket_and_shard_ranges(zlib):
     # a rank whose shard is all padding
     L = zlib.zero_layout([9], 4, align=8)
     assert zlib.zero_shard_range(L, 3) == (24, 32, 24)
+    # a hand-made layout whose ranges would overflow int64 is refused
+    L = zlib.zero_layout([1000], 3, align=8, bucket_elems=100)
+    L.shard = 1 << 62
+    with pytest.raises(zlib.ZeroError):
+        zlib.zero_shard_range(L, 2)
+    L = zlib.zero_layout([1000], 3, align=8, bucket_elems=100)
+    L.bucket, L.n_buckets = 1 << 58, 8          # the library's element limit is 2^63 / 8
+    with pytest.raises(zlib.ZeroError):
+        zlib.zero_bucket_range(L, 4)
+    assert zlib.zero_bucket_range(L, 0) == (0, L.padded_n)
 
 
 def test_memory_and_comm_helpers_match_oracle(zlib):

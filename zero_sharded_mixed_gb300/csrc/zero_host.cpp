@@ -58,17 +58,18 @@ extern "C" int zero_layout(const int64_t* numel, int32_t n_tensors, int32_t n_dp
 
 extern "C" int zero_bucket_range(const zero_layout_t* L, int64_t b, int64_t* begin, int64_t* end) {
     if (!L || !begin || !end || b < 0 || b >= L->n_buckets || L->bucket < 1) return ZERO_EINVAL;
-    *begin = b * L->bucket;
-    int64_t e = *begin + L->bucket;
+    int64_t lo = 0, e = 0;                  // a caller's layout: no product past kMaxElems
+    if (!mul_ok(b, L->bucket, &lo) || !add_ok(lo, L->bucket, &e)) return ZERO_EINVAL;
+    *begin = lo;
     *end = e < L->padded_n ? e : L->padded_n;
     return ZERO_OK;
 }
 
 extern "C" int zero_shard_range(const zero_layout_t* L, int32_t rank, int64_t* begin, int64_t* end,
                                 int64_t* valid_end) {
-    if (!L || !begin || !end || rank < 0 || rank >= L->n_dp) return ZERO_EINVAL;
-    int64_t b = (int64_t)rank * L->shard;
-    int64_t e = b + L->shard;
+    if (!L || !begin || !end || rank < 0 || rank >= L->n_dp || L->shard < 0) return ZERO_EINVAL;
+    int64_t b = 0, e = 0;                   // a caller's layout: no product past kMaxElems
+    if (!mul_ok(rank, L->shard, &b) || !add_ok(b, L->shard, &e)) return ZERO_EINVAL;
     *begin = b;
     *end = e;
     if (valid_end) *valid_end = L->n < b ? b : (L->n < e ? L->n : e);
