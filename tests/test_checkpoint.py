@@ -2,6 +2,8 @@
 CRC-32 against zlib's (a library routine), corruption detection, consolidation
 (padding dropped, tensors split at their offsets) and resharding to another
 number of ranks."""
+import ctypes
+import os
 import zlib as zlib_ref
 
 import numpy as np
@@ -85,6 +87,18 @@ def test_header_validation(zlib, tmp_path):
         with pytest.raises(zb.ZeroError) as e:
             ck.write_shard(str(tmp_path / "x.bin"), h, x, x, x)
         assert e.value.code == zb.ZERO_EINVAL
+
+
+def test_header_whose_size_overflows_is_refused(zlib, tmp_path):
+    """A header with shard * n_dp past int64 (2^62 * 4 wraps to the padded_n 0
+    given) is refused by the writer before any byte count is formed; the
+    arrays passed are never read."""
+    x = np.zeros(8, np.float32)
+    h = zb.ZeroCkptHeader(0, 0, 1 << 62, 8, 1, 4, 0, 0, 0, 0, 0, 0, 0)
+    path = tmp_path / "x.bin"
+    rc = zb.load().zero_ckpt_write_shard(os.fsencode(str(path)), ctypes.byref(h), *[x.ctypes.data] * 3, None)
+    assert rc == zb.ZERO_EINVAL
+    assert not path.exists()
 
 
 def test_save_consolidate_reshard(zlib, tmp_path):

@@ -23,6 +23,8 @@ namespace {
 
 constexpr char kMagic[8] = {'Z', 'G', 'B', 'S', 'H', 'A', 'R', 'D'};
 constexpr uint32_t kVersion = 1;
+// The library's element limit (that of zero_layout): every byte count below fits.
+constexpr int64_t kMaxShardElems = INT64_MAX / 8;
 
 uint32_t g_crc_table[8][256];
 std::once_flag g_crc_once;
@@ -91,6 +93,7 @@ extern "C" int zero_ckpt_write_shard(const char* path, const zero_ckpt_header_t*
     std::call_once(g_crc_once, build_crc_table);
     if (!path || !h || !master || !m || !v) return ZERO_EINVAL;
     if (h->n_dp < 1 || h->rank < 0 || h->rank >= h->n_dp || h->shard < 0 || h->step < 0 ||
+        h->shard > kMaxShardElems / h->n_dp ||                  // before the product can overflow
         h->padded_n != h->shard * (int64_t)h->n_dp || h->n < 0 || h->n > h->padded_n)
         return ZERO_EINVAL;
     FileHeader fh;
@@ -153,7 +156,7 @@ extern "C" int zero_ckpt_read_shard(const char* path, zero_ckpt_header_t* h, flo
     if (std::fread(&fh, 1, sizeof fh, f) != sizeof fh ||
         std::memcmp(fh.magic, kMagic, sizeof kMagic) != 0 || fh.version != kVersion) {
         rc = ZERO_ECORRUPT;
-    } else if (fh.h.shard < 0 || fh.h.shard > capacity) {
+    } else if (fh.h.shard < 0 || fh.h.shard > capacity || fh.h.shard > kMaxShardElems) {
         rc = ZERO_ERANGE;
     } else if (w_bf16 && !(fh.flags & 1u)) {
         rc = ZERO_EINVAL;   // asked for bf16 weights the file does not hold
