@@ -333,6 +333,8 @@ def test_schedule_fill_matches_the_oracle_bias_corrections(zlib):
     assert lib.zero_schedule_fill(None, 1, 4, None, FAKE) == -1
     assert lib.zero_schedule_fill(ctypes.byref(hp), 0, 4, None, FAKE) == -1
     assert lib.zero_schedule_fill(ctypes.byref(hp), 1, 0, None, FAKE) == -1
+    assert lib.zero_schedule_fill(ctypes.byref(hp), (1 << 63) - 1, 2, None, FAKE) == -1   # step past int64
+    assert lib.zero_schedule_fill(ctypes.byref(hp), 1, 1 << 62, None, FAKE) == -1         # index past int64
     assert lib.zero_schedule_advance(None, 4, FAKE, FAKE, None) == -1
     assert lib.zero_schedule_advance(FAKE, 0, FAKE, FAKE, None) == -1
     assert lib.zero_schedule_advance(FAKE, 4, FAKE + 4, FAKE, None) == -2      # index 8-byte aligned

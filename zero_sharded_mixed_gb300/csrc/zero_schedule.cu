@@ -51,6 +51,7 @@ int take_schedule_status() {
 extern "C" int zero_schedule_fill(const zero_adamw_t* hp, int64_t first_step, int64_t n_steps,
                                   const float* lrs, float* table) {
     if (!hp || !table || first_step < 1 || n_steps < 1) return ZERO_EINVAL;
+    if (n_steps > INT64_MAX - first_step || n_steps > INT64_MAX / 3) return ZERO_EINVAL;   // step and index in range
     if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
         return ZERO_EINVAL;
     for (int64_t k = 0; k < n_steps; ++k) {
