@@ -26,6 +26,10 @@
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Work is enqueued on it asynchronously.
  *  - Pointer arrays (`src`, `shards`) are HOST arrays of device pointers.
+ *  - Layouts: a zero_layout_t passed in must have the shape zero_layout()
+ *    gives (n_dp >= 1, shard >= 0, padded_n = shard * n_dp, at most
+ *    2^63 / 8 elements); a hand-made struct outside that shape gives
+ *    ZERO_EINVAL, checked before any product of its fields is formed.
  *
  * Notation ("ZeRO and FSDP", section "The idea, one stage at a time"): all
  * parameters are flattened into one vector of N elements and cut into n_dp
